@@ -1,0 +1,386 @@
+// CPU oracle of the W4A4 MXFP4 mixture-of-experts expert layer.
+//
+// TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the
+// benchmark's CPU-baseline leg may load this library.  The product (the CUDA
+// library and its Python binding) never calls it and shares no code with it.
+//
+// It restates, plainly and slowly, what the layer computes, in the order the
+// pages describe it:
+//   * "[deepseek-v4] Bump sgl-deep-gemm for packed FP4xFP4 mega-MoE (W4A4)"
+//     (top, and Appendix B): a packed FP4 x FP4 (W4A4) mega-MoE kernel on a
+//     DeepSeek-V4-Flash layer (hidden 4096, inter 2048, 256 experts, top-6).
+//   * prhub digest of SGLang PR #37279, section "实现拆解" items 3-4 and the
+//     mega_moe.py source excerpt: pre_dispatch quantises bf16 hidden states
+//     to packed E2M1 with group_size=32 for mma_type "mxf4xmxf4"; the expert
+//     buffer uses activation "swiglu"; the gate/up rows of the first weight
+//     are interleaved with gran=16 (even/odd) for MXFP4 activations.
+//   * SGLang PR #48424, "DeepGEMM producers write FlashInfer's 128x4 scale
+//     layout": the 4-D int32 scale shape [ceil(rows/128), K/128, 32, 4].
+//
+// Readings where the pages are silent (each is listed in the design notes):
+//   R1 E2M1 code s*8+m decodes to (-1)^s * {0,0.5,1,1.5,2,3,4,6}[m] (OCP MX);
+//      element 2i of a row sits in the low nibble of byte i.
+//   R2 The per-32 scale is 2^e with e the smallest integer such that
+//      amax <= 6 * 2^e (i.e. e = ceil(log2(amax/6)) evaluated exactly),
+//      clamped to [-127, 127]; amax = 0 gives e = -127.  Stored as the UE8M0
+//      byte e + 127.
+//   R3 Each element x becomes the E2M1 value nearest to x * 2^-e; a tie goes
+//      to the code with even mantissa index; the sign bit follows x (so a
+//      negative value that rounds to zero is code 0x8).
+//   R4 Gate rows are the first I rows of the first weight, up rows the last I.
+//   R5 Within an expert, assignments (t, j) are ordered by ascending t then j.
+//   R6 h = silu(g) * u = g / (1 + exp(-g)) * u from exact g, u, rounded once to
+//      fp32; h is requantised with R2/R3 over 32-groups along I (no bf16 step).
+//   R7 The routing weight is applied at the combine, after the down
+//      projection: out[t] = bf16_rne(sum_j w[t,j] * y[(t,j)]), summed in j
+//      order in double.
+//   R8 Routing ids outside [0, E) contribute nothing.
+//
+// Every matrix product is the plain definition: a sum over K of products of
+// dequantised values, in double.  Each product is a dyadic rational with at
+// most 8 significant bits, so these sums are exact for the shapes used here.
+
+#include <cassert>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <algorithm>
+#include <functional>
+#include <thread>
+#include <vector>
+
+namespace {
+
+// R1: the eight E2M1 magnitudes, indexed by the 3-bit exponent/mantissa field.
+const double kE2M1Magnitude[8] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
+
+void parallel_for(int64_t n, int nthreads, const std::function<void(int64_t, int64_t)>& fn) {
+    if (n <= 0) return;
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > 256) nthreads = 256;
+    if (nthreads == 1 || n == 1) {
+        fn(0, n);
+        return;
+    }
+    const int64_t parts = std::min<int64_t>(n, nthreads);
+    std::vector<std::thread> pool;
+    pool.reserve((size_t)parts);
+    for (int64_t p = 0; p < parts; ++p) {
+        const int64_t b = n * p / parts, e = n * (p + 1) / parts;
+        pool.emplace_back([&fn, b, e]() { fn(b, e); });
+    }
+    for (auto& th : pool) th.join();
+}
+
+double bf16_bits_to_double(uint16_t b) {
+    const uint32_t u = (uint32_t)b << 16;
+    float f;
+    std::memcpy(&f, &u, 4);
+    return (double)f;
+}
+
+}  // namespace
+
+extern "C" {
+
+// R1: value of one 4-bit code.
+double oracle_e2m1_value(int code) {
+    const double m = kE2M1Magnitude[code & 7];
+    return (code & 8) ? -m : m;
+}
+
+// R2: smallest e with amax <= 6 * 2^e, clamped to [-127, 127].
+int oracle_mx_exponent(double amax) {
+    assert(std::isfinite(amax) && amax >= 0.0);
+    if (amax == 0.0) return -127;
+    int p = 0;
+    (void)std::frexp(amax, &p);  // amax = f * 2^p with f in [0.5, 1)
+    int e = p - 4;               // 6 * 2^(p-4) = 0.375 * 2^p < amax: too small
+    assert(amax > std::ldexp(6.0, e));
+    while (amax > std::ldexp(6.0, e)) ++e;
+    if (e < -127) e = -127;
+    if (e > 127) e = 127;
+    return e;
+}
+
+// R3: nearest E2M1 code to q (|q| <= 6), ties to the even mantissa index,
+// sign bit taken from q.
+int oracle_e2m1_encode(double q) {
+    const int sign = std::signbit(q) ? 8 : 0;
+    const double a = std::fabs(q);
+    assert(a <= 6.0);
+    int best = 0;
+    double best_d = a;
+    for (int m = 1; m < 8; ++m) {
+        const double d = std::fabs(kE2M1Magnitude[m] - a);
+        if (d < best_d || (d == best_d && (m % 2) == 0)) {
+            best = m;
+            best_d = d;
+        }
+    }
+    return sign | best;
+}
+
+// Quantises one group of 32 values (R2, R3); writes 16 packed bytes and one
+// scale byte.
+static void quantize_group(const double* v, uint8_t* codes16, uint8_t* sf) {
+    double amax = 0.0;
+    for (int i = 0; i < 32; ++i) amax = std::max(amax, std::fabs(v[i]));
+    const int e = oracle_mx_exponent(amax);
+    int c[32];
+    for (int i = 0; i < 32; ++i) c[i] = oracle_e2m1_encode(std::ldexp(v[i], -e));
+    for (int i = 0; i < 16; ++i) codes16[i] = (uint8_t)(c[2 * i] | (c[2 * i + 1] << 4));
+    *sf = (uint8_t)(e + 127);
+}
+
+// Row-major fp32 [rows, K] -> codes [rows, K/2], scales [rows, K/32].
+void oracle_quantize_f32(const float* x, int64_t rows, int64_t K, uint8_t* codes, uint8_t* sf,
+                         int nthreads) {
+    assert(K % 32 == 0);
+    parallel_for(rows, nthreads, [&](int64_t r0, int64_t r1) {
+        double v[32];
+        for (int64_t r = r0; r < r1; ++r)
+            for (int64_t g = 0; g < K / 32; ++g) {
+                for (int i = 0; i < 32; ++i) v[i] = (double)x[r * K + g * 32 + i];
+                quantize_group(v, codes + r * (K / 2) + g * 16, sf + r * (K / 32) + g);
+            }
+    });
+}
+
+// Row-major bf16 bits [rows, K] -> codes, scales (bf16 widens exactly).
+void oracle_quantize_bf16(const uint16_t* x, int64_t rows, int64_t K, uint8_t* codes, uint8_t* sf,
+                          int nthreads) {
+    assert(K % 32 == 0);
+    parallel_for(rows, nthreads, [&](int64_t r0, int64_t r1) {
+        double v[32];
+        for (int64_t r = r0; r < r1; ++r)
+            for (int64_t g = 0; g < K / 32; ++g) {
+                for (int i = 0; i < 32; ++i) v[i] = bf16_bits_to_double(x[r * K + g * 32 + i]);
+                quantize_group(v, codes + r * (K / 2) + g * 16, sf + r * (K / 32) + g);
+            }
+    });
+}
+
+// codes/scales -> double values, row-major [rows, K].
+void oracle_dequantize(const uint8_t* codes, const uint8_t* sf, int64_t rows, int64_t K,
+                       double* out) {
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t k = 0; k < K; ++k) {
+            const uint8_t byte = codes[r * (K / 2) + k / 2];
+            const int code = (k % 2 == 0) ? (byte & 0xF) : (byte >> 4);
+            const int e = (int)sf[r * (K / 32) + k / 32] - 127;
+            out[r * K + k] = std::ldexp(oracle_e2m1_value(code), e);
+        }
+}
+
+// double -> bf16 bits, round to nearest, ties to even; overflow to infinity.
+uint16_t oracle_bf16_round(double v) {
+    double r;
+    if (v == 0.0 || !std::isfinite(v)) {
+        r = v;
+    } else {
+        int p = std::ilogb(v);            // |v| in [2^p, 2^(p+1))
+        if (p < -126) p = -126;           // below that bf16 is subnormal: fixed quantum
+        const double quantum = std::ldexp(1.0, p - 7);
+        r = std::nearbyint(v / quantum) * quantum;  // default mode: ties to even
+        if (std::fabs(r) >= std::ldexp(1.0, 128)) r = std::copysign(INFINITY, v);
+    }
+    const float f = (float)r;  // exact: r has at most 8 significant bits
+    uint32_t u;
+    std::memcpy(&u, &f, 4);
+    return (uint16_t)(u >> 16);
+}
+
+// gran=16 gate/up interleave of the first weight, for MXFP4 activations
+// (digest of PR #37279, item 4): each chunk of 16 gate rows and the matching
+// 16 up rows becomes [gate even (8), up even (8), gate odd (8), up odd (8)].
+// Returns the canonical row (gate rows 0..I-1, up rows I..2I-1) that lands at
+// prepared row r.
+int64_t oracle_interleave_source_row(int64_t r, int64_t I) {
+    const int64_t c = r / 32, o = r % 32;
+    if (o < 8) return c * 16 + 2 * o;
+    if (o < 16) return I + c * 16 + 2 * (o - 8);
+    if (o < 24) return c * 16 + 2 * (o - 16) + 1;
+    return I + c * 16 + 2 * (o - 24) + 1;
+}
+
+// Byte offset of scale (row r, scale column s) in the 128x4 block layout whose
+// int32 view has shape [ceil(rows/128), Kc/4, 32, 4] (PR #48424): each block of
+// 128 rows x 4 scale columns is 512 contiguous bytes, row r%32 picks the 16-byte
+// line, (r%128)/32 the int32 within it and s%4 the byte.  Kc = K/32.
+int64_t oracle_scale_block_offset(int64_t r, int64_t s, int64_t Kc) {
+    return ((r / 128) * (Kc / 4) + s / 4) * 512 + (r % 32) * 16 + ((r % 128) / 32) * 4 + (s % 4);
+}
+
+// R5: counts per expert, canonical offsets (exclusive prefix sum of counts)
+// and, for slot p = offsets[e] + rank, the (t, j) it holds.  Returns the
+// number of (t, j) whose id is outside [0, E).
+int64_t oracle_bucket(const int32_t* ids, int64_t T, int64_t k, int64_t E, int64_t* counts,
+                      int64_t* offsets, int32_t* slot_t, int32_t* slot_j) {
+    int64_t bad = 0;
+    for (int64_t e = 0; e < E; ++e) counts[e] = 0;
+    for (int64_t a = 0; a < T * k; ++a) {
+        if (ids[a] < 0 || ids[a] >= E) {
+            ++bad;
+            continue;
+        }
+        ++counts[ids[a]];
+    }
+    offsets[0] = 0;
+    for (int64_t e = 0; e < E; ++e) offsets[e + 1] = offsets[e] + counts[e];
+    std::vector<int64_t> fill(offsets, offsets + E);
+    for (int64_t t = 0; t < T; ++t)
+        for (int64_t j = 0; j < k; ++j) {
+            const int32_t e = ids[t * k + j];
+            if (e < 0 || e >= E) continue;
+            const int64_t p = fill[e]++;
+            slot_t[p] = (int32_t)t;
+            slot_j[p] = (int32_t)j;
+        }
+    return bad;
+}
+
+struct oracle_shape {
+    int64_t T, H, I, E, k;
+};
+
+// Grouped down projection and combine from given intermediate codes:
+// y[a] = dequant(h[a]) . dequant(W2[e])^T for every valid assignment a = t*k+j,
+// then R7.  Used on its own to check the down projection against any given
+// intermediate, and as the tail of oracle_moe.
+static void down_and_combine(const oracle_shape* s, const int32_t* ids, const float* tw,
+                             const uint8_t* w2_codes, const uint8_t* w2_sf, const uint8_t* h_codes,
+                             const uint8_t* h_sf, double* y_out, double* out_f64,
+                             uint16_t* out_bf16, int nthreads) {
+    const int64_t T = s->T, H = s->H, I = s->I, E = s->E, k = s->k, A = T * k;
+    std::vector<int64_t> counts(E), offsets(E + 1);
+    std::vector<int32_t> st(A), sj(A);
+    oracle_bucket(ids, T, k, E, counts.data(), offsets.data(), st.data(), sj.data());
+
+    std::vector<double> y((size_t)A * H, 0.0);
+    std::vector<double> hdq((size_t)A * I);
+    parallel_for(A, nthreads, [&](int64_t a0, int64_t a1) {
+        for (int64_t a = a0; a < a1; ++a)
+            if (ids[a] >= 0 && ids[a] < E)
+                oracle_dequantize(h_codes + a * (I / 2), h_sf + a * (I / 32), 1, I, &hdq[(size_t)a * I]);
+    });
+    for (int64_t e = 0; e < E; ++e) {
+        if (counts[e] == 0) continue;
+        parallel_for(H, nthreads, [&](int64_t n0, int64_t n1) {
+            std::vector<double> wrow((size_t)I);
+            for (int64_t n = n0; n < n1; ++n) {
+                oracle_dequantize(w2_codes + (e * H + n) * (I / 2), w2_sf + (e * H + n) * (I / 32), 1,
+                                  I, wrow.data());
+                for (int64_t p = offsets[e]; p < offsets[e + 1]; ++p) {
+                    const int64_t a = (int64_t)st[p] * k + sj[p];
+                    double acc = 0.0;
+                    for (int64_t i = 0; i < I; ++i) acc += hdq[(size_t)a * I + i] * wrow[i];
+                    y[(size_t)a * H + n] = acc;
+                }
+            }
+        });
+    }
+    if (y_out) std::memcpy(y_out, y.data(), sizeof(double) * (size_t)A * H);
+    parallel_for(T, nthreads, [&](int64_t t0, int64_t t1) {
+        for (int64_t t = t0; t < t1; ++t)
+            for (int64_t n = 0; n < H; ++n) {
+                double acc = 0.0;
+                for (int64_t j = 0; j < k; ++j) {
+                    const int32_t e = ids[t * k + j];
+                    if (e < 0 || e >= E) continue;
+                    acc += (double)tw[t * k + j] * y[(size_t)(t * k + j) * H + n];
+                }
+                if (out_f64) out_f64[t * H + n] = acc;
+                if (out_bf16) out_bf16[t * H + n] = oracle_bf16_round(acc);
+            }
+    });
+}
+
+// The whole layer.  Optional outputs (nullable):
+//   x_codes [T, H/2], x_sf [T, H/32]          quantised hidden states
+//   gate_up [A, 2I] (double)                   g (cols 0..I-1) and u (cols I..2I-1)
+//   h_codes [A, I/2], h_sf [A, I/32]           requantised intermediate
+//   y [A, H] (double)                          down projection per assignment
+//   out_f64 [T, H], out_bf16 [T, H]            combined output
+// Assignment a = t*k + j.  Weights are canonical (un-interleaved) MXFP4:
+// w1 [E, 2I, H] (gate rows then up rows), w2 [E, H, I].  Returns the number
+// of ids outside [0, E).
+int64_t oracle_moe(const oracle_shape* s, const uint16_t* x_bf16, const int32_t* ids,
+                   const float* tw, const uint8_t* w1_codes, const uint8_t* w1_sf,
+                   const uint8_t* w2_codes, const uint8_t* w2_sf, double* out_f64,
+                   uint16_t* out_bf16, uint8_t* x_codes_out, uint8_t* x_sf_out, double* gate_up_out,
+                   uint8_t* h_codes_out, uint8_t* h_sf_out, double* y_out, int nthreads) {
+    const int64_t T = s->T, H = s->H, I = s->I, E = s->E, k = s->k, A = T * k;
+    assert(H % 32 == 0 && I % 32 == 0);
+
+    // 1. quantise the hidden states (pre_dispatch, group_size=32)
+    std::vector<uint8_t> xc((size_t)T * H / 2), xs((size_t)T * H / 32);
+    oracle_quantize_bf16(x_bf16, T, H, xc.data(), xs.data(), nthreads);
+    if (x_codes_out) std::memcpy(x_codes_out, xc.data(), xc.size());
+    if (x_sf_out) std::memcpy(x_sf_out, xs.data(), xs.size());
+
+    // 2. bucket the assignments by expert
+    std::vector<int64_t> counts(E), offsets(E + 1);
+    std::vector<int32_t> st(A), sj(A);
+    const int64_t bad =
+        oracle_bucket(ids, T, k, E, counts.data(), offsets.data(), st.data(), sj.data());
+
+    std::vector<double> xdq((size_t)T * H);
+    parallel_for(T, nthreads, [&](int64_t t0, int64_t t1) {
+        for (int64_t t = t0; t < t1; ++t)
+            oracle_dequantize(&xc[(size_t)t * H / 2], &xs[(size_t)t * H / 32], 1, H, &xdq[(size_t)t * H]);
+    });
+
+    // 3. grouped gate/up projection: gu[a][n] = sum_k x[t][k] * W1[e][n][k]
+    std::vector<double> gu((size_t)A * 2 * I, 0.0);
+    for (int64_t e = 0; e < E; ++e) {
+        if (counts[e] == 0) continue;
+        parallel_for(2 * I, nthreads, [&](int64_t n0, int64_t n1) {
+            std::vector<double> wrow((size_t)H);
+            for (int64_t n = n0; n < n1; ++n) {
+                oracle_dequantize(w1_codes + (e * 2 * I + n) * (H / 2),
+                                  w1_sf + (e * 2 * I + n) * (H / 32), 1, H, wrow.data());
+                for (int64_t p = offsets[e]; p < offsets[e + 1]; ++p) {
+                    const int64_t t = st[p], a = t * k + sj[p];
+                    double acc = 0.0;
+                    for (int64_t kk = 0; kk < H; ++kk) acc += xdq[(size_t)t * H + kk] * wrow[kk];
+                    gu[(size_t)a * 2 * I + n] = acc;
+                }
+            }
+        });
+    }
+    if (gate_up_out) std::memcpy(gate_up_out, gu.data(), sizeof(double) * gu.size());
+
+    // 4-5. SwiGLU (R6) and requantisation of h along I
+    std::vector<uint8_t> hc((size_t)A * I / 2, 0), hs((size_t)A * I / 32, 0);
+    parallel_for(A, nthreads, [&](int64_t a0, int64_t a1) {
+        std::vector<float> h((size_t)I);
+        for (int64_t a = a0; a < a1; ++a) {
+            if (ids[a] < 0 || ids[a] >= E) continue;
+            for (int64_t i = 0; i < I; ++i) {
+                const double g = gu[(size_t)a * 2 * I + i];
+                const double u = gu[(size_t)a * 2 * I + I + i];
+                h[i] = (float)(g / (1.0 + std::exp(-g)) * u);
+            }
+            oracle_quantize_f32(h.data(), 1, I, &hc[(size_t)a * I / 2], &hs[(size_t)a * I / 32], 1);
+        }
+    });
+    if (h_codes_out) std::memcpy(h_codes_out, hc.data(), hc.size());
+    if (h_sf_out) std::memcpy(h_sf_out, hs.data(), hs.size());
+
+    // 6-7. grouped down projection and top-k weighted combine
+    down_and_combine(s, ids, tw, w2_codes, w2_sf, hc.data(), hs.data(), y_out, out_f64, out_bf16,
+                     nthreads);
+    return bad;
+}
+
+// Down projection + combine from caller-given intermediate codes [A, I/2],
+// scales [A, I/32] (a = t*k + j).  Same arithmetic as the tail of oracle_moe.
+void oracle_moe_down(const oracle_shape* s, const int32_t* ids, const float* tw,
+                     const uint8_t* w2_codes, const uint8_t* w2_sf, const uint8_t* h_codes,
+                     const uint8_t* h_sf, double* out_f64, uint16_t* out_bf16, int nthreads) {
+    down_and_combine(s, ids, tw, w2_codes, w2_sf, h_codes, h_sf, nullptr, out_f64, out_bf16,
+                     nthreads);
+}
+
+}  // extern "C"
