@@ -1,0 +1,645 @@
+// C ABI of libmxmoe (declared in include/mxmoe.h): argument checks, workspace and
+// prepared-weight layouts, the workspace registry, launches, debug readback and
+// timing hooks.  No entry point here allocates device memory.
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "common.cuh"
+#include "mxmoe.h"
+
+using namespace mxmoe;
+
+namespace {
+
+thread_local std::string g_err;
+
+moe_status fail(moe_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return s;
+}
+
+moe_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(MOE_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+constexpr size_t kAlign = 1024;
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool dims_equal(const moe_dims& a, const moe_dims& b) {
+  return a.hidden == b.hidden && a.inter == b.inter && a.num_experts == b.num_experts &&
+         a.topk == b.topk && a.max_tokens == b.max_tokens && a.mma_type == b.mma_type;
+}
+
+WsLayout ws_layout(const moe_dims& d) {
+  WsLayout L;
+  const int64_t H = d.hidden, I = d.inter, E = d.num_experts, k = d.topk;
+  L.T_cap = d.max_tokens;
+  L.A_cap = L.T_cap * k;
+  L.R_cap = (int64_t)align_up((size_t)L.A_cap, kBN) + (int64_t)kBN * E;
+  L.tiles_cap = L.A_cap / kBN + E + 1;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o = align_up(o + bytes, kAlign);
+    return at;
+  };
+  L.off_header = take(256);
+  L.off_flags = take(64 * sizeof(int32_t));
+  L.off_counts = take((size_t)E * 4);
+  L.off_seg = take((size_t)(E + 1) * 4);
+  L.off_tiles = take((size_t)L.tiles_cap * 16);
+  L.off_assign = take((size_t)L.A_cap * 4);
+  L.off_slot_token = take((size_t)L.R_cap * 4);
+  L.off_slot_assign = take((size_t)L.R_cap * 4);
+  L.off_slot_weight = take((size_t)L.R_cap * 4);
+  L.off_xb = take((size_t)L.R_cap * H / 2);
+  L.off_xsf = take((size_t)L.R_cap * H / 32);
+  L.off_hb = take((size_t)L.R_cap * I / 2);
+  L.off_hsf = take((size_t)L.R_cap * I / 32);
+  L.off_acc = take((size_t)L.T_cap * H * 4);
+  L.off_stage_x = take((size_t)L.T_cap * H * 2);
+  L.off_stage_ids = take((size_t)L.A_cap * 4);
+  L.off_stage_w = take((size_t)L.A_cap * 4);
+  L.off_stage_out = take((size_t)L.T_cap * H * 2);
+  L.total = o;
+  return L;
+}
+
+WsPtrs ws_ptrs(void* ws, const WsLayout& L) {
+  uint8_t* b = static_cast<uint8_t*>(ws);
+  WsPtrs p;
+  p.flags = reinterpret_cast<int32_t*>(b + L.off_flags);
+  p.counts = reinterpret_cast<int32_t*>(b + L.off_counts);
+  p.seg = reinterpret_cast<int32_t*>(b + L.off_seg);
+  p.tiles = reinterpret_cast<int4*>(b + L.off_tiles);
+  p.assign_slot = reinterpret_cast<int32_t*>(b + L.off_assign);
+  p.slot_token = reinterpret_cast<int32_t*>(b + L.off_slot_token);
+  p.slot_assign = reinterpret_cast<int32_t*>(b + L.off_slot_assign);
+  p.slot_weight = reinterpret_cast<float*>(b + L.off_slot_weight);
+  p.xb = b + L.off_xb;
+  p.xsf = b + L.off_xsf;
+  p.hb = b + L.off_hb;
+  p.hsf = b + L.off_hsf;
+  p.acc = reinterpret_cast<float*>(b + L.off_acc);
+  return p;
+}
+
+PrepLayout prep_layout(const moe_dims& d) {
+  PrepLayout P;
+  const size_t H = d.hidden, I = d.inter, E = d.num_experts;
+  size_t o = 0;
+  P.off_w1c = o;
+  o = align_up(o + E * 2 * I * H / 2, kAlign);
+  P.off_w1s = o;
+  o = align_up(o + E * 2 * I * H / 32, kAlign);
+  P.off_w2c = o;
+  o = align_up(o + E * H * I / 2, kAlign);
+  P.off_w2s = o;
+  o = align_up(o + E * H * I / 32, kAlign);
+  P.total = o;
+  return P;
+}
+
+Shape shape_of(const moe_dims& d) { return Shape{d.hidden, d.inter, d.num_experts, d.topk}; }
+
+// Workspaces initialised by moe_workspace_init, with the dims they were laid out for.
+std::mutex g_reg_mu;
+std::map<const void*, moe_dims> g_registry;
+
+// Timing hooks.
+struct ProfRec {
+  const char* name;
+  cudaEvent_t a, b;
+};
+std::mutex g_prof_mu;
+bool g_prof_on = false;
+std::vector<ProfRec> g_prof;
+struct ProfSum {
+  double ms = 0.0;
+  int launches = 0;
+  const char* name = nullptr;
+};
+std::map<std::string, ProfSum> g_prof_done;
+
+struct ProfScope {
+  const char* name;
+  cudaStream_t st;
+  cudaEvent_t a = nullptr;
+  ProfScope(const char* n, cudaStream_t s) : name(n), st(s) {
+    if (!g_prof_on) return;
+    if (cudaEventCreate(&a) == cudaSuccess)
+      cudaEventRecord(a, st);
+    else
+      a = nullptr;
+  }
+  ~ProfScope() {
+    if (!a) return;
+    cudaEvent_t b = nullptr;
+    if (cudaEventCreate(&b) == cudaSuccess) {
+      cudaEventRecord(b, st);
+      std::lock_guard<std::mutex> lk(g_prof_mu);
+      g_prof.push_back({name, a, b});
+    } else {
+      cudaEventDestroy(a);
+    }
+  }
+};
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+moe_status check_dims(const moe_dims* d) {
+  if (!d) return fail(MOE_ERR_INVALID_ARG, "dims is NULL");
+  if (d->mma_type != MOE_MMA_MXF4xMXF4)
+    return fail(MOE_ERR_UNSUPPORTED, "mma_type %d: only MOE_MMA_MXF4xMXF4 (mxf4xmxf4) is built",
+                d->mma_type);
+  if (d->hidden < 256 || d->hidden % 128 != 0 || d->hidden > 65536)
+    return fail(MOE_ERR_INVALID_ARG, "hidden %d must be a multiple of 128 in [256, 65536]",
+                d->hidden);
+  if (d->inter < 128 || d->inter % 128 != 0 || d->inter > 65536)
+    return fail(MOE_ERR_INVALID_ARG, "inter %d must be a multiple of 128 in [128, 65536]",
+                d->inter);
+  if (d->num_experts < 1 || d->num_experts > 1024)
+    return fail(MOE_ERR_INVALID_ARG, "num_experts %d outside [1, 1024]", d->num_experts);
+  if (d->topk < 1 || d->topk > 32 || d->topk > d->num_experts)
+    return fail(MOE_ERR_INVALID_ARG, "topk %d outside [1, min(num_experts, 32)]", d->topk);
+  if (d->max_tokens < 1 || d->max_tokens > 65536)
+    return fail(MOE_ERR_INVALID_ARG, "max_tokens %d outside [1, 65536]", d->max_tokens);
+  return MOE_OK;
+}
+
+moe_status check_ws(const moe_dims* d, const void* ws, size_t ws_bytes) {
+  if (!ws) return fail(MOE_ERR_INVALID_ARG, "workspace is NULL");
+  if (!aligned(ws, 256)) return fail(MOE_ERR_INVALID_ARG, "workspace not 256-byte aligned");
+  const size_t need = ws_layout(*d).total;
+  if (ws_bytes < need)
+    return fail(MOE_ERR_WORKSPACE_TOO_SMALL, "workspace has %zu bytes, needs %zu", ws_bytes, need);
+  std::lock_guard<std::mutex> lk(g_reg_mu);
+  auto it = g_registry.find(ws);
+  if (it == g_registry.end())
+    return fail(MOE_ERR_WORKSPACE_MISMATCH,
+                "workspace %p was not initialised by moe_workspace_init", ws);
+  if (!dims_equal(it->second, *d))
+    return fail(MOE_ERR_WORKSPACE_MISMATCH,
+                "workspace %p was initialised for other dims or mma_type", ws);
+  return MOE_OK;
+}
+
+moe_status check_tokens(const moe_dims* d, int32_t T) {
+  if (T < 0 || T > d->max_tokens)
+    return fail(MOE_ERR_INVALID_ARG, "num_tokens %d outside [0, max_tokens=%d]", T,
+                d->max_tokens);
+  return MOE_OK;
+}
+
+__global__ void write_header_kernel(int32_t* hdr, moe_dims d, unsigned long long total) {
+  hdr[0] = 0x454F4D58;  // "XMOE"
+  hdr[1] = 1;           // layout version
+  hdr[2] = d.hidden;
+  hdr[3] = d.inter;
+  hdr[4] = d.num_experts;
+  hdr[5] = d.topk;
+  hdr[6] = d.max_tokens;
+  hdr[7] = d.mma_type;
+  *reinterpret_cast<unsigned long long*>(hdr + 8) = total;
+}
+
+moe_status pre_dispatch_impl(const moe_dims* d, const void* x, const int32_t* ids,
+                             const float* tw, int32_t T, void* ws, cudaStream_t st) {
+  const WsLayout L = ws_layout(*d);
+  const WsPtrs p = ws_ptrs(ws, L);
+  const Shape s = shape_of(*d);
+  cudaError_t e;
+  {
+    ProfScope ps("bucket", st);
+    e = launch_bucket(s, ids, tw, T, p, st);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "bucket kernel");
+  {
+    ProfScope ps("quantize_scatter", st);
+    e = launch_quantize_scatter(s, x, T, p, st);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "quantize kernel");
+  return MOE_OK;
+}
+
+moe_status forward_impl(const moe_dims* d, const void* prepared, void* ws, void* out, int32_t T,
+                        cudaStream_t st) {
+  const WsLayout L = ws_layout(*d);
+  const PrepLayout P = prep_layout(*d);
+  const WsPtrs p = ws_ptrs(ws, L);
+  const uint8_t* prep = static_cast<const uint8_t*>(prepared);
+  const int nsm = sm_count();
+  if (nsm <= 0) return fail(MOE_ERR_CUDA, "no CUDA device");
+  GemmLaunch g;
+  g.shape = shape_of(*d);
+  g.ws = p;
+  g.R_cap = L.R_cap;
+  g.num_sms = nsm;
+  g.gate_up_debug = nullptr;
+  cudaError_t e;
+  // gate/up projection + SwiGLU + requantisation
+  g.mode = kGemmSwiglu;
+  g.w_codes = prep + P.off_w1c;
+  g.w_sf = prep + P.off_w1s;
+  g.t_codes = p.xb;
+  g.t_sf = p.xsf;
+  g.rows_per_expert = 2 * d->inter;
+  g.K = d->hidden;
+  {
+    ProfScope ps("gemm1_swiglu", st);
+    e = launch_gemm(g, st);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "gate/up GEMM");
+  // down projection + combine
+  g.mode = kGemmCombine;
+  g.w_codes = prep + P.off_w2c;
+  g.w_sf = prep + P.off_w2s;
+  g.t_codes = p.hb;
+  g.t_sf = p.hsf;
+  g.rows_per_expert = d->hidden;
+  g.K = d->inter;
+  {
+    ProfScope ps("gemm2_combine", st);
+    e = launch_gemm(g, st);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "down GEMM");
+  {
+    ProfScope ps("convert_out", st);
+    e = launch_convert_out(p.acc, out, (int64_t)T * d->hidden, st);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "output conversion");
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_last_error(void) { return g_err.c_str(); }
+
+const char* moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
+    case MOE_ERR_WORKSPACE_TOO_SMALL: return "MOE_ERR_WORKSPACE_TOO_SMALL";
+    case MOE_ERR_WORKSPACE_MISMATCH: return "MOE_ERR_WORKSPACE_MISMATCH";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+    case MOE_ERR_ROUTING: return "MOE_ERR_ROUTING";
+    case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT";
+    default: return "MOE_ERR_UNKNOWN";
+  }
+}
+
+moe_status moe_validate_dims(const moe_dims* dims) { return check_dims(dims); }
+
+size_t moe_prepared_weights_size(const moe_dims* dims) {
+  if (check_dims(dims) != MOE_OK) return 0;
+  return prep_layout(*dims).total;
+}
+
+size_t moe_workspace_size(const moe_dims* dims) {
+  if (check_dims(dims) != MOE_OK) return 0;
+  return ws_layout(*dims).total;
+}
+
+moe_status moe_workspace_init(const moe_dims* dims, void* ws, size_t ws_bytes, void* stream) {
+  moe_status s = check_dims(dims);
+  if (s) return s;
+  if (!ws) return fail(MOE_ERR_INVALID_ARG, "workspace is NULL");
+  if (!aligned(ws, 256)) return fail(MOE_ERR_INVALID_ARG, "workspace not 256-byte aligned");
+  const WsLayout L = ws_layout(*dims);
+  if (ws_bytes < L.total)
+    return fail(MOE_ERR_WORKSPACE_TOO_SMALL, "workspace has %zu bytes, needs %zu", ws_bytes,
+                L.total);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(ws, 0, L.total, st);
+  if (e != cudaSuccess) return cuda_fail(e, "workspace clear");
+  write_header_kernel<<<1, 1, 0, st>>>(static_cast<int32_t*>(ws), *dims,
+                                       (unsigned long long)L.total);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "workspace header");
+  std::lock_guard<std::mutex> lk(g_reg_mu);
+  g_registry[ws] = *dims;
+  return MOE_OK;
+}
+
+moe_status moe_quantize_mxfp4(const float* src, int64_t rows, int32_t K, uint8_t* codes,
+                              uint8_t* scales, void* stream) {
+  if (rows < 0 || K <= 0 || K % 32 != 0)
+    return fail(MOE_ERR_INVALID_ARG, "rows %lld / K %d: need rows >= 0 and K %% 32 == 0",
+                (long long)rows, K);
+  if (rows == 0) return MOE_OK;
+  if (!src || !codes || !scales) return fail(MOE_ERR_INVALID_ARG, "NULL pointer");
+  if (!aligned(src, 16) || !aligned(codes, 4))
+    return fail(MOE_ERR_INVALID_ARG, "src must be 16-byte and codes 4-byte aligned");
+  cudaError_t e =
+      launch_quantize_rows(src, rows, K, codes, scales, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "quantize kernel");
+  return MOE_OK;
+}
+
+moe_status moe_prepare_weights(const moe_dims* dims, const uint8_t* w1c, const uint8_t* w1s,
+                               const uint8_t* w2c, const uint8_t* w2s, void* prepared,
+                               size_t prepared_bytes, void* stream) {
+  moe_status s = check_dims(dims);
+  if (s) return s;
+  if (!w1c || !w1s || !w2c || !w2s || !prepared)
+    return fail(MOE_ERR_INVALID_ARG, "NULL pointer");
+  if (!aligned(w1c, 16) || !aligned(w2c, 16) || !aligned(prepared, 256))
+    return fail(MOE_ERR_INVALID_ARG,
+                "weight codes must be 16-byte aligned and the prepared blob 256-byte aligned");
+  const PrepLayout P = prep_layout(*dims);
+  if (prepared_bytes < P.total)
+    return fail(MOE_ERR_INVALID_ARG, "prepared blob has %zu bytes, needs %zu", prepared_bytes,
+                P.total);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_prepare(shape_of(*dims), w1c, w1s, w2c, w2s,
+                                 static_cast<uint8_t*>(prepared), P, st);
+  if (e != cudaSuccess) return cuda_fail(e, "weight preparation");
+  return MOE_OK;
+}
+
+moe_status moe_pre_dispatch(const moe_dims* dims, const void* x, const int32_t* ids,
+                            const float* tw, int32_t T, void* ws, size_t ws_bytes, void* stream) {
+  moe_status s = check_dims(dims);
+  if (s) return s;
+  if ((s = check_tokens(dims, T))) return s;
+  if ((s = check_ws(dims, ws, ws_bytes))) return s;
+  if (T == 0) return MOE_OK;
+  if (!x || !ids || !tw) return fail(MOE_ERR_INVALID_ARG, "NULL input pointer");
+  if (!aligned(x, 16) || !aligned(ids, 4) || !aligned(tw, 4))
+    return fail(MOE_ERR_INVALID_ARG, "x must be 16-byte aligned, ids/weights 4-byte aligned");
+  return pre_dispatch_impl(dims, x, ids, tw, T, ws, static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_forward(const moe_dims* dims, const void* prepared, void* ws, size_t ws_bytes,
+                       void* out, int32_t T, void* stream) {
+  moe_status s = check_dims(dims);
+  if (s) return s;
+  if ((s = check_tokens(dims, T))) return s;
+  if ((s = check_ws(dims, ws, ws_bytes))) return s;
+  if (T == 0) return MOE_OK;
+  if (!prepared || !out) return fail(MOE_ERR_INVALID_ARG, "NULL pointer");
+  if (!aligned(prepared, 256) || !aligned(out, 16))
+    return fail(MOE_ERR_INVALID_ARG, "prepared must be 256-byte and out 16-byte aligned");
+  return forward_impl(dims, prepared, ws, out, T, static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_run_host(const moe_dims* dims, const void* prepared, void* ws, size_t ws_bytes,
+                        const void* x_host, const int32_t* ids_host, const float* tw_host,
+                        void* out_host, int32_t T, void* stream) {
+  moe_status s = check_dims(dims);
+  if (s) return s;
+  if ((s = check_tokens(dims, T))) return s;
+  if ((s = check_ws(dims, ws, ws_bytes))) return s;
+  if (T == 0) return MOE_OK;
+  if (!prepared || !x_host || !ids_host || !tw_host || !out_host)
+    return fail(MOE_ERR_INVALID_ARG, "NULL pointer");
+  if (!aligned(prepared, 256)) return fail(MOE_ERR_INVALID_ARG, "prepared not 256-byte aligned");
+  const WsLayout L = ws_layout(*dims);
+  uint8_t* b = static_cast<uint8_t*>(ws);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t xbytes = (size_t)T * dims->hidden * 2, abytes = (size_t)T * dims->topk * 4;
+  cudaError_t e;
+  if ((e = cudaMemcpyAsync(b + L.off_stage_x, x_host, xbytes, cudaMemcpyHostToDevice, st)) ||
+      (e = cudaMemcpyAsync(b + L.off_stage_ids, ids_host, abytes, cudaMemcpyHostToDevice, st)) ||
+      (e = cudaMemcpyAsync(b + L.off_stage_w, tw_host, abytes, cudaMemcpyHostToDevice, st)))
+    return cuda_fail(e, "input copy");
+  s = pre_dispatch_impl(dims, b + L.off_stage_x, reinterpret_cast<int32_t*>(b + L.off_stage_ids),
+                        reinterpret_cast<float*>(b + L.off_stage_w), T, ws, st);
+  if (s) return s;
+  s = forward_impl(dims, prepared, ws, b + L.off_stage_out, T, st);
+  if (s) return s;
+  if ((e = cudaMemcpyAsync(out_host, b + L.off_stage_out, xbytes, cudaMemcpyDeviceToHost, st)))
+    return cuda_fail(e, "output copy");
+  if ((e = cudaStreamSynchronize(st))) return cuda_fail(e, "stream synchronize");
+  return MOE_OK;
+}
+
+moe_status moe_check(void* ws, void* stream) {
+  if (!ws) return fail(MOE_ERR_INVALID_ARG, "workspace is NULL");
+  moe_dims d;
+  {
+    std::lock_guard<std::mutex> lk(g_reg_mu);
+    auto it = g_registry.find(ws);
+    if (it == g_registry.end())
+      return fail(MOE_ERR_WORKSPACE_MISMATCH, "workspace %p was not initialised", ws);
+    d = it->second;
+  }
+  const WsLayout L = ws_layout(d);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
+  int32_t flag = 0;
+  int32_t* dflag = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ws) + L.off_flags);
+  if ((e = cudaMemcpy(&flag, dflag, sizeof(flag), cudaMemcpyDeviceToHost)))
+    return cuda_fail(e, "flag read");
+  if ((e = cudaMemset(dflag, 0, sizeof(int32_t)))) return cuda_fail(e, "flag clear");
+  if (flag & kErrTimeout) return fail(MOE_ERR_TIMEOUT, "a device wait ran past its limit");
+  if (flag & kErrRouting)
+    return fail(MOE_ERR_ROUTING, "topk ids outside [0, num_experts) were skipped");
+  return MOE_OK;
+}
+
+moe_status moe_read_dispatch(const moe_dims* dims, const void* ws, int32_t T, int32_t* counts_host,
+                             int32_t* assign_host, uint8_t* xc_host, uint8_t* xs_host,
+                             int32_t* slot_token_host) {
+  moe_status s = check_dims(dims);
+  if (s) return s;
+  if ((s = check_tokens(dims, T))) return s;
+  if (!ws) return fail(MOE_ERR_INVALID_ARG, "workspace is NULL");
+  const WsLayout L = ws_layout(*dims);
+  const uint8_t* b = static_cast<const uint8_t*>(ws);
+  const int E = dims->num_experts, k = dims->topk, H = dims->hidden;
+  const int64_t A = (int64_t)T * k;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e) return cuda_fail(e, "synchronize");
+  if (counts_host &&
+      (e = cudaMemcpy(counts_host, b + L.off_counts, (size_t)E * 4, cudaMemcpyDeviceToHost)))
+    return cuda_fail(e, "counts read");
+  std::vector<int32_t> assign((size_t)A);
+  if (A &&
+      (e = cudaMemcpy(assign.data(), b + L.off_assign, (size_t)A * 4, cudaMemcpyDeviceToHost)))
+    return cuda_fail(e, "assign read");
+  if (assign_host) std::memcpy(assign_host, assign.data(), (size_t)A * 4);
+  std::vector<int32_t> seg((size_t)E + 1);
+  if ((e = cudaMemcpy(seg.data(), b + L.off_seg, (size_t)(E + 1) * 4, cudaMemcpyDeviceToHost)))
+    return cuda_fail(e, "seg read");
+  const int64_t R = seg[E];
+  if (R < 0 || R > L.R_cap) return fail(MOE_ERR_CUDA, "corrupt segment table");
+  if (slot_token_host) {
+    std::vector<int32_t> st((size_t)R);
+    if (R && (e = cudaMemcpy(st.data(), b + L.off_slot_token, (size_t)R * 4,
+                             cudaMemcpyDeviceToHost)))
+      return cuda_fail(e, "slot read");
+    for (int64_t a = 0; a < A; ++a)
+      slot_token_host[a] = (assign[a] >= 0 && assign[a] < R) ? st[assign[a]] : -1;
+  }
+  if (xc_host || xs_host) {
+    std::vector<uint8_t> codes((size_t)R * H / 2), sf((size_t)R * H / 32);
+    if (R && (e = cudaMemcpy(codes.data(), b + L.off_xb, codes.size(), cudaMemcpyDeviceToHost)))
+      return cuda_fail(e, "codes read");
+    if (R && (e = cudaMemcpy(sf.data(), b + L.off_xsf, sf.size(), cudaMemcpyDeviceToHost)))
+      return cuda_fail(e, "scales read");
+    for (int64_t a = 0; a < A; ++a) {
+      const int32_t r = assign[a];
+      const bool ok = r >= 0 && r < R;
+      if (xc_host) {
+        if (ok)
+          std::memcpy(xc_host + a * (H / 2), codes.data() + (size_t)r * H / 2, (size_t)H / 2);
+        else
+          std::memset(xc_host + a * (H / 2), 0, (size_t)H / 2);
+      }
+      if (xs_host)
+        for (int g = 0; g < H / 32; ++g)
+          xs_host[a * (H / 32) + g] = ok ? sf[sf_atom_offset((size_t)r, g, H / 128)] : 0;
+    }
+  }
+  return MOE_OK;
+}
+
+moe_status moe_read_intermediate(const moe_dims* dims, const void* ws, int32_t T,
+                                 uint8_t* hc_host, uint8_t* hs_host) {
+  moe_status s = check_dims(dims);
+  if (s) return s;
+  if ((s = check_tokens(dims, T))) return s;
+  if (!ws) return fail(MOE_ERR_INVALID_ARG, "workspace is NULL");
+  const WsLayout L = ws_layout(*dims);
+  const uint8_t* b = static_cast<const uint8_t*>(ws);
+  const int E = dims->num_experts, k = dims->topk, I = dims->inter;
+  const int64_t A = (int64_t)T * k;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e) return cuda_fail(e, "synchronize");
+  std::vector<int32_t> assign((size_t)A), seg((size_t)E + 1);
+  if (A &&
+      (e = cudaMemcpy(assign.data(), b + L.off_assign, (size_t)A * 4, cudaMemcpyDeviceToHost)))
+    return cuda_fail(e, "assign read");
+  if ((e = cudaMemcpy(seg.data(), b + L.off_seg, (size_t)(E + 1) * 4, cudaMemcpyDeviceToHost)))
+    return cuda_fail(e, "seg read");
+  const int64_t R = seg[E];
+  if (R < 0 || R > L.R_cap) return fail(MOE_ERR_CUDA, "corrupt segment table");
+  std::vector<uint8_t> codes((size_t)R * I / 2), sf((size_t)R * I / 32);
+  if (R && (e = cudaMemcpy(codes.data(), b + L.off_hb, codes.size(), cudaMemcpyDeviceToHost)))
+    return cuda_fail(e, "codes read");
+  if (R && (e = cudaMemcpy(sf.data(), b + L.off_hsf, sf.size(), cudaMemcpyDeviceToHost)))
+    return cuda_fail(e, "scales read");
+  for (int64_t a = 0; a < A; ++a) {
+    const int32_t r = assign[a];
+    const bool ok = r >= 0 && r < R;
+    if (hc_host) {
+      if (ok)
+        std::memcpy(hc_host + a * (I / 2), codes.data() + (size_t)r * I / 2, (size_t)I / 2);
+      else
+        std::memset(hc_host + a * (I / 2), 0, (size_t)I / 2);
+    }
+    if (hs_host)
+      for (int g = 0; g < I / 32; ++g)
+        hs_host[a * (I / 32) + g] = ok ? sf[sf_atom_offset((size_t)r, g, I / 128)] : 0;
+  }
+  return MOE_OK;
+}
+
+moe_status moe_debug_gate_up(const moe_dims* dims, const void* prepared, void* ws,
+                             size_t ws_bytes, float* gate_up, int32_t T, void* stream) {
+  moe_status s = check_dims(dims);
+  if (s) return s;
+  if ((s = check_tokens(dims, T))) return s;
+  if ((s = check_ws(dims, ws, ws_bytes))) return s;
+  if (T == 0) return MOE_OK;
+  if (!prepared || !gate_up) return fail(MOE_ERR_INVALID_ARG, "NULL pointer");
+  if (!aligned(prepared, 256)) return fail(MOE_ERR_INVALID_ARG, "prepared not 256-byte aligned");
+  const WsLayout L = ws_layout(*dims);
+  const PrepLayout P = prep_layout(*dims);
+  const uint8_t* prep = static_cast<const uint8_t*>(prepared);
+  GemmLaunch g;
+  g.mode = kGemmRaw;
+  g.shape = shape_of(*dims);
+  g.ws = ws_ptrs(ws, L);
+  g.R_cap = L.R_cap;
+  g.num_sms = sm_count();
+  if (g.num_sms <= 0) return fail(MOE_ERR_CUDA, "no CUDA device");
+  g.gate_up_debug = gate_up;
+  g.w_codes = prep + P.off_w1c;
+  g.w_sf = prep + P.off_w1s;
+  g.t_codes = g.ws.xb;
+  g.t_sf = g.ws.xsf;
+  g.rows_per_expert = 2 * dims->inter;
+  g.K = dims->hidden;
+  cudaError_t e = launch_gemm(g, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "gate/up GEMM (raw)");
+  return MOE_OK;
+}
+
+moe_status moe_profile_enable(int32_t on) {
+  g_prof_on = on != 0;
+  return MOE_OK;
+}
+
+int32_t moe_profile_read(const char** names_out, float* ms_out, int32_t* launches_out,
+                         int32_t max_kernels) {
+  std::vector<ProfRec> recs;
+  {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    recs.swap(g_prof);
+  }
+  for (auto& r : recs) {
+    float ms = 0.f;
+    if (cudaEventSynchronize(r.b) == cudaSuccess &&
+        cudaEventElapsedTime(&ms, r.a, r.b) == cudaSuccess) {
+      std::lock_guard<std::mutex> lk(g_prof_mu);
+      ProfSum& sum = g_prof_done[r.name];
+      sum.ms += ms;
+      sum.launches += 1;
+      sum.name = r.name;
+    }
+    cudaEventDestroy(r.a);
+    cudaEventDestroy(r.b);
+  }
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  int32_t n = 0;
+  for (auto& kv : g_prof_done) {
+    if (n >= max_kernels) break;
+    if (names_out) names_out[n] = kv.second.name;
+    if (ms_out) ms_out[n] = (float)kv.second.ms;
+    if (launches_out) launches_out[n] = kv.second.launches;
+    ++n;
+  }
+  return n;
+}
+
+void moe_profile_reset(void) {
+  std::vector<ProfRec> recs;
+  {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    recs.swap(g_prof);
+    g_prof_done.clear();
+  }
+  for (auto& r : recs) {
+    cudaEventSynchronize(r.b);
+    cudaEventDestroy(r.a);
+    cudaEventDestroy(r.b);
+  }
+}
+
+int32_t moe_device_sm_count(void) { return sm_count(); }
+
+}  // extern "C"

@@ -1,0 +1,113 @@
+// Internal definitions shared by the CUDA translation units of libmxmoe.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "mxmoe.h"
+
+namespace mxmoe {
+
+// ---------------------------------------------------------------------------
+// Tile geometry of the grouped GEMMs (weights on the MMA M side, tokens on N).
+constexpr int kBM = 128;            // weight rows per tile (MMA M)
+constexpr int kBN = 128;            // token rows per tile (max MMA N); expert segments are
+                                    // padded to multiples of kBN rows
+constexpr int kBK = 256;            // FP4 elements per k-block = one 128-byte swizzle row
+constexpr int kBKBytes = kBK / 2;   // 128
+constexpr int kATileBytes = kBM * kBKBytes;   // 16 KiB
+constexpr int kBTileBytes = kBN * kBKBytes;   // 16 KiB
+constexpr int kBBoxRows = 32;                 // token rows per TMA box
+constexpr int kSFAtomBytes = 512;             // 128 rows x 4 scale bytes
+constexpr int kSFStageBytes = 2 * kSFAtomBytes;  // 8 scale columns per k-block
+
+// Device error bits in ws.flags[0].
+constexpr int kErrRouting = 1;
+constexpr int kErrTimeout = 2;
+
+// Bounded waits give up after this many nanoseconds of %globaltimer.
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+
+// Byte offset of scale column s of row `row` in the 128x4 block layout
+// (int32 view [rows/128][Kc/4][32][4]); kc4 = Kc / 4.
+__host__ __device__ __forceinline__ size_t sf_atom_offset(size_t row, int s, int kc4) {
+  return (((row >> 7) * (size_t)kc4 + (size_t)(s >> 2)) << 9) + ((row & 31) << 4) +
+         (((row >> 5) & 3) << 2) + (size_t)(s & 3);
+}
+
+// Canonical row (gate 0..I-1, up I..2I-1) of the first weight stored at prepared
+// row r under the gran=16 even/odd interleave.
+__host__ __device__ __forceinline__ int gate_up_source_row(int r, int I) {
+  const int chunk = r >> 5, within = r & 31;
+  const int odd = within >> 4;
+  const int is_up = (within >> 3) & 1;
+  return is_up * I + chunk * 16 + (within & 7) * 2 + odd;
+}
+
+// ---------------------------------------------------------------------------
+// Workspace layout (computed on the host from the dims, passed to kernels).
+struct WsLayout {
+  int64_t T_cap, A_cap, R_cap, tiles_cap;
+  size_t off_header, off_flags, off_counts, off_seg, off_tiles, off_assign, off_slot_token,
+      off_slot_assign, off_slot_weight, off_xb, off_xsf, off_hb, off_hsf, off_acc, off_stage_x,
+      off_stage_ids, off_stage_w, off_stage_out, total;
+};
+
+struct WsPtrs {
+  int32_t* flags;        // [0] error bits, [1] number of tiles, [2] valid assignments
+  int32_t* counts;       // [E]
+  int32_t* seg;          // [E+1] first workspace row of each expert (multiples of kBN)
+  int4* tiles;           // [tiles_cap] (expert, first row, rows, 0)
+  int32_t* assign_slot;  // [A_cap] workspace row of assignment t*k+j, -1 if skipped
+  int32_t* slot_token;   // [R_cap]
+  int32_t* slot_assign;  // [R_cap]
+  float* slot_weight;    // [R_cap]
+  uint8_t* xb;           // [R_cap, H/2] quantised token rows
+  uint8_t* xsf;          // 128x4 blocks of [R_cap, H/32]
+  uint8_t* hb;           // [R_cap, I/2] requantised intermediate rows
+  uint8_t* hsf;          // 128x4 blocks of [R_cap, I/32]
+  float* acc;            // [T_cap, H] fp32 combine accumulator
+};
+
+struct PrepLayout {
+  size_t off_w1c, off_w1s, off_w2c, off_w2s, total;
+};
+
+struct Shape {
+  int H, I, E, k;
+};
+
+// ---------------------------------------------------------------------------
+// Launchers implemented in dispatch.cu / gemm.cu.  Each returns the cudaError_t
+// of its launch.
+cudaError_t launch_bucket(const Shape& s, const int32_t* ids, const float* tw, int T,
+                          const WsPtrs& ws, cudaStream_t st);
+cudaError_t launch_quantize_scatter(const Shape& s, const void* x, int T, const WsPtrs& ws,
+                                    cudaStream_t st);
+cudaError_t launch_convert_out(const float* acc, void* out, int64_t n, cudaStream_t st);
+cudaError_t launch_quantize_rows(const float* src, int64_t rows, int K, uint8_t* codes,
+                                 uint8_t* sf, cudaStream_t st);
+cudaError_t launch_prepare(const Shape& s, const uint8_t* w1c, const uint8_t* w1s,
+                           const uint8_t* w2c, const uint8_t* w2s, uint8_t* prep,
+                           const PrepLayout& pl, cudaStream_t st);
+
+enum GemmMode { kGemmRaw = 0, kGemmSwiglu = 1, kGemmCombine = 2 };
+
+struct GemmLaunch {
+  int mode;
+  const uint8_t* w_codes;   // prepared weight codes [E*rows, K/2]
+  const uint8_t* w_sf;      // prepared weight scale blocks
+  const uint8_t* t_codes;   // token-side codes [R_cap, K/2]
+  const uint8_t* t_sf;      // token-side scale blocks
+  int64_t R_cap;
+  int rows_per_expert;      // 2I (gate/up) or H (down)
+  int K;                    // H (gate/up) or I (down)
+  Shape shape;
+  WsPtrs ws;
+  float* gate_up_debug;     // kGemmRaw only
+  int num_sms;
+};
+cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t st);
+
+}  // namespace mxmoe

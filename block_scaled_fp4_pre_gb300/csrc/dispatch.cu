@@ -1,0 +1,333 @@
+// pre_dispatch (quantise + bucket), weight preparation, MXFP4 quantisation of fp32
+// rows, and the fp32 -> bf16 output conversion.
+//
+// Pages: prhub digest of SGLang PR #37279, section 实现拆解 items 3-4 (pre_dispatch
+// writes E2M1 codes and group_size=32 scales plus the routing copies; the weight
+// transform and the gran=16 interleave for MXFP4 activations); SGLang PR #48424,
+// "DeepGEMM producers write FlashInfer's 128x4 scale layout" (scale blocks).
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace mxmoe {
+namespace {
+
+constexpr unsigned kFull = 0xFFFFFFFFu;
+
+// ---------------------------------------------------------------------------
+// Bucketing: one block of 32 warps.  Warp w owns the contiguous assignment range
+// [w*per, (w+1)*per) of a = t*k + j (ascending t, then j), so concatenating the
+// warps' ranges in warp order keeps that order.  Counts per (warp, expert) are
+// order-free shared-memory atomics; a per-expert scan over warps gives each warp
+// its base inside the expert; warp 0 scans the experts (segment starts padded to
+// kBN rows, and tile starts); finally every warp walks its range 32 assignments at
+// a time and ranks equal experts inside the chunk with __match_any_sync.
+__global__ void __launch_bounds__(1024) bucket_kernel(const int32_t* __restrict__ ids,
+                                                      const float* __restrict__ tw, int T, int k,
+                                                      int E, WsPtrs ws) {
+  extern __shared__ int32_t sh[];
+  int32_t* cnt = sh;             // [32][E]
+  int32_t* tot = cnt + 32 * E;   // [E]
+  int32_t* seg = tot + E;        // [E+1]
+  int32_t* tst = seg + E + 1;    // [E+1]
+  __shared__ int32_t bad;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int A = T * k;
+  const int per = (A + 31) / 32;
+  const int a0 = min(A, warp * per), a1 = min(A, a0 + per);
+
+  for (int i = tid; i < 32 * E; i += blockDim.x) cnt[i] = 0;
+  if (tid == 0) bad = 0;
+  __syncthreads();
+
+  for (int a = a0 + lane; a < a1; a += 32) {
+    const int e = ids[a];
+    if (e >= 0 && e < E)
+      atomicAdd(&cnt[warp * E + e], 1);
+    else
+      atomicAdd(&bad, 1);
+  }
+  __syncthreads();
+
+  for (int e = tid; e < E; e += blockDim.x) {
+    int run = 0;
+    for (int w = 0; w < 32; ++w) {
+      const int c = cnt[w * E + e];
+      cnt[w * E + e] = run;
+      run += c;
+    }
+    tot[e] = run;
+  }
+  __syncthreads();
+
+  if (warp == 0) {
+    int carry_rows = 0, carry_tiles = 0;
+    for (int e0 = 0; e0 < E; e0 += 32) {
+      const int e = e0 + lane;
+      const int n = e < E ? tot[e] : 0;
+      const int tiles = (n + kBN - 1) / kBN;
+      const int rows = tiles * kBN;
+      int ir = rows, it = tiles;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int vr = __shfl_up_sync(kFull, ir, o), vt = __shfl_up_sync(kFull, it, o);
+        if (lane >= o) {
+          ir += vr;
+          it += vt;
+        }
+      }
+      if (e < E) {
+        seg[e] = carry_rows + ir - rows;
+        tst[e] = carry_tiles + it - tiles;
+      }
+      carry_rows += __shfl_sync(kFull, ir, 31);
+      carry_tiles += __shfl_sync(kFull, it, 31);
+    }
+    if (lane == 0) {
+      seg[E] = carry_rows;
+      tst[E] = carry_tiles;
+    }
+  }
+  __syncthreads();
+
+  const unsigned lt_mask = (1u << lane) - 1u;
+  for (int base = a0; base < a1; base += 32) {
+    const int a = base + lane;
+    const bool in = a < a1;
+    const int e = in ? ids[a] : -1;
+    const bool ok = in && e >= 0 && e < E;
+    const unsigned peers = __match_any_sync(kFull, ok ? e : -1);
+    const int rank = __popc(peers & lt_mask);
+    if (ok) {
+      const int slot = seg[e] + cnt[warp * E + e] + rank;
+      ws.assign_slot[a] = slot;
+      ws.slot_token[slot] = a / k;
+      ws.slot_assign[slot] = a;
+      ws.slot_weight[slot] = tw[a];
+    } else if (in) {
+      ws.assign_slot[a] = -1;
+    }
+    __syncwarp();
+    if (ok && rank == 0) cnt[warp * E + e] += __popc(peers);
+    __syncwarp();
+  }
+
+  for (int e = tid; e < E; e += blockDim.x) {
+    const int n = tot[e];
+    ws.counts[e] = n;
+    ws.seg[e] = seg[e];
+    for (int i = 0, r = 0; r < n; ++i, r += kBN)
+      ws.tiles[tst[e] + i] = make_int4(e, seg[e] + r, min(kBN, n - r), 0);
+  }
+  if (tid == 0) {
+    ws.seg[E] = seg[E];
+    ws.flags[1] = tst[E];
+    ws.flags[2] = A - bad;
+    if (bad) atomicOr(&ws.flags[0], kErrRouting);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Quantise one token row per block and scatter it to the token's k workspace rows.
+// A thread owns 8 consecutive elements; 4 adjacent threads form one 32-group.
+// The block also clears the token's fp32 combine accumulator row.
+__global__ void __launch_bounds__(256) quantize_scatter_kernel(const __nv_bfloat16* __restrict__ x,
+                                                               int H, int k, WsPtrs ws) {
+  __shared__ int32_t slots[32];
+  const int t = blockIdx.x, tid = threadIdx.x;
+  if (tid < k) slots[tid] = ws.assign_slot[(size_t)t * k + tid];
+  {
+    float4* acc = reinterpret_cast<float4*>(ws.acc + (size_t)t * H);
+    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int i = tid; i < H / 4; i += blockDim.x) acc[i] = z;
+  }
+  __syncthreads();
+  const int kc4 = H / 128;
+  const size_t row_bytes = (size_t)H / 2;
+  for (int base = tid * 8; base < H; base += blockDim.x * 8) {
+    const uint4 raw = *reinterpret_cast<const uint4*>(x + (size_t)t * H + base);
+    const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
+    float v[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = __bfloat1622float2(p2[i]);
+      v[2 * i] = f.x;
+      v[2 * i + 1] = f.y;
+    }
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2));
+    const int e = ptx::mx_scale_exponent(amax);
+    const float inv = ptx::pow2_neg(e);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] *= inv;
+    const uint32_t codes = ptx::e2m1x8(v);
+    for (int j = 0; j < k; ++j) {
+      const int slot = slots[j];
+      if (slot < 0) continue;
+      *reinterpret_cast<uint32_t*>(ws.xb + (size_t)slot * row_bytes + base / 2) = codes;
+      if ((tid & 3) == 0) ws.xsf[sf_atom_offset((size_t)slot, base / 32, kc4)] = (uint8_t)(e + 127);
+    }
+  }
+}
+
+// fp32 rows -> canonical MXFP4 codes/scales.  A thread owns 8 elements.
+__global__ void quantize_rows_kernel(const float* __restrict__ src, int64_t n_threads,
+                                     uint8_t* __restrict__ codes, uint8_t* __restrict__ sf) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  // n_threads is a multiple of 4, so a 4-lane group is either wholly in range or
+  // wholly past the end; lanes past the end work on a clamped copy and store nothing.
+  const int64_t ic = i < n_threads ? i : n_threads - 1;
+  const int64_t elem = ic * 8;
+  const float4 a = *reinterpret_cast<const float4*>(src + elem);
+  const float4 b = *reinterpret_cast<const float4*>(src + elem + 4);
+  float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  float amax = 0.f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(v[j]));
+  amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
+  amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2));
+  const int e = ptx::mx_scale_exponent(amax);
+  const float inv = ptx::pow2_neg(e);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) v[j] *= inv;
+  const uint32_t c = ptx::e2m1x8(v);
+  if (i < n_threads) {
+    reinterpret_cast<uint32_t*>(codes)[ic] = c;
+    if ((ic & 3) == 0) sf[elem / 32] = (uint8_t)(e + 127);
+  }
+}
+
+// Row copy with the optional gran=16 interleave: 16 bytes per thread.
+__global__ void copy_rows_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst,
+                                 int64_t total_chunks, int chunks_per_row, int rows_per_expert,
+                                 int I, int interleave) {
+  for (int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; c < total_chunks;
+       c += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t row = c / chunks_per_row;
+    const int part = (int)(c % chunks_per_row);
+    const int64_t e = row / rows_per_expert;
+    const int r = (int)(row % rows_per_expert);
+    const int sr = interleave ? gate_up_source_row(r, I) : r;
+    const uint4 v = reinterpret_cast<const uint4*>(src + ((size_t)e * rows_per_expert + sr) *
+                                                             (size_t)chunks_per_row * 16)[part];
+    reinterpret_cast<uint4*>(dst)[c] = v;
+  }
+}
+
+// Canonical scales [E*rows, Kc] -> 128x4 blocks, one int32 (4 scale columns of one
+// row) per thread, written in block order.
+__global__ void scale_blocks_kernel(const uint8_t* __restrict__ src, uint32_t* __restrict__ dst,
+                                    int64_t total_words, int rows_per_expert, int Kc, int I,
+                                    int interleave) {
+  const int kc4 = Kc / 4;
+  for (int64_t w = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; w < total_words;
+       w += (int64_t)gridDim.x * blockDim.x) {
+    // word index = ((rb * kc4 + kb) * 32 + i) * 4 + q
+    const int q = (int)(w & 3);
+    const int i = (int)((w >> 2) & 31);
+    const int64_t blk = w >> 7;
+    const int kb = (int)(blk % kc4);
+    const int64_t rb = blk / kc4;                       // 128-row block over E*rows
+    const int64_t row = rb * 128 + q * 32 + i;          // row over E*rows
+    const int64_t e = row / rows_per_expert;
+    const int r = (int)(row % rows_per_expert);
+    const int sr = interleave ? gate_up_source_row(r, I) : r;
+    const uint8_t* s = src + ((size_t)e * rows_per_expert + sr) * (size_t)Kc + 4 * kb;
+    dst[w] = (uint32_t)s[0] | ((uint32_t)s[1] << 8) | ((uint32_t)s[2] << 16) |
+             ((uint32_t)s[3] << 24);
+  }
+}
+
+// acc fp32 -> bf16, 8 elements per thread.
+__global__ void convert_out_kernel(const float* __restrict__ acc, __nv_bfloat16* __restrict__ out,
+                                   int64_t n8) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const float4 a = reinterpret_cast<const float4*>(acc)[2 * i];
+    const float4 b = reinterpret_cast<const float4*>(acc)[2 * i + 1];
+    __nv_bfloat162 o[4] = {__floats2bfloat162_rn(a.x, a.y), __floats2bfloat162_rn(a.z, a.w),
+                           __floats2bfloat162_rn(b.x, b.y), __floats2bfloat162_rn(b.z, b.w)};
+    reinterpret_cast<uint4*>(out)[i] = *reinterpret_cast<const uint4*>(o);
+  }
+}
+
+// Blocks for a grid-stride loop over `work` items, capped at `cap`.
+unsigned grid_for(int64_t work, int block, int64_t cap) {
+  int64_t g = (work + block - 1) / block;
+  if (g > cap) g = cap;
+  return (unsigned)(g < 1 ? 1 : g);
+}
+
+}  // namespace
+
+cudaError_t launch_bucket(const Shape& s, const int32_t* ids, const float* tw, int T,
+                          const WsPtrs& ws, cudaStream_t st) {
+  const size_t smem = (size_t)(32 * s.E + 3 * s.E + 2) * sizeof(int32_t);
+  cudaError_t err = cudaFuncSetAttribute(bucket_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+  if (err != cudaSuccess) return err;
+  bucket_kernel<<<1, 1024, smem, st>>>(ids, tw, T, s.k, s.E, ws);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_scatter(const Shape& s, const void* x, int T, const WsPtrs& ws,
+                                    cudaStream_t st) {
+  quantize_scatter_kernel<<<T, 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(x), s.H, s.k,
+                                             ws);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_convert_out(const float* acc, void* out, int64_t n, cudaStream_t st) {
+  const int64_t n8 = n / 8;
+  convert_out_kernel<<<grid_for(n8, 256, 4096), 256, 0, st>>>(
+      acc, reinterpret_cast<__nv_bfloat16*>(out), n8);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_rows(const float* src, int64_t rows, int K, uint8_t* codes,
+                                 uint8_t* sf, cudaStream_t st) {
+  const int64_t n_threads = rows * (int64_t)K / 8;
+  const int64_t blocks = (n_threads + 255) / 256;
+  if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+  quantize_rows_kernel<<<(unsigned)blocks, 256, 0, st>>>(src, n_threads, codes, sf);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prepare(const Shape& s, const uint8_t* w1c, const uint8_t* w1s,
+                           const uint8_t* w2c, const uint8_t* w2s, uint8_t* prep,
+                           const PrepLayout& pl, cudaStream_t st) {
+  const int64_t E = s.E, H = s.H, I = s.I;
+  {  // W1 codes: interleaved rows
+    const int cpr = (int)(H / 2 / 16);
+    const int64_t total = E * 2 * I * cpr;
+    copy_rows_kernel<<<grid_for(total, 256, 16384), 256, 0, st>>>(w1c, prep + pl.off_w1c, total,
+                                                                  cpr, (int)(2 * I), (int)I, 1);
+  }
+  {  // W1 scales: interleaved rows, 128x4 blocks
+    const int64_t words = E * 2 * I * (H / 32) / 4;
+    scale_blocks_kernel<<<grid_for(words, 256, 16384), 256, 0, st>>>(
+        w1s, reinterpret_cast<uint32_t*>(prep + pl.off_w1s), words, (int)(2 * I), (int)(H / 32),
+        (int)I, 1);
+  }
+  {  // W2 codes: rows unchanged
+    const int cpr = (int)(I / 2 / 16);
+    const int64_t total = E * H * cpr;
+    copy_rows_kernel<<<grid_for(total, 256, 16384), 256, 0, st>>>(w2c, prep + pl.off_w2c, total,
+                                                                  cpr, (int)H, (int)I, 0);
+  }
+  {  // W2 scales: 128x4 blocks
+    const int64_t words = E * H * (I / 32) / 4;
+    scale_blocks_kernel<<<grid_for(words, 256, 16384), 256, 0, st>>>(
+        w2s, reinterpret_cast<uint32_t*>(prep + pl.off_w2s), words, (int)H, (int)(I / 32), (int)I,
+        0);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace mxmoe

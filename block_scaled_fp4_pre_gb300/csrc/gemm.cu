@@ -1,0 +1,424 @@
+// Persistent grouped block-scaled FP4 x FP4 GEMM for sm_103a (tcgen05 + TMEM + TMA),
+// with three epilogues:
+//   kGemmSwiglu   gate/up projection -> SwiGLU -> MXFP4 requantisation of h
+//   kGemmCombine  down projection -> top-k weighted combine (fp32 reductions)
+//   kGemmRaw      gate/up projection -> raw fp32 accumulators (debug readback)
+//
+// Pages: "[deepseek-v4] Bump sgl-deep-gemm for packed FP4xFP4 mega-MoE (W4A4)",
+// Appendix B (the layer streams every touched expert's packed FP4 weights and is
+// memory bound at ntok=512: memory SOL 85%, compute 34%, BLOCK_K=256); SGLang
+// PR #48424 summary (block_m 64 for decode loads); prhub digest of PR #37279
+// (activation "swiglu"; gran=16 interleave so that SwiGLU pairs sit together).
+//
+// Orientation: the weight slab is the MMA's M=128 operand and the expert's tokens
+// are the N operand (N = 32..128), so one instruction shape serves a decode load of
+// a few tokens per expert as well as a prefill tile of 128 tokens.  The work items
+// are (token tile, 128-row weight slab); consecutive items share a token tile, so
+// its rows stay in L2 while the weight slabs stream from HBM once.
+//
+// Roles (192 threads, one persistent block per SM):
+//   warp 0      TMA producer: weight slab box (128 rows x 128 B), token boxes
+//               (32 rows x 128 B each), and both operands' 128x4 scale blocks.
+//   warp 1      TMEM allocator; lane 0 issues tcgen05.cp (scales) + tcgen05.mma.
+//   warps 2-5   epilogue: tcgen05.ld of the fp32 accumulator (lane quarter
+//               warp % 4), then the mode's math and global stores.
+// Every mbarrier wait is bounded (kWaitLimitNs); a timeout sets the workspace
+// error flag and all roles leave their loops, free TMEM and return.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace mxmoe {
+namespace {
+
+constexpr int kStages = 6;
+constexpr int kThreads = 192;
+constexpr int kTmemCols = 512;
+constexpr int kAccCols = kBN;              // fp32 accumulator columns per buffer
+constexpr int kSfTmemBase = 2 * kAccCols;  // scale registers after the two accumulators
+constexpr unsigned kFull = 0xFFFFFFFFu;
+
+struct __align__(8) SmemTail {
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint64_t acc_full[2];
+  uint64_t acc_empty[2];
+  uint64_t mma_done;
+  uint32_t tmem_base;
+  int abort;
+  float xchg[2][4][32];
+};
+
+constexpr size_t kSmemA = 0;
+constexpr size_t kSmemB = kSmemA + (size_t)kStages * kATileBytes;
+constexpr size_t kSmemSFA = kSmemB + (size_t)kStages * kBTileBytes;
+constexpr size_t kSmemSFB = kSmemSFA + (size_t)kStages * kSFStageBytes;
+constexpr size_t kSmemTail = kSmemSFB + (size_t)kStages * kSFStageBytes;
+constexpr size_t kSmemBytes = kSmemTail + sizeof(SmemTail) + 1024;  // + alignment slack
+
+struct GemmArgs {
+  const uint8_t* w_sf;
+  const uint8_t* t_sf;
+  int rows_per_expert;
+  int K;
+  int m_tiles;
+  int H, I;
+  WsPtrs ws;
+  float* gate_up_debug;
+};
+
+__device__ __forceinline__ float silu_times(float g, float u) {
+  return g / (1.0f + expf(-g)) * u;
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kThreads, 1)
+    moe_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
+                    const __grid_constant__ CUtensorMap tmap_t, const GemmArgs args) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  SmemTail* tail = reinterpret_cast<SmemTail*>(smem + kSmemTail);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int num_tiles = args.ws.flags[1];
+  const int num_items = num_tiles * args.m_tiles;
+  if ((int)blockIdx.x >= num_items) return;  // uniform for the whole block
+
+  const int num_kb = (args.K + kBK - 1) / kBK;
+  const int kc4 = args.K / 128;  // scale blocks per 128-row group
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      ptx::mbar_init(&tail->full[s], 1);
+      ptx::mbar_init(&tail->empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(&tail->acc_full[b], 1);
+      ptx::mbar_init(&tail->acc_empty[b], 128);
+    }
+    ptx::mbar_init(&tail->mma_done, 1);
+    tail->abort = 0;
+    ptx::fence_mbar_init();
+    ptx::prefetch_tmap(&tmap_w);
+    ptx::prefetch_tmap(&tmap_t);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(&tail->tmem_base, kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = tail->tmem_base;
+  volatile int* abort_flag = &tail->abort;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const uint64_t pol_w = ptx::policy_evict_first();
+      const uint64_t pol_t = ptx::policy_evict_last();
+      int stage = 0;
+      uint32_t phase = 0;
+      int64_t issued = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; ok && item < num_items; item += gridDim.x) {
+        const int tile = item / args.m_tiles, mt = item % args.m_tiles;
+        const int4 ti = args.ws.tiles[tile];
+        const int e = ti.x, row0 = ti.y, n = ti.z;
+        const int nb = (n + kBBoxRows - 1) / kBBoxRows;
+        const int wrow = e * args.rows_per_expert + mt * kBM;
+        const uint8_t* wsf = args.w_sf + ((size_t)(e * args.m_tiles + mt) * kc4) * kSFAtomBytes;
+        const uint8_t* tsf = args.t_sf + ((size_t)(row0 / kBN) * kc4) * kSFAtomBytes;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!ptx::mbar_wait(&tail->empty[stage], phase ^ 1u, abort_flag, kWaitLimitNs)) {
+            ok = false;
+            break;
+          }
+          const int kvalid = min(kBK, args.K - kb * kBK);
+          const int atoms = kvalid / 128;
+          const uint32_t bytes =
+              kATileBytes + nb * (kBBoxRows * kBKBytes) + 2u * atoms * kSFAtomBytes;
+          uint64_t* bar = &tail->full[stage];
+          ptx::mbar_arrive_expect_tx(bar, bytes);
+          ptx::tma_load_2d(smem + kSmemA + (size_t)stage * kATileBytes, &tmap_w, kb * kBKBytes,
+                           wrow, bar, pol_w);
+          ptx::bulk_load(smem + kSmemSFA + (size_t)stage * kSFStageBytes,
+                         wsf + (size_t)kb * 2 * kSFAtomBytes, atoms * kSFAtomBytes, bar, pol_w);
+          for (int j = 0; j < nb; ++j)
+            ptx::tma_load_2d(smem + kSmemB + (size_t)stage * kBTileBytes + j * kBBoxRows * kBKBytes,
+                             &tmap_t, kb * kBKBytes, row0 + j * kBBoxRows, bar, pol_t);
+          ptx::bulk_load(smem + kSmemSFB + (size_t)stage * kSFStageBytes,
+                         tsf + (size_t)kb * 2 * kSFAtomBytes, atoms * kSFAtomBytes, bar, pol_t);
+          ++issued;
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) atomicOr(&args.ws.flags[0], kErrTimeout);
+      // Drain: every copy this thread issued must have landed before the block
+      // exits (normally they all have, because the MMA consumed them).
+      const int64_t first = issued > kStages ? issued - kStages : 0;
+      for (int64_t i = first; i < issued; ++i) {
+        const int s = (int)(i % kStages);
+        const uint32_t par = (uint32_t)((i / kStages) & 1);
+        int never = 0;
+        ptx::mbar_wait(&tail->full[s], par, &never, kWaitLimitNs);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int ab = 0;
+      uint32_t acc_phase = 0;
+      uint32_t sfbuf = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; ok && item < num_items; item += gridDim.x) {
+        const int tile = item / args.m_tiles;
+        const int n = args.ws.tiles[tile].z;
+        const int n_mma = (n + kBBoxRows - 1) / kBBoxRows * kBBoxRows;
+        if (!ptx::mbar_wait(&tail->acc_empty[ab], acc_phase ^ 1u, abort_flag, kWaitLimitNs)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(ab * kAccCols);
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!ptx::mbar_wait(&tail->full[stage], phase, abort_flag, kWaitLimitNs)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const int kvalid = min(kBK, args.K - kb * kBK);
+          const int atoms = kvalid / 128;
+          const uint32_t sfa_t = tmem_base + (uint32_t)(kSfTmemBase + sfbuf * 16);
+          const uint32_t sfb_t = sfa_t + 8;
+          const uint32_t sa = ptx::smem_addr(smem + kSmemSFA + (size_t)stage * kSFStageBytes);
+          const uint32_t sb = ptx::smem_addr(smem + kSmemSFB + (size_t)stage * kSFStageBytes);
+          for (int a = 0; a < atoms; ++a) {
+            ptx::tc_cp_sf(sfa_t + a * 4, ptx::desc_sf(sa + a * kSFAtomBytes));
+            ptx::tc_cp_sf(sfb_t + a * 4, ptx::desc_sf(sb + a * kSFAtomBytes));
+          }
+          const uint32_t a_base = ptx::smem_addr(smem + kSmemA + (size_t)stage * kATileBytes);
+          const uint32_t b_base = ptx::smem_addr(smem + kSmemB + (size_t)stage * kBTileBytes);
+          const int steps = kvalid / 64;
+          for (int s = 0; s < steps; ++s) {
+            const uint32_t idesc = ptx::idesc_mxf4(n_mma, (s & 1) * 2);
+            ptx::tc_mma_mxf4(d_tmem, ptx::desc_sw128(a_base + s * 32),
+                             ptx::desc_sw128(b_base + s * 32), idesc, sfa_t + (s >> 1) * 4,
+                             sfb_t + (s >> 1) * 4, (kb | s) != 0 ? 1u : 0u);
+          }
+          ptx::tc_commit(&tail->empty[stage]);
+          sfbuf ^= 1u;
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        ptx::tc_commit(&tail->acc_full[ab]);
+        if (++ab == 2) {
+          ab = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      if (!ok) atomicOr(&args.ws.flags[0], kErrTimeout);
+      // Whatever happened, wait until every MMA issued here has finished before
+      // the block may release its tensor memory.
+      ptx::tc_commit(&tail->mma_done);
+      int never = 0;
+      ptx::mbar_wait(&tail->mma_done, 0, &never, kWaitLimitNs);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int ep_tid = threadIdx.x - 64;
+    int ab = 0;
+    uint32_t acc_phase = 0;
+    int xb = 0;
+    for (int item = blockIdx.x; item < num_items; item += gridDim.x) {
+      const int tile = item / args.m_tiles, mt = item % args.m_tiles;
+      const int4 ti = args.ws.tiles[tile];
+      const int row0 = ti.y, n = ti.z;
+      if (!ptx::mbar_wait(&tail->acc_full[ab], acc_phase, abort_flag, kWaitLimitNs)) {
+        if (ep_tid == 0) atomicOr(&args.ws.flags[0], kErrTimeout);
+        break;
+      }
+      ptx::tc_fence_after();
+      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(ab * kAccCols);
+      for (int c0 = 0; c0 < n; c0 += 32) {
+        float v[32];
+        ptx::tmem_ld32(taddr + (uint32_t)c0, v);
+        const int ncol = min(32, n - c0);
+        if constexpr (MODE == kGemmSwiglu) {
+          // Rows of this warp: chunk c of 32 interleaved gate/up rows =
+          // [gate even 8 | up even 8 | gate odd 8 | up odd 8] of features c*16..c*16+15.
+          const int c = mt * 4 + q;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            if (j < ncol) {
+              const float u = __shfl_down_sync(kFull, v[j], 8);
+              const float h = silu_times(v[j], u);
+              v[j] = (lane & 8) ? 0.f : h;
+              float a = fabsf(v[j]);
+              a = fmaxf(a, __shfl_xor_sync(kFull, a, 16));
+              a = fmaxf(a, __shfl_xor_sync(kFull, a, 4));
+              a = fmaxf(a, __shfl_xor_sync(kFull, a, 2));
+              a = fmaxf(a, __shfl_xor_sync(kFull, a, 1));
+              if (lane == 0) tail->xchg[xb][q][j] = a;
+            }
+          }
+          ptx::named_bar_sync(1, 128);
+          const int i_kc4 = args.I / 128;
+          const size_t hrow_bytes = (size_t)args.I / 2;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            if (j < ncol) {
+              // 32-feature group = this warp's 16 features + the partner warp's 16.
+              const float amax = fmaxf(tail->xchg[xb][q][j], tail->xchg[xb][q ^ 1][j]);
+              const int e = ptx::mx_scale_exponent(amax);
+              const float qv = v[j] * ptx::pow2_neg(e);
+              const float qodd = __shfl_down_sync(kFull, qv, 16);
+              uint32_t w = (lane < 8) ? (ptx::e2m1x2(qv, qodd) << (8 * (lane & 3))) : 0u;
+              w |= __shfl_xor_sync(kFull, w, 1);
+              w |= __shfl_xor_sync(kFull, w, 2);
+              const uint32_t w_hi = __shfl_sync(kFull, w, 4);
+              const size_t row = (size_t)row0 + c0 + j;
+              if (lane == 0) {
+                *reinterpret_cast<uint2*>(args.ws.hb + row * hrow_bytes + (size_t)c * 8) =
+                    make_uint2(w, w_hi);
+                if ((q & 1) == 0)
+                  args.ws.hsf[sf_atom_offset(row, c >> 1, i_kc4)] = (uint8_t)(e + 127);
+              }
+            }
+          }
+          xb ^= 1;
+        } else if constexpr (MODE == kGemmCombine) {
+          int my_tok = 0;
+          float my_w = 0.f;
+          if (lane < ncol) {
+            my_tok = args.ws.slot_token[row0 + c0 + lane];
+            my_w = args.ws.slot_weight[row0 + c0 + lane];
+          }
+          const int feat = mt * kBM + q * 32 + lane;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int tok = __shfl_sync(kFull, my_tok, j);
+            const float wt = __shfl_sync(kFull, my_w, j);
+            if (j < ncol) atomicAdd(args.ws.acc + (size_t)tok * args.H + feat, wt * v[j]);
+          }
+        } else {
+          const int m = mt * kBM + q * 32 + lane;
+          const int col = gate_up_source_row(m, args.I);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            if (j < ncol) {
+              const int a = args.ws.slot_assign[row0 + c0 + j];
+              args.gate_up_debug[(size_t)a * 2 * args.I + col] = v[j];
+            }
+          }
+        }
+      }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(&tail->acc_empty[ab]);
+      if (++ab == 2) {
+        ab = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host side: tensor maps through the driver entry point (no libcuda link).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// Row-major uint8 matrix [rows, row_bytes] read in boxes of 128 bytes x box_rows,
+// 128-byte swizzle.
+cudaError_t make_tmap(CUtensorMap* m, const void* base, uint64_t row_bytes, uint64_t rows,
+                      uint32_t box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return cudaErrorNotSupported;
+  const cuuint64_t dims[2] = {row_bytes, rows};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {128, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
+                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <int MODE>
+cudaError_t launch_mode(const GemmLaunch& g, const CUtensorMap& tw, const CUtensorMap& tt,
+                        const GemmArgs& a, cudaStream_t st) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t err = cudaFuncSetAttribute(moe_gemm_kernel<MODE>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)kSmemBytes);
+    if (err != cudaSuccess) return err;
+    attr_set = true;
+  }
+  moe_gemm_kernel<MODE><<<g.num_sms, kThreads, kSmemBytes, st>>>(tw, tt, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t st) {
+  CUtensorMap tw, tt;
+  const uint64_t row_bytes = (uint64_t)g.K / 2;
+  cudaError_t err =
+      make_tmap(&tw, g.w_codes, row_bytes, (uint64_t)g.shape.E * g.rows_per_expert, kBM);
+  if (err != cudaSuccess) return err;
+  err = make_tmap(&tt, g.t_codes, row_bytes, (uint64_t)g.R_cap, kBBoxRows);
+  if (err != cudaSuccess) return err;
+  GemmArgs a;
+  a.w_sf = g.w_sf;
+  a.t_sf = g.t_sf;
+  a.rows_per_expert = g.rows_per_expert;
+  a.K = g.K;
+  a.m_tiles = g.rows_per_expert / kBM;
+  a.H = g.shape.H;
+  a.I = g.shape.I;
+  a.ws = g.ws;
+  a.gate_up_debug = g.gate_up_debug;
+  switch (g.mode) {
+    case kGemmSwiglu: return launch_mode<kGemmSwiglu>(g, tw, tt, a, st);
+    case kGemmCombine: return launch_mode<kGemmCombine>(g, tw, tt, a, st);
+    default: return launch_mode<kGemmRaw>(g, tw, tt, a, st);
+  }
+}
+
+}  // namespace mxmoe

@@ -1,0 +1,204 @@
+/*
+ * mxmoe.h -- C ABI of a GB300 (sm_103a) W4A4 MXFP4 mixture-of-experts expert layer.
+ *
+ * The layer: bf16 tokens are quantised to packed E2M1 with one UE8M0 scale per 32
+ * elements, bucketed by their top-k experts, multiplied with each expert's gate/up
+ * weight (MXFP4) through a SwiGLU, requantised to MXFP4, multiplied with the
+ * expert's down weight (MXFP4), and summed over the k experts with the routing
+ * weights into a bf16 output.  Sources:
+ *   - "[deepseek-v4] Bump sgl-deep-gemm for packed FP4xFP4 mega-MoE (W4A4)": the
+ *     packed FP4 x FP4 mega-MoE kernel on a DeepSeek-V4-Flash layer (hidden 4096,
+ *     inter 2048, 256 experts, top-6), Appendix B.
+ *   - prhub digest of SGLang PR #37279 ("升级 sgl-deep-gemm 至 0.1.7，MegaMoE 改用
+ *     mma_type API 支持 MXFP4"): sections 实现拆解 items 1-4 and the mega_moe.py
+ *     excerpt -- the explicit mma_type "mxf4xmxf4", the per-mma-type buffer,
+ *     pre_dispatch(hidden, topk ids, topk weights, ..., num_tokens, group_size=32),
+ *     the weight transform and the gran=16 gate/up interleave.
+ *   - SGLang PR #48424, "DeepGEMM producers write FlashInfer's 128x4 scale layout":
+ *     scales as 4-D int32 [ceil(rows/128), K/128, 32, 4]; live rows are a prefix.
+ *
+ * Conventions for every entry point:
+ *   - Pointers named *_dev are CUDA device pointers, *_host host pointers.  Device
+ *     buffers are allocated and freed by the caller; no hot entry point allocates.
+ *   - Device pointers passed to kernels must be 16-byte aligned (256-byte for the
+ *     prepared weights and the workspace); otherwise MOE_ERR_INVALID_ARG.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Work is enqueued
+ *     asynchronously and stream-ordered; only moe_check, moe_run_host and the
+ *     moe_read_* debug calls synchronise.
+ *   - A failing call returns a nonzero moe_status and records a message readable
+ *     with moe_last_error() (per thread).  Nothing is enqueued after a failed
+ *     argument check.
+ *   - Element formats: E2M1 codes are packed two per byte, element 2i in the low
+ *     nibble of byte i.  A scale byte b means 2^(b-127) (UE8M0).  The scale of a
+ *     group of 32 is 2^e with e the smallest integer such that amax <= 6 * 2^e,
+ *     clamped to [-127, 127]; elements round to the nearest E2M1 value, ties to
+ *     the even code, and keep their sign.
+ */
+#ifndef MXMOE_H
+#define MXMOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MXMOE_API __attribute__((visibility("default")))
+#else
+#define MXMOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes. */
+typedef int32_t moe_status;
+enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,         /* null/misaligned pointer, bad size or shape   */
+    MOE_ERR_UNSUPPORTED = 2,         /* mma_type other than MOE_MMA_MXF4xMXF4        */
+    MOE_ERR_WORKSPACE_TOO_SMALL = 3, /* ws_bytes < moe_workspace_size(dims)          */
+    MOE_ERR_WORKSPACE_MISMATCH = 4,  /* workspace initialised for other dims/mma    */
+    MOE_ERR_CUDA = 5,                /* a CUDA runtime/driver call failed            */
+    MOE_ERR_ROUTING = 6,             /* device saw topk ids outside [0, E)           */
+    MOE_ERR_TIMEOUT = 7              /* a device wait ran past its limit             */
+};
+
+/* Operand types of the expert GEMMs.  Only MXFP4 x MXFP4 (the pages' "mxf4xmxf4")
+ * is built; every other value returns MOE_ERR_UNSUPPORTED. */
+enum { MOE_MMA_MXF4xMXF4 = 1 };
+
+/* Layer dimensions.  hidden H and inter I must be multiples of 128 (H >= 256);
+ * 1 <= topk <= min(num_experts, 32); 1 <= num_experts <= 1024;
+ * 1 <= max_tokens <= 65536 (the capacity a workspace is sized for). */
+typedef struct moe_dims {
+    int32_t hidden;
+    int32_t inter;
+    int32_t num_experts;
+    int32_t topk;
+    int32_t max_tokens;
+    int32_t mma_type;
+} moe_dims;
+
+/* Message of the last failure on this thread ("" if none). */
+MXMOE_API const char *moe_last_error(void);
+
+/* Static name of a status code. */
+MXMOE_API const char *moe_status_string(moe_status s);
+
+/* Checks dims as described above.  Host only; no CUDA call. */
+MXMOE_API moe_status moe_validate_dims(const moe_dims *dims);
+
+/* Bytes of the prepared-weight blob moe_prepare_weights writes; 0 for bad dims.
+ * Equal to the canonical MXFP4 bytes of both weights (rounded up to 1 KiB per
+ * section).  Host only. */
+MXMOE_API size_t moe_prepared_weights_size(const moe_dims *dims);
+
+/* Bytes of the workspace for dims->max_tokens tokens; 0 for bad dims.  Host only.
+ * (The pages' symmetric buffer sized by num_max_tokens_per_rank, one per
+ * mma_type; this build is single-GPU, so it is plain device memory.) */
+MXMOE_API size_t moe_workspace_size(const moe_dims *dims);
+
+/* Initialises a workspace: clears it and records dims and mma_type in its header
+ * and in a host-side registry, so that later calls with other dims return
+ * MOE_ERR_WORKSPACE_MISMATCH (the pages key their buffer cache on the dims and
+ * mma_type for the same reason).  Must precede the first pre_dispatch on it. */
+MXMOE_API moe_status moe_workspace_init(const moe_dims *dims, void *ws_dev, size_t ws_bytes,
+                                        void *stream);
+
+/* Quantises row-major fp32 src_dev [rows, K] (K % 32 == 0) to MXFP4 with the rule
+ * above: codes_dev [rows, K/2], scales_dev [rows, K/32], both row-major.  A helper
+ * for producing canonical MXFP4 weights on the device. */
+MXMOE_API moe_status moe_quantize_mxfp4(const float *src_dev, int64_t rows, int32_t K,
+                                        uint8_t *codes_dev, uint8_t *scales_dev, void *stream);
+
+/* Weight transform (the pages' transform_weights_for_mega_moe with mma_type
+ * mxf4xmxf4).  Inputs are canonical MXFP4, row-major:
+ *   w1_codes_dev [E, 2I, H/2], w1_scales_dev [E, 2I, H/32]   gate rows 0..I-1, up rows I..2I-1
+ *   w2_codes_dev [E, H, I/2],  w2_scales_dev [E, H, I/32]
+ * Output `prepared_dev` (prepared_bytes >= moe_prepared_weights_size): W1 rows
+ * interleaved with gran=16 (each chunk of 16 gate and 16 up rows becomes
+ * [gate even, up even, gate odd, up odd]), codes and scales alike, and both
+ * weights' scales in the 128x4 block layout.  Inputs are not modified; the
+ * caller may free them afterwards. */
+MXMOE_API moe_status moe_prepare_weights(const moe_dims *dims, const uint8_t *w1_codes_dev,
+                                         const uint8_t *w1_scales_dev, const uint8_t *w2_codes_dev,
+                                         const uint8_t *w2_scales_dev, void *prepared_dev,
+                                         size_t prepared_bytes, void *stream);
+
+/* Quantise-and-bucket (the pages' mega_moe_pre_dispatch, group_size 32).
+ *   x_dev            bf16 [num_tokens, H] row-major, finite values
+ *   topk_ids_dev     int32 [num_tokens, k]; ids outside [0, E) are skipped and
+ *                    raise MOE_ERR_ROUTING at the next moe_check
+ *   topk_weights_dev fp32 [num_tokens, k], used as given (no renormalisation)
+ * num_tokens <= dims->max_tokens; num_tokens == 0 is a no-op.  Writes the
+ * quantised token rows, per-expert counts and slots into the workspace.
+ * Within an expert, slots are ordered by ascending token, then ascending k index. */
+MXMOE_API moe_status moe_pre_dispatch(const moe_dims *dims, const void *x_dev,
+                                      const int32_t *topk_ids_dev, const float *topk_weights_dev,
+                                      int32_t num_tokens, void *ws_dev, size_t ws_bytes,
+                                      void *stream);
+
+/* The expert layer on the buffers of the last moe_pre_dispatch on this workspace
+ * (same num_tokens): grouped gate/up GEMM with SwiGLU and MXFP4 requantisation,
+ * grouped down GEMM, top-k weighted combine.  out_dev: bf16 [num_tokens, H]. */
+MXMOE_API moe_status moe_forward(const moe_dims *dims, const void *prepared_dev, void *ws_dev,
+                                 size_t ws_bytes, void *out_dev, int32_t num_tokens, void *stream);
+
+/* End-to-end call on HOST buffers: copies x_host (bf16 [T, H]), topk_ids_host and
+ * topk_weights_host into staging areas of the workspace, runs moe_pre_dispatch and
+ * moe_forward, copies the bf16 result to out_host [T, H] and synchronises the
+ * stream.  Pinned host memory gives asynchronous copies. */
+MXMOE_API moe_status moe_run_host(const moe_dims *dims, const void *prepared_dev, void *ws_dev,
+                                  size_t ws_bytes, const void *x_host,
+                                  const int32_t *topk_ids_host, const float *topk_weights_host,
+                                  void *out_host, int32_t num_tokens, void *stream);
+
+/* Synchronises `stream`, then reads and clears the workspace's device error
+ * flags: MOE_ERR_ROUTING, MOE_ERR_TIMEOUT, or MOE_OK. */
+MXMOE_API moe_status moe_check(void *ws_dev, void *stream);
+
+/* ---- debug readback (tests only; synchronous, allocate nothing on the device) ----
+ * Canonical views of what the last pre_dispatch/forward wrote for num_tokens
+ * tokens.  Assignment a = t*k + j.  A null output pointer skips that output.
+ *   counts_host        int32 [E]          tokens routed to each expert
+ *   assign_slot_host   int32 [T*k]        workspace row of assignment a (-1: skipped)
+ *   x_codes_host       uint8 [T*k, H/2]   quantised token row as stored for assignment a
+ *   x_scales_host      uint8 [T*k, H/32]
+ *   slot_token_host    int32 [T*k]        token recorded in row assign_slot[a] (check) */
+MXMOE_API moe_status moe_read_dispatch(const moe_dims *dims, const void *ws_dev,
+                                       int32_t num_tokens, int32_t *counts_host,
+                                       int32_t *assign_slot_host, uint8_t *x_codes_host,
+                                       uint8_t *x_scales_host, int32_t *slot_token_host);
+
+/*   h_codes_host  uint8 [T*k, I/2]   requantised SwiGLU output of assignment a
+ *   h_scales_host uint8 [T*k, I/32]                                                   */
+MXMOE_API moe_status moe_read_intermediate(const moe_dims *dims, const void *ws_dev,
+                                           int32_t num_tokens, uint8_t *h_codes_host,
+                                           uint8_t *h_scales_host);
+
+/* Debug variant of the gate/up GEMM: writes the raw fp32 accumulators of every
+ * assignment, de-interleaved, to gate_up_dev [T*k, 2I] (columns 0..I-1 gate,
+ * I..2I-1 up) instead of running SwiGLU.  Runs after moe_pre_dispatch. */
+MXMOE_API moe_status moe_debug_gate_up(const moe_dims *dims, const void *prepared_dev,
+                                       void *ws_dev, size_t ws_bytes, float *gate_up_dev,
+                                       int32_t num_tokens, void *stream);
+
+/* ---- timing hooks ----
+ * When enabled, moe_pre_dispatch and moe_forward record CUDA events around each
+ * kernel they launch (on the launch stream).  moe_profile_read synchronises and
+ * returns, per kernel name, the summed milliseconds and launch count since the
+ * last reset.  names_out receives up to max_kernels static strings. */
+MXMOE_API moe_status moe_profile_enable(int32_t on);
+MXMOE_API int32_t moe_profile_read(const char **names_out, float *ms_out, int32_t *launches_out,
+                                   int32_t max_kernels);
+MXMOE_API void moe_profile_reset(void);
+
+/* Number of SMs of the current device (what the persistent kernels size their
+ * grids for); 0 if no device. */
+MXMOE_API int32_t moe_device_sm_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MXMOE_H */
