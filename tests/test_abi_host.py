@@ -1,0 +1,116 @@
+"""Host-side checks of the C ABI (no GPU needed, no compute call): the library
+loads, exports every entry point declared in include/mxmoe.h, and its host-only
+argument checks and sizing behave as documented."""
+from __future__ import annotations
+
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mxmoe.h")
+
+
+@pytest.fixture(scope="module")
+def mx():
+    from block_scaled_fp4_pre_gb300 import build
+
+    build.build()
+    import block_scaled_fp4_pre_gb300 as m
+
+    m.lib()
+    return m
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    return sorted(set(re.findall(r"MXMOE_API[^;(]*?\b(moe_\w+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("moe_prepare_weights", "moe_pre_dispatch", "moe_forward",
+                     "moe_workspace_size", "moe_prepared_weights_size", "moe_check",
+                     "moe_last_error"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(mx):
+    out = subprocess.run(["nm", "-D", "--defined-only", mx.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r" T (moe_\w+)$", out, flags=re.M))
+    assert set(declared_functions()) <= exported
+    for name in declared_functions():
+        assert hasattr(mx.lib(), name)
+
+
+def test_header_compiles_as_c():
+    r = subprocess.run(["gcc", "-std=c99", "-fsyntax-only", "-Wall", "-Werror", "-x", "c", "-"],
+                       input=f'#include "{HEADER}"\nint main(void){{return 0;}}\n',
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+
+
+def test_dims_validation(mx):
+    ok = mx.make_dims(4096, 2048, 256, 6, 512)
+    mx.moe_validate_dims(ok)
+    bad = [
+        (mx.make_dims(4096, 2048, 256, 6, 512, mma_type=2), mx.MOE_ERR_UNSUPPORTED),
+        (mx.make_dims(4096, 2048, 256, 6, 512, mma_type=0), mx.MOE_ERR_UNSUPPORTED),
+        (mx.make_dims(4000, 2048, 256, 6, 512), mx.MOE_ERR_INVALID_ARG),
+        (mx.make_dims(128, 2048, 256, 6, 512), mx.MOE_ERR_INVALID_ARG),
+        (mx.make_dims(4096, 2000, 256, 6, 512), mx.MOE_ERR_INVALID_ARG),
+        (mx.make_dims(4096, 2048, 0, 1, 512), mx.MOE_ERR_INVALID_ARG),
+        (mx.make_dims(4096, 2048, 4, 6, 512), mx.MOE_ERR_INVALID_ARG),
+        (mx.make_dims(4096, 2048, 256, 0, 512), mx.MOE_ERR_INVALID_ARG),
+        (mx.make_dims(4096, 2048, 256, 6, 0), mx.MOE_ERR_INVALID_ARG),
+        (mx.make_dims(4096, 2048, 2048, 6, 512), mx.MOE_ERR_INVALID_ARG),
+    ]
+    for d, want in bad:
+        with pytest.raises(mx.MoeError) as ei:
+            mx.moe_validate_dims(d)
+        assert ei.value.status == want, d
+        assert mx.moe_workspace_size(d) == 0 and mx.moe_prepared_weights_size(d) == 0
+        assert mx.moe_last_error()
+
+
+def test_prepared_size_is_canonical_mxfp4_bytes(mx):
+    d = mx.make_dims(4096, 2048, 256, 6, 512)
+    # gate/up [E, 2I, H] + down [E, H, I] at 4 bits plus one byte per 32 elements
+    assert mx.moe_prepared_weights_size(d) == 256 * (2 * 2048 * 4096 + 4096 * 2048) * 17 // 32
+    assert mx.moe_prepared_weights_size(d) == 3_422_552_064
+
+
+def test_workspace_size_grows_with_capacity(mx):
+    a = mx.moe_workspace_size(mx.make_dims(4096, 2048, 256, 6, 512))
+    b = mx.moe_workspace_size(mx.make_dims(4096, 2048, 256, 6, 16384))
+    assert 0 < a < b
+    assert b < 2 * 2 ** 30   # well under the device memory
+
+
+def test_hot_calls_reject_uninitialised_workspace_without_touching_the_gpu(mx):
+    d = mx.make_dims(256, 128, 8, 2, 16)
+    fake = 256 * 1024   # never dereferenced: the host check fails first
+    lib = mx.lib()
+    import ctypes
+
+    rc = lib.moe_pre_dispatch(ctypes.byref(d), 16, 16, 16, 4, fake, 1 << 30, None)
+    assert rc == mx.MOE_ERR_WORKSPACE_MISMATCH
+    rc = lib.moe_forward(ctypes.byref(d), 256, fake, 1 << 30, 16, 4, None)
+    assert rc == mx.MOE_ERR_WORKSPACE_MISMATCH
+    rc = lib.moe_pre_dispatch(ctypes.byref(d), 16, 16, 16, 17, fake, 1 << 30, None)
+    assert rc == mx.MOE_ERR_INVALID_ARG           # num_tokens > max_tokens
+    rc = lib.moe_pre_dispatch(ctypes.byref(d), 16, 16, 16, 4, fake, 10, None)
+    assert rc == mx.MOE_ERR_WORKSPACE_TOO_SMALL
+    rc = lib.moe_pre_dispatch(ctypes.byref(d), 16, 16, 16, 4, fake + 8, 1 << 30, None)
+    assert rc == mx.MOE_ERR_INVALID_ARG           # misaligned workspace
+    rc = lib.moe_quantize_mxfp4(16, 4, 48, 16, 16, None)
+    assert rc == mx.MOE_ERR_INVALID_ARG           # K not a multiple of 32
+    assert lib.moe_status_string(mx.MOE_ERR_ROUTING) == b"MOE_ERR_ROUTING"
+
+
+def test_binding_has_the_c_names(mx):
+    for name in declared_functions():
+        assert hasattr(mx, name), name

@@ -1,0 +1,311 @@
+"""CUDA path against the CPU oracle, through the C ABI (GB300 only).
+
+Bars: quantised codes, scales and bucketing bit-exact; gate/up accumulators within
+fp32 accumulation error of the exact sums; intermediate FP4 codes differing in at
+most 0.1% of elements, each by one grid step; final output normwise relative error
+<= 2e-3 against the oracle (before its bf16 rounding and after it).
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+import block_scaled_fp4_pre_gb300 as mx  # noqa: E402
+import oracle  # noqa: E402
+import synth  # noqa: E402
+from tests.gpu_common import DeviceLayer, compare_full, device, to_dev  # noqa: E402
+from tests.helpers import compact_problem, normwise_rel_err, oracle_expert_weights  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+# Small shapes that span several tiles, ragged token tails and a ragged K block.
+SMALL = {
+    "tiny": synth.WORKLOADS["tiny"],
+    # ~175 tokens per expert: two token tiles each (128 + tail); I = 384 gives a
+    # 128-wide last k-block in the down projection; 6 gate/up slabs, 4 down slabs.
+    "ragged": synth.Workload("ragged", T=700, H=512, I=384, E=8, k=2),
+    # skewed routing: expert 0 gets several tiles, the rarest a handful of tokens
+    "zipf": synth.Workload("zipf", T=1024, H=256, I=256, E=32, k=4, routing="zipf",
+                           outlier_frac=0.001),
+    "top1": synth.Workload("top1", T=96, H=256, I=128, E=1, k=1),
+}
+
+
+@pytest.fixture(scope="module")
+def layers():
+    cache = {}
+
+    def get(name):
+        if name not in cache:
+            w = SMALL[name]
+            cache[name] = (DeviceLayer(w, keep_canonical=True), oracle_expert_weights(w, range(w.E)))
+        return cache[name]
+
+    return get
+
+
+# --------------------------------------------------------------------------
+# Quantiser
+
+def test_quantize_mxfp4_bit_exact_adversarial():
+    rng = np.random.default_rng(11)
+    rows = [rng.standard_normal(256) * 10.0 ** rng.uniform(-6, 6) for _ in range(64)]
+    ties = np.array([6.0, 0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0] * 32)
+    rows += [ties, -ties, ties * 2.0 ** -100, ties * 2.0 ** 100]
+    z = np.zeros(256); z[5] = -0.0; z[9] = -1e-40; rows.append(z)
+    rows.append(np.full(256, 6.0 * (1 + 2.0 ** -23)))
+    rows.append(np.full(256, 2.0 ** -130))
+    o = rng.standard_normal(256); o[::37] *= 50; rows.append(o)
+    x = np.stack(rows).astype(np.float32)
+    codes = torch.empty((x.shape[0], 128), dtype=torch.uint8, device=device())
+    sf = torch.empty((x.shape[0], 8), dtype=torch.uint8, device=device())
+    mx.moe_quantize_mxfp4(to_dev(x), codes, sf)
+    rc, rs = oracle.quantize_f32(x)
+    assert np.array_equal(sf.cpu().numpy(), rs)
+    assert np.array_equal(codes.cpu().numpy(), rc)
+
+
+def test_quantize_mxfp4_all_bf16_values():
+    bits = np.arange(65536, dtype=np.uint32)
+    finite = (bits & 0x7F80) != 0x7F80
+    vals = ((bits[finite] << 16).astype(np.uint32)).view(np.float32)
+    rng = np.random.default_rng(12)
+    vals = vals[rng.permutation(vals.size)]            # mix magnitudes inside groups
+    pad = (-vals.size) % 256
+    vals = np.concatenate([vals, np.zeros(pad, np.float32)]).reshape(-1, 256)
+    sorted_vals = np.sort(np.abs(vals.reshape(-1))).reshape(-1, 256)   # and similar ones together
+    x = np.concatenate([vals, sorted_vals]).astype(np.float32)
+    codes = torch.empty((x.shape[0], 128), dtype=torch.uint8, device=device())
+    sf = torch.empty((x.shape[0], 8), dtype=torch.uint8, device=device())
+    mx.moe_quantize_mxfp4(to_dev(x), codes, sf)
+    rc, rs = oracle.quantize_f32(x)
+    assert np.array_equal(sf.cpu().numpy(), rs)
+    assert np.array_equal(codes.cpu().numpy(), rc)
+
+
+# --------------------------------------------------------------------------
+# Weight preparation
+
+@pytest.mark.parametrize("name", ["tiny", "ragged"])
+def test_weights_quantised_and_prepared_bit_exact(layers, name):
+    layer, W = layers(name)
+    w = layer.w
+    can = {k: v.cpu().numpy() for k, v in layer.canonical.items()}
+    for got, ref in zip((can["w1_codes"], can["w1_scales"], can["w2_codes"], can["w2_scales"]), W):
+        assert np.array_equal(got, ref)
+    blob = layer.prepared.cpu().numpy()
+    src = oracle.interleave_source_rows(w.I)
+    E, H, I = w.E, w.H, w.I
+    w1c_p = W[0][:, src, :]
+    w1s_p = W[1][:, src, :]
+    off = 0
+    n = E * 2 * I * H // 2
+    assert np.array_equal(blob[off:off + n], w1c_p.reshape(-1))
+    off = (off + n + 1023) // 1024 * 1024
+    n = E * 2 * I * H // 32
+    assert np.array_equal(blob[off:off + n], oracle.scale_block_layout(w1s_p.reshape(E * 2 * I, -1)))
+    off = (off + n + 1023) // 1024 * 1024
+    n = E * H * I // 2
+    assert np.array_equal(blob[off:off + n], W[2].reshape(-1))
+    off = (off + n + 1023) // 1024 * 1024
+    n = E * H * I // 32
+    assert np.array_equal(blob[off:off + n], oracle.scale_block_layout(W[3].reshape(E * H, -1)))
+
+
+# --------------------------------------------------------------------------
+# pre_dispatch
+
+@pytest.mark.parametrize("name", ["tiny", "ragged", "zipf", "top1"])
+def test_pre_dispatch_bit_exact(layers, name):
+    layer, W = layers(name)
+    w = layer.w
+    x = synth.hidden_bf16(w)
+    ids, tw = synth.routing(w) if w.E > 1 else (np.zeros((w.T, 1), np.int32),
+                                                 np.ones((w.T, 1), np.float32))
+    mx.moe_pre_dispatch(layer.dims, to_dev(x), to_dev(ids), to_dev(tw), w.T, layer.ws)
+    mx.moe_check(layer.ws)
+    d = mx.moe_read_dispatch(layer.dims, layer.ws, w.T)
+    counts, offsets, st, sj, bad = oracle.bucket(ids, w.E)
+    assert bad == 0
+    assert np.array_equal(d["counts"], counts)
+    assert np.array_equal(d["slot_token"], np.repeat(np.arange(w.T), w.k))
+    # within an expert the rows follow ascending (t, j): the oracle's slot order
+    slot = d["assign_slot"]
+    for e in range(w.E):
+        a_sorted = (st[offsets[e]:offsets[e + 1]].astype(np.int64) * w.k + sj[offsets[e]:offsets[e + 1]])
+        rows = slot[a_sorted]
+        assert np.all(np.diff(rows) == 1)
+    xc, xs = oracle.quantize_bf16(x)
+    assert np.array_equal(d["x_codes"], np.repeat(xc, w.k, axis=0))
+    assert np.array_equal(d["x_scales"], np.repeat(xs, w.k, axis=0))
+
+
+# --------------------------------------------------------------------------
+# Gate/up GEMM accumulators
+
+@pytest.mark.parametrize("name", ["tiny", "ragged", "zipf"])
+def test_gate_up_accumulators(layers, name):
+    layer, W = layers(name)
+    w = layer.w
+    x = synth.hidden_bf16(w)
+    ids, tw = synth.routing(w)
+    mx.moe_pre_dispatch(layer.dims, to_dev(x), to_dev(ids), to_dev(tw), w.T, layer.ws)
+    gu = torch.full((w.T * w.k, 2 * w.I), float("nan"), dtype=torch.float32, device=device())
+    mx.moe_debug_gate_up(layer.dims, layer.prepared, layer.ws, gu, w.T)
+    mx.moe_check(layer.ws)
+    got = gu.cpu().numpy().astype(np.float64)
+    ref = oracle.moe(x, ids, tw, *W, want_intermediates=True)["gate_up"]
+    xd = np.abs(oracle.dequantize(*oracle.quantize_bf16(x)))
+    wd = [np.abs(oracle.dequantize(W[0][e], W[1][e])) for e in range(w.E)]
+    bound = np.zeros_like(ref)
+    for t in range(w.T):
+        for j in range(w.k):
+            bound[t * w.k + j] = wd[ids[t, j]] @ xd[t]
+    assert np.all(np.isfinite(got))
+    assert np.all(np.abs(got - ref) <= 1e-5 * bound + 1e-30)
+
+
+# --------------------------------------------------------------------------
+# Whole layer
+
+@pytest.mark.parametrize("name", ["tiny", "ragged", "zipf", "top1"])
+def test_forward_matches_oracle(layers, name):
+    layer, W = layers(name)
+    w = layer.w
+    x = synth.hidden_bf16(w)
+    ids, tw = synth.routing(w) if w.E > 1 else (np.zeros((w.T, 1), np.int32),
+                                                 np.ones((w.T, 1), np.float32))
+    got = layer.run(x, ids, tw)
+    m = compare_full(layer, x, ids, tw, got, W)
+    print(name, {k: v for k, v in m.items() if k != "ref"})
+    assert m["flip_frac"] <= 1e-3 and m["flips_one_step"]
+    assert m["err_f64"] <= 2e-3
+    assert m["err_bf16"] <= 2e-3
+    # down projection + combine alone, on the GPU's own intermediate codes
+    assert m["err_own_h"] <= 2e-3 and m["own_h_bf16_equal"] >= 0.99
+
+
+def test_forward_is_repeatable_and_host_path_matches(layers):
+    layer, W = layers("ragged")
+    w = layer.w
+    x = synth.hidden_bf16(w)
+    ids, tw = synth.routing(w)
+    a = layer.run(x, ids, tw)
+    inter_a = mx.moe_read_intermediate(layer.dims, layer.ws, w.T)
+    b = layer.run(x, ids, tw)
+    inter_b = mx.moe_read_intermediate(layer.dims, layer.ws, w.T)
+    assert np.array_equal(inter_a["h_codes"], inter_b["h_codes"])
+    # fp32 reductions in arbitrary order: outputs agree to bf16 rounding
+    assert normwise_rel_err(oracle.bf16_bits_to_f64(a), oracle.bf16_bits_to_f64(b)) <= 1e-3
+    xh = torch.from_numpy(x.view(np.int16)).pin_memory()
+    out_h = torch.empty((w.T, w.H), dtype=torch.int16).pin_memory()
+    mx.moe_run_host(layer.dims, layer.prepared, layer.ws, xh, torch.from_numpy(ids),
+                    torch.from_numpy(tw), out_h, w.T)
+    c = out_h.numpy().view(np.uint16)
+    assert normwise_rel_err(oracle.bf16_bits_to_f64(c), oracle.bf16_bits_to_f64(a)) <= 1e-3
+
+
+def test_partial_batch_and_edge_token_counts(layers):
+    layer, W = layers("ragged")
+    w = layer.w
+    x = synth.hidden_bf16(w)
+    ids, tw = synth.routing(w)
+    for T in (1, 2, 127, 129):
+        got = layer.run(x[:T], ids[:T], tw[:T])
+        ref = oracle.moe(x[:T], ids[:T], tw[:T], *W)
+        assert normwise_rel_err(oracle.bf16_bits_to_f64(got), ref["out_f64"]) <= 2e-3, T
+    # zero tokens is a no-op
+    out = torch.empty((1, w.H), dtype=torch.bfloat16, device=device())
+    mx.moe_pre_dispatch(layer.dims, out, out, out, 0, layer.ws)
+    mx.moe_forward(layer.dims, layer.prepared, layer.ws, out, 0)
+
+
+def test_all_tokens_on_one_expert(layers):
+    layer, W = layers("ragged")
+    w = layer.w
+    T = w.T
+    x = synth.hidden_bf16(w)
+    ids = np.stack([np.full(T, 3), np.full(T, 5)], axis=1).astype(np.int32)   # 700 rows each
+    tw = np.full((T, 2), 0.5, np.float32)
+    got = layer.run(x, ids, tw)
+    ref = oracle.moe(x, ids, tw, *W)
+    assert normwise_rel_err(oracle.bf16_bits_to_f64(got), ref["out_f64"]) <= 2e-3
+
+
+def test_invalid_ids_are_skipped_and_reported(layers):
+    layer, W = layers("tiny")
+    w = layer.w
+    x = synth.hidden_bf16(w)
+    ids, tw = synth.routing(w)
+    bad = ids.copy()
+    bad[2, 0] = -1
+    bad[7, 1] = w.E
+    T = w.T
+    out = torch.empty((T, w.H), dtype=torch.bfloat16, device=device())
+    mx.moe_pre_dispatch(layer.dims, to_dev(x), to_dev(bad), to_dev(tw), T, layer.ws)
+    mx.moe_forward(layer.dims, layer.prepared, layer.ws, out, T)
+    with pytest.raises(mx.MoeError) as ei:
+        mx.moe_check(layer.ws)
+    assert ei.value.status == mx.MOE_ERR_ROUTING
+    mx.moe_check(layer.ws)          # the flag was cleared
+    got = out.view(torch.int16).cpu().numpy().view(np.uint16)
+    ref = oracle.moe(x, bad, tw, *W)
+    assert ref["invalid_ids"] == 2
+    assert normwise_rel_err(oracle.bf16_bits_to_f64(got), ref["out_f64"]) <= 2e-3
+
+
+def test_workspace_checks(layers):
+    layer, _ = layers("tiny")
+    other = mx.make_dims(layer.dims.hidden, layer.dims.inter, layer.dims.num_experts,
+                         layer.dims.topk, layer.dims.max_tokens + 1)
+    x = torch.zeros((1, layer.dims.hidden), dtype=torch.bfloat16, device=device())
+    with pytest.raises(mx.MoeError) as ei:
+        mx.moe_pre_dispatch(other, x, x, x, 1, layer.ws)
+    assert ei.value.status in (mx.MOE_ERR_WORKSPACE_MISMATCH, mx.MOE_ERR_WORKSPACE_TOO_SMALL)
+    with pytest.raises(mx.MoeError) as ei:
+        mx.moe_pre_dispatch(layer.dims, x, x, x, layer.dims.max_tokens + 1, layer.ws)
+    assert ei.value.status == mx.MOE_ERR_INVALID_ARG
+
+
+# --------------------------------------------------------------------------
+# Full DeepSeek-V4-Flash shape, in the launch configuration the benchmark times:
+# every expert on the device, outputs of sampled tokens against the oracle.
+
+@pytest.fixture(scope="module")
+def dsv4_layer():
+    w = synth.WORKLOADS["prefill_T16384_zipf"]
+    return DeviceLayer(w, max_tokens=w.T)
+
+
+@pytest.mark.parametrize("name", ["decode_T64", "layer_T512", "prefill_T4096",
+                                  "prefill_T16384_zipf"])
+def test_full_size_sampled_tokens(dsv4_layer, name):
+    w = synth.WORKLOADS[name]
+    layer = dsv4_layer
+    x = synth.hidden_bf16(w)
+    ids, tw = synth.routing(w)
+    got = layer.run(x, ids, tw)
+    d = mx.moe_read_dispatch(layer.dims, layer.ws, w.T)
+    counts, _, _, _, _ = oracle.bucket(ids, w.E)
+    assert np.array_equal(d["counts"], counts)
+    assert np.array_equal(d["slot_token"], np.repeat(np.arange(w.T), w.k))
+    rng = np.random.default_rng(13)
+    tokens = np.unique(np.concatenate([[0, w.T - 1], rng.choice(w.T, 4, replace=False)]))
+    if w.routing == "zipf":   # include a token routed to the most popular expert
+        tokens = np.unique(np.append(tokens, np.nonzero((ids == 0).any(1))[0][-1]))
+    sub_ids, experts = compact_problem(ids, tokens)
+    Wc = oracle_expert_weights(w, experts)
+    ref = oracle.moe(x[tokens], sub_ids, tw[tokens], *Wc)
+    xc, xs = oracle.quantize_bf16(x[tokens])
+    for i, t in enumerate(tokens):
+        for j in range(w.k):
+            assert np.array_equal(d["x_codes"][t * w.k + j], xc[i])
+            assert np.array_equal(d["x_scales"][t * w.k + j], xs[i])
+    err = normwise_rel_err(oracle.bf16_bits_to_f64(got[tokens]), ref["out_f64"])
+    print(name, "sampled tokens", tokens.tolist(), "normwise err", err)
+    assert err <= 2e-3
+    assert np.all(np.isfinite(oracle.bf16_bits_to_f64(got)))
