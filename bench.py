@@ -1,0 +1,426 @@
+"""Benchmark of the W4A4 MXFP4 mixture-of-experts layer on GB300.
+
+One step = one pass of the whole layer (moe_pre_dispatch + moe_forward) over one batch
+of synthetic tokens: quantise + bucket, gate/up GEMM + SwiGLU + requantisation, down
+GEMM + top-k weighted combine.  Default workload: the DeepSeek-V4-Flash layer at
+T=512 tokens (hidden 4096, inter 2048, 256 experts, top-6), the point the pages
+measure in isolation ("[deepseek-v4] Bump sgl-deep-gemm for packed FP4xFP4 mega-MoE
+(W4A4)", Appendix B).
+
+Prints one JSON line.  `value` is tokens/s of the whole job (all ranks) with inputs
+resident in HBM; `e2e` is the same metric through moe_run_host on pinned host buffers
+(copies included); `roofline` is the dominant kernel's achieved HBM bandwidth against
+the measured copy peak; `cpu_baseline` times the CPU oracle on a bounded sample.
+--impl reference times the CPU oracle as the reference arm.
+Multi-GPU (torchrun): independent replicas, one per GPU (the layer does not shard here).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+L2_FLUSH_BYTES = 512 << 20          # > 2x the 129 MB L2
+KERNELS_PER_STEP = 5                # bucket, quantize_scatter, gemm1, gemm2, convert
+METRIC = "W4A4 MoE layer tokens/s (E=256, top-6, T=512; also us/layer and HBM TB/s)"
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default="layer_T512", choices=sorted(synth.WORKLOADS))
+    p.add_argument("--experts", type=int, default=0,
+                   help="override the expert count (small cases for profiler captures)")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-sample-tokens", type=int, default=0)
+    return p.parse_args()
+
+
+def workload(args) -> synth.Workload:
+    w = synth.WORKLOADS[args.workload]
+    if args.experts:
+        w = synth.Workload(w.name + f"_E{args.experts}", T=w.T, H=w.H, I=w.I, E=args.experts,
+                           k=min(w.k, args.experts), routing=w.routing, zipf_s=w.zipf_s,
+                           outlier_frac=w.outlier_frac)
+    return w
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except OSError:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# Clock sampling during the timed region
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.gpu)], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [s.strip() for s in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# Algorithmic bytes and FLOPs
+
+def touched_experts(ids, E):
+    return int(np.count_nonzero(np.bincount(ids.reshape(-1), minlength=E)))
+
+
+def algorithmic(w: synth.Workload, ids) -> dict:
+    """Bytes a perfect implementation must move, and FLOPs."""
+    H, I, k, T = w.H, w.I, w.k, w.T
+    A = T * k
+    u = touched_experts(ids, w.E)
+    w1 = 2 * I * H // 2 + 2 * I * H // 32           # gate/up codes + scales per expert
+    w2 = H * I // 2 + H * I // 32                   # down codes + scales per expert
+    return {
+        "touched_experts": u,
+        "layer_bytes": u * (w1 + w2) + 2 * T * H + 2 * T * H + 8 * T * k,
+        # gate/up kernel: its weights, the quantised token rows it reads once, h it writes
+        "gemm1_bytes": u * w1 + A * (H // 2 + H // 32) + A * (I // 2 + I // 32),
+        # down kernel: its weights, h it reads once, fp32 combine reductions (read+write)
+        "gemm2_bytes": u * w2 + A * (I // 2 + I // 32) + 2 * 4 * T * H,
+        "flops": 6 * A * H * I,
+    }
+
+
+def gemm_source_hash() -> str:
+    with open(os.path.join(ROOT, "block_scaled_fp4_pre_gb300", "csrc", "gemm.cu"), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload_name: str):
+    """DRAM bytes per launch from a committed ncu summary, if it still matches gemm.cu."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload_name}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    vals = {}
+    for line in text.splitlines():
+        if line.startswith("- ") and ":" in line:
+            k, v = line[2:].split(":", 1)
+            vals[k.strip()] = v.strip().strip("`")
+    if vals.get("gemm.cu sha256[:16]") != gemm_source_hash():
+        return None
+    try:
+        return float(vals["dram bytes per launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (baseline and reference arm)
+
+def oracle_sample(w: synth.Workload, x, ids, tw, n_tokens: int):
+    import oracle
+    from tests.helpers import compact_problem, oracle_expert_weights
+
+    tokens = np.arange(min(n_tokens, w.T))
+    sub, experts = compact_problem(ids, tokens)
+    Wc = oracle_expert_weights(w, experts)          # offline weight preparation, untimed
+    return tokens, sub, Wc
+
+
+def time_oracle(w, x, ids, tw, n_tokens: int, repeats: int = 1):
+    import oracle
+
+    tokens, sub, Wc = oracle_sample(w, x, ids, tw, n_tokens)
+    times = []
+    for _ in range(repeats):
+        t0 = time.perf_counter()
+        oracle.moe(x[tokens], sub, tw[tokens], *Wc)
+        times.append(time.perf_counter() - t0)
+    return {"tokens": len(tokens), "seconds": times, "threads": oracle.threads()}
+
+
+def default_cpu_tokens(w):
+    return 24 if w.H >= 4096 else min(w.T, 512)
+
+
+# ---------------------------------------------------------------------------
+
+def dist_setup(args):
+    import torch
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(world, v: float) -> float:
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    w = workload(args)
+    x = synth.hidden_bf16(w)
+    ids, tw = synth.routing(w)
+    n = args.cpu_sample_tokens or max(4, default_cpu_tokens(w) // 3)
+    import oracle
+
+    tokens, sub, Wc = oracle_sample(w, x, ids, tw, n)
+    for _ in range(args.warmup):
+        oracle.moe(x[tokens[:2]], sub[:2], tw[tokens[:2]], *Wc)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.moe(x[tokens], sub, tw[tokens], *Wc)
+    dt = (time.perf_counter() - t0) / args.steps
+    value = len(tokens) / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value,
+        "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_dict(w, world),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.threads(),
+                         "kind": "oracle",
+                         "sample": f"first {len(tokens)} of {w.T} tokens per step, all their experts"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_dict(w, world):
+    return {"workload": w.name, "tokens": w.T, "hidden": w.H, "inter": w.I, "experts": w.E,
+            "topk": w.k, "routing": w.routing, "parallelism": f"replicas{world}",
+            "l2": "flushed between timed steps (512 MiB write)"}
+
+
+def run_ours(args):
+    import torch
+
+    import block_scaled_fp4_pre_gb300 as mx
+    from block_scaled_fp4_pre_gb300 import weights as mxw
+
+    world, rank, local = dist_setup(args)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = workload(args)
+    dims = mx.make_dims(w.H, w.I, w.E, w.k, w.T)
+    stream = torch.cuda.Stream(dev)
+
+    t_setup = time.perf_counter()
+    can = mxw.quantize_experts(dims, lambda e, o: synth.expert_w1_f32(w, e, out=o),
+                               lambda e, o: synth.expert_w2_f32(w, e, out=o), dev, stream)
+    prepared = mxw.prepare(dims, can, dev, stream)
+    stream.synchronize()
+    del can
+    torch.cuda.empty_cache()
+    x = synth.hidden_bf16(w)
+    ids, tw = synth.routing(w)
+    xd = torch.from_numpy(x.view(np.int16)).to(dev)
+    idd = torch.from_numpy(ids).to(dev)
+    twd = torch.from_numpy(tw).to(dev)
+    out = torch.empty((w.T, w.H), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(mx.moe_workspace_size(dims), dtype=torch.uint8, device=dev)
+    mx.moe_workspace_init(dims, ws, stream)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    setup_s = time.perf_counter() - t_setup
+
+    def step():
+        mx.moe_pre_dispatch(dims, xd, idd, twd, w.T, ws, stream)
+        mx.moe_forward(dims, prepared, ws, out, w.T, stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            flush.zero_()
+            step()
+    mx.moe_check(ws, stream)
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    mx.moe_profile_reset()
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clocks:
+        with torch.cuda.stream(stream):
+            mx.moe_profile_enable(True)
+            for i in range(args.steps):
+                flush.zero_()
+                starts[i].record(stream)
+                step()
+                ends[i].record(stream)
+            mx.moe_profile_enable(False)
+        torch.cuda.synchronize(dev)
+    barrier(world)
+    mx.moe_check(ws, stream)
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    per_kernel = mx.moe_profile_read()
+    ms_local = statistics.mean(step_ms)
+    ms = max_over_ranks(world, ms_local)
+    value = world * w.T / (ms / 1e3)
+
+    alg = algorithmic(w, ids)
+    peaks, peak_kind = measured_peaks()
+    hbm_peak = float(peaks["hbm_gbs"])
+    kern_ms = {k: v[0] / max(v[1], 1) for k, v in per_kernel.items()}
+    dominant = max(("gemm1_swiglu", "gemm2_combine"), key=lambda k: kern_ms.get(k, 0.0))
+    dom_bytes = alg["gemm1_bytes"] if dominant == "gemm1_swiglu" else alg["gemm2_bytes"]
+    dom_ms = kern_ms.get(dominant, float("nan"))
+    achieved = dom_bytes / (dom_ms / 1e3) / 1e9
+    traffic = recorded_traffic(dominant, w.name)
+
+    e2e = None
+    if not args.no_e2e:
+        xh = torch.from_numpy(x.view(np.int16)).pin_memory()
+        idh = torch.from_numpy(ids).pin_memory()
+        twh = torch.from_numpy(tw).pin_memory()
+        outh = torch.empty((w.T, w.H), dtype=torch.int16).pin_memory()
+        for _ in range(max(1, args.warmup)):
+            mx.moe_run_host(dims, prepared, ws, xh, idh, twh, outh, w.T, stream)
+        times = []
+        for _ in range(args.steps):
+            with torch.cuda.stream(stream):
+                flush.zero_()
+            stream.synchronize()
+            t0 = time.perf_counter()
+            mx.moe_run_host(dims, prepared, ws, xh, idh, twh, outh, w.T, stream)
+            times.append(time.perf_counter() - t0)
+        e2e_s = max_over_ranks(world, statistics.mean(times))
+        e2e = {"value": world * w.T / e2e_s, "unit": "tokens/s",
+               "h2d_bytes_per_step": w.T * w.H * 2 + w.T * w.k * 8,
+               "d2h_bytes_per_step": w.T * w.H * 2, "ms_per_step": e2e_s * 1e3}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        n = args.cpu_sample_tokens or default_cpu_tokens(w)
+        r = time_oracle(w, x, ids, tw, n)
+        cpu = {"value": r["tokens"] / r["seconds"][0], "unit": "tokens/s", "cores": r["threads"],
+               "kind": "oracle",
+               "sample": f"first {r['tokens']} of {w.T} tokens with all {w.k} experts each "
+                         f"({r['seconds'][0]:.1f} s of oracle time)"}
+
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC,
+        "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "us_per_layer": ms * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "mxfp4 (e2m1 x ue8m0), fp32 accumulate", "data": "synthetic",
+        "config": config_dict(w, world),
+        "layer_hbm_tbs": alg["layer_bytes"] / (ms / 1e3) / 1e12,
+        "layer_roofline_frac": (alg["layer_bytes"] / (hbm_peak * 1e9)) / (ms / 1e3),
+        "touched_experts": alg["touched_experts"],
+        "roofline": {"kernel": dominant, "bound": "hbm", "achieved": achieved, "peak": hbm_peak,
+                     "unit": "GB/s", "frac": achieved / hbm_peak, "traffic": traffic,
+                     "algorithmic_bytes": dom_bytes, "avg_ms": dom_ms,
+                     "peak_kind": f"{peak_kind} copy bandwidth"},
+        "kernels_ms": kern_ms,
+        "clocks": clocks.summary(),
+        "gpu_launches": KERNELS_PER_STEP * args.steps,
+        "setup_s": setup_s,
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()
