@@ -82,6 +82,7 @@ def lib() -> ctypes.CDLL:
             "moe_profile_read": ([ctypes.POINTER(ctypes.c_char_p), vp, vp, i32], i32),
             "moe_profile_reset": ([], None),
             "moe_device_sm_count": ([], i32),
+            "moe_bucket_noalloc": ([D, vp, vp, i32, vp, vp, vp], i32),
         }
         for name, (args, res) in sigs.items():
             f = getattr(l, name)
@@ -233,3 +234,11 @@ def moe_profile_reset() -> None:
 
 def moe_device_sm_count() -> int:
     return int(lib().moe_device_sm_count())
+
+
+def moe_bucket_noalloc(dims: MoeDims, topk_ids, topk_weights, num_tokens: int, counts,
+                       assign_slot, stream=None) -> None:
+    """Bucketing with the library's own static scratch; allocates nothing on the device."""
+    _check(lib().moe_bucket_noalloc(ctypes.byref(dims), _ptr(topk_ids), _ptr(topk_weights),
+                                    int(num_tokens), _ptr(counts), _ptr(assign_slot),
+                                    _stream(stream)))

@@ -291,6 +291,8 @@ moe_status forward_impl(const moe_dims* d, const void* prepared, void* ws, void*
 
 }  // namespace
 
+void mxmoe::set_last_error(const char* msg) { g_err = msg; }
+
 extern "C" {
 
 const char* moe_last_error(void) { return g_err.c_str(); }

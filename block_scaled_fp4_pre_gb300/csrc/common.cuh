@@ -92,6 +92,9 @@ cudaError_t launch_prepare(const Shape& s, const uint8_t* w1c, const uint8_t* w1
                            const uint8_t* w2c, const uint8_t* w2s, uint8_t* prep,
                            const PrepLayout& pl, cudaStream_t st);
 
+// Records the message moe_last_error() returns on this thread.
+void set_last_error(const char* msg);
+
 enum GemmMode { kGemmRaw = 0, kGemmSwiglu = 1, kGemmCombine = 2 };
 
 struct GemmLaunch {

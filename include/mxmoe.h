@@ -197,6 +197,35 @@ MXMOE_API void moe_profile_reset(void);
  * grids for); 0 if no device. */
 MXMOE_API int32_t moe_device_sm_count(void);
 
+/* ---- bucketing without any device allocation ----
+ * The pages have no counterpart to this entry point; it exists for callers that
+ * cannot allocate device memory where they route tokens: runtimes that plan every
+ * device buffer ahead of time and forbid allocation afterwards, and latency-critical
+ * threads that cannot afford cudaMalloc's implicit device-wide synchronisation.
+ * Such a caller passes only its inputs and outputs.
+ *
+ * Runs the same bucketing kernel as moe_pre_dispatch on topk_ids_dev [T, k] and
+ * topk_weights_dev [T, k] (T = num_tokens) and writes:
+ *   counts_dev       int32 [E]    tokens routed to each expert
+ *   assign_slot_dev  int32 [T*k]  row of assignment t*k+j in the expert-grouped order
+ *                                 (experts' rows start at multiples of 128, tokens
+ *                                 ascending inside an expert; -1 for ids outside [0, E))
+ * -- the values moe_pre_dispatch stores in a workspace (see moe_read_dispatch).
+ * The kernel's other buffers live in a static device array of the library, about
+ * 0.5 MiB, which every GPU that loads the library holds until the process exits.
+ * Limits: num_experts <= 256 and num_tokens * topk <= 8192; larger sizes return
+ * MOE_ERR_INVALID_ARG without launching.  dims->max_tokens is not used.
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  All calls share the array and it keeps the previous call's contents
+ * (the error flags are cleared on every call); calls that overlap on the GPU --
+ * on different streams or from different host threads -- race on it, so
+ * serialise them.  Allocates nothing: no cudaMalloc, no cudaFree. */
+MXMOE_API moe_status moe_bucket_noalloc(const moe_dims *dims, const int32_t *topk_ids_dev,
+                                        const float *topk_weights_dev, int32_t num_tokens,
+                                        int32_t *counts_dev, int32_t *assign_slot_dev,
+                                        void *stream);
+
 #ifdef __cplusplus
 }
 #endif
