@@ -47,6 +47,7 @@ def parse_args():
     p.add_argument("--workload", default="layer_T512", choices=sorted(synth.WORKLOADS))
     p.add_argument("--experts", type=int, default=0,
                    help="override the expert count (small cases for profiler captures)")
+    p.add_argument("--tokens", type=int, default=0, help="override the token count")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-sample-tokens", type=int, default=0)
@@ -55,10 +56,11 @@ def parse_args():
 
 def workload(args) -> synth.Workload:
     w = synth.WORKLOADS[args.workload]
-    if args.experts:
-        w = synth.Workload(w.name + f"_E{args.experts}", T=w.T, H=w.H, I=w.I, E=args.experts,
-                           k=min(w.k, args.experts), routing=w.routing, zipf_s=w.zipf_s,
-                           outlier_frac=w.outlier_frac)
+    if args.experts or args.tokens:
+        E = args.experts or w.E
+        T = args.tokens or w.T
+        w = synth.Workload(f"{w.name}_T{T}_E{E}", T=T, H=w.H, I=w.I, E=E, k=min(w.k, E),
+                           routing=w.routing, zipf_s=w.zipf_s, outlier_frac=w.outlier_frac)
     return w
 
 

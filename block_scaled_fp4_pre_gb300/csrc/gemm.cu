@@ -16,7 +16,9 @@
 // are (token tile, 128-row weight slab); consecutive items share a token tile, so
 // its rows stay in L2 while the weight slabs stream from HBM once.
 //
-// Roles (192 threads, one persistent block per SM):
+// Roles (192 threads; two persistent blocks per SM, so that one block's MMA issue
+// and epilogue overlap the other's -- a single block per SM leaves the stream
+// waiting on its one MMA-issuing thread):
 //   warp 0      TMA producer: weight slab box (128 rows x 128 B), token boxes
 //               (32 rows x 128 B each), and both operands' 128x4 scale blocks.
 //   warp 1      TMEM allocator; lane 0 issues tcgen05.cp (scales) + tcgen05.mma.
@@ -33,22 +35,24 @@
 namespace mxmoe {
 namespace {
 
-constexpr int kStages = 6;
+constexpr int kStages = 3;
 constexpr int kThreads = 192;
-constexpr int kTmemCols = 512;
-constexpr int kAccCols = kBN;              // fp32 accumulator columns per buffer
-constexpr int kSfTmemBase = 2 * kAccCols;  // scale registers after the two accumulators
+constexpr int kBlocksPerSM = 2;
+constexpr int kTmemCols = 256;             // half of the SM's tensor memory per block
+constexpr int kAccCols = kBN;              // one fp32 accumulator of up to 128 columns
+constexpr int kSfTmemBase = kAccCols;      // scale registers (2 x 16 columns) after it
+constexpr int kEpiCols = 16;               // accumulator columns per epilogue load
 constexpr unsigned kFull = 0xFFFFFFFFu;
 
 struct __align__(8) SmemTail {
   uint64_t full[kStages];
   uint64_t empty[kStages];
-  uint64_t acc_full[2];
-  uint64_t acc_empty[2];
+  uint64_t acc_full;
+  uint64_t acc_empty;
   uint64_t mma_done;
   uint32_t tmem_base;
   int abort;
-  float xchg[2][4][32];
+  float xchg[2][4][kEpiCols];
 };
 
 constexpr size_t kSmemA = 0;
@@ -74,7 +78,7 @@ __device__ __forceinline__ float silu_times(float g, float u) {
 }
 
 template <int MODE>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, kBlocksPerSM)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
                     const __grid_constant__ CUtensorMap tmap_t, const GemmArgs args) {
   extern __shared__ uint8_t smem_raw[];
@@ -95,10 +99,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(&tail->full[s], 1);
       ptx::mbar_init(&tail->empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      ptx::mbar_init(&tail->acc_full[b], 1);
-      ptx::mbar_init(&tail->acc_empty[b], 128);
-    }
+    ptx::mbar_init(&tail->acc_full, 1);
+    ptx::mbar_init(&tail->acc_empty, 128);
     ptx::mbar_init(&tail->mma_done, 1);
     tail->abort = 0;
     ptx::fence_mbar_init();
@@ -175,7 +177,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
-      int ab = 0;
       uint32_t acc_phase = 0;
       uint32_t sfbuf = 0;
       bool ok = true;
@@ -183,12 +184,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int tile = item / args.m_tiles;
         const int n = args.ws.tiles[tile].z;
         const int n_mma = (n + kBBoxRows - 1) / kBBoxRows * kBBoxRows;
-        if (!ptx::mbar_wait(&tail->acc_empty[ab], acc_phase ^ 1u, abort_flag, kWaitLimitNs)) {
+        if (!ptx::mbar_wait(&tail->acc_empty, acc_phase ^ 1u, abort_flag, kWaitLimitNs)) {
           ok = false;
           break;
         }
         ptx::tc_fence_after();
-        const uint32_t d_tmem = tmem_base + (uint32_t)(ab * kAccCols);
+        const uint32_t d_tmem = tmem_base;
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!ptx::mbar_wait(&tail->full[stage], phase, abort_flag, kWaitLimitNs)) {
             ok = false;
@@ -222,11 +223,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (!ok) break;
-        ptx::tc_commit(&tail->acc_full[ab]);
-        if (++ab == 2) {
-          ab = 0;
-          acc_phase ^= 1u;
-        }
+        ptx::tc_commit(&tail->acc_full);
+        acc_phase ^= 1u;
       }
       if (!ok) atomicOr(&args.ws.flags[0], kErrTimeout);
       // Whatever happened, wait until every MMA issued here has finished before
@@ -239,63 +237,60 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int ep_tid = threadIdx.x - 64;
-    int ab = 0;
     uint32_t acc_phase = 0;
     int xb = 0;
     for (int item = blockIdx.x; item < num_items; item += gridDim.x) {
       const int tile = item / args.m_tiles, mt = item % args.m_tiles;
       const int4 ti = args.ws.tiles[tile];
       const int row0 = ti.y, n = ti.z;
-      if (!ptx::mbar_wait(&tail->acc_full[ab], acc_phase, abort_flag, kWaitLimitNs)) {
+      if (!ptx::mbar_wait(&tail->acc_full, acc_phase, abort_flag, kWaitLimitNs)) {
         if (ep_tid == 0) atomicOr(&args.ws.flags[0], kErrTimeout);
         break;
       }
+      acc_phase ^= 1u;
       ptx::tc_fence_after();
-      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(ab * kAccCols);
-      for (int c0 = 0; c0 < n; c0 += 32) {
-        float v[32];
-        ptx::tmem_ld32(taddr + (uint32_t)c0, v);
-        const int ncol = min(32, n - c0);
+      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16);
+      for (int c0 = 0; c0 < n; c0 += kEpiCols) {
+        float v[kEpiCols];
+        ptx::tmem_ld16(taddr + (uint32_t)c0, v);
+        if (c0 + kEpiCols >= n) {
+          // Last load of this item: hand the accumulator back to the MMA issuer
+          // before the math, so the next item's MMAs overlap it.
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(&tail->acc_empty);
+        }
+        const int ncol = min(kEpiCols, n - c0);
         if constexpr (MODE == kGemmSwiglu) {
           // Rows of this warp: chunk c of 32 interleaved gate/up rows =
           // [gate even 8 | up even 8 | gate odd 8 | up odd 8] of features c*16..c*16+15.
           const int c = mt * 4 + q;
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
+          for (int j = 0; j < kEpiCols; ++j) {
             if (j < ncol) {
               const float u = __shfl_down_sync(kFull, v[j], 8);
-              const float h = silu_times(v[j], u);
-              v[j] = (lane & 8) ? 0.f : h;
-              float a = fabsf(v[j]);
-              a = fmaxf(a, __shfl_xor_sync(kFull, a, 16));
-              a = fmaxf(a, __shfl_xor_sync(kFull, a, 4));
-              a = fmaxf(a, __shfl_xor_sync(kFull, a, 2));
-              a = fmaxf(a, __shfl_xor_sync(kFull, a, 1));
-              if (lane == 0) tail->xchg[xb][q][j] = a;
+              v[j] = (lane & 8) ? 0.f : silu_times(v[j], u);
+              // |h| >= 0, so its bit pattern orders like the value
+              const unsigned a = __reduce_max_sync(kFull, __float_as_uint(fabsf(v[j])));
+              if (lane == 0) tail->xchg[xb][q][j] = __uint_as_float(a);
             }
           }
           ptx::named_bar_sync(1, 128);
           const int i_kc4 = args.I / 128;
           const size_t hrow_bytes = (size_t)args.I / 2;
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
+          for (int j = 0; j < kEpiCols; ++j) {
             if (j < ncol) {
               // 32-feature group = this warp's 16 features + the partner warp's 16.
               const float amax = fmaxf(tail->xchg[xb][q][j], tail->xchg[xb][q ^ 1][j]);
               const int e = ptx::mx_scale_exponent(amax);
               const float qv = v[j] * ptx::pow2_neg(e);
               const float qodd = __shfl_down_sync(kFull, qv, 16);
-              uint32_t w = (lane < 8) ? (ptx::e2m1x2(qv, qodd) << (8 * (lane & 3))) : 0u;
-              w |= __shfl_xor_sync(kFull, w, 1);
-              w |= __shfl_xor_sync(kFull, w, 2);
-              const uint32_t w_hi = __shfl_sync(kFull, w, 4);
               const size_t row = (size_t)row0 + c0 + j;
-              if (lane == 0) {
-                *reinterpret_cast<uint2*>(args.ws.hb + row * hrow_bytes + (size_t)c * 8) =
-                    make_uint2(w, w_hi);
-                if ((q & 1) == 0)
-                  args.ws.hsf[sf_atom_offset(row, c >> 1, i_kc4)] = (uint8_t)(e + 127);
-              }
+              // lanes 0..7 write the 8 consecutive bytes of features c*16..c*16+15
+              if (lane < 8)
+                args.ws.hb[row * hrow_bytes + (size_t)c * 8 + lane] = (uint8_t)ptx::e2m1x2(qv, qodd);
+              if (lane == 0 && (q & 1) == 0)
+                args.ws.hsf[sf_atom_offset(row, c >> 1, i_kc4)] = (uint8_t)(e + 127);
             }
           }
           xb ^= 1;
@@ -308,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const int feat = mt * kBM + q * 32 + lane;
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
+          for (int j = 0; j < kEpiCols; ++j) {
             const int tok = __shfl_sync(kFull, my_tok, j);
             const float wt = __shfl_sync(kFull, my_w, j);
             if (j < ncol) atomicAdd(args.ws.acc + (size_t)tok * args.H + feat, wt * v[j]);
@@ -317,19 +312,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int m = mt * kBM + q * 32 + lane;
           const int col = gate_up_source_row(m, args.I);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
+          for (int j = 0; j < kEpiCols; ++j) {
             if (j < ncol) {
               const int a = args.ws.slot_assign[row0 + c0 + j];
               args.gate_up_debug[(size_t)a * 2 * args.I + col] = v[j];
             }
           }
         }
-      }
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(&tail->acc_empty[ab]);
-      if (++ab == 2) {
-        ab = 0;
-        acc_phase ^= 1u;
       }
     }
   }
@@ -390,7 +379,7 @@ cudaError_t launch_mode(const GemmLaunch& g, const CUtensorMap& tw, const CUtens
     if (err != cudaSuccess) return err;
     attr_set = true;
   }
-  moe_gemm_kernel<MODE><<<g.num_sms, kThreads, kSmemBytes, st>>>(tw, tt, a);
+  moe_gemm_kernel<MODE><<<kBlocksPerSM * g.num_sms, kThreads, kSmemBytes, st>>>(tw, tt, a);
   return cudaGetLastError();
 }
 

@@ -197,6 +197,21 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 32 lanes x 16 consecutive fp32 columns of tensor memory into registers.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
@@ -245,8 +260,14 @@ __device__ __forceinline__ uint32_t e2m1x8(const float (&v)[8]) {
 
 // E2M1 byte of two scaled values with their signs, `a` in the low nibble.
 __device__ __forceinline__ uint32_t e2m1x2(float a, float b) {
-  const uint32_t mag = e2m1x8_mag(fabsf(a), fabsf(b), 0.f, 0.f, 0.f, 0.f, 0.f, 0.f) & 0xFFu;
-  return mag | ((__float_as_uint(a) >> 31) << 3) | ((__float_as_uint(b) >> 31) << 7);
+  uint16_t r;
+  asm("{\n\t.reg .b8 t;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\t"
+      "mov.b16 %0, {t, t};\n\t}"
+      : "=h"(r)
+      : "f"(fabsf(b)), "f"(fabsf(a)));
+  return ((uint32_t)r & 0xFFu) | ((__float_as_uint(a) >> 31) << 3) |
+         ((__float_as_uint(b) >> 31) << 7);
 }
 
 }  // namespace ptx
