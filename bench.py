@@ -325,14 +325,18 @@ def run_ours(args):
             step()
     mx.moe_check(ws, stream)
 
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    mx.moe_profile_reset()
-    barrier(world)
-    torch.cuda.synchronize(dev)
-    with ClockSampler(local) as clocks:
+    def timed_pass(profile: bool):
+        """K steps, L2 flushed before each; CUDA events on the launch stream bracket
+        each step.  With profile=True the library also records events around each
+        of its kernels (which can keep consecutive kernels from overlapping), so the
+        headline numbers come from the plain pass."""
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        mx.moe_profile_reset()
+        barrier(world)
+        torch.cuda.synchronize(dev)
         with torch.cuda.stream(stream):
-            mx.moe_profile_enable(True)
+            mx.moe_profile_enable(profile)
             for i in range(args.steps):
                 flush.zero_()
                 starts[i].record(stream)
@@ -340,10 +344,13 @@ def run_ours(args):
                 ends[i].record(stream)
             mx.moe_profile_enable(False)
         torch.cuda.synchronize(dev)
-    barrier(world)
-    mx.moe_check(ws, stream)
-    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    per_kernel = mx.moe_profile_read()
+        barrier(world)
+        mx.moe_check(ws, stream)
+        return [s_.elapsed_time(e_) for s_, e_ in zip(starts, ends)], mx.moe_profile_read()
+
+    with ClockSampler(local) as clocks:
+        step_ms, _ = timed_pass(False)
+        prof_step_ms, per_kernel = timed_pass(True)
     ms_local = statistics.mean(step_ms)
     ms = max_over_ranks(world, ms_local)
     value = world * w.T / (ms / 1e3)
@@ -405,8 +412,9 @@ def run_ours(args):
                      "algorithmic_bytes": dom_bytes, "avg_ms": dom_ms,
                      "peak_kind": f"{peak_kind} copy bandwidth"},
         "kernels_ms": kern_ms,
+        "profiled_ms_per_step": statistics.mean(prof_step_ms),
         "clocks": clocks.summary(),
-        "gpu_launches": KERNELS_PER_STEP * args.steps,
+        "gpu_launches": KERNELS_PER_STEP * args.steps,   # in the headline timed pass
         "setup_s": setup_s,
     }
     if e2e is not None:

@@ -34,6 +34,7 @@ __global__ void __launch_bounds__(1024) bucket_kernel(const int32_t* __restrict_
   int32_t* tst = seg + E + 1;    // [E+1]
   __shared__ int32_t bad;
 
+  ptx::pdl_launch_dependents();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int A = T * k;
   const int per = (A + 31) / 32;
@@ -133,20 +134,22 @@ __global__ void __launch_bounds__(1024) bucket_kernel(const int32_t* __restrict_
 // ---------------------------------------------------------------------------
 // Quantise one token row per block and scatter it to the token's k workspace rows.
 // A thread owns 8 consecutive elements; 4 adjacent threads form one 32-group.
-// The block also clears the token's fp32 combine accumulator row.
+// The row is quantised into shared memory (and the token's fp32 combine
+// accumulator row cleared) while the bucketing kernel may still be running; the
+// block then waits for it and copies the row to each of the token's k slots.
 __global__ void __launch_bounds__(256) quantize_scatter_kernel(const __nv_bfloat16* __restrict__ x,
                                                                int H, int k, WsPtrs ws) {
+  extern __shared__ __align__(16) uint8_t qsh[];       // [H/2 codes | H/32 scales]
   __shared__ int32_t slots[32];
+  uint8_t* codes_sh = qsh;
+  uint8_t* sf_sh = qsh + H / 2;
   const int t = blockIdx.x, tid = threadIdx.x;
-  if (tid < k) slots[tid] = ws.assign_slot[(size_t)t * k + tid];
+  ptx::pdl_launch_dependents();
   {
     float4* acc = reinterpret_cast<float4*>(ws.acc + (size_t)t * H);
     const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int i = tid; i < H / 4; i += blockDim.x) acc[i] = z;
   }
-  __syncthreads();
-  const int kc4 = H / 128;
-  const size_t row_bytes = (size_t)H / 2;
   for (int base = tid * 8; base < H; base += blockDim.x * 8) {
     const uint4 raw = *reinterpret_cast<const uint4*>(x + (size_t)t * H + base);
     const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
@@ -166,12 +169,21 @@ __global__ void __launch_bounds__(256) quantize_scatter_kernel(const __nv_bfloat
     const float inv = ptx::pow2_neg(e);
 #pragma unroll
     for (int i = 0; i < 8; ++i) v[i] *= inv;
-    const uint32_t codes = ptx::e2m1x8(v);
-    for (int j = 0; j < k; ++j) {
-      const int slot = slots[j];
-      if (slot < 0) continue;
-      *reinterpret_cast<uint32_t*>(ws.xb + (size_t)slot * row_bytes + base / 2) = codes;
-      if ((tid & 3) == 0) ws.xsf[sf_atom_offset((size_t)slot, base / 32, kc4)] = (uint8_t)(e + 127);
+    *reinterpret_cast<uint32_t*>(codes_sh + base / 2) = ptx::e2m1x8(v);
+    if ((tid & 3) == 0) sf_sh[base / 32] = (uint8_t)(e + 127);
+  }
+  ptx::pdl_wait();
+  if (tid < k) slots[tid] = ws.assign_slot[(size_t)t * k + tid];
+  __syncthreads();
+  const int kc4 = H / 128;
+  const size_t row_bytes = (size_t)H / 2;
+  for (int j = 0; j < k; ++j) {
+    const int slot = slots[j];
+    if (slot < 0) continue;
+    uint4* dst = reinterpret_cast<uint4*>(ws.xb + (size_t)slot * row_bytes);
+    for (int i = tid; i < H / 32; i += blockDim.x) {   // 16-byte chunks of the code row
+      dst[i] = reinterpret_cast<const uint4*>(codes_sh)[i];
+      ws.xsf[sf_atom_offset((size_t)slot, i, kc4)] = sf_sh[i];
     }
   }
 }
@@ -247,6 +259,7 @@ __global__ void scale_blocks_kernel(const uint8_t* __restrict__ src, uint32_t* _
 // acc fp32 -> bf16, 8 elements per thread.
 __global__ void convert_out_kernel(const float* __restrict__ acc, __nv_bfloat16* __restrict__ out,
                                    int64_t n8) {
+  ptx::pdl_wait();
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8;
        i += (int64_t)gridDim.x * blockDim.x) {
     const float4 a = reinterpret_cast<const float4*>(acc)[2 * i];
@@ -278,16 +291,14 @@ cudaError_t launch_bucket(const Shape& s, const int32_t* ids, const float* tw, i
 
 cudaError_t launch_quantize_scatter(const Shape& s, const void* x, int T, const WsPtrs& ws,
                                     cudaStream_t st) {
-  quantize_scatter_kernel<<<T, 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(x), s.H, s.k,
-                                             ws);
-  return cudaGetLastError();
+  return launch_pdl(quantize_scatter_kernel, dim3(T), dim3(256), (size_t)s.H / 2 + s.H / 32, st,
+                    reinterpret_cast<const __nv_bfloat16*>(x), s.H, s.k, ws);
 }
 
 cudaError_t launch_convert_out(const float* acc, void* out, int64_t n, cudaStream_t st) {
   const int64_t n8 = n / 8;
-  convert_out_kernel<<<grid_for(n8, 256, 4096), 256, 0, st>>>(
-      acc, reinterpret_cast<__nv_bfloat16*>(out), n8);
-  return cudaGetLastError();
+  return launch_pdl(convert_out_kernel, dim3(grid_for(n8, 256, 4096)), dim3(256), 0, st, acc,
+                    reinterpret_cast<__nv_bfloat16*>(out), n8);
 }
 
 cudaError_t launch_quantize_rows(const float* src, int64_t rows, int K, uint8_t* codes,

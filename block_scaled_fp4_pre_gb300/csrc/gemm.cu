@@ -87,10 +87,6 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
   SmemTail* tail = reinterpret_cast<SmemTail*>(smem + kSmemTail);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int num_tiles = args.ws.flags[1];
-  const int num_items = num_tiles * args.m_tiles;
-  if ((int)blockIdx.x >= num_items) return;  // uniform for the whole block
-
   const int num_kb = (args.K + kBK - 1) / kBK;
   const int kc4 = args.K / 128;  // scale blocks per 128-row group
 
@@ -116,6 +112,11 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
   ptx::tc_fence_after();
   const uint32_t tmem_base = tail->tmem_base;
   volatile int* abort_flag = &tail->abort;
+  // Set-up above overlaps the previous kernel; its outputs are read only from here on.
+  ptx::pdl_launch_dependents();
+  ptx::pdl_wait();
+  const int num_tiles = args.ws.flags[1];
+  const int num_items = num_tiles * args.m_tiles;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -379,8 +380,8 @@ cudaError_t launch_mode(const GemmLaunch& g, const CUtensorMap& tw, const CUtens
     if (err != cudaSuccess) return err;
     attr_set = true;
   }
-  moe_gemm_kernel<MODE><<<kBlocksPerSM * g.num_sms, kThreads, kSmemBytes, st>>>(tw, tt, a);
-  return cudaGetLastError();
+  return launch_pdl(moe_gemm_kernel<MODE>, dim3(kBlocksPerSM * g.num_sms), dim3(kThreads),
+                    kSmemBytes, st, tw, tt, a);
 }
 
 }  // namespace

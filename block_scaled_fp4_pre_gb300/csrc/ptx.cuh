@@ -17,6 +17,16 @@ __device__ __forceinline__ unsigned long long globaltimer() {
   return t;
 }
 
+// ---- programmatic dependent launch ------------------------------------------
+// Lets the next kernel in the stream be scheduled now (its blocks start once
+// resources allow and wait in pdl_wait for this grid's memory).
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Waits until the previous kernel in the stream has completed and its writes are
+// visible.  A no-op for kernels launched without the programmatic attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---- mbarrier --------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
