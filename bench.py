@@ -34,7 +34,7 @@ sys.path.insert(0, ROOT)
 import synth  # noqa: E402
 
 L2_FLUSH_BYTES = 512 << 20          # > 2x the 129 MB L2
-KERNELS_PER_STEP = 5                # bucket, quantize_scatter, gemm1, gemm2, convert
+KERNELS_PER_STEP = 4                # bucket, quantize_scatter, layer (both GEMMs + combine), convert
 METRIC = "W4A4 MoE layer tokens/s (E=256, top-6, T=512; also us/layer and HBM TB/s)"
 
 
@@ -148,15 +148,14 @@ def algorithmic(w: synth.Workload, ids) -> dict:
     return {
         "touched_experts": u,
         "layer_bytes": u * (w1 + w2) + 2 * T * H + 2 * T * H + 8 * T * k,
-        # gate/up kernel: its weights, the quantised token rows it reads once, h it writes
-        "gemm1_bytes": u * w1 + A * (H // 2 + H // 32) + A * (I // 2 + I // 32),
-        # down kernel: its weights, h it reads once, fp32 combine reductions (read+write)
-        "gemm2_bytes": u * w2 + A * (I // 2 + I // 32) + 2 * 4 * T * H,
+        # layer kernel: every touched expert's weights and the quantised token rows it
+        # reads once
+        "layer_kernel_bytes": u * (w1 + w2) + A * (H // 2 + H // 32),
         "flops": 6 * A * H * I,
     }
 
 
-def gemm_source_hash() -> str:
+def kernel_source_hash() -> str:
     with open(os.path.join(ROOT, "block_scaled_fp4_pre_gb300", "csrc", "gemm.cu"), "rb") as f:
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
@@ -173,7 +172,7 @@ def recorded_traffic(kernel: str, workload_name: str):
         if line.startswith("- ") and ":" in line:
             k, v = line[2:].split(":", 1)
             vals[k.strip()] = v.strip().strip("`")
-    if vals.get("gemm.cu sha256[:16]") != gemm_source_hash():
+    if vals.get("gemm.cu sha256[:16]") != kernel_source_hash():
         return None
     try:
         return float(vals["dram bytes per launch"])
@@ -359,8 +358,8 @@ def run_ours(args):
     peaks, peak_kind = measured_peaks()
     hbm_peak = float(peaks["hbm_gbs"])
     kern_ms = {k: v[0] / max(v[1], 1) for k, v in per_kernel.items()}
-    dominant = max(("gemm1_swiglu", "gemm2_combine"), key=lambda k: kern_ms.get(k, 0.0))
-    dom_bytes = alg["gemm1_bytes"] if dominant == "gemm1_swiglu" else alg["gemm2_bytes"]
+    dominant = "layer"
+    dom_bytes = alg["layer_kernel_bytes"]
     dom_ms = kern_ms.get(dominant, float("nan"))
     achieved = dom_bytes / (dom_ms / 1e3) / 1e9
     traffic = recorded_traffic(dominant, w.name)

@@ -61,6 +61,7 @@ WsLayout ws_layout(const moe_dims& d) {
   L.off_counts = take((size_t)E * 4);
   L.off_seg = take((size_t)(E + 1) * 4);
   L.off_tiles = take((size_t)L.tiles_cap * 16);
+  L.off_tile_done = take((size_t)L.tiles_cap * 4);
   L.off_assign = take((size_t)L.A_cap * 4);
   L.off_slot_token = take((size_t)L.R_cap * 4);
   L.off_slot_assign = take((size_t)L.R_cap * 4);
@@ -85,6 +86,7 @@ WsPtrs ws_ptrs(void* ws, const WsLayout& L) {
   p.counts = reinterpret_cast<int32_t*>(b + L.off_counts);
   p.seg = reinterpret_cast<int32_t*>(b + L.off_seg);
   p.tiles = reinterpret_cast<int4*>(b + L.off_tiles);
+  p.tile_done = reinterpret_cast<int32_t*>(b + L.off_tile_done);
   p.assign_slot = reinterpret_cast<int32_t*>(b + L.off_assign);
   p.slot_token = reinterpret_cast<int32_t*>(b + L.off_slot_token);
   p.slot_assign = reinterpret_cast<int32_t*>(b + L.off_slot_assign);
@@ -240,50 +242,38 @@ moe_status pre_dispatch_impl(const moe_dims* d, const void* x, const int32_t* id
   return MOE_OK;
 }
 
-moe_status forward_impl(const moe_dims* d, const void* prepared, void* ws, void* out, int32_t T,
-                        cudaStream_t st) {
+LayerLaunch layer_launch(const moe_dims* d, const void* prepared, void* ws, int32_t T) {
   const WsLayout L = ws_layout(*d);
   const PrepLayout P = prep_layout(*d);
-  const WsPtrs p = ws_ptrs(ws, L);
   const uint8_t* prep = static_cast<const uint8_t*>(prepared);
-  const int nsm = sm_count();
-  if (nsm <= 0) return fail(MOE_ERR_CUDA, "no CUDA device");
-  GemmLaunch g;
-  g.shape = shape_of(*d);
-  g.ws = p;
+  LayerLaunch g;
+  g.w1_codes = prep + P.off_w1c;
+  g.w1_sf = prep + P.off_w1s;
+  g.w2_codes = prep + P.off_w2c;
+  g.w2_sf = prep + P.off_w2s;
   g.R_cap = L.R_cap;
-  g.num_sms = nsm;
+  g.shape = shape_of(*d);
+  g.T = T;
+  g.num_phases = 2;
+  g.ws = ws_ptrs(ws, L);
   g.gate_up_debug = nullptr;
+  g.num_sms = sm_count();
+  return g;
+}
+
+moe_status forward_impl(const moe_dims* d, const void* prepared, void* ws, void* out, int32_t T,
+                        cudaStream_t st) {
+  LayerLaunch g = layer_launch(d, prepared, ws, T);
+  if (g.num_sms <= 0) return fail(MOE_ERR_CUDA, "no CUDA device");
   cudaError_t e;
-  // gate/up projection + SwiGLU + requantisation
-  g.mode = kGemmSwiglu;
-  g.w_codes = prep + P.off_w1c;
-  g.w_sf = prep + P.off_w1s;
-  g.t_codes = p.xb;
-  g.t_sf = p.xsf;
-  g.rows_per_expert = 2 * d->inter;
-  g.K = d->hidden;
   {
-    ProfScope ps("gemm1_swiglu", st);
-    e = launch_gemm(g, st);
+    ProfScope ps("layer", st);
+    e = launch_layer(g, st);
   }
-  if (e != cudaSuccess) return cuda_fail(e, "gate/up GEMM");
-  // down projection + combine
-  g.mode = kGemmCombine;
-  g.w_codes = prep + P.off_w2c;
-  g.w_sf = prep + P.off_w2s;
-  g.t_codes = p.hb;
-  g.t_sf = p.hsf;
-  g.rows_per_expert = d->hidden;
-  g.K = d->inter;
-  {
-    ProfScope ps("gemm2_combine", st);
-    e = launch_gemm(g, st);
-  }
-  if (e != cudaSuccess) return cuda_fail(e, "down GEMM");
+  if (e != cudaSuccess) return cuda_fail(e, "layer kernel");
   {
     ProfScope ps("convert_out", st);
-    e = launch_convert_out(p.acc, out, (int64_t)T * d->hidden, st);
+    e = launch_convert_out(g.ws.acc, out, (int64_t)T * d->hidden, st);
   }
   if (e != cudaSuccess) return cuda_fail(e, "output conversion");
   return MOE_OK;
@@ -569,24 +559,11 @@ moe_status moe_debug_gate_up(const moe_dims* dims, const void* prepared, void* w
   if (T == 0) return MOE_OK;
   if (!prepared || !gate_up) return fail(MOE_ERR_INVALID_ARG, "NULL pointer");
   if (!aligned(prepared, 256)) return fail(MOE_ERR_INVALID_ARG, "prepared not 256-byte aligned");
-  const WsLayout L = ws_layout(*dims);
-  const PrepLayout P = prep_layout(*dims);
-  const uint8_t* prep = static_cast<const uint8_t*>(prepared);
-  GemmLaunch g;
-  g.mode = kGemmRaw;
-  g.shape = shape_of(*dims);
-  g.ws = ws_ptrs(ws, L);
-  g.R_cap = L.R_cap;
-  g.num_sms = sm_count();
+  LayerLaunch g = layer_launch(dims, prepared, ws, T);
   if (g.num_sms <= 0) return fail(MOE_ERR_CUDA, "no CUDA device");
+  g.num_phases = 1;
   g.gate_up_debug = gate_up;
-  g.w_codes = prep + P.off_w1c;
-  g.w_sf = prep + P.off_w1s;
-  g.t_codes = g.ws.xb;
-  g.t_sf = g.ws.xsf;
-  g.rows_per_expert = 2 * dims->inter;
-  g.K = dims->hidden;
-  cudaError_t e = launch_gemm(g, static_cast<cudaStream_t>(stream));
+  cudaError_t e = launch_layer(g, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "gate/up GEMM (raw)");
   return MOE_OK;
 }

@@ -28,6 +28,13 @@ constexpr int kSFStageBytes = 2 * kSFAtomBytes;  // 8 scale columns per k-block
 constexpr int kErrRouting = 1;
 constexpr int kErrTimeout = 2;
 
+// Other words of ws.flags: [1] number of token tiles, [2] valid assignments,
+// [3] next work item of the layer kernel, [4] blocks of the layer kernel done.
+constexpr int kFlagTiles = 1;
+constexpr int kFlagValid = 2;
+constexpr int kFlagSched = 3;
+constexpr int kFlagExit = 4;
+
 // Bounded waits give up after this many nanoseconds of %globaltimer.
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
@@ -51,16 +58,17 @@ __host__ __device__ __forceinline__ int gate_up_source_row(int r, int I) {
 // Workspace layout (computed on the host from the dims, passed to kernels).
 struct WsLayout {
   int64_t T_cap, A_cap, R_cap, tiles_cap;
-  size_t off_header, off_flags, off_counts, off_seg, off_tiles, off_assign, off_slot_token,
-      off_slot_assign, off_slot_weight, off_xb, off_xsf, off_hb, off_hsf, off_acc, off_stage_x,
-      off_stage_ids, off_stage_w, off_stage_out, total;
+  size_t off_header, off_flags, off_counts, off_seg, off_tiles, off_tile_done, off_assign,
+      off_slot_token, off_slot_assign, off_slot_weight, off_xb, off_xsf, off_hb,
+      off_hsf, off_acc, off_stage_x, off_stage_ids, off_stage_w, off_stage_out, total;
 };
 
 struct WsPtrs {
-  int32_t* flags;        // [0] error bits, [1] number of tiles, [2] valid assignments
+  int32_t* flags;        // error bits and counters, see kFlag*
   int32_t* counts;       // [E]
   int32_t* seg;          // [E+1] first workspace row of each expert (multiples of kBN)
   int4* tiles;           // [tiles_cap] (expert, first row, rows, 0)
+  int32_t* tile_done;    // [tiles_cap] gate/up items finished per token tile
   int32_t* assign_slot;  // [A_cap] workspace row of assignment t*k+j, -1 if skipped
   int32_t* slot_token;   // [R_cap]
   int32_t* slot_assign;  // [R_cap]
@@ -69,7 +77,7 @@ struct WsPtrs {
   uint8_t* xsf;          // 128x4 blocks of [R_cap, H/32]
   uint8_t* hb;           // [R_cap, I/2] requantised intermediate rows
   uint8_t* hsf;          // 128x4 blocks of [R_cap, I/32]
-  float* acc;            // [T_cap, H] fp32 combine accumulator
+  float* acc;            // [T_cap, H] fp32 combine accumulator (zero between layers)
 };
 
 struct PrepLayout {
@@ -106,7 +114,8 @@ cudaError_t launch_bucket(const Shape& s, const int32_t* ids, const float* tw, i
                           const WsPtrs& ws, cudaStream_t st);
 cudaError_t launch_quantize_scatter(const Shape& s, const void* x, int T, const WsPtrs& ws,
                                     cudaStream_t st);
-cudaError_t launch_convert_out(const float* acc, void* out, int64_t n, cudaStream_t st);
+// acc [n] fp32 -> out [n] bf16 (round to nearest even), clearing acc.
+cudaError_t launch_convert_out(float* acc, void* out, int64_t n, cudaStream_t st);
 cudaError_t launch_quantize_rows(const float* src, int64_t rows, int K, uint8_t* codes,
                                  uint8_t* sf, cudaStream_t st);
 cudaError_t launch_prepare(const Shape& s, const uint8_t* w1c, const uint8_t* w1s,
@@ -116,22 +125,22 @@ cudaError_t launch_prepare(const Shape& s, const uint8_t* w1c, const uint8_t* w1
 // Records the message moe_last_error() returns on this thread.
 void set_last_error(const char* msg);
 
-enum GemmMode { kGemmRaw = 0, kGemmSwiglu = 1, kGemmCombine = 2 };
-
-struct GemmLaunch {
-  int mode;
-  const uint8_t* w_codes;   // prepared weight codes [E*rows, K/2]
-  const uint8_t* w_sf;      // prepared weight scale blocks
-  const uint8_t* t_codes;   // token-side codes [R_cap, K/2]
-  const uint8_t* t_sf;      // token-side scale blocks
+// The layer kernel: gate/up GEMM + SwiGLU + requantisation, then down GEMM +
+// weighted combine into the fp32 accumulator, in one persistent launch.  With num_phases == 1
+// and gate_up_debug set it runs only the gate/up GEMM and writes raw accumulators.
+struct LayerLaunch {
+  const uint8_t* w1_codes;   // prepared gate/up codes [E*2I, H/2]
+  const uint8_t* w1_sf;      // their scale blocks
+  const uint8_t* w2_codes;   // prepared down codes [E*H, I/2]
+  const uint8_t* w2_sf;
   int64_t R_cap;
-  int rows_per_expert;      // 2I (gate/up) or H (down)
-  int K;                    // H (gate/up) or I (down)
   Shape shape;
+  int T;
+  int num_phases;
   WsPtrs ws;
-  float* gate_up_debug;     // kGemmRaw only
+  float* gate_up_debug;      // [T*k, 2I] (num_phases == 1)
   int num_sms;
 };
-cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t st);
+cudaError_t launch_layer(const LayerLaunch& g, cudaStream_t st);
 
 }  // namespace mxmoe

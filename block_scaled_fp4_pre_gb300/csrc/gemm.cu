@@ -1,31 +1,37 @@
-// Persistent grouped block-scaled FP4 x FP4 GEMM for sm_103a (tcgen05 + TMEM + TMA),
-// with three epilogues:
-//   kGemmSwiglu   gate/up projection -> SwiGLU -> MXFP4 requantisation of h
-//   kGemmCombine  down projection -> top-k weighted combine (fp32 reductions)
-//   kGemmRaw      gate/up projection -> raw fp32 accumulators (debug readback)
+// The expert layer in one persistent kernel for sm_103a (tcgen05 + TMEM + TMA):
+//   phase 0  grouped gate/up GEMM (block-scaled FP4 x FP4) -> SwiGLU -> MXFP4
+//            requantisation of h
+//   phase 1  grouped down GEMM -> top-k weighted combine (fp32 reductions into the
+//            workspace accumulator; a small kernel then writes the bf16 output)
+// plus a debug mode that runs phase 0 only and writes the raw fp32 accumulators.
 //
 // Pages: "[deepseek-v4] Bump sgl-deep-gemm for packed FP4xFP4 mega-MoE (W4A4)",
-// Appendix B (the layer streams every touched expert's packed FP4 weights and is
-// memory bound at ntok=512: memory SOL 85%, compute 34%, BLOCK_K=256); SGLang
-// PR #48424 summary (block_m 64 for decode loads); prhub digest of PR #37279
-// (activation "swiglu"; gran=16 interleave so that SwiGLU pairs sit together).
+// Appendix B (one fused "mega" layer kernel that streams every touched expert's
+// packed FP4 weights and is memory bound at ntok=512, BLOCK_K=256); SGLang PR #48424
+// summary (block_m 64 for decode loads); prhub digest of PR #37279 (activation
+// "swiglu"; the gran=16 interleave keeps each SwiGLU pair in one 32-row chunk).
 //
 // Orientation: the weight slab is the MMA's M=128 operand and the expert's tokens
 // are the N operand (N = 32..128), so one instruction shape serves a decode load of
-// a few tokens per expert as well as a prefill tile of 128 tokens.  The work items
-// are (token tile, 128-row weight slab); consecutive items share a token tile, so
-// its rows stay in L2 while the weight slabs stream from HBM once.
+// a few tokens per expert as well as a prefill tile of 128 tokens.
+//
+// Work items are (token tile, 128-row weight slab): first every gate/up item, token
+// tile by token tile, then every down item.  Blocks take items from a global
+// counter, so all gate/up items are claimed (by running blocks, with no
+// dependencies) before any down item is, and a down item's wait for its tile's
+// intermediate rows always ends -- whatever number of blocks is resident.  The
+// last block to finish resets the counters for the next call.
 //
 // Roles (192 threads; two persistent blocks per SM, so that one block's MMA issue
 // and epilogue overlap the other's -- a single block per SM leaves the stream
 // waiting on its one MMA-issuing thread):
-//   warp 0      TMA producer: weight slab box (128 rows x 128 B), token boxes
-//               (32 rows x 128 B each), and both operands' 128x4 scale blocks.
+//   warp 0      scheduler + TMA producer: weight slab box (128 rows x 128 B), token
+//               boxes (32 rows x 128 B each), both operands' 128x4 scale blocks.
 //   warp 1      TMEM allocator; lane 0 issues tcgen05.cp (scales) + tcgen05.mma.
 //   warps 2-5   epilogue: tcgen05.ld of the fp32 accumulator (lane quarter
-//               warp % 4), then the mode's math and global stores.
-// Every mbarrier wait is bounded (kWaitLimitNs); a timeout sets the workspace
-// error flag and all roles leave their loops, free TMEM and return.
+//               warp % 4), then the phase's math and global stores.
+// Every wait is bounded (kWaitLimitNs); a timeout sets the workspace error flag and
+// all roles leave their loops, drain their copies and MMAs, free TMEM and return.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -42,7 +48,10 @@ constexpr int kTmemCols = 256;             // half of the SM's tensor memory per
 constexpr int kAccCols = kBN;              // one fp32 accumulator of up to 128 columns
 constexpr int kSfTmemBase = kAccCols;      // scale registers (2 x 16 columns) after it
 constexpr int kEpiCols = 16;               // accumulator columns per epilogue load
+constexpr int kRing = 8;                   // work items in flight inside a block
 constexpr unsigned kFull = 0xFFFFFFFFu;
+
+enum LayerMode { kModeLayer = 0, kModeRaw = 1 };
 
 struct __align__(8) SmemTail {
   uint64_t full[kStages];
@@ -50,6 +59,9 @@ struct __align__(8) SmemTail {
   uint64_t acc_full;
   uint64_t acc_empty;
   uint64_t mma_done;
+  uint64_t ring_full[kRing];
+  uint64_t ring_empty[kRing];
+  int4 ring[kRing];          // (item, expert, first row, rows) or item = -1: stop
   uint32_t tmem_base;
   int abort;
   float xchg[2][4][kEpiCols];
@@ -62,33 +74,73 @@ constexpr size_t kSmemSFB = kSmemSFA + (size_t)kStages * kSFStageBytes;
 constexpr size_t kSmemTail = kSmemSFB + (size_t)kStages * kSFStageBytes;
 constexpr size_t kSmemBytes = kSmemTail + sizeof(SmemTail) + 1024;  // + alignment slack
 
-struct GemmArgs {
-  const uint8_t* w_sf;
-  const uint8_t* t_sf;
-  int rows_per_expert;
-  int K;
-  int m_tiles;
-  int H, I;
+struct PhaseArgs {
+  const uint8_t* w_sf;   // weight scale blocks
+  const uint8_t* t_sf;   // token-side scale blocks
+  int rows_per_expert;   // 2I (gate/up) or H (down)
+  int K;                 // H (gate/up) or I (down)
+  int m_tiles;           // rows_per_expert / 128
+  int num_kb;            // k-blocks of 256 elements (the last may be 128 wide)
+  int kc4;               // K / 128: scale blocks per 128-row group
+};
+
+struct LayerArgs {
+  PhaseArgs ph[2];
+  int num_phases;
+  int H, I, T;
   WsPtrs ws;
   float* gate_up_debug;
 };
+
+struct Item {
+  int phase, tile, mt;
+};
+
+__device__ __forceinline__ Item decode_item(int g, int n0, int m0, int m1) {
+  Item it;
+  if (g < n0) {
+    it.phase = 0;
+    it.tile = g / m0;
+    it.mt = g % m0;
+  } else {
+    g -= n0;
+    it.phase = 1;
+    it.tile = g / m1;
+    it.mt = g % m1;
+  }
+  return it;
+}
 
 __device__ __forceinline__ float silu_times(float g, float u) {
   return g / (1.0f + expf(-g)) * u;
 }
 
+// Waits until *p >= target (acquire), bounded like the mbarrier waits.
+__device__ __forceinline__ bool wait_counter(const int32_t* p, int target, volatile int* abort) {
+  if (ptx::ld_acquire(p) >= target) return true;
+  const unsigned long long t0 = ptx::globaltimer();
+  while (true) {
+    __nanosleep(128);
+    if (ptx::ld_acquire(p) >= target) return true;
+    if (*abort) return false;
+    if (ptx::globaltimer() - t0 > kWaitLimitNs) {
+      *abort = 1;
+      return false;
+    }
+  }
+}
+
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
-    moe_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
-                    const __grid_constant__ CUtensorMap tmap_t, const GemmArgs args) {
+    moe_layer_kernel(const __grid_constant__ CUtensorMap tmap_w1,
+                     const __grid_constant__ CUtensorMap tmap_x,
+                     const __grid_constant__ CUtensorMap tmap_w2,
+                     const __grid_constant__ CUtensorMap tmap_h, const LayerArgs args) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   SmemTail* tail = reinterpret_cast<SmemTail*>(smem + kSmemTail);
-
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int num_kb = (args.K + kBK - 1) / kBK;
-  const int kc4 = args.K / 128;  // scale blocks per 128-row group
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -98,10 +150,16 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
     ptx::mbar_init(&tail->acc_full, 1);
     ptx::mbar_init(&tail->acc_empty, 128);
     ptx::mbar_init(&tail->mma_done, 1);
+    for (int r = 0; r < kRing; ++r) {
+      ptx::mbar_init(&tail->ring_full[r], 1);
+      ptx::mbar_init(&tail->ring_empty[r], 5);  // the MMA thread + 4 epilogue warps
+    }
     tail->abort = 0;
     ptx::fence_mbar_init();
-    ptx::prefetch_tmap(&tmap_w);
-    ptx::prefetch_tmap(&tmap_t);
+    ptx::prefetch_tmap(&tmap_w1);
+    ptx::prefetch_tmap(&tmap_x);
+    ptx::prefetch_tmap(&tmap_w2);
+    ptx::prefetch_tmap(&tmap_h);
   }
   if (warp == 1) {
     ptx::tmem_alloc(&tail->tmem_base, kTmemCols);
@@ -115,44 +173,77 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
   // Set-up above overlaps the previous kernel; its outputs are read only from here on.
   ptx::pdl_launch_dependents();
   ptx::pdl_wait();
-  const int num_tiles = args.ws.flags[1];
-  const int num_items = num_tiles * args.m_tiles;
+
+  const int num_tiles = args.ws.flags[kFlagTiles];
+  const int m0 = args.ph[0].m_tiles, m1 = args.ph[1].m_tiles;
+  const int n0 = num_tiles * m0;
+  const int total = n0 + (args.num_phases == 2 ? num_tiles * m1 : 0);
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producer
+    // ------------------------------------------------- scheduler + producer
     if (lane == 0) {
       const uint64_t pol_w = ptx::policy_evict_first();
       const uint64_t pol_t = ptx::policy_evict_last();
-      int stage = 0;
-      uint32_t phase = 0;
+      int stage = 0, r = 0;
+      uint32_t phase = 0, rph = 0;
       int64_t issued = 0;
       bool ok = true;
-      for (int item = blockIdx.x; ok && item < num_items; item += gridDim.x) {
-        const int tile = item / args.m_tiles, mt = item % args.m_tiles;
-        const int4 ti = args.ws.tiles[tile];
+      // Items are claimed one ahead so that the claim and the tile-table read of
+      // the next item overlap the loads of the current one.
+      int g = atomicAdd(&args.ws.flags[kFlagSched], 1);
+      int4 ti = make_int4(0, 0, 0, 0);
+      if (g < total) ti = args.ws.tiles[decode_item(g, n0, m0, m1).tile];
+      while (true) {
+        const int item = g < total ? g : -1;
+        if (!ptx::mbar_wait(&tail->ring_empty[r], rph ^ 1u, abort_flag, kWaitLimitNs)) {
+          ok = false;
+          break;
+        }
+        tail->ring[r] = make_int4(item, ti.x, ti.y, ti.z);
+        ptx::mbar_arrive(&tail->ring_full[r]);
+        if (++r == kRing) {
+          r = 0;
+          rph ^= 1u;
+        }
+        if (item < 0) break;
+        const int g_next = atomicAdd(&args.ws.flags[kFlagSched], 1);
+        int4 ti_next = make_int4(0, 0, 0, 0);
+        const Item it = decode_item(item, n0, m0, m1);
+        const PhaseArgs& P = args.ph[it.phase];
+        const CUtensorMap* tw = it.phase ? &tmap_w2 : &tmap_w1;
+        const CUtensorMap* tt = it.phase ? &tmap_h : &tmap_x;
         const int e = ti.x, row0 = ti.y, n = ti.z;
         const int nb = (n + kBBoxRows - 1) / kBBoxRows;
-        const int wrow = e * args.rows_per_expert + mt * kBM;
-        const uint8_t* wsf = args.w_sf + ((size_t)(e * args.m_tiles + mt) * kc4) * kSFAtomBytes;
-        const uint8_t* tsf = args.t_sf + ((size_t)(row0 / kBN) * kc4) * kSFAtomBytes;
-        for (int kb = 0; kb < num_kb; ++kb) {
+        const int wrow = e * P.rows_per_expert + it.mt * kBM;
+        const uint8_t* wsf = P.w_sf + ((size_t)(e * P.m_tiles + it.mt) * P.kc4) * kSFAtomBytes;
+        const uint8_t* tsf = P.t_sf + ((size_t)(row0 / kBN) * P.kc4) * kSFAtomBytes;
+        if (it.phase == 1) {
+          // The down projection reads the intermediate rows that this tile's
+          // gate/up items wrote with ordinary stores.
+          if (!wait_counter(&args.ws.tile_done[it.tile], m0, abort_flag)) {
+            ok = false;
+            break;
+          }
+          ptx::fence_proxy_async_global();
+        }
+        for (int kb = 0; kb < P.num_kb; ++kb) {
           if (!ptx::mbar_wait(&tail->empty[stage], phase ^ 1u, abort_flag, kWaitLimitNs)) {
             ok = false;
             break;
           }
-          const int kvalid = min(kBK, args.K - kb * kBK);
+          const int kvalid = min(kBK, P.K - kb * kBK);
           const int atoms = kvalid / 128;
           const uint32_t bytes =
               kATileBytes + nb * (kBBoxRows * kBKBytes) + 2u * atoms * kSFAtomBytes;
           uint64_t* bar = &tail->full[stage];
           ptx::mbar_arrive_expect_tx(bar, bytes);
-          ptx::tma_load_2d(smem + kSmemA + (size_t)stage * kATileBytes, &tmap_w, kb * kBKBytes,
-                           wrow, bar, pol_w);
+          ptx::tma_load_2d(smem + kSmemA + (size_t)stage * kATileBytes, tw, kb * kBKBytes, wrow,
+                           bar, pol_w);
           ptx::bulk_load(smem + kSmemSFA + (size_t)stage * kSFStageBytes,
                          wsf + (size_t)kb * 2 * kSFAtomBytes, atoms * kSFAtomBytes, bar, pol_w);
           for (int j = 0; j < nb; ++j)
             ptx::tma_load_2d(smem + kSmemB + (size_t)stage * kBTileBytes + j * kBBoxRows * kBKBytes,
-                             &tmap_t, kb * kBKBytes, row0 + j * kBBoxRows, bar, pol_t);
+                             tt, kb * kBKBytes, row0 + j * kBBoxRows, bar, pol_t);
           ptx::bulk_load(smem + kSmemSFB + (size_t)stage * kSFStageBytes,
                          tsf + (size_t)kb * 2 * kSFAtomBytes, atoms * kSFAtomBytes, bar, pol_t);
           ++issued;
@@ -160,7 +251,11 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
             stage = 0;
             phase ^= 1u;
           }
+          if (kb == 0 && g_next < total) ti_next = args.ws.tiles[decode_item(g_next, n0, m0, m1).tile];
         }
+        if (!ok) break;
+        g = g_next;
+        ti = ti_next;
       }
       if (!ok) atomicOr(&args.ws.flags[0], kErrTimeout);
       // Drain: every copy this thread issued must have landed before the block
@@ -176,28 +271,38 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      uint32_t acc_phase = 0;
-      uint32_t sfbuf = 0;
+      int stage = 0, r = 0;
+      uint32_t phase = 0, rph = 0, acc_phase = 0, sfbuf = 0;
       bool ok = true;
-      for (int item = blockIdx.x; ok && item < num_items; item += gridDim.x) {
-        const int tile = item / args.m_tiles;
-        const int n = args.ws.tiles[tile].z;
+      while (true) {
+        if (!ptx::mbar_wait(&tail->ring_full[r], rph, abort_flag, kWaitLimitNs)) {
+          ok = false;
+          break;
+        }
+        const int4 rec = tail->ring[r];
+        ptx::mbar_arrive(&tail->ring_empty[r]);
+        if (++r == kRing) {
+          r = 0;
+          rph ^= 1u;
+        }
+        const int item = rec.x;
+        if (item < 0) break;
+        const Item it = decode_item(item, n0, m0, m1);
+        const PhaseArgs& P = args.ph[it.phase];
+        const int n = rec.w;
         const int n_mma = (n + kBBoxRows - 1) / kBBoxRows * kBBoxRows;
         if (!ptx::mbar_wait(&tail->acc_empty, acc_phase ^ 1u, abort_flag, kWaitLimitNs)) {
           ok = false;
           break;
         }
         ptx::tc_fence_after();
-        const uint32_t d_tmem = tmem_base;
-        for (int kb = 0; kb < num_kb; ++kb) {
+        for (int kb = 0; kb < P.num_kb; ++kb) {
           if (!ptx::mbar_wait(&tail->full[stage], phase, abort_flag, kWaitLimitNs)) {
             ok = false;
             break;
           }
           ptx::tc_fence_after();
-          const int kvalid = min(kBK, args.K - kb * kBK);
+          const int kvalid = min(kBK, P.K - kb * kBK);
           const int atoms = kvalid / 128;
           const uint32_t sfa_t = tmem_base + (uint32_t)(kSfTmemBase + sfbuf * 16);
           const uint32_t sfb_t = sfa_t + 8;
@@ -212,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
           const int steps = kvalid / 64;
           for (int s = 0; s < steps; ++s) {
             const uint32_t idesc = ptx::idesc_mxf4(n_mma, (s & 1) * 2);
-            ptx::tc_mma_mxf4(d_tmem, ptx::desc_sw128(a_base + s * 32),
+            ptx::tc_mma_mxf4(tmem_base, ptx::desc_sw128(a_base + s * 32),
                              ptx::desc_sw128(b_base + s * 32), idesc, sfa_t + (s >> 1) * 4,
                              sfb_t + (s >> 1) * 4, (kb | s) != 0 ? 1u : 0u);
           }
@@ -238,12 +343,24 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int ep_tid = threadIdx.x - 64;
-    uint32_t acc_phase = 0;
-    int xb = 0;
-    for (int item = blockIdx.x; item < num_items; item += gridDim.x) {
-      const int tile = item / args.m_tiles, mt = item % args.m_tiles;
-      const int4 ti = args.ws.tiles[tile];
-      const int row0 = ti.y, n = ti.z;
+    int r = 0, xb = 0;
+    uint32_t rph = 0, acc_phase = 0;
+    while (true) {
+      if (!ptx::mbar_wait(&tail->ring_full[r], rph, abort_flag, kWaitLimitNs)) {
+        if (ep_tid == 0) atomicOr(&args.ws.flags[0], kErrTimeout);
+        break;
+      }
+      const int4 rec = tail->ring[r];
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&tail->ring_empty[r]);
+      if (++r == kRing) {
+        r = 0;
+        rph ^= 1u;
+      }
+      const int item = rec.x;
+      if (item < 0) break;
+      const Item it = decode_item(item, n0, m0, m1);
+      const int row0 = rec.z, n = rec.w, mt = it.mt;
       if (!ptx::mbar_wait(&tail->acc_full, acc_phase, abort_flag, kWaitLimitNs)) {
         if (ep_tid == 0) atomicOr(&args.ws.flags[0], kErrTimeout);
         break;
@@ -261,7 +378,17 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
           ptx::mbar_arrive(&tail->acc_empty);
         }
         const int ncol = min(kEpiCols, n - c0);
-        if constexpr (MODE == kGemmSwiglu) {
+        if (MODE == kModeRaw) {
+          const int m = mt * kBM + q * 32 + lane;
+          const int col = gate_up_source_row(m, args.I);
+#pragma unroll
+          for (int j = 0; j < kEpiCols; ++j) {
+            if (j < ncol) {
+              const int a = args.ws.slot_assign[row0 + c0 + j];
+              args.gate_up_debug[(size_t)a * 2 * args.I + col] = v[j];
+            }
+          }
+        } else if (it.phase == 0) {
           // Rows of this warp: chunk c of 32 interleaved gate/up rows =
           // [gate even 8 | up even 8 | gate odd 8 | up odd 8] of features c*16..c*16+15.
           const int c = mt * 4 + q;
@@ -289,36 +416,38 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
               const size_t row = (size_t)row0 + c0 + j;
               // lanes 0..7 write the 8 consecutive bytes of features c*16..c*16+15
               if (lane < 8)
-                args.ws.hb[row * hrow_bytes + (size_t)c * 8 + lane] = (uint8_t)ptx::e2m1x2(qv, qodd);
+                args.ws.hb[row * hrow_bytes + (size_t)c * 8 + lane] =
+                    (uint8_t)ptx::e2m1x2(qv, qodd);
               if (lane == 0 && (q & 1) == 0)
                 args.ws.hsf[sf_atom_offset(row, c >> 1, i_kc4)] = (uint8_t)(e + 127);
             }
           }
           xb ^= 1;
-        } else if constexpr (MODE == kGemmCombine) {
+        } else {
+          // Down projection: this warp holds output features mt*128 + q*32 + lane of
+          // up to 16 token columns; add them, weighted, into the fp32 accumulator.
           int my_tok = 0;
           float my_w = 0.f;
           if (lane < ncol) {
             my_tok = args.ws.slot_token[row0 + c0 + lane];
             my_w = args.ws.slot_weight[row0 + c0 + lane];
           }
-          const int feat = mt * kBM + q * 32 + lane;
+          const size_t feat = (size_t)mt * kBM + q * 32 + lane;
 #pragma unroll
           for (int j = 0; j < kEpiCols; ++j) {
             const int tok = __shfl_sync(kFull, my_tok, j);
             const float wt = __shfl_sync(kFull, my_w, j);
             if (j < ncol) atomicAdd(args.ws.acc + (size_t)tok * args.H + feat, wt * v[j]);
           }
-        } else {
-          const int m = mt * kBM + q * 32 + lane;
-          const int col = gate_up_source_row(m, args.I);
-#pragma unroll
-          for (int j = 0; j < kEpiCols; ++j) {
-            if (j < ncol) {
-              const int a = args.ws.slot_assign[row0 + c0 + j];
-              args.gate_up_debug[(size_t)a * 2 * args.I + col] = v[j];
-            }
-          }
+        }
+      }
+      if (MODE == kModeLayer && it.phase == 0) {
+        // Publish: this item's intermediate rows (and scales) are written.
+        __threadfence();
+        ptx::named_bar_sync(2, 128);
+        if (ep_tid == 0) {
+          ptx::fence_proxy_async_global();
+          atomicAdd(&args.ws.tile_done[it.tile], 1);
         }
       }
     }
@@ -329,6 +458,16 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
   if (warp == 1) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem_base, kTmemCols);
+  }
+  if (threadIdx.x == 0) {
+    // The last block out resets the scheduler and tile counters for the next call.
+    __threadfence();
+    if (atomicAdd(&args.ws.flags[kFlagExit], 1) == (int)gridDim.x - 1) {
+      args.ws.flags[kFlagSched] = 0;
+      args.ws.flags[kFlagExit] = 0;
+      for (int t = 0; t < num_tiles; ++t) args.ws.tile_done[t] = 0;
+      __threadfence();
+    }
   }
 }
 
@@ -369,46 +508,55 @@ cudaError_t make_tmap(CUtensorMap* m, const void* base, uint64_t row_bytes, uint
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+PhaseArgs phase_args(const uint8_t* w_sf, const uint8_t* t_sf, int rows_per_expert, int K) {
+  PhaseArgs p;
+  p.w_sf = w_sf;
+  p.t_sf = t_sf;
+  p.rows_per_expert = rows_per_expert;
+  p.K = K;
+  p.m_tiles = rows_per_expert / kBM;
+  p.num_kb = (K + kBK - 1) / kBK;
+  p.kc4 = K / 128;
+  return p;
+}
+
 template <int MODE>
-cudaError_t launch_mode(const GemmLaunch& g, const CUtensorMap& tw, const CUtensorMap& tt,
-                        const GemmArgs& a, cudaStream_t st) {
+cudaError_t launch_mode(const LayerLaunch& g, const CUtensorMap* maps, const LayerArgs& a,
+                        cudaStream_t st) {
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t err = cudaFuncSetAttribute(moe_gemm_kernel<MODE>,
+    cudaError_t err = cudaFuncSetAttribute(moe_layer_kernel<MODE>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)kSmemBytes);
     if (err != cudaSuccess) return err;
     attr_set = true;
   }
-  return launch_pdl(moe_gemm_kernel<MODE>, dim3(kBlocksPerSM * g.num_sms), dim3(kThreads),
-                    kSmemBytes, st, tw, tt, a);
+  return launch_pdl(moe_layer_kernel<MODE>, dim3(kBlocksPerSM * g.num_sms), dim3(kThreads),
+                    kSmemBytes, st, maps[0], maps[1], maps[2], maps[3], a);
 }
 
 }  // namespace
 
-cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t st) {
-  CUtensorMap tw, tt;
-  const uint64_t row_bytes = (uint64_t)g.K / 2;
-  cudaError_t err =
-      make_tmap(&tw, g.w_codes, row_bytes, (uint64_t)g.shape.E * g.rows_per_expert, kBM);
-  if (err != cudaSuccess) return err;
-  err = make_tmap(&tt, g.t_codes, row_bytes, (uint64_t)g.R_cap, kBBoxRows);
-  if (err != cudaSuccess) return err;
-  GemmArgs a;
-  a.w_sf = g.w_sf;
-  a.t_sf = g.t_sf;
-  a.rows_per_expert = g.rows_per_expert;
-  a.K = g.K;
-  a.m_tiles = g.rows_per_expert / kBM;
-  a.H = g.shape.H;
-  a.I = g.shape.I;
+cudaError_t launch_layer(const LayerLaunch& g, cudaStream_t st) {
+  const Shape& s = g.shape;
+  CUtensorMap maps[4];
+  cudaError_t err;
+  if ((err = make_tmap(&maps[0], g.w1_codes, (uint64_t)s.H / 2, (uint64_t)s.E * 2 * s.I, kBM)) ||
+      (err = make_tmap(&maps[1], g.ws.xb, (uint64_t)s.H / 2, (uint64_t)g.R_cap, kBBoxRows)) ||
+      (err = make_tmap(&maps[2], g.w2_codes, (uint64_t)s.I / 2, (uint64_t)s.E * s.H, kBM)) ||
+      (err = make_tmap(&maps[3], g.ws.hb, (uint64_t)s.I / 2, (uint64_t)g.R_cap, kBBoxRows)))
+    return err;
+  LayerArgs a;
+  a.ph[0] = phase_args(g.w1_sf, g.ws.xsf, 2 * s.I, s.H);
+  a.ph[1] = phase_args(g.w2_sf, g.ws.hsf, s.H, s.I);
+  a.num_phases = g.num_phases;
+  a.H = s.H;
+  a.I = s.I;
+  a.T = g.T;
   a.ws = g.ws;
   a.gate_up_debug = g.gate_up_debug;
-  switch (g.mode) {
-    case kGemmSwiglu: return launch_mode<kGemmSwiglu>(g, tw, tt, a, st);
-    case kGemmCombine: return launch_mode<kGemmCombine>(g, tw, tt, a, st);
-    default: return launch_mode<kGemmRaw>(g, tw, tt, a, st);
-  }
+  return g.num_phases == 2 ? launch_mode<kModeLayer>(g, maps, a, st)
+                           : launch_mode<kModeRaw>(g, maps, a, st);
 }
 
 }  // namespace mxmoe

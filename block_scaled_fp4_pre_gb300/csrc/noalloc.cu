@@ -5,8 +5,8 @@
 // plan every device buffer up front and forbid allocation afterwards, and
 // latency-critical threads for which cudaMalloc's implicit device-wide
 // synchronisation is unacceptable.  They pass only their inputs and outputs; the
-// bucketing kernel's other buffers (segment starts, tile list, per-row slot tables,
-// error flags) live in g_bucket_scratch below.  The kernel is the same one
+// bucketing kernel's other buffers (segment starts, tile list and tile counters,
+// per-row slot tables, flags) live in g_bucket_scratch below.  The kernel is the same one
 // moe_pre_dispatch launches; only where its scratch lives differs.
 #include <cuda_runtime.h>
 
@@ -29,7 +29,8 @@ constexpr size_t align256(size_t v) { return (v + 255) / 256 * 256; }
 constexpr size_t kOffFlags = 0;
 constexpr size_t kOffSeg = kOffFlags + align256(64 * sizeof(int32_t));
 constexpr size_t kOffTiles = kOffSeg + align256((kMaxExperts + 1) * sizeof(int32_t));
-constexpr size_t kOffSlotToken = kOffTiles + align256(kMaxTiles * sizeof(int4));
+constexpr size_t kOffTileDone = kOffTiles + align256(kMaxTiles * sizeof(int4));
+constexpr size_t kOffSlotToken = kOffTileDone + align256(kMaxTiles * sizeof(int32_t));
 constexpr size_t kOffSlotAssign = kOffSlotToken + align256(kMaxRows * sizeof(int32_t));
 constexpr size_t kOffSlotWeight = kOffSlotAssign + align256(kMaxRows * sizeof(int32_t));
 constexpr size_t kScratchBytes = kOffSlotWeight + align256(kMaxRows * sizeof(float));  // ~0.5 MiB
@@ -103,6 +104,7 @@ extern "C" moe_status moe_bucket_noalloc(const moe_dims* dims, const int32_t* to
   p.counts = counts_dev;
   p.seg = reinterpret_cast<int32_t*>(base + kOffSeg);
   p.tiles = reinterpret_cast<int4*>(base + kOffTiles);
+  p.tile_done = reinterpret_cast<int32_t*>(base + kOffTileDone);
   p.assign_slot = assign_slot_dev;
   p.slot_token = reinterpret_cast<int32_t*>(base + kOffSlotToken);
   p.slot_assign = reinterpret_cast<int32_t*>(base + kOffSlotAssign);

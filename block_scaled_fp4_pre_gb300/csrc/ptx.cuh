@@ -76,6 +76,18 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
+// ---- global-memory ordering ---------------------------------------------------
+__device__ __forceinline__ int ld_acquire(const int32_t* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+// Orders this thread's generic-proxy global accesses with its async-proxy (TMA)
+// accesses to global memory.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // ---- L2 cache policies -----------------------------------------------------
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
