@@ -63,6 +63,8 @@ WsLayout ws_layout(const moe_dims& d) {
   L.off_tiles = take((size_t)L.tiles_cap * 16);
   L.off_tile_done = take((size_t)L.tiles_cap * 4);
   L.off_assign = take((size_t)L.A_cap * 4);
+  L.off_local_rank = take((size_t)L.A_cap * 4);
+  L.off_blk_base = take((size_t)(L.A_cap / kBucketChunk + 1) * E * 4);
   L.off_slot_token = take((size_t)L.R_cap * 4);
   L.off_slot_assign = take((size_t)L.R_cap * 4);
   L.off_slot_weight = take((size_t)L.R_cap * 4);
@@ -88,6 +90,8 @@ WsPtrs ws_ptrs(void* ws, const WsLayout& L) {
   p.tiles = reinterpret_cast<int4*>(b + L.off_tiles);
   p.tile_done = reinterpret_cast<int32_t*>(b + L.off_tile_done);
   p.assign_slot = reinterpret_cast<int32_t*>(b + L.off_assign);
+  p.local_rank = reinterpret_cast<int32_t*>(b + L.off_local_rank);
+  p.blk_base = reinterpret_cast<int32_t*>(b + L.off_blk_base);
   p.slot_token = reinterpret_cast<int32_t*>(b + L.off_slot_token);
   p.slot_assign = reinterpret_cast<int32_t*>(b + L.off_slot_assign);
   p.slot_weight = reinterpret_cast<float*>(b + L.off_slot_weight);
@@ -231,12 +235,12 @@ moe_status pre_dispatch_impl(const moe_dims* d, const void* x, const int32_t* id
   cudaError_t e;
   {
     ProfScope ps("bucket", st);
-    e = launch_bucket(s, ids, tw, T, p, st);
+    e = launch_bucket(s, ids, T, p, st);
   }
   if (e != cudaSuccess) return cuda_fail(e, "bucket kernel");
   {
     ProfScope ps("quantize_scatter", st);
-    e = launch_quantize_scatter(s, x, T, p, st);
+    e = launch_quantize_scatter(s, x, ids, tw, T, p, st);
   }
   if (e != cudaSuccess) return cuda_fail(e, "quantize kernel");
   return MOE_OK;

@@ -34,6 +34,11 @@ constexpr int kFlagTiles = 1;
 constexpr int kFlagValid = 2;
 constexpr int kFlagSched = 3;
 constexpr int kFlagExit = 4;
+constexpr int kFlagBucketTicket = 5;   // blocks of the bucketing kernel done
+constexpr int kFlagBucketBad = 6;      // ids outside [0, E) seen by the bucketing kernel
+
+// Assignments (t*k + j) ranked by one block of the bucketing kernel.
+constexpr int kBucketChunk = 8192;
 
 // Bounded waits give up after this many nanoseconds of %globaltimer.
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
@@ -59,6 +64,7 @@ __host__ __device__ __forceinline__ int gate_up_source_row(int r, int I) {
 struct WsLayout {
   int64_t T_cap, A_cap, R_cap, tiles_cap;
   size_t off_header, off_flags, off_counts, off_seg, off_tiles, off_tile_done, off_assign,
+      off_local_rank, off_blk_base,
       off_slot_token, off_slot_assign, off_slot_weight, off_xb, off_xsf, off_hb,
       off_hsf, off_acc, off_stage_x, off_stage_ids, off_stage_w, off_stage_out, total;
 };
@@ -70,6 +76,8 @@ struct WsPtrs {
   int4* tiles;           // [tiles_cap] (expert, first row, rows, 0)
   int32_t* tile_done;    // [tiles_cap] gate/up items finished per token tile
   int32_t* assign_slot;  // [A_cap] workspace row of assignment t*k+j, -1 if skipped
+  int32_t* local_rank;   // [A_cap] rank of an assignment among its expert's, in its chunk
+  int32_t* blk_base;     // [A_cap/kBucketChunk + 1][E] rows of an expert in earlier chunks
   int32_t* slot_token;   // [R_cap]
   int32_t* slot_assign;  // [R_cap]
   float* slot_weight;    // [R_cap]
@@ -110,10 +118,16 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 // ---------------------------------------------------------------------------
 // Launchers implemented in dispatch.cu / gemm.cu.  Each returns the cudaError_t
 // of its launch.
-cudaError_t launch_bucket(const Shape& s, const int32_t* ids, const float* tw, int T,
-                          const WsPtrs& ws, cudaStream_t st);
-cudaError_t launch_quantize_scatter(const Shape& s, const void* x, int T, const WsPtrs& ws,
-                                    cudaStream_t st);
+// Bucketing: per-expert counts and segment starts, the tile list, and each
+// assignment's rank; the quantiser (or launch_assign_slots) turns ranks into rows.
+cudaError_t launch_bucket(const Shape& s, const int32_t* ids, int T, const WsPtrs& ws,
+                          cudaStream_t st);
+// Quantise the tokens, give every assignment its row and copy the token there.
+cudaError_t launch_quantize_scatter(const Shape& s, const void* x, const int32_t* ids,
+                                    const float* tw, int T, const WsPtrs& ws, cudaStream_t st);
+// Rows of all assignments and the per-row tables, without quantising anything.
+cudaError_t launch_assign_slots(const Shape& s, const int32_t* ids, const float* tw, int T,
+                                const WsPtrs& ws, cudaStream_t st);
 // acc [n] fp32 -> out [n] bf16 (round to nearest even), clearing acc.
 cudaError_t launch_convert_out(float* acc, void* out, int64_t n, cudaStream_t st);
 cudaError_t launch_quantize_rows(const float* src, int64_t rows, int K, uint8_t* codes,

@@ -17,39 +17,65 @@ namespace {
 constexpr unsigned kFull = 0xFFFFFFFFu;
 
 // ---------------------------------------------------------------------------
-// Bucketing: one block of 32 warps.  Warp w owns the contiguous assignment range
-// [w*per, (w+1)*per) of a = t*k + j (ascending t, then j), so concatenating the
-// warps' ranges in warp order keeps that order.  Counts per (warp, expert) are
-// order-free shared-memory atomics; a per-expert scan over warps gives each warp
-// its base inside the expert; warp 0 scans the experts (segment starts padded to
-// kBN rows, and tile starts); finally every warp walks its range 32 assignments at
-// a time and ranks equal experts inside the chunk with __match_any_sync.
-__global__ void __launch_bounds__(1024) bucket_kernel(const int32_t* __restrict__ ids,
-                                                      const float* __restrict__ tw, int T, int k,
-                                                      int E, WsPtrs ws) {
+// Bucketing.  Block b ranks the assignments a = t*k + j of chunk b (kBucketChunk of
+// them, ascending a, i.e. ascending t then j) among those of the same expert:
+// warp w owns a contiguous run of the chunk, walked 32 at a time; lanes holding the
+// same expert are found with one ballot per bit of the expert id, the lowest of
+// them advances the warp's count for that expert, and a scan over warps turns the
+// counts into each warp's base.  Each block publishes its per-expert totals; the
+// last block to finish scans them over blocks (bases of later chunks) and over
+// experts (segment starts padded to kBN rows, tile list).  Row of an assignment =
+// segment start + its chunk's base + its rank in the chunk.
+
+// Lanes whose key equals this lane's key (keys < 2^nbits).
+__device__ __forceinline__ unsigned peers_of(int key, int nbits) {
+  unsigned m = kFull;
+  for (int b = 0; b < nbits; ++b) {
+    const bool bit = (key >> b) & 1;
+    const unsigned bal = __ballot_sync(kFull, bit);
+    m &= bit ? bal : ~bal;
+  }
+  return m;
+}
+
+__global__ void __launch_bounds__(1024) bucket_kernel(const int32_t* __restrict__ ids, int T,
+                                                      int k, int E, WsPtrs ws) {
   extern __shared__ int32_t sh[];
-  int32_t* cnt = sh;             // [32][E]
-  int32_t* tot = cnt + 32 * E;   // [E]
-  int32_t* seg = tot + E;        // [E+1]
-  int32_t* tst = seg + E + 1;    // [E+1]
+  int32_t* cnt = sh;                        // [32][E] per-warp counts, then bases
+  int32_t* key_sh = cnt + 32 * E;           // [kBucketChunk] expert id, E if invalid
   __shared__ int32_t bad;
+  __shared__ int32_t is_last;
 
   ptx::pdl_launch_dependents();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int A = T * k;
-  const int per = (A + 31) / 32;
-  const int a0 = min(A, warp * per), a1 = min(A, a0 + per);
+  const int c0 = blockIdx.x * kBucketChunk;
+  const int len = min(kBucketChunk, A - c0);
+  // per-warp runs are whole multiples of 32 so that every round is one aligned chunk
+  const int per = ((len + 32 * 32 - 1) / (32 * 32)) * 32;
+  const int w0 = min(len, warp * per), w1 = min(len, w0 + per);
+  int nbits = 1;
+  while ((1 << nbits) <= E + 1) ++nbits;  // keys 0..E+1
 
   for (int i = tid; i < 32 * E; i += blockDim.x) cnt[i] = 0;
+  for (int i = tid; i < len; i += blockDim.x) {
+    const int e = ids[c0 + i];
+    key_sh[i] = (e >= 0 && e < E) ? e : E;
+  }
   if (tid == 0) bad = 0;
   __syncthreads();
 
-  for (int a = a0 + lane; a < a1; a += 32) {
-    const int e = ids[a];
-    if (e >= 0 && e < E)
-      atomicAdd(&cnt[warp * E + e], 1);
-    else
-      atomicAdd(&bad, 1);
+  const unsigned lt_mask = (1u << lane) - 1u;
+  for (int base = w0; base < w1; base += 32) {
+    const int i = base + lane;
+    const int key = i < w1 ? key_sh[i] : E + 1;
+    const unsigned peers = peers_of(key, nbits);
+    if ((peers & lt_mask) == 0) {  // lowest lane of its group
+      if (key < E)
+        cnt[warp * E + key] += __popc(peers);
+      else if (key == E)
+        atomicAdd(&bad, __popc(peers));
+    }
   }
   __syncthreads();
 
@@ -58,6 +84,44 @@ __global__ void __launch_bounds__(1024) bucket_kernel(const int32_t* __restrict_
     for (int w = 0; w < 32; ++w) {
       const int c = cnt[w * E + e];
       cnt[w * E + e] = run;
+      run += c;
+    }
+    ws.blk_base[(size_t)blockIdx.x * E + e] = run;  // this chunk's total, for now
+  }
+  __syncthreads();
+
+  for (int base = w0; base < w1; base += 32) {
+    const int i = base + lane;
+    const int key = i < w1 ? key_sh[i] : E + 1;
+    const unsigned peers = peers_of(key, nbits);
+    const int rank = __popc(peers & lt_mask);
+    if (key < E) ws.local_rank[c0 + i] = cnt[warp * E + key] + rank;
+    __syncwarp();
+    if (key < E && rank == 0) cnt[warp * E + key] += __popc(peers);
+    __syncwarp();
+  }
+
+  // Publish this chunk's totals; the last block to finish does the global scans.
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    if (bad) atomicAdd(&ws.flags[kFlagBucketBad], bad);
+    is_last = atomicAdd(&ws.flags[kFlagBucketTicket], 1) == (int)gridDim.x - 1;
+  }
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+
+  int32_t* tot = cnt;            // [E]   (per-warp counts are no longer needed)
+  int32_t* seg = tot + E;        // [E+1]
+  int32_t* tst = seg + E + 1;    // [E+1]
+  const int nblk = gridDim.x;
+  for (int e = tid; e < E; e += blockDim.x) {
+    int run = 0;
+    for (int b = 0; b < nblk; ++b) {
+      int32_t* p = ws.blk_base + (size_t)b * E + e;
+      const int c = __ldcg(p);
+      *p = run;
       run += c;
     }
     tot[e] = run;
@@ -94,28 +158,6 @@ __global__ void __launch_bounds__(1024) bucket_kernel(const int32_t* __restrict_
   }
   __syncthreads();
 
-  const unsigned lt_mask = (1u << lane) - 1u;
-  for (int base = a0; base < a1; base += 32) {
-    const int a = base + lane;
-    const bool in = a < a1;
-    const int e = in ? ids[a] : -1;
-    const bool ok = in && e >= 0 && e < E;
-    const unsigned peers = __match_any_sync(kFull, ok ? e : -1);
-    const int rank = __popc(peers & lt_mask);
-    if (ok) {
-      const int slot = seg[e] + cnt[warp * E + e] + rank;
-      ws.assign_slot[a] = slot;
-      ws.slot_token[slot] = a / k;
-      ws.slot_assign[slot] = a;
-      ws.slot_weight[slot] = tw[a];
-    } else if (in) {
-      ws.assign_slot[a] = -1;
-    }
-    __syncwarp();
-    if (ok && rank == 0) cnt[warp * E + e] += __popc(peers);
-    __syncwarp();
-  }
-
   for (int e = tid; e < E; e += blockDim.x) {
     const int n = tot[e];
     ws.counts[e] = n;
@@ -126,22 +168,50 @@ __global__ void __launch_bounds__(1024) bucket_kernel(const int32_t* __restrict_
     }
   }
   if (tid == 0) {
+    const int bad_all = __ldcg(&ws.flags[kFlagBucketBad]);
     ws.seg[E] = seg[E];
     ws.flags[kFlagTiles] = tst[E];
-    ws.flags[kFlagValid] = A - bad;
+    ws.flags[kFlagValid] = A - bad_all;
     ws.flags[kFlagSched] = 0;
     ws.flags[kFlagExit] = 0;
-    if (bad) atomicOr(&ws.flags[0], kErrRouting);
+    ws.flags[kFlagBucketTicket] = 0;
+    ws.flags[kFlagBucketBad] = 0;
+    if (bad_all) atomicOr(&ws.flags[0], kErrRouting);
   }
+}
+
+// Row of assignment a (or -1 for an id outside [0, E)), and the per-row tables.
+__device__ __forceinline__ int assign_slot(int a, int k, int E, const int32_t* __restrict__ ids,
+                                           const float* __restrict__ tw, const WsPtrs& ws) {
+  const int e = ids[a];
+  int slot = -1;
+  if (e >= 0 && e < E) {
+    slot = ws.seg[e] + ws.blk_base[(size_t)(a / kBucketChunk) * E + e] + ws.local_rank[a];
+    ws.slot_token[slot] = a / k;
+    ws.slot_assign[slot] = a;
+    ws.slot_weight[slot] = tw[a];
+  }
+  ws.assign_slot[a] = slot;
+  return slot;
+}
+
+__global__ void assign_slots_kernel(const int32_t* __restrict__ ids, const float* __restrict__ tw,
+                                    int A, int k, int E, WsPtrs ws) {
+  ptx::pdl_wait();
+  for (int a = blockIdx.x * blockDim.x + threadIdx.x; a < A; a += gridDim.x * blockDim.x)
+    assign_slot(a, k, E, ids, tw, ws);
 }
 
 // ---------------------------------------------------------------------------
 // Quantise one token row per block and scatter it to the token's k workspace rows.
 // A thread owns 8 consecutive elements; 4 adjacent threads form one 32-group.
 // The row is quantised into shared memory while the bucketing kernel may still be
-// running; the block then waits for it and copies the row to each of the token's k slots.
+// running; the block then waits for it, gives the token's k assignments their rows
+// and copies the row to each of them.
 __global__ void __launch_bounds__(256) quantize_scatter_kernel(const __nv_bfloat16* __restrict__ x,
-                                                               int H, int k, WsPtrs ws) {
+                                                               const int32_t* __restrict__ ids,
+                                                               const float* __restrict__ tw,
+                                                               int H, int k, int E, WsPtrs ws) {
   extern __shared__ __align__(16) uint8_t qsh[];       // [H/2 codes | H/32 scales]
   __shared__ int32_t slots[32];
   uint8_t* codes_sh = qsh;
@@ -171,7 +241,7 @@ __global__ void __launch_bounds__(256) quantize_scatter_kernel(const __nv_bfloat
     if ((tid & 3) == 0) sf_sh[base / 32] = (uint8_t)(e + 127);
   }
   ptx::pdl_wait();
-  if (tid < k) slots[tid] = ws.assign_slot[(size_t)t * k + tid];
+  if (tid < k) slots[tid] = assign_slot(t * k + tid, k, E, ids, tw, ws);
   __syncthreads();
   const int kc4 = H / 128;
   const size_t row_bytes = (size_t)H / 2;
@@ -281,20 +351,28 @@ unsigned grid_for(int64_t work, int block, int64_t cap) {
 
 }  // namespace
 
-cudaError_t launch_bucket(const Shape& s, const int32_t* ids, const float* tw, int T,
-                          const WsPtrs& ws, cudaStream_t st) {
-  const size_t smem = (size_t)(32 * s.E + 3 * s.E + 2) * sizeof(int32_t);
+cudaError_t launch_bucket(const Shape& s, const int32_t* ids, int T, const WsPtrs& ws,
+                          cudaStream_t st) {
+  const size_t smem = ((size_t)32 * s.E + kBucketChunk) * sizeof(int32_t);
   cudaError_t err = cudaFuncSetAttribute(bucket_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
   if (err != cudaSuccess) return err;
-  bucket_kernel<<<1, 1024, smem, st>>>(ids, tw, T, s.k, s.E, ws);
+  const int A = T * s.k;
+  bucket_kernel<<<(A + kBucketChunk - 1) / kBucketChunk, 1024, smem, st>>>(ids, T, s.k, s.E, ws);
   return cudaGetLastError();
 }
 
-cudaError_t launch_quantize_scatter(const Shape& s, const void* x, int T, const WsPtrs& ws,
-                                    cudaStream_t st) {
+cudaError_t launch_quantize_scatter(const Shape& s, const void* x, const int32_t* ids,
+                                    const float* tw, int T, const WsPtrs& ws, cudaStream_t st) {
   return launch_pdl(quantize_scatter_kernel, dim3(T), dim3(256), (size_t)s.H / 2 + s.H / 32, st,
-                    reinterpret_cast<const __nv_bfloat16*>(x), s.H, s.k, ws);
+                    reinterpret_cast<const __nv_bfloat16*>(x), ids, tw, s.H, s.k, s.E, ws);
+}
+
+cudaError_t launch_assign_slots(const Shape& s, const int32_t* ids, const float* tw, int T,
+                                const WsPtrs& ws, cudaStream_t st) {
+  const int A = T * s.k;
+  return launch_pdl(assign_slots_kernel, dim3(grid_for(A, 256, 4096)), dim3(256), 0, st, ids, tw,
+                    A, s.k, s.E, ws);
 }
 
 cudaError_t launch_convert_out(float* acc, void* out, int64_t n, cudaStream_t st) {

@@ -5,9 +5,10 @@
 // plan every device buffer up front and forbid allocation afterwards, and
 // latency-critical threads for which cudaMalloc's implicit device-wide
 // synchronisation is unacceptable.  They pass only their inputs and outputs; the
-// bucketing kernel's other buffers (segment starts, tile list and tile counters,
-// per-row slot tables, flags) live in g_bucket_scratch below.  The kernel is the same one
-// moe_pre_dispatch launches; only where its scratch lives differs.
+// bucketing kernels' other buffers (segment starts, tile list and tile counters,
+// per-chunk ranks and bases, per-row slot tables, flags) live in g_bucket_scratch
+// below.  The kernels are the ones moe_pre_dispatch launches; only where their
+// scratch lives differs.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -18,8 +19,8 @@
 namespace mxmoe {
 namespace {
 
-// Limits of the static scratch: at most 8192 assignments (num_tokens * topk) and
-// 256 experts per call.
+// Limits of the static scratch: at most 8192 assignments (num_tokens * topk, one
+// chunk of the bucketing kernel) and 256 experts per call.
 constexpr int64_t kMaxAssignments = 8192;
 constexpr int64_t kMaxExperts = 256;
 constexpr int64_t kMaxRows = kMaxAssignments + (int64_t)kBN * kMaxExperts;
@@ -30,7 +31,9 @@ constexpr size_t kOffFlags = 0;
 constexpr size_t kOffSeg = kOffFlags + align256(64 * sizeof(int32_t));
 constexpr size_t kOffTiles = kOffSeg + align256((kMaxExperts + 1) * sizeof(int32_t));
 constexpr size_t kOffTileDone = kOffTiles + align256(kMaxTiles * sizeof(int4));
-constexpr size_t kOffSlotToken = kOffTileDone + align256(kMaxTiles * sizeof(int32_t));
+constexpr size_t kOffLocalRank = kOffTileDone + align256(kMaxTiles * sizeof(int32_t));
+constexpr size_t kOffBlkBase = kOffLocalRank + align256(kMaxAssignments * sizeof(int32_t));
+constexpr size_t kOffSlotToken = kOffBlkBase + align256(kMaxExperts * sizeof(int32_t));
 constexpr size_t kOffSlotAssign = kOffSlotToken + align256(kMaxRows * sizeof(int32_t));
 constexpr size_t kOffSlotWeight = kOffSlotAssign + align256(kMaxRows * sizeof(int32_t));
 constexpr size_t kScratchBytes = kOffSlotWeight + align256(kMaxRows * sizeof(float));  // ~0.5 MiB
@@ -105,12 +108,16 @@ extern "C" moe_status moe_bucket_noalloc(const moe_dims* dims, const int32_t* to
   p.seg = reinterpret_cast<int32_t*>(base + kOffSeg);
   p.tiles = reinterpret_cast<int4*>(base + kOffTiles);
   p.tile_done = reinterpret_cast<int32_t*>(base + kOffTileDone);
+  p.local_rank = reinterpret_cast<int32_t*>(base + kOffLocalRank);
+  p.blk_base = reinterpret_cast<int32_t*>(base + kOffBlkBase);
   p.assign_slot = assign_slot_dev;
   p.slot_token = reinterpret_cast<int32_t*>(base + kOffSlotToken);
   p.slot_assign = reinterpret_cast<int32_t*>(base + kOffSlotAssign);
   p.slot_weight = reinterpret_cast<float*>(base + kOffSlotWeight);
   const Shape shape{dims->hidden, dims->inter, dims->num_experts, dims->topk};
-  e = launch_bucket(shape, topk_ids_dev, topk_weights_dev, num_tokens, p, st);
+  e = launch_bucket(shape, topk_ids_dev, num_tokens, p, st);
+  if (e != cudaSuccess) return fail(MOE_ERR_CUDA, cudaGetErrorString(e));
+  e = launch_assign_slots(shape, topk_ids_dev, topk_weights_dev, num_tokens, p, st);
   if (e != cudaSuccess) return fail(MOE_ERR_CUDA, cudaGetErrorString(e));
   return MOE_OK;
 }
