@@ -62,6 +62,7 @@ WsLayout ws_layout(const moe_dims& d) {
   L.off_seg = take((size_t)(E + 1) * 4);
   L.off_tiles = take((size_t)L.tiles_cap * 16);
   L.off_tile_done = take((size_t)L.tiles_cap * 4);
+  L.off_tile_start = take((size_t)(E + 1) * 4);
   L.off_assign = take((size_t)L.A_cap * 4);
   L.off_local_rank = take((size_t)L.A_cap * 4);
   L.off_blk_base = take((size_t)(L.A_cap / kBucketChunk + 1) * E * 4);
@@ -89,6 +90,7 @@ WsPtrs ws_ptrs(void* ws, const WsLayout& L) {
   p.seg = reinterpret_cast<int32_t*>(b + L.off_seg);
   p.tiles = reinterpret_cast<int4*>(b + L.off_tiles);
   p.tile_done = reinterpret_cast<int32_t*>(b + L.off_tile_done);
+  p.tile_start = reinterpret_cast<int32_t*>(b + L.off_tile_start);
   p.assign_slot = reinterpret_cast<int32_t*>(b + L.off_assign);
   p.local_rank = reinterpret_cast<int32_t*>(b + L.off_local_rank);
   p.blk_base = reinterpret_cast<int32_t*>(b + L.off_blk_base);

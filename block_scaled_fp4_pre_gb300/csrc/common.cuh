@@ -64,7 +64,7 @@ __host__ __device__ __forceinline__ int gate_up_source_row(int r, int I) {
 struct WsLayout {
   int64_t T_cap, A_cap, R_cap, tiles_cap;
   size_t off_header, off_flags, off_counts, off_seg, off_tiles, off_tile_done, off_assign,
-      off_local_rank, off_blk_base,
+      off_local_rank, off_blk_base, off_tile_start,
       off_slot_token, off_slot_assign, off_slot_weight, off_xb, off_xsf, off_hb,
       off_hsf, off_acc, off_stage_x, off_stage_ids, off_stage_w, off_stage_out, total;
 };
@@ -73,7 +73,8 @@ struct WsPtrs {
   int32_t* flags;        // error bits and counters, see kFlag*
   int32_t* counts;       // [E]
   int32_t* seg;          // [E+1] first workspace row of each expert (multiples of kBN)
-  int4* tiles;           // [tiles_cap] (expert, first row, rows, 0)
+  int4* tiles;           // [tiles_cap] (expert, first row, rows, 0), experts in order
+  int32_t* tile_start;   // [E+1] first tile of each expert (exclusive prefix of tiles)
   int32_t* tile_done;    // [tiles_cap] gate/up items finished per token tile
   int32_t* assign_slot;  // [A_cap] workspace row of assignment t*k+j, -1 if skipped
   int32_t* local_rank;   // [A_cap] rank of an assignment among its expert's, in its chunk

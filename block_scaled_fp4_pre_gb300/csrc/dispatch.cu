@@ -158,6 +158,7 @@ __global__ void __launch_bounds__(1024) bucket_kernel(const int32_t* __restrict_
   }
   __syncthreads();
 
+  for (int e = tid; e <= E; e += blockDim.x) ws.tile_start[e] = tst[e];
   for (int e = tid; e < E; e += blockDim.x) {
     const int n = tot[e];
     ws.counts[e] = n;

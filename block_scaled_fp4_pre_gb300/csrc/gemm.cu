@@ -15,8 +15,10 @@
 // are the N operand (N = 32..128), so one instruction shape serves a decode load of
 // a few tokens per expert as well as a prefill tile of 128 tokens.
 //
-// Work items are (token tile, 128-row weight slab): first every gate/up item, token
-// tile by token tile, then every down item.  Blocks take items from a global
+// Work items are (token tile, 128-row weight slab): first every gate/up item, then
+// every down item, each phase ordered expert by expert, then slab by slab, then by
+// the expert's token tiles -- so the tiles of a busy expert take a weight slab in
+// turn while it is in L2, and the expert's token rows stay in L2 for all its slabs.  Blocks take items from a global
 // counter, so all gate/up items are claimed (by running blocks, with no
 // dependencies) before any down item is, and a down item's wait for its tile's
 // intermediate rows always ends -- whatever number of blocks is resident.  The
@@ -61,10 +63,11 @@ struct __align__(8) SmemTail {
   uint64_t mma_done;
   uint64_t ring_full[kRing];
   uint64_t ring_empty[kRing];
-  int4 ring[kRing];          // (item, expert, first row, rows) or item = -1: stop
+  int4 ring[kRing];          // (item, first row, rows | slab << 8, tile); item = -1: stop
   uint32_t tmem_base;
   int abort;
   float xchg[2][4][kEpiCols];
+  int32_t tile_start[1025];   // first tile of each expert (E <= 1024), see decode_item
 };
 
 constexpr size_t kSmemA = 0;
@@ -87,32 +90,48 @@ struct PhaseArgs {
 struct LayerArgs {
   PhaseArgs ph[2];
   int num_phases;
-  int H, I, T;
+  int H, I, T, E;
   WsPtrs ws;
   float* gate_up_debug;
 };
 
 struct Item {
-  int phase, tile, mt;
+  int phase, tile, mt, e, ntiles;
 };
 
-__device__ __forceinline__ Item decode_item(int g, int n0, int m0, int m1) {
+// Item g of the phase-major, expert-major, slab-major, tile-minor order.
+// tile_start[e] is the first tile of expert e (experts without tokens repeat it).
+__device__ __forceinline__ Item decode_item(int g, int n0, int m0, int m1, int E,
+                                            const int32_t* __restrict__ tile_start) {
   Item it;
-  if (g < n0) {
-    it.phase = 0;
-    it.tile = g / m0;
-    it.mt = g % m0;
-  } else {
+  int m = m0;
+  it.phase = 0;
+  if (g >= n0) {
     g -= n0;
+    m = m1;
     it.phase = 1;
-    it.tile = g / m1;
-    it.mt = g % m1;
   }
+  // last expert e with tile_start[e] * m <= g (that expert has tiles)
+  int lo = 0, hi = E - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (tile_start[mid] * m <= g)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  const int t0 = tile_start[lo];
+  it.e = lo;
+  it.ntiles = tile_start[lo + 1] - t0;
+  const int local = g - t0 * m;
+  it.mt = local / it.ntiles;
+  it.tile = t0 + local % it.ntiles;
   return it;
 }
 
+// silu(g) * u with fast exp and divide (a few ulp; well inside the MXFP4 rounding)
 __device__ __forceinline__ float silu_times(float g, float u) {
-  return g / (1.0f + expf(-g)) * u;
+  return __fdividef(g, 1.0f + __expf(-g)) * u;
 }
 
 // Waits until *p >= target (acquire), bounded like the mbarrier waits.
@@ -175,6 +194,10 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
   ptx::pdl_wait();
 
   const int num_tiles = args.ws.flags[kFlagTiles];
+  const int E = args.E;
+  const int32_t* tile_start = tail->tile_start;
+  for (int e = threadIdx.x; e <= E; e += blockDim.x) tail->tile_start[e] = args.ws.tile_start[e];
+  __syncthreads();
   const int m0 = args.ph[0].m_tiles, m1 = args.ph[1].m_tiles;
   const int n0 = num_tiles * m0;
   const int total = n0 + (args.num_phases == 2 ? num_tiles * m1 : 0);
@@ -182,24 +205,29 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
   if (warp == 0) {
     // ------------------------------------------------- scheduler + producer
     if (lane == 0) {
-      const uint64_t pol_w = ptx::policy_evict_first();
+      const uint64_t pol_once = ptx::policy_evict_first();
+      const uint64_t pol_shared = ptx::policy_evict_normal();
       const uint64_t pol_t = ptx::policy_evict_last();
       int stage = 0, r = 0;
       uint32_t phase = 0, rph = 0;
       int64_t issued = 0;
       bool ok = true;
-      // Items are claimed one ahead so that the claim and the tile-table read of
-      // the next item overlap the loads of the current one.
+      // Items are claimed one ahead so that the claim and the table reads of the
+      // next item overlap the loads of the current one.
       int g = atomicAdd(&args.ws.flags[kFlagSched], 1);
+      Item it = {};
       int4 ti = make_int4(0, 0, 0, 0);
-      if (g < total) ti = args.ws.tiles[decode_item(g, n0, m0, m1).tile];
+      if (g < total) {
+        it = decode_item(g, n0, m0, m1, E, tile_start);
+        ti = args.ws.tiles[it.tile];
+      }
       while (true) {
         const int item = g < total ? g : -1;
         if (!ptx::mbar_wait(&tail->ring_empty[r], rph ^ 1u, abort_flag, kWaitLimitNs)) {
           ok = false;
           break;
         }
-        tail->ring[r] = make_int4(item, ti.x, ti.y, ti.z);
+        tail->ring[r] = make_int4(item, ti.y, ti.z | (it.mt << 8), it.tile);
         ptx::mbar_arrive(&tail->ring_full[r]);
         if (++r == kRing) {
           r = 0;
@@ -207,12 +235,15 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
         }
         if (item < 0) break;
         const int g_next = atomicAdd(&args.ws.flags[kFlagSched], 1);
+        Item it_next = {};
         int4 ti_next = make_int4(0, 0, 0, 0);
-        const Item it = decode_item(item, n0, m0, m1);
         const PhaseArgs& P = args.ph[it.phase];
         const CUtensorMap* tw = it.phase ? &tmap_w2 : &tmap_w1;
         const CUtensorMap* tt = it.phase ? &tmap_h : &tmap_x;
-        const int e = ti.x, row0 = ti.y, n = ti.z;
+        // A slab read by one token tile only is not kept; one shared by several
+        // tiles of the expert stays for them.
+        const uint64_t pol_w = it.ntiles > 1 ? pol_shared : pol_once;
+        const int e = it.e, row0 = ti.y, n = ti.z;
         const int nb = (n + kBBoxRows - 1) / kBBoxRows;
         const int wrow = e * P.rows_per_expert + it.mt * kBM;
         const uint8_t* wsf = P.w_sf + ((size_t)(e * P.m_tiles + it.mt) * P.kc4) * kSFAtomBytes;
@@ -251,10 +282,14 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
             stage = 0;
             phase ^= 1u;
           }
-          if (kb == 0 && g_next < total) ti_next = args.ws.tiles[decode_item(g_next, n0, m0, m1).tile];
+          if (kb == 0 && g_next < total) {
+            it_next = decode_item(g_next, n0, m0, m1, E, tile_start);
+            ti_next = args.ws.tiles[it_next.tile];
+          }
         }
         if (!ok) break;
         g = g_next;
+        it = it_next;
         ti = ti_next;
       }
       if (!ok) atomicOr(&args.ws.flags[0], kErrTimeout);
@@ -287,9 +322,8 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
         }
         const int item = rec.x;
         if (item < 0) break;
-        const Item it = decode_item(item, n0, m0, m1);
-        const PhaseArgs& P = args.ph[it.phase];
-        const int n = rec.w;
+        const PhaseArgs& P = args.ph[item < n0 ? 0 : 1];
+        const int n = rec.z & 0xFF;
         const int n_mma = (n + kBBoxRows - 1) / kBBoxRows * kBBoxRows;
         if (!ptx::mbar_wait(&tail->acc_empty, acc_phase ^ 1u, abort_flag, kWaitLimitNs)) {
           ok = false;
@@ -359,8 +393,8 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
       }
       const int item = rec.x;
       if (item < 0) break;
-      const Item it = decode_item(item, n0, m0, m1);
-      const int row0 = rec.z, n = rec.w, mt = it.mt;
+      const int item_phase = item < n0 ? 0 : 1;
+      const int row0 = rec.y, n = rec.z & 0xFF, mt = rec.z >> 8, item_tile = rec.w;
       if (!ptx::mbar_wait(&tail->acc_full, acc_phase, abort_flag, kWaitLimitNs)) {
         if (ep_tid == 0) atomicOr(&args.ws.flags[0], kErrTimeout);
         break;
@@ -388,37 +422,46 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
               args.gate_up_debug[(size_t)a * 2 * args.I + col] = v[j];
             }
           }
-        } else if (it.phase == 0) {
+        } else if (item_phase == 0) {
           // Rows of this warp: chunk c of 32 interleaved gate/up rows =
           // [gate even 8 | up even 8 | gate odd 8 | up odd 8] of features c*16..c*16+15.
+          // Columns go in pairs: gate lanes (0-7, 16-23) compute column 2p from their
+          // gate and the up of lane+8, up lanes (8-15, 24-31) column 2p+1 from their up
+          // and the gate of lane-8 -- one exchange, and no lane idles.
           const int c = mt * 4 + q;
+          const bool up_lane = (lane & 8) != 0;
+          float hv[kEpiCols / 2];
 #pragma unroll
-          for (int j = 0; j < kEpiCols; ++j) {
-            if (j < ncol) {
-              const float u = __shfl_down_sync(kFull, v[j], 8);
-              v[j] = (lane & 8) ? 0.f : silu_times(v[j], u);
-              // |h| >= 0, so its bit pattern orders like the value
-              const unsigned a = __reduce_max_sync(kFull, __float_as_uint(fabsf(v[j])));
-              if (lane == 0) tail->xchg[xb][q][j] = __uint_as_float(a);
-            }
+          for (int p = 0; p < kEpiCols / 2; ++p) {
+            const float x = __shfl_xor_sync(kFull, up_lane ? v[2 * p] : v[2 * p + 1], 8);
+            const float h = up_lane ? silu_times(x, v[2 * p + 1]) : silu_times(v[2 * p], x);
+            hv[p] = h;
+            // max |h| over the 16 lanes of this column (lanes differing in bits 0-2, 4)
+            float a = fabsf(h);
+            a = fmaxf(a, __shfl_xor_sync(kFull, a, 1));
+            a = fmaxf(a, __shfl_xor_sync(kFull, a, 2));
+            a = fmaxf(a, __shfl_xor_sync(kFull, a, 4));
+            a = fmaxf(a, __shfl_xor_sync(kFull, a, 16));
+            if ((lane & 23) == 0) tail->xchg[xb][q][2 * p + (up_lane ? 1 : 0)] = a;  // lanes 0, 8
           }
           ptx::named_bar_sync(1, 128);
           const int i_kc4 = args.I / 128;
           const size_t hrow_bytes = (size_t)args.I / 2;
 #pragma unroll
-          for (int j = 0; j < kEpiCols; ++j) {
-            if (j < ncol) {
-              // 32-feature group = this warp's 16 features + the partner warp's 16.
-              const float amax = fmaxf(tail->xchg[xb][q][j], tail->xchg[xb][q ^ 1][j]);
-              const int e = ptx::mx_scale_exponent(amax);
-              const float qv = v[j] * ptx::pow2_neg(e);
-              const float qodd = __shfl_down_sync(kFull, qv, 16);
-              const size_t row = (size_t)row0 + c0 + j;
-              // lanes 0..7 write the 8 consecutive bytes of features c*16..c*16+15
-              if (lane < 8)
-                args.ws.hb[row * hrow_bytes + (size_t)c * 8 + lane] =
-                    (uint8_t)ptx::e2m1x2(qv, qodd);
-              if (lane == 0 && (q & 1) == 0)
+          for (int p = 0; p < kEpiCols / 2; ++p) {
+            const int jc = 2 * p + (up_lane ? 1 : 0);  // this lane's column
+            // 32-feature group = this warp's 16 features + the partner warp's 16.
+            const float amax = fmaxf(tail->xchg[xb][q][jc], tail->xchg[xb][q ^ 1][jc]);
+            const int e = ptx::mx_scale_exponent(amax);
+            const float qv = hv[p] * ptx::pow2_neg(e);
+            const float qodd = __shfl_down_sync(kFull, qv, 16);
+            if (lane < 16 && jc < ncol) {
+              const size_t row = (size_t)row0 + c0 + jc;
+              // lanes 0-7 (column 2p) and 8-15 (column 2p+1) each write the 8 bytes of
+              // features c*16..c*16+15 of their column
+              args.ws.hb[row * hrow_bytes + (size_t)c * 8 + (lane & 7)] =
+                  (uint8_t)ptx::e2m1x2(qv, qodd);
+              if ((lane & 7) == 0 && (q & 1) == 0)
                 args.ws.hsf[sf_atom_offset(row, c >> 1, i_kc4)] = (uint8_t)(e + 127);
             }
           }
@@ -441,13 +484,13 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
           }
         }
       }
-      if (MODE == kModeLayer && it.phase == 0) {
+      if (MODE == kModeLayer && item_phase == 0) {
         // Publish: this item's intermediate rows (and scales) are written.
         __threadfence();
         ptx::named_bar_sync(2, 128);
         if (ep_tid == 0) {
           ptx::fence_proxy_async_global();
-          atomicAdd(&args.ws.tile_done[it.tile], 1);
+          atomicAdd(&args.ws.tile_done[item_tile], 1);
         }
       }
     }
@@ -553,6 +596,7 @@ cudaError_t launch_layer(const LayerLaunch& g, cudaStream_t st) {
   a.H = s.H;
   a.I = s.I;
   a.T = g.T;
+  a.E = s.E;
   a.ws = g.ws;
   a.gate_up_debug = g.gate_up_debug;
   return g.num_phases == 2 ? launch_mode<kModeLayer>(g, maps, a, st)

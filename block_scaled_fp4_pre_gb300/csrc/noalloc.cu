@@ -31,7 +31,8 @@ constexpr size_t kOffFlags = 0;
 constexpr size_t kOffSeg = kOffFlags + align256(64 * sizeof(int32_t));
 constexpr size_t kOffTiles = kOffSeg + align256((kMaxExperts + 1) * sizeof(int32_t));
 constexpr size_t kOffTileDone = kOffTiles + align256(kMaxTiles * sizeof(int4));
-constexpr size_t kOffLocalRank = kOffTileDone + align256(kMaxTiles * sizeof(int32_t));
+constexpr size_t kOffTileStart = kOffTileDone + align256(kMaxTiles * sizeof(int32_t));
+constexpr size_t kOffLocalRank = kOffTileStart + align256((kMaxExperts + 1) * sizeof(int32_t));
 constexpr size_t kOffBlkBase = kOffLocalRank + align256(kMaxAssignments * sizeof(int32_t));
 constexpr size_t kOffSlotToken = kOffBlkBase + align256(kMaxExperts * sizeof(int32_t));
 constexpr size_t kOffSlotAssign = kOffSlotToken + align256(kMaxRows * sizeof(int32_t));
@@ -108,6 +109,7 @@ extern "C" moe_status moe_bucket_noalloc(const moe_dims* dims, const int32_t* to
   p.seg = reinterpret_cast<int32_t*>(base + kOffSeg);
   p.tiles = reinterpret_cast<int4*>(base + kOffTiles);
   p.tile_done = reinterpret_cast<int32_t*>(base + kOffTileDone);
+  p.tile_start = reinterpret_cast<int32_t*>(base + kOffTileStart);
   p.local_rank = reinterpret_cast<int32_t*>(base + kOffLocalRank);
   p.blk_base = reinterpret_cast<int32_t*>(base + kOffBlkBase);
   p.assign_slot = assign_slot_dev;
