@@ -123,9 +123,31 @@ PrepLayout prep_layout(const moe_dims& d) {
 
 Shape shape_of(const moe_dims& d) { return Shape{d.hidden, d.inter, d.num_experts, d.topk}; }
 
-// Workspaces initialised by moe_workspace_init, with the dims they were laid out for.
+// Workspaces initialised by moe_workspace_init, with the dims they were laid out for
+// and whether their accumulator holds a fresh pre_dispatch (cleared rows, no sums
+// yet): moe_pre_dispatch sets it, moe_forward consumes it.
+struct WsState {
+  moe_dims dims;
+  bool dispatched;
+};
 std::mutex g_reg_mu;
-std::map<const void*, moe_dims> g_registry;
+std::map<const void*, WsState> g_registry;
+
+// Marks the workspace's pre_dispatch as consumed; returns whether it was fresh.
+bool take_dispatch(const void* ws) {
+  std::lock_guard<std::mutex> lk(g_reg_mu);
+  auto it = g_registry.find(ws);
+  if (it == g_registry.end()) return false;
+  const bool fresh = it->second.dispatched;
+  it->second.dispatched = false;
+  return fresh;
+}
+
+void mark_dispatched(const void* ws) {
+  std::lock_guard<std::mutex> lk(g_reg_mu);
+  auto it = g_registry.find(ws);
+  if (it != g_registry.end()) it->second.dispatched = true;
+}
 
 // Timing hooks.
 struct ProfRec {
@@ -204,7 +226,7 @@ moe_status check_ws(const moe_dims* d, const void* ws, size_t ws_bytes) {
   if (it == g_registry.end())
     return fail(MOE_ERR_WORKSPACE_MISMATCH,
                 "workspace %p was not initialised by moe_workspace_init", ws);
-  if (!dims_equal(it->second, *d))
+  if (!dims_equal(it->second.dims, *d))
     return fail(MOE_ERR_WORKSPACE_MISMATCH,
                 "workspace %p was initialised for other dims or mma_type", ws);
   return MOE_OK;
@@ -245,6 +267,7 @@ moe_status pre_dispatch_impl(const moe_dims* d, const void* x, const int32_t* id
     e = launch_quantize_scatter(s, x, ids, tw, T, p, st);
   }
   if (e != cudaSuccess) return cuda_fail(e, "quantize kernel");
+  mark_dispatched(ws);
   return MOE_OK;
 }
 
@@ -272,6 +295,12 @@ moe_status forward_impl(const moe_dims* d, const void* prepared, void* ws, void*
   LayerLaunch g = layer_launch(d, prepared, ws, T);
   if (g.num_sms <= 0) return fail(MOE_ERR_CUDA, "no CUDA device");
   cudaError_t e;
+  if (!take_dispatch(ws)) {
+    // A second forward on the same pre_dispatch: its rows still hold the first
+    // call's sums, so clear them before adding again.
+    e = cudaMemsetAsync(g.ws.acc, 0, (size_t)T * d->hidden * sizeof(float), st);
+    if (e != cudaSuccess) return cuda_fail(e, "accumulator clear");
+  }
   {
     ProfScope ps("layer", st);
     e = launch_layer(g, st);
@@ -336,7 +365,7 @@ moe_status moe_workspace_init(const moe_dims* dims, void* ws, size_t ws_bytes, v
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "workspace header");
   std::lock_guard<std::mutex> lk(g_reg_mu);
-  g_registry[ws] = *dims;
+  g_registry[ws] = WsState{*dims, false};
   return MOE_OK;
 }
 
@@ -441,7 +470,7 @@ moe_status moe_check(void* ws, void* stream) {
     auto it = g_registry.find(ws);
     if (it == g_registry.end())
       return fail(MOE_ERR_WORKSPACE_MISMATCH, "workspace %p was not initialised", ws);
-    d = it->second;
+    d = it->second.dims;
   }
   const WsLayout L = ws_layout(d);
   cudaStream_t st = static_cast<cudaStream_t>(stream);

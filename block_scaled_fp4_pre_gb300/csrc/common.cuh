@@ -86,7 +86,7 @@ struct WsPtrs {
   uint8_t* xsf;          // 128x4 blocks of [R_cap, H/32]
   uint8_t* hb;           // [R_cap, I/2] requantised intermediate rows
   uint8_t* hsf;          // 128x4 blocks of [R_cap, I/32]
-  float* acc;            // [T_cap, H] fp32 combine accumulator (zero between layers)
+  float* acc;            // [T_cap, H] fp32 combine accumulator, cleared by pre_dispatch
 };
 
 struct PrepLayout {
@@ -129,8 +129,8 @@ cudaError_t launch_quantize_scatter(const Shape& s, const void* x, const int32_t
 // Rows of all assignments and the per-row tables, without quantising anything.
 cudaError_t launch_assign_slots(const Shape& s, const int32_t* ids, const float* tw, int T,
                                 const WsPtrs& ws, cudaStream_t st);
-// acc [n] fp32 -> out [n] bf16 (round to nearest even), clearing acc.
-cudaError_t launch_convert_out(float* acc, void* out, int64_t n, cudaStream_t st);
+// acc [n] fp32 -> out [n] bf16 (round to nearest even).
+cudaError_t launch_convert_out(const float* acc, void* out, int64_t n, cudaStream_t st);
 cudaError_t launch_quantize_rows(const float* src, int64_t rows, int K, uint8_t* codes,
                                  uint8_t* sf, cudaStream_t st);
 cudaError_t launch_prepare(const Shape& s, const uint8_t* w1c, const uint8_t* w1s,

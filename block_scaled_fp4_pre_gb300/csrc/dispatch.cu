@@ -206,9 +206,9 @@ __global__ void assign_slots_kernel(const int32_t* __restrict__ ids, const float
 // ---------------------------------------------------------------------------
 // Quantise one token row per block and scatter it to the token's k workspace rows.
 // A thread owns 8 consecutive elements; 4 adjacent threads form one 32-group.
-// The row is quantised into shared memory while the bucketing kernel may still be
-// running; the block then waits for it, gives the token's k assignments their rows
-// and copies the row to each of them.
+// The row is quantised into shared memory (and the token's fp32 combine row
+// cleared) while the bucketing kernel may still be running; the block then waits
+// for it, gives the token's k assignments their rows and copies the row to each.
 __global__ void __launch_bounds__(256) quantize_scatter_kernel(const __nv_bfloat16* __restrict__ x,
                                                                const int32_t* __restrict__ ids,
                                                                const float* __restrict__ tw,
@@ -219,6 +219,12 @@ __global__ void __launch_bounds__(256) quantize_scatter_kernel(const __nv_bfloat
   uint8_t* sf_sh = qsh + H / 2;
   const int t = blockIdx.x, tid = threadIdx.x;
   ptx::pdl_launch_dependents();
+  {
+    // The down projection adds this token's k contributions into its fp32 row.
+    float4* acc = reinterpret_cast<float4*>(ws.acc + (size_t)t * H);
+    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int i = tid; i < H / 4; i += blockDim.x) acc[i] = z;
+  }
   for (int base = tid * 8; base < H; base += blockDim.x * 8) {
     const uint4 raw = *reinterpret_cast<const uint4*>(x + (size_t)t * H + base);
     const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
@@ -325,18 +331,15 @@ __global__ void scale_blocks_kernel(const uint8_t* __restrict__ src, uint32_t* _
   }
 }
 
-// acc fp32 -> bf16, 8 elements per thread; leaves acc zero for the next layer call.
-__global__ void convert_out_kernel(float* __restrict__ acc, __nv_bfloat16* __restrict__ out,
+// acc fp32 -> bf16, 8 elements per thread.
+__global__ void convert_out_kernel(const float* __restrict__ acc, __nv_bfloat16* __restrict__ out,
                                    int64_t n8) {
   ptx::pdl_wait();
-  const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8;
        i += (int64_t)gridDim.x * blockDim.x) {
-    float4* a4 = reinterpret_cast<float4*>(acc) + 2 * i;
+    const float4* a4 = reinterpret_cast<const float4*>(acc) + 2 * i;
     const float4 a = a4[0];
     const float4 b = a4[1];
-    a4[0] = z;
-    a4[1] = z;
     __nv_bfloat162 o[4] = {__floats2bfloat162_rn(a.x, a.y), __floats2bfloat162_rn(a.z, a.w),
                            __floats2bfloat162_rn(b.x, b.y), __floats2bfloat162_rn(b.z, b.w)};
     reinterpret_cast<uint4*>(out)[i] = *reinterpret_cast<const uint4*>(o);
@@ -376,7 +379,7 @@ cudaError_t launch_assign_slots(const Shape& s, const int32_t* ids, const float*
                     A, s.k, s.E, ws);
 }
 
-cudaError_t launch_convert_out(float* acc, void* out, int64_t n, cudaStream_t st) {
+cudaError_t launch_convert_out(const float* acc, void* out, int64_t n, cudaStream_t st) {
   const int64_t n8 = n / 8;
   return launch_pdl(convert_out_kernel, dim3(grid_for(n8, 256, 4096)), dim3(256), 0, st, acc,
                     reinterpret_cast<__nv_bfloat16*>(out), n8);

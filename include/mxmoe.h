@@ -140,7 +140,9 @@ MXMOE_API moe_status moe_pre_dispatch(const moe_dims *dims, const void *x_dev,
 
 /* The expert layer on the buffers of the last moe_pre_dispatch on this workspace
  * (same num_tokens): grouped gate/up GEMM with SwiGLU and MXFP4 requantisation,
- * grouped down GEMM, top-k weighted combine.  out_dev: bf16 [num_tokens, H]. */
+ * grouped down GEMM, top-k weighted combine.  out_dev: bf16 [num_tokens, H].
+ * Calling it again without a new moe_pre_dispatch recomputes the same layer (the
+ * library then clears the accumulator rows first). */
 MXMOE_API moe_status moe_forward(const moe_dims *dims, const void *prepared_dev, void *ws_dev,
                                  size_t ws_bytes, void *out_dev, int32_t num_tokens, void *stream);
 

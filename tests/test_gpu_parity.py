@@ -209,6 +209,24 @@ def test_forward_is_repeatable_and_host_path_matches(layers):
     assert normwise_rel_err(oracle.bf16_bits_to_f64(c), oracle.bf16_bits_to_f64(a)) <= 1e-3
 
 
+def test_forward_twice_on_one_pre_dispatch(layers):
+    layer, W = layers("ragged")
+    w = layer.w
+    x = synth.hidden_bf16(w)
+    ids, tw = synth.routing(w)
+    out = torch.empty((w.T, w.H), dtype=torch.bfloat16, device=device())
+    mx.moe_pre_dispatch(layer.dims, to_dev(x), to_dev(ids), to_dev(tw), w.T, layer.ws)
+    mx.moe_forward(layer.dims, layer.prepared, layer.ws, out, w.T)
+    first = out.view(torch.int16).cpu().numpy().view(np.uint16)
+    out.zero_()
+    mx.moe_forward(layer.dims, layer.prepared, layer.ws, out, w.T)   # no new pre_dispatch
+    mx.moe_check(layer.ws)
+    second = out.view(torch.int16).cpu().numpy().view(np.uint16)
+    ref = oracle.moe(x, ids, tw, *W)
+    for got in (first, second):
+        assert normwise_rel_err(oracle.bf16_bits_to_f64(got), ref["out_f64"]) <= 2e-3
+
+
 def test_partial_batch_and_edge_token_counts(layers):
     layer, W = layers("ragged")
     w = layer.w
