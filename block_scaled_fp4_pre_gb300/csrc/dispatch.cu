@@ -43,6 +43,9 @@ __global__ void __launch_bounds__(1024) bucket_kernel(const int32_t* __restrict_
   extern __shared__ int32_t sh[];
   int32_t* cnt = sh;                        // [32][E] per-warp counts, then bases
   int32_t* key_sh = cnt + 32 * E;           // [kBucketChunk] expert id, E if invalid
+  int32_t* tot = key_sh + kBucketChunk;     // [E]   tokens per expert (all chunks)
+  int32_t* seg = tot + E;                   // [E+1] segment starts
+  int32_t* tst = seg + E + 1;               // [E+1] tile starts
   __shared__ int32_t bad;
   __shared__ int32_t is_last;
 
@@ -86,7 +89,12 @@ __global__ void __launch_bounds__(1024) bucket_kernel(const int32_t* __restrict_
       cnt[w * E + e] = run;
       run += c;
     }
-    ws.blk_base[(size_t)blockIdx.x * E + e] = run;  // this chunk's total, for now
+    if (gridDim.x == 1) {
+      ws.blk_base[e] = 0;
+      tot[e] = run;
+    } else {
+      ws.blk_base[(size_t)blockIdx.x * E + e] = run;  // this chunk's total, for now
+    }
   }
   __syncthreads();
 
@@ -101,32 +109,35 @@ __global__ void __launch_bounds__(1024) bucket_kernel(const int32_t* __restrict_
     __syncwarp();
   }
 
-  // Publish this chunk's totals; the last block to finish does the global scans.
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) {
-    if (bad) atomicAdd(&ws.flags[kFlagBucketBad], bad);
-    is_last = atomicAdd(&ws.flags[kFlagBucketTicket], 1) == (int)gridDim.x - 1;
-  }
-  __syncthreads();
-  if (!is_last) return;
-  __threadfence();
-
-  int32_t* tot = cnt;            // [E]   (per-warp counts are no longer needed)
-  int32_t* seg = tot + E;        // [E+1]
-  int32_t* tst = seg + E + 1;    // [E+1]
-  const int nblk = gridDim.x;
-  for (int e = tid; e < E; e += blockDim.x) {
-    int run = 0;
-    for (int b = 0; b < nblk; ++b) {
-      int32_t* p = ws.blk_base + (size_t)b * E + e;
-      const int c = __ldcg(p);
-      *p = run;
-      run += c;
+  int bad_all;
+  if (gridDim.x == 1) {
+    __syncthreads();
+    bad_all = bad;
+  } else {
+    // Publish this chunk's totals; the last block to finish does the global scans.
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+      if (bad) atomicAdd(&ws.flags[kFlagBucketBad], bad);
+      is_last = atomicAdd(&ws.flags[kFlagBucketTicket], 1) == (int)gridDim.x - 1;
     }
-    tot[e] = run;
+    __syncthreads();
+    if (!is_last) return;
+    __threadfence();
+    const int nblk = gridDim.x;
+    for (int e = tid; e < E; e += blockDim.x) {
+      int run = 0;
+      for (int b = 0; b < nblk; ++b) {
+        int32_t* p = ws.blk_base + (size_t)b * E + e;
+        const int c = __ldcg(p);
+        *p = run;
+        run += c;
+      }
+      tot[e] = run;
+    }
+    __syncthreads();
+    bad_all = __ldcg(&ws.flags[kFlagBucketBad]);
   }
-  __syncthreads();
 
   if (warp == 0) {
     int carry_rows = 0, carry_tiles = 0;
@@ -169,7 +180,6 @@ __global__ void __launch_bounds__(1024) bucket_kernel(const int32_t* __restrict_
     }
   }
   if (tid == 0) {
-    const int bad_all = __ldcg(&ws.flags[kFlagBucketBad]);
     ws.seg[E] = seg[E];
     ws.flags[kFlagTiles] = tst[E];
     ws.flags[kFlagValid] = A - bad_all;
@@ -357,7 +367,7 @@ unsigned grid_for(int64_t work, int block, int64_t cap) {
 
 cudaError_t launch_bucket(const Shape& s, const int32_t* ids, int T, const WsPtrs& ws,
                           cudaStream_t st) {
-  const size_t smem = ((size_t)32 * s.E + kBucketChunk) * sizeof(int32_t);
+  const size_t smem = ((size_t)35 * s.E + kBucketChunk + 2) * sizeof(int32_t);
   cudaError_t err = cudaFuncSetAttribute(bucket_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
   if (err != cudaSuccess) return err;

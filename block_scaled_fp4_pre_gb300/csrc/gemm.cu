@@ -191,6 +191,17 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
   volatile int* abort_flag = &tail->abort;
   // Set-up above overlaps the previous kernel; its outputs are read only from here on.
   ptx::pdl_launch_dependents();
+  if (MODE == kModeLayer && threadIdx.x == 0 && blockIdx.x < args.E * args.ph[0].m_tiles) {
+    // While the token dispatch finishes, pull into L2 the gate/up slab this block
+    // most likely takes first when every expert has one token tile (decode-sized
+    // loads): item b = (expert b / slabs, slab b % slabs).  Only a hint.
+    const PhaseArgs& P = args.ph[0];
+    const int e = blockIdx.x / P.m_tiles, mt = blockIdx.x % P.m_tiles;
+    for (int kb = 0; kb < P.num_kb; ++kb)
+      ptx::tma_prefetch_2d(&tmap_w1, kb * kBKBytes, e * P.rows_per_expert + mt * kBM);
+    ptx::bulk_prefetch(P.w_sf + ((size_t)(e * P.m_tiles + mt) * P.kc4) * kSFAtomBytes,
+                       (uint32_t)P.kc4 * kSFAtomBytes);
+  }
   ptx::pdl_wait();
 
   const int num_tiles = args.ws.flags[kFlagTiles];
