@@ -83,6 +83,7 @@ def lib() -> ctypes.CDLL:
             "moe_profile_reset": ([], None),
             "moe_device_sm_count": ([], i32),
             "moe_bucket_noalloc": ([D, vp, vp, i32, vp, vp, vp], i32),
+            "moe_debug_wait_probe": ([vp, i64, vp], i32),
         }
         for name, (args, res) in sigs.items():
             f = getattr(l, name)
@@ -214,6 +215,10 @@ def moe_read_intermediate(dims: MoeDims, ws, num_tokens: int) -> dict:
 def moe_debug_gate_up(dims: MoeDims, prepared, ws, gate_up, num_tokens: int, stream=None) -> None:
     _check(lib().moe_debug_gate_up(ctypes.byref(dims), _ptr(prepared), _ptr(ws), _nbytes(ws),
                                    _ptr(gate_up), int(num_tokens), _stream(stream)))
+
+
+def moe_debug_wait_probe(ws, limit_ns: int, stream=None) -> None:
+    _check(lib().moe_debug_wait_probe(_ptr(ws), int(limit_ns), _stream(stream)))
 
 
 def moe_profile_enable(on: bool) -> None:

@@ -603,6 +603,25 @@ moe_status moe_debug_gate_up(const moe_dims* dims, const void* prepared, void* w
   return MOE_OK;
 }
 
+moe_status moe_debug_wait_probe(void* ws, int64_t limit_ns, void* stream) {
+  if (!ws) return fail(MOE_ERR_INVALID_ARG, "workspace is NULL");
+  if (limit_ns < 1000 || limit_ns > 1000000000)
+    return fail(MOE_ERR_INVALID_ARG, "limit_ns %lld outside [1 us, 1 s]", (long long)limit_ns);
+  moe_dims d;
+  {
+    std::lock_guard<std::mutex> lk(g_reg_mu);
+    auto it = g_registry.find(ws);
+    if (it == g_registry.end())
+      return fail(MOE_ERR_WORKSPACE_MISMATCH, "workspace %p was not initialised", ws);
+    d = it->second.dims;
+  }
+  int32_t* flags = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ws) + ws_layout(d).off_flags);
+  cudaError_t e = launch_wait_probe(flags, (unsigned long long)limit_ns,
+                                    static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "wait probe");
+  return MOE_OK;
+}
+
 moe_status moe_profile_enable(int32_t on) {
   g_prof_on = on != 0;
   return MOE_OK;

@@ -37,6 +37,8 @@ constexpr int kFlagExit = 4;
 constexpr int kFlagBucketTicket = 5;   // blocks of the bucketing kernel done
 constexpr int kFlagBucketBad = 6;      // ids outside [0, E) seen by the bucketing kernel
 
+constexpr int kFlagProbe = 8;          // a counter nothing increments (wait probe)
+
 // Assignments (t*k + j) ranked by one block of the bucketing kernel.
 constexpr int kBucketChunk = 8192;
 
@@ -136,6 +138,10 @@ cudaError_t launch_quantize_rows(const float* src, int64_t rows, int K, uint8_t*
 cudaError_t launch_prepare(const Shape& s, const uint8_t* w1c, const uint8_t* w1s,
                            const uint8_t* w2c, const uint8_t* w2s, uint8_t* prep,
                            const PrepLayout& pl, cudaStream_t st);
+
+// One block waiting, with the given limit, on an mbarrier no one arrives at and on a
+// counter no one increments, through the same bounded waits as the layer kernel.
+cudaError_t launch_wait_probe(int32_t* flags, unsigned long long limit_ns, cudaStream_t st);
 
 // Records the message moe_last_error() returns on this thread.
 void set_last_error(const char* msg);

@@ -356,6 +356,21 @@ __global__ void convert_out_kernel(const float* __restrict__ acc, __nv_bfloat16*
   }
 }
 
+__global__ void wait_probe_kernel(int32_t* flags, unsigned long long limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(&bar, 1);
+    abort_flag = 0;
+    ptx::fence_mbar_init();
+    // phase 0 of `bar` never completes: nothing arrives on it
+    const bool got_bar = ptx::mbar_wait(&bar, 0, &abort_flag, limit_ns);
+    abort_flag = 0;
+    const bool got_count = ptx::wait_counter(&flags[kFlagProbe], 1, &abort_flag, limit_ns);
+    if (!got_bar && !got_count) atomicOr(&flags[0], kErrTimeout);
+  }
+}
+
 // Blocks for a grid-stride loop over `work` items, capped at `cap`.
 unsigned grid_for(int64_t work, int block, int64_t cap) {
   int64_t g = (work + block - 1) / block;
@@ -393,6 +408,11 @@ cudaError_t launch_convert_out(const float* acc, void* out, int64_t n, cudaStrea
   const int64_t n8 = n / 8;
   return launch_pdl(convert_out_kernel, dim3(grid_for(n8, 256, 4096)), dim3(256), 0, st, acc,
                     reinterpret_cast<__nv_bfloat16*>(out), n8);
+}
+
+cudaError_t launch_wait_probe(int32_t* flags, unsigned long long limit_ns, cudaStream_t st) {
+  wait_probe_kernel<<<1, 32, 0, st>>>(flags, limit_ns);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_quantize_rows(const float* src, int64_t rows, int K, uint8_t* codes,

@@ -134,21 +134,6 @@ __device__ __forceinline__ float silu_times(float g, float u) {
   return __fdividef(g, 1.0f + __expf(-g)) * u;
 }
 
-// Waits until *p >= target (acquire), bounded like the mbarrier waits.
-__device__ __forceinline__ bool wait_counter(const int32_t* p, int target, volatile int* abort) {
-  if (ptx::ld_acquire(p) >= target) return true;
-  const unsigned long long t0 = ptx::globaltimer();
-  while (true) {
-    __nanosleep(128);
-    if (ptx::ld_acquire(p) >= target) return true;
-    if (*abort) return false;
-    if (ptx::globaltimer() - t0 > kWaitLimitNs) {
-      *abort = 1;
-      return false;
-    }
-  }
-}
-
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
     moe_layer_kernel(const __grid_constant__ CUtensorMap tmap_w1,
@@ -262,7 +247,7 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
         if (it.phase == 1) {
           // The down projection reads the intermediate rows that this tile's
           // gate/up items wrote with ordinary stores.
-          if (!wait_counter(&args.ws.tile_done[it.tile], m0, abort_flag)) {
+          if (!ptx::wait_counter(&args.ws.tile_done[it.tile], m0, abort_flag, kWaitLimitNs)) {
             ok = false;
             break;
           }

@@ -82,6 +82,23 @@ __device__ __forceinline__ int ld_acquire(const int32_t* p) {
   asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
+// Waits until *p >= target (acquire), bounded like mbar_wait: gives up when *abort
+// becomes nonzero or after limit_ns, setting *abort in the latter case.
+__device__ __forceinline__ bool wait_counter(const int32_t* p, int target, volatile int* abort,
+                                             unsigned long long limit_ns) {
+  if (ld_acquire(p) >= target) return true;
+  const unsigned long long t0 = globaltimer();
+  while (true) {
+    __nanosleep(128);
+    if (ld_acquire(p) >= target) return true;
+    if (*abort) return false;
+    if (globaltimer() - t0 > limit_ns) {
+      *abort = 1;
+      return false;
+    }
+  }
+}
+
 // Orders this thread's generic-proxy global accesses with its async-proxy (TMA)
 // accesses to global memory.
 __device__ __forceinline__ void fence_proxy_async_global() {

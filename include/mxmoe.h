@@ -185,6 +185,14 @@ MXMOE_API moe_status moe_debug_gate_up(const moe_dims *dims, const void *prepare
                                        void *ws_dev, size_t ws_bytes, float *gate_up_dev,
                                        int32_t num_tokens, void *stream);
 
+/* Debug: exercises the bounded-wait failure path without any fault.  Launches one
+ * block that waits, each time for at most limit_ns (1 us .. 1 s), on an mbarrier
+ * nothing arrives at and on a workspace counter nothing increments -- the same
+ * bounded waits the layer kernel uses.  Both give up; the block records a timeout
+ * in the workspace flags and exits normally, so the context stays usable and the
+ * next moe_check returns MOE_ERR_TIMEOUT. */
+MXMOE_API moe_status moe_debug_wait_probe(void *ws_dev, int64_t limit_ns, void *stream);
+
 /* ---- timing hooks ----
  * When enabled, moe_pre_dispatch and moe_forward record CUDA events around each
  * kernel they launch (on the launch stream).  moe_profile_read synchronises and

@@ -276,6 +276,22 @@ def test_invalid_ids_are_skipped_and_reported(layers):
     assert normwise_rel_err(oracle.bf16_bits_to_f64(got), ref["out_f64"]) <= 2e-3
 
 
+def test_bounded_wait_reports_timeout_and_context_survives(layers):
+    layer, W = layers("tiny")
+    w = layer.w
+    mx.moe_check(layer.ws)
+    mx.moe_debug_wait_probe(layer.ws, 10_000_000)       # 10 ms per wait
+    with pytest.raises(mx.MoeError) as ei:
+        mx.moe_check(layer.ws)
+    assert ei.value.status == mx.MOE_ERR_TIMEOUT
+    mx.moe_check(layer.ws)                              # reported once, then cleared
+    x = synth.hidden_bf16(w)
+    ids, tw = synth.routing(w)
+    got = layer.run(x, ids, tw)                         # the context still works
+    ref = oracle.moe(x, ids, tw, *W)
+    assert normwise_rel_err(oracle.bf16_bits_to_f64(got), ref["out_f64"]) <= 2e-3
+
+
 def test_workspace_checks(layers):
     layer, _ = layers("tiny")
     other = mx.make_dims(layer.dims.hidden, layer.dims.inter, layer.dims.num_experts,
