@@ -84,6 +84,7 @@ def lib() -> ctypes.CDLL:
             "moe_device_sm_count": ([], i32),
             "moe_bucket_noalloc": ([D, vp, vp, i32, vp, vp, vp], i32),
             "moe_debug_wait_probe": ([vp, i64, vp], i32),
+            "moe_fp4_mma_probe": ([vp, i32, i32, i32, i64, vp], i32),
         }
         for name, (args, res) in sigs.items():
             f = getattr(l, name)
@@ -219,6 +220,12 @@ def moe_debug_gate_up(dims: MoeDims, prepared, ws, gate_up, num_tokens: int, str
 
 def moe_debug_wait_probe(ws, limit_ns: int, stream=None) -> None:
     _check(lib().moe_debug_wait_probe(_ptr(ws), int(limit_ns), _stream(stream)))
+
+
+def moe_fp4_mma_probe(ws, n: int, blocks_per_sm: int, blocks: int, mma_count: int,
+                      stream=None) -> None:
+    _check(lib().moe_fp4_mma_probe(_ptr(ws), int(n), int(blocks_per_sm), int(blocks),
+                                   int(mma_count), _stream(stream)))
 
 
 def moe_profile_enable(on: bool) -> None:

@@ -622,6 +622,34 @@ moe_status moe_debug_wait_probe(void* ws, int64_t limit_ns, void* stream) {
   return MOE_OK;
 }
 
+moe_status moe_fp4_mma_probe(void* ws, int32_t n, int32_t blocks_per_sm, int32_t blocks,
+                             int64_t mma_count, void* stream) {
+  if (!ws) return fail(MOE_ERR_INVALID_ARG, "workspace is NULL");
+  if (n != 32 && n != 64 && n != 128 && n != 256)
+    return fail(MOE_ERR_INVALID_ARG, "n = %d: must be 32, 64, 128 or 256", n);
+  if (blocks_per_sm != 1 && blocks_per_sm != 2)
+    return fail(MOE_ERR_INVALID_ARG, "blocks_per_sm = %d: must be 1 or 2", blocks_per_sm);
+  if (blocks_per_sm == 2 && n > 128)
+    return fail(MOE_ERR_INVALID_ARG, "n = %d needs the whole tensor memory: blocks_per_sm = 1", n);
+  if (blocks < 1 || blocks > 65536)
+    return fail(MOE_ERR_INVALID_ARG, "blocks = %d outside [1, 65536]", blocks);
+  if (mma_count < 1 || mma_count > ((int64_t)1 << 20))
+    return fail(MOE_ERR_INVALID_ARG, "mma_count = %lld outside [1, 2^20]", (long long)mma_count);
+  moe_dims d;
+  {
+    std::lock_guard<std::mutex> lk(g_reg_mu);
+    auto it = g_registry.find(ws);
+    if (it == g_registry.end())
+      return fail(MOE_ERR_WORKSPACE_MISMATCH, "workspace %p was not initialised", ws);
+    d = it->second.dims;
+  }
+  int32_t* flags = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ws) + ws_layout(d).off_flags);
+  cudaError_t e = launch_fp4_mma_probe(n, blocks_per_sm, blocks, (long long)mma_count, flags,
+                                       static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "fp4 mma probe");
+  return MOE_OK;
+}
+
 moe_status moe_profile_enable(int32_t on) {
   g_prof_on = on != 0;
   return MOE_OK;

@@ -106,6 +106,12 @@ __device__ __forceinline__ void fence_proxy_async_global() {
 }
 
 // ---- L2 cache policies -----------------------------------------------------
+// Orders this thread's earlier generic-proxy shared-memory writes before later
+// async-proxy (TMA, tensor core) accesses of the same memory.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));

@@ -193,6 +193,21 @@ MXMOE_API moe_status moe_debug_gate_up(const moe_dims *dims, const void *prepare
  * next moe_check returns MOE_ERR_TIMEOUT. */
 MXMOE_API moe_status moe_debug_wait_probe(void *ws_dev, int64_t limit_ns, void *stream);
 
+/* FP4 tensor-core throughput probe (measurement only; the denominator of the
+ * layer's compute roofline).  Launches `blocks` blocks of 128 threads on `stream`,
+ * blocks_per_sm (1 or 2) of them resident per SM, each of which issues mma_count
+ * (1 .. 2^20) block-scaled MXFP4 MMAs of shape M=128 x N=n x K=64 -- the layer's
+ * instruction (kind::mxf4, UE8M0 scale per 32) -- on operands held in shared
+ * memory, with no global-memory traffic.  n is 32, 64, 128 or 256 (256 only with
+ * blocks_per_sm = 1).  The work is blocks * mma_count * 2*128*n*64 FLOP; the caller
+ * times the launch with events on `stream`.  ws_dev is an initialised workspace
+ * whose error flags receive MOE_ERR_TIMEOUT if the final wait exceeds 2 s (read by
+ * moe_check).  Nothing is written to global memory otherwise.
+ * Pages: "[deepseek-v4] Bump sgl-deep-gemm for packed FP4xFP4 mega-MoE (W4A4)",
+ * Appendix B (Compute SOL of the layer kernel). */
+MXMOE_API moe_status moe_fp4_mma_probe(void *ws_dev, int32_t n, int32_t blocks_per_sm,
+                                       int32_t blocks, int64_t mma_count, void *stream);
+
 /* ---- timing hooks ----
  * When enabled, moe_pre_dispatch and moe_forward record CUDA events around each
  * kernel they launch (on the launch stream).  moe_profile_read synchronises and

@@ -292,6 +292,32 @@ def test_bounded_wait_reports_timeout_and_context_survives(layers):
     assert normwise_rel_err(oracle.bf16_bits_to_f64(got), ref["out_f64"]) <= 2e-3
 
 
+def test_fp4_mma_probe_runs_and_rejects_bad_shapes(layers):
+    """The FP4 throughput probe completes with a clean status at each tile shape, and
+    its rate is plausible for the part: below the nominal dense FP4 peak with margin
+    (13.5 PFLOP/s; a rate above it would mean the timed launch skipped work) and
+    above a tenth of it."""
+    layer, _ = layers("tiny")
+    sms = mx.moe_device_sm_count()
+    for n, bps in ((32, 2), (128, 2), (256, 1)):
+        count = 1 << 16
+        mx.moe_fp4_mma_probe(layer.ws, n, bps, sms * bps, count)    # warm-up
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        mx.moe_fp4_mma_probe(layer.ws, n, bps, sms * bps, count)
+        b.record()
+        b.synchronize()
+        mx.moe_check(layer.ws)
+        tflops = sms * bps * count * 2.0 * 128 * n * 64 / (a.elapsed_time(b) / 1e3) / 1e12
+        if n >= 128:
+            assert 1350 < tflops < 1.2 * 13500, (n, bps, tflops)
+    for bad in ((48, 2, sms, 16), (256, 2, sms, 16), (128, 3, sms, 16), (128, 2, 0, 16),
+                (128, 2, sms, 0), (128, 2, sms, (1 << 20) + 1)):
+        with pytest.raises(mx.MoeError) as ei:
+            mx.moe_fp4_mma_probe(layer.ws, *bad)
+        assert ei.value.status == mx.MOE_ERR_INVALID_ARG
+
+
 def test_workspace_checks(layers):
     layer, _ = layers("tiny")
     other = mx.make_dims(layer.dims.hidden, layer.dims.inter, layer.dims.num_experts,
