@@ -55,7 +55,7 @@ constexpr unsigned kFull = 0xFFFFFFFFu;
 
 enum LayerMode { kModeLayer = 0, kModeRaw = 1 };
 
-struct __align__(8) SmemTail {
+struct __align__(16) SmemTail {
   uint64_t full[kStages];
   uint64_t empty[kStages];
   uint64_t acc_full;
@@ -67,6 +67,11 @@ struct __align__(8) SmemTail {
   uint32_t tmem_base;
   int abort;
   float xchg[2][4][kEpiCols];
+  // One chunk of intermediate rows, gathered from the four epilogue warps before
+  // it is stored: per column, the item's 64 features (32 code bytes) and their two
+  // scale bytes.  Double-buffered across chunks.
+  alignas(16) uint8_t hstage[2][kEpiCols][32];
+  uint8_t sstage[2][kEpiCols][2];
   int32_t tile_start[1025];   // first tile of each expert (E <= 1024), see decode_item
 };
 
@@ -134,29 +139,58 @@ __device__ __forceinline__ float silu_times(float g, float u) {
   return __fdividef(g, 1.0f + __expf(-g)) * u;
 }
 
-template <int MODE>
+// Ring hand-over of work items to the MMA issuer and the epilogue.  In a pair,
+// block 0 writes both blocks' rings and owns the slot-free barrier, on which the
+// second block's readers arrive remotely.
+template <bool PAIR>
+__device__ __forceinline__ bool ring_wait(uint64_t* full, uint32_t parity, volatile int* abort) {
+  return PAIR ? ptx::mbar_wait_cluster(full, parity, abort, kWaitLimitNs)
+              : ptx::mbar_wait(full, parity, abort, kWaitLimitNs);
+}
+template <bool PAIR>
+__device__ __forceinline__ void ring_release(uint64_t* empty, int rank) {
+  if (!PAIR || rank == 0)
+    ptx::mbar_arrive(empty);
+  else
+    ptx::mbar_arrive_cluster(ptx::cluster_addr(empty, 0));
+}
+
+// PAIR: the kernel runs as clusters of two blocks that take the same token tile
+// and adjacent weight slabs (2p, 2p+1) of each item; each block loads half of the
+// token boxes and multicasts them into both, which halves the token rows read
+// from L2.  Block 0 of the pair claims the items and hands each to both blocks.
+template <int MODE, bool PAIR>
 __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
     moe_layer_kernel(const __grid_constant__ CUtensorMap tmap_w1,
                      const __grid_constant__ CUtensorMap tmap_x,
                      const __grid_constant__ CUtensorMap tmap_w2,
-                     const __grid_constant__ CUtensorMap tmap_h, const LayerArgs args) {
+                     const __grid_constant__ CUtensorMap tmap_h,
+                     const __grid_constant__ CUtensorMap tmap_x_full,
+                     const __grid_constant__ CUtensorMap tmap_h_full, const LayerArgs args) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   SmemTail* tail = reinterpret_cast<SmemTail*>(smem + kSmemTail);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // Position in the pair (0 without pairing): block 0 schedules, both load.
+  const int rank = PAIR ? (int)ptx::cluster_ctarank() : 0;
+  constexpr uint16_t kPairMask = 0x3;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(&tail->full[s], 1);
-      ptx::mbar_init(&tail->empty[s], 1);
+      // a stage is free again once the MMAs of both blocks of a pair have read it
+      // (the partner's token boxes land in this block's stage too)
+      ptx::mbar_init(&tail->empty[s], PAIR ? 2 : 1);
     }
     ptx::mbar_init(&tail->acc_full, 1);
     ptx::mbar_init(&tail->acc_empty, 128);
     ptx::mbar_init(&tail->mma_done, 1);
     for (int r = 0; r < kRing; ++r) {
       ptx::mbar_init(&tail->ring_full[r], 1);
-      ptx::mbar_init(&tail->ring_empty[r], 5);  // the MMA thread + 4 epilogue warps
+      // the MMA thread + 4 epilogue warps (of both blocks of a pair, plus the
+      // second block's producer; only block 0's count is used)
+      ptx::mbar_init(&tail->ring_empty[r], PAIR ? 11 : 5);
     }
     tail->abort = 0;
     ptx::fence_mbar_init();
@@ -164,6 +198,8 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
     ptx::prefetch_tmap(&tmap_x);
     ptx::prefetch_tmap(&tmap_w2);
     ptx::prefetch_tmap(&tmap_h);
+    ptx::prefetch_tmap(&tmap_x_full);
+    ptx::prefetch_tmap(&tmap_h_full);
   }
   if (warp == 1) {
     ptx::tmem_alloc(&tail->tmem_base, kTmemCols);
@@ -171,6 +207,8 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
   }
   ptx::tc_fence_before();
   __syncthreads();
+  // A pair's blocks touch each other's barriers from here on: both must be set up.
+  if (PAIR) ptx::cluster_sync_all();
   ptx::tc_fence_after();
   const uint32_t tmem_base = tail->tmem_base;
   volatile int* abort_flag = &tail->abort;
@@ -180,8 +218,11 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
     // While the token dispatch finishes, pull into L2 the gate/up slab this block
     // most likely takes first when every expert has one token tile (decode-sized
     // loads): item b = (expert b / slabs, slab b % slabs).  Only a hint.
+    // (with pairing: item b/2 = (expert, slab pair), this block's slab of it)
     const PhaseArgs& P = args.ph[0];
-    const int e = blockIdx.x / P.m_tiles, mt = blockIdx.x % P.m_tiles;
+    const int per_e = PAIR ? P.m_tiles / 2 : P.m_tiles;
+    const int b = PAIR ? (int)blockIdx.x / 2 : (int)blockIdx.x;
+    const int e = b / per_e, mt = (b % per_e) * (PAIR ? 2 : 1) + rank;
     for (int kb = 0; kb < P.num_kb; ++kb)
       ptx::tma_prefetch_2d(&tmap_w1, kb * kBKBytes, e * P.rows_per_expert + mt * kBM);
     ptx::bulk_prefetch(P.w_sf + ((size_t)(e * P.m_tiles + mt) * P.kc4) * kSFAtomBytes,
@@ -194,9 +235,13 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
   const int32_t* tile_start = tail->tile_start;
   for (int e = threadIdx.x; e <= E; e += blockDim.x) tail->tile_start[e] = args.ws.tile_start[e];
   __syncthreads();
-  const int m0 = args.ph[0].m_tiles, m1 = args.ph[1].m_tiles;
+  // Items per token tile and phase: one per weight slab, or per slab pair.
+  const int m0 = args.ph[0].m_tiles / (PAIR ? 2 : 1), m1 = args.ph[1].m_tiles / (PAIR ? 2 : 1);
   const int n0 = num_tiles * m0;
   const int total = n0 + (args.num_phases == 2 ? num_tiles * m1 : 0);
+  // A tile's intermediate rows are complete once every gate/up slab has stored its
+  // part (one count per slab, from whichever block computed it).
+  const int slabs0 = args.ph[0].m_tiles;
 
   if (warp == 0) {
     // ------------------------------------------------- scheduler + producer
@@ -204,50 +249,83 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
       const uint64_t pol_once = ptx::policy_evict_first();
       const uint64_t pol_shared = ptx::policy_evict_normal();
       const uint64_t pol_t = ptx::policy_evict_last();
+      const bool scheduler = rank == 0;
       int stage = 0, r = 0;
       uint32_t phase = 0, rph = 0;
       int64_t issued = 0;
       bool ok = true;
       // Items are claimed one ahead so that the claim and the table reads of the
       // next item overlap the loads of the current one.
-      int g = atomicAdd(&args.ws.flags[kFlagSched], 1);
+      int g = 0;
       Item it = {};
       int4 ti = make_int4(0, 0, 0, 0);
-      if (g < total) {
-        it = decode_item(g, n0, m0, m1, E, tile_start);
-        ti = args.ws.tiles[it.tile];
+      if (scheduler) {
+        g = atomicAdd(&args.ws.flags[kFlagSched], 1);
+        if (g < total) {
+          it = decode_item(g, n0, m0, m1, E, tile_start);
+          ti = args.ws.tiles[it.tile];
+        }
       }
       while (true) {
-        const int item = g < total ? g : -1;
-        if (!ptx::mbar_wait(&tail->ring_empty[r], rph ^ 1u, abort_flag, kWaitLimitNs)) {
-          ok = false;
-          break;
+        int item;
+        if (scheduler) {
+          item = g < total ? g : -1;
+          if (!ptx::mbar_wait(&tail->ring_empty[r], rph ^ 1u, abort_flag, kWaitLimitNs)) {
+            ok = false;
+            break;
+          }
+          const int4 rec = make_int4(item, ti.y, ti.z | (it.mt << 8), it.tile);
+          tail->ring[r] = rec;
+          ptx::mbar_arrive(&tail->ring_full[r]);
+          if (PAIR) {
+            // hand the same item to the second block of the pair
+            ptx::st_cluster_v4(ptx::cluster_addr(&tail->ring[r], 1), rec);
+            ptx::mbar_arrive_cluster(ptx::cluster_addr(&tail->ring_full[r], 1));
+          }
+        } else {
+          // second block of a pair: the item block 0 handed over
+          if (!ptx::mbar_wait_cluster(&tail->ring_full[r], rph, abort_flag, kWaitLimitNs)) {
+            ok = false;
+            break;
+          }
+          const int4 rec = tail->ring[r];
+          ptx::mbar_arrive_cluster(ptx::cluster_addr(&tail->ring_empty[r], 0));
+          item = rec.x;
+          if (item >= 0) {
+            it.phase = item < n0 ? 0 : 1;
+            it.tile = rec.w;
+            it.mt = rec.z >> 8;
+            it.e = args.ws.tiles[it.tile].x;
+            it.ntiles = tile_start[it.e + 1] - tile_start[it.e];
+            ti = make_int4(it.e, rec.y, rec.z & 0xFF, 0);
+          }
         }
-        tail->ring[r] = make_int4(item, ti.y, ti.z | (it.mt << 8), it.tile);
-        ptx::mbar_arrive(&tail->ring_full[r]);
         if (++r == kRing) {
           r = 0;
           rph ^= 1u;
         }
         if (item < 0) break;
-        const int g_next = atomicAdd(&args.ws.flags[kFlagSched], 1);
+        const int g_next = scheduler ? atomicAdd(&args.ws.flags[kFlagSched], 1) : total;
         Item it_next = {};
         int4 ti_next = make_int4(0, 0, 0, 0);
         const PhaseArgs& P = args.ph[it.phase];
         const CUtensorMap* tw = it.phase ? &tmap_w2 : &tmap_w1;
         const CUtensorMap* tt = it.phase ? &tmap_h : &tmap_x;
+        // a full tile's token rows in one box (one half-tile box per block of a pair)
+        const CUtensorMap* tt_full = it.phase ? &tmap_h_full : &tmap_x_full;
         // A slab read by one token tile only is not kept; one shared by several
         // tiles of the expert stays for them.
         const uint64_t pol_w = it.ntiles > 1 ? pol_shared : pol_once;
         const int e = it.e, row0 = ti.y, n = ti.z;
         const int nb = (n + kBBoxRows - 1) / kBBoxRows;
-        const int wrow = e * P.rows_per_expert + it.mt * kBM;
-        const uint8_t* wsf = P.w_sf + ((size_t)(e * P.m_tiles + it.mt) * P.kc4) * kSFAtomBytes;
+        const int mt = it.mt * (PAIR ? 2 : 1) + rank;   // this block's weight slab
+        const int wrow = e * P.rows_per_expert + mt * kBM;
+        const uint8_t* wsf = P.w_sf + ((size_t)(e * P.m_tiles + mt) * P.kc4) * kSFAtomBytes;
         const uint8_t* tsf = P.t_sf + ((size_t)(row0 / kBN) * P.kc4) * kSFAtomBytes;
         if (it.phase == 1) {
           // The down projection reads the intermediate rows that this tile's
           // gate/up items wrote with ordinary stores.
-          if (!ptx::wait_counter(&args.ws.tile_done[it.tile], m0, abort_flag, kWaitLimitNs)) {
+          if (!ptx::wait_counter(&args.ws.tile_done[it.tile], slabs0, abort_flag, kWaitLimitNs)) {
             ok = false;
             break;
           }
@@ -260,6 +338,8 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
           }
           const int kvalid = min(kBK, P.K - kb * kBK);
           const int atoms = kvalid / 128;
+          // every token box lands here: this block's own and, in a pair, the
+          // partner's multicast ones
           const uint32_t bytes =
               kATileBytes + nb * (kBBoxRows * kBKBytes) + 2u * atoms * kSFAtomBytes;
           uint64_t* bar = &tail->full[stage];
@@ -268,9 +348,25 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
                            bar, pol_w);
           ptx::bulk_load(smem + kSmemSFA + (size_t)stage * kSFStageBytes,
                          wsf + (size_t)kb * 2 * kSFAtomBytes, atoms * kSFAtomBytes, bar, pol_w);
-          for (int j = 0; j < nb; ++j)
-            ptx::tma_load_2d(smem + kSmemB + (size_t)stage * kBTileBytes + j * kBBoxRows * kBKBytes,
-                             tt, kb * kBKBytes, row0 + j * kBBoxRows, bar, pol_t);
+          uint8_t* b_dst = smem + kSmemB + (size_t)stage * kBTileBytes;
+          if (nb * kBBoxRows == kBN) {
+            if (!PAIR) {
+              ptx::tma_load_2d(b_dst, tt_full, kb * kBKBytes, row0, bar, pol_t);
+            } else {
+              const int half = rank * (kBN / 2);
+              ptx::tma_load_2d_multicast(b_dst + half * kBKBytes, tt_full, kb * kBKBytes,
+                                         row0 + half, bar, kPairMask, pol_t);
+            }
+          } else {
+            for (int j = 0; j < nb; ++j) {
+              uint8_t* dst = b_dst + j * kBBoxRows * kBKBytes;
+              if (!PAIR)
+                ptx::tma_load_2d(dst, tt, kb * kBKBytes, row0 + j * kBBoxRows, bar, pol_t);
+              else if ((j & 1) == rank)
+                ptx::tma_load_2d_multicast(dst, tt, kb * kBKBytes, row0 + j * kBBoxRows, bar,
+                                           kPairMask, pol_t);
+            }
+          }
           ptx::bulk_load(smem + kSmemSFB + (size_t)stage * kSFStageBytes,
                          tsf + (size_t)kb * 2 * kSFAtomBytes, atoms * kSFAtomBytes, bar, pol_t);
           ++issued;
@@ -306,12 +402,12 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
       uint32_t phase = 0, rph = 0, acc_phase = 0, sfbuf = 0;
       bool ok = true;
       while (true) {
-        if (!ptx::mbar_wait(&tail->ring_full[r], rph, abort_flag, kWaitLimitNs)) {
+        if (!ring_wait<PAIR>(&tail->ring_full[r], rph, abort_flag)) {
           ok = false;
           break;
         }
         const int4 rec = tail->ring[r];
-        ptx::mbar_arrive(&tail->ring_empty[r]);
+        ring_release<PAIR>(&tail->ring_empty[r], rank);
         if (++r == kRing) {
           r = 0;
           rph ^= 1u;
@@ -351,7 +447,11 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
                              ptx::desc_sw128(b_base + s * 32), idesc, sfa_t + (s >> 1) * 4,
                              sfb_t + (s >> 1) * 4, (kb | s) != 0 ? 1u : 0u);
           }
-          ptx::tc_commit(&tail->empty[stage]);
+          // the stage is free once both blocks of a pair have read it
+          if (PAIR)
+            ptx::tc_commit_multicast(&tail->empty[stage], kPairMask);
+          else
+            ptx::tc_commit(&tail->empty[stage]);
           sfbuf ^= 1u;
           if (++stage == kStages) {
             stage = 0;
@@ -376,13 +476,13 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
     int r = 0, xb = 0;
     uint32_t rph = 0, acc_phase = 0;
     while (true) {
-      if (!ptx::mbar_wait(&tail->ring_full[r], rph, abort_flag, kWaitLimitNs)) {
+      if (!ring_wait<PAIR>(&tail->ring_full[r], rph, abort_flag)) {
         if (ep_tid == 0) atomicOr(&args.ws.flags[0], kErrTimeout);
         break;
       }
       const int4 rec = tail->ring[r];
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&tail->ring_empty[r]);
+      if (lane == 0) ring_release<PAIR>(&tail->ring_empty[r], rank);
       if (++r == kRing) {
         r = 0;
         rph ^= 1u;
@@ -390,7 +490,22 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
       const int item = rec.x;
       if (item < 0) break;
       const int item_phase = item < n0 ? 0 : 1;
-      const int row0 = rec.y, n = rec.z & 0xFF, mt = rec.z >> 8, item_tile = rec.w;
+      // this block's weight slab of the item (the item names a slab pair when paired)
+      const int row0 = rec.y, n = rec.z & 0xFF, mt = (rec.z >> 8) * (PAIR ? 2 : 1) + rank,
+                item_tile = rec.w;
+      // Row metadata of a down item, read while the MMAs run: lane l holds rows
+      // l, l+32, l+64, l+96 of the tile.
+      int tok_r[kBN / 32];
+      float w_r[kBN / 32];
+#pragma unroll
+      for (int i = 0; i < kBN / 32; ++i) {
+        tok_r[i] = 0;
+        w_r[i] = 0.f;
+        if (MODE == kModeLayer && item_phase == 1 && lane + 32 * i < n) {
+          tok_r[i] = args.ws.slot_token[row0 + lane + 32 * i];
+          w_r[i] = args.ws.slot_weight[row0 + lane + 32 * i];
+        }
+      }
       if (!ptx::mbar_wait(&tail->acc_full, acc_phase, abort_flag, kWaitLimitNs)) {
         if (ep_tid == 0) atomicOr(&args.ws.flags[0], kErrTimeout);
         break;
@@ -398,15 +513,28 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
       acc_phase ^= 1u;
       ptx::tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16);
-      for (int c0 = 0; c0 < n; c0 += kEpiCols) {
-        float v[kEpiCols];
-        ptx::tmem_ld16(taddr + (uint32_t)c0, v);
-        if (c0 + kEpiCols >= n) {
-          // Last load of this item: hand the accumulator back to the MMA issuer
-          // before the math, so the next item's MMAs overlap it.
+      // Chunks of 16 columns; the load of chunk ci+1 runs during the math of ci.
+      uint32_t ra[kEpiCols], rb[kEpiCols];
+      ptx::tmem_ld16_issue(taddr, ra);
+      ptx::tmem_wait_ld(ra);
+#pragma unroll
+      for (int ci = 0; ci < kBN / kEpiCols; ++ci) {
+        const int c0 = ci * kEpiCols;
+        if (c0 >= n) break;
+        uint32_t(&cur)[kEpiCols] = (ci & 1) ? rb : ra;
+        uint32_t(&nxt)[kEpiCols] = (ci & 1) ? ra : rb;
+        const bool more = c0 + kEpiCols < n;
+        if (more) {
+          ptx::tmem_ld16_issue(taddr + (uint32_t)(c0 + kEpiCols), nxt);
+        } else {
+          // Every load of this item is done: hand the accumulator back to the MMA
+          // issuer before the last chunk's math, so the next item's MMAs overlap it.
           ptx::tc_fence_before();
           ptx::mbar_arrive(&tail->acc_empty);
         }
+        float v[kEpiCols];
+#pragma unroll
+        for (int j = 0; j < kEpiCols; ++j) v[j] = __uint_as_float(cur[j]);
         const int ncol = min(kEpiCols, n - c0);
         if (MODE == kModeRaw) {
           const int m = mt * kBM + q * 32 + lane;
@@ -424,7 +552,6 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
           // Columns go in pairs: gate lanes (0-7, 16-23) compute column 2p from their
           // gate and the up of lane+8, up lanes (8-15, 24-31) column 2p+1 from their up
           // and the gate of lane-8 -- one exchange, and no lane idles.
-          const int c = mt * 4 + q;
           const bool up_lane = (lane & 8) != 0;
           float hv[kEpiCols / 2];
 #pragma unroll
@@ -443,42 +570,72 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
           ptx::named_bar_sync(1, 128);
           const int i_kc4 = args.I / 128;
           const size_t hrow_bytes = (size_t)args.I / 2;
+          // All shared-memory reads first, then the arithmetic, then the writes: the
+          // eight columns' work is independent and overlaps instead of forming one
+          // chain through shared memory.
+          float amax[kEpiCols / 2];
 #pragma unroll
           for (int p = 0; p < kEpiCols / 2; ++p) {
             const int jc = 2 * p + (up_lane ? 1 : 0);  // this lane's column
             // 32-feature group = this warp's 16 features + the partner warp's 16.
-            const float amax = fmaxf(tail->xchg[xb][q][jc], tail->xchg[xb][q ^ 1][jc]);
-            const int e = ptx::mx_scale_exponent(amax);
-            const float qv = hv[p] * ptx::pow2_neg(e);
+            amax[p] = fmaxf(tail->xchg[xb][q][jc], tail->xchg[xb][q ^ 1][jc]);
+          }
+          uint32_t code[kEpiCols / 2];
+          int ex[kEpiCols / 2];
+#pragma unroll
+          for (int p = 0; p < kEpiCols / 2; ++p) {
+            ex[p] = ptx::mx_scale_exponent(amax[p]);
+            const float qv = hv[p] * ptx::pow2_neg(ex[p]);
             const float qodd = __shfl_down_sync(kFull, qv, 16);
-            if (lane < 16 && jc < ncol) {
-              const size_t row = (size_t)row0 + c0 + jc;
-              // lanes 0-7 (column 2p) and 8-15 (column 2p+1) each write the 8 bytes of
-              // features c*16..c*16+15 of their column
-              args.ws.hb[row * hrow_bytes + (size_t)c * 8 + (lane & 7)] =
-                  (uint8_t)ptx::e2m1x2(qv, qodd);
+            code[p] = ptx::e2m1x2(qv, qodd);
+          }
+          if (lane < 16) {
+            // lanes 0-7 (column 2p) and 8-15 (column 2p+1) each hold one of the 8
+            // bytes of features c*16..c*16+15 of their column (c = 4*slab + q)
+#pragma unroll
+            for (int p = 0; p < kEpiCols / 2; ++p) {
+              const int jc = 2 * p + (up_lane ? 1 : 0);
+              tail->hstage[xb][jc][q * 8 + (lane & 7)] = (uint8_t)code[p];
               if ((lane & 7) == 0 && (q & 1) == 0)
-                args.ws.hsf[sf_atom_offset(row, c >> 1, i_kc4)] = (uint8_t)(e + 127);
+                tail->sstage[xb][jc][q >> 1] = (uint8_t)(ex[p] + 127);
+            }
+          }
+          ptx::named_bar_sync(1, 128);
+          // The chunk's rows, whole: warp q stores columns 4q..4q+3, 16 code bytes a
+          // lane (two lanes fill a row's 32-byte sector) and the two scale bytes.
+          if (lane < 8) {
+            const int jc = q * 4 + (lane >> 1);
+            if (jc < ncol) {
+              const size_t row = (size_t)row0 + c0 + jc;
+              const uint4 cv = *reinterpret_cast<const uint4*>(&tail->hstage[xb][jc][(lane & 1) * 16]);
+              *reinterpret_cast<uint4*>(args.ws.hb + row * hrow_bytes + (size_t)mt * 32 +
+                                        (lane & 1) * 16) = cv;
+            }
+          } else if (lane < 12) {
+            const int jc = q * 4 + (lane - 8);
+            if (jc < ncol) {
+              const size_t row = (size_t)row0 + c0 + jc;
+              const uint16_t sv = *reinterpret_cast<const uint16_t*>(&tail->sstage[xb][jc][0]);
+              *reinterpret_cast<uint16_t*>(args.ws.hsf + sf_atom_offset(row, mt * 2, i_kc4)) = sv;
             }
           }
           xb ^= 1;
         } else {
           // Down projection: this warp holds output features mt*128 + q*32 + lane of
           // up to 16 token columns; add them, weighted, into the fp32 accumulator.
-          int my_tok = 0;
-          float my_w = 0.f;
-          if (lane < ncol) {
-            my_tok = args.ws.slot_token[row0 + c0 + lane];
-            my_w = args.ws.slot_weight[row0 + c0 + lane];
-          }
+          // Column c0+j's row metadata sits in lane (c0+j) % 32, register (c0+j) / 32.
+          const int my_tok = tok_r[ci >> 1];
+          const float my_w = w_r[ci >> 1];
           const size_t feat = (size_t)mt * kBM + q * 32 + lane;
 #pragma unroll
           for (int j = 0; j < kEpiCols; ++j) {
-            const int tok = __shfl_sync(kFull, my_tok, j);
-            const float wt = __shfl_sync(kFull, my_w, j);
+            const int src = (ci & 1) * kEpiCols + j;
+            const int tok = __shfl_sync(kFull, my_tok, src);
+            const float wt = __shfl_sync(kFull, my_w, src);
             if (j < ncol) atomicAdd(args.ws.acc + (size_t)tok * args.H + feat, wt * v[j]);
           }
         }
+        if (more) ptx::tmem_wait_ld(nxt);
       }
       if (MODE == kModeLayer && item_phase == 0) {
         // Publish: this item's intermediate rows (and scales) are written.
@@ -494,6 +651,9 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
 
   ptx::tc_fence_before();
   __syncthreads();
+  // Neither block of a pair leaves while the other may still write into its shared
+  // memory (multicast copies) or arrive on its barriers.
+  if (PAIR) ptx::cluster_sync_all();
   if (warp == 1) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem_base, kTmemCols);
@@ -559,27 +719,45 @@ PhaseArgs phase_args(const uint8_t* w_sf, const uint8_t* t_sf, int rows_per_expe
   return p;
 }
 
-template <int MODE>
+// Pairs pay off once token tiles are wide: below this many assignments per expert
+// on average the token boxes are a small part of each stage and the single-block
+// kernel is used.
+constexpr int kPairMinRowsPerExpert = 64;
+
+template <int MODE, bool PAIR>
 cudaError_t launch_mode(const LayerLaunch& g, const CUtensorMap* maps, const LayerArgs& a,
                         cudaStream_t st) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t err = cudaFuncSetAttribute(moe_layer_kernel<MODE>,
+  static int grid = 0;   // per instantiation, for the device of the first launch
+  if (grid == 0) {
+    cudaError_t err = cudaFuncSetAttribute(moe_layer_kernel<MODE, PAIR>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)kSmemBytes);
     if (err != cudaSuccess) return err;
-    attr_set = true;
+    // Pairs too: two blocks of each SM, whichever pair they belong to (the
+    // occupancy query for clusters undercounts this; the work queue needs no
+    // particular number of resident blocks anyway).
+    const int blocks = kBlocksPerSM * g.num_sms;
+    grid = blocks;
   }
-  return launch_pdl(moe_layer_kernel<MODE>, dim3(kBlocksPerSM * g.num_sms), dim3(kThreads),
-                    kSmemBytes, st, maps[0], maps[1], maps[2], maps[3], a);
+  return launch_pdl_cluster(moe_layer_kernel<MODE, PAIR>, dim3(grid), dim3(kThreads), kSmemBytes,
+                            PAIR ? 2u : 1u, st, maps[0], maps[1], maps[2], maps[3], maps[4],
+                            maps[5], a);
 }
 
 }  // namespace
 
 cudaError_t launch_layer(const LayerLaunch& g, cudaStream_t st) {
   const Shape& s = g.shape;
-  CUtensorMap maps[4];
+  // Pairs split each slab count in two: both phases need an even number of slabs.
+  const bool pair = (2 * s.I / kBM) % 2 == 0 && (s.H / kBM) % 2 == 0 &&
+                    (int64_t)g.T * s.k >= (int64_t)kPairMinRowsPerExpert * s.E;
+  // Full token tiles come in one box per block: all 128 rows, or a pair's half.
+  const uint32_t full_rows = pair ? kBN / 2 : kBN;
+  CUtensorMap maps[6];
   cudaError_t err;
+  if ((err = make_tmap(&maps[4], g.ws.xb, (uint64_t)s.H / 2, (uint64_t)g.R_cap, full_rows)) ||
+      (err = make_tmap(&maps[5], g.ws.hb, (uint64_t)s.I / 2, (uint64_t)g.R_cap, full_rows)))
+    return err;
   if ((err = make_tmap(&maps[0], g.w1_codes, (uint64_t)s.H / 2, (uint64_t)s.E * 2 * s.I, kBM)) ||
       (err = make_tmap(&maps[1], g.ws.xb, (uint64_t)s.H / 2, (uint64_t)g.R_cap, kBBoxRows)) ||
       (err = make_tmap(&maps[2], g.w2_codes, (uint64_t)s.I / 2, (uint64_t)s.E * s.H, kBM)) ||
@@ -595,8 +773,11 @@ cudaError_t launch_layer(const LayerLaunch& g, cudaStream_t st) {
   a.E = s.E;
   a.ws = g.ws;
   a.gate_up_debug = g.gate_up_debug;
-  return g.num_phases == 2 ? launch_mode<kModeLayer>(g, maps, a, st)
-                           : launch_mode<kModeRaw>(g, maps, a, st);
+  if (g.num_phases == 2)
+    return pair ? launch_mode<kModeLayer, true>(g, maps, a, st)
+                : launch_mode<kModeLayer, false>(g, maps, a, st);
+  return pair ? launch_mode<kModeRaw, true>(g, maps, a, st)
+              : launch_mode<kModeRaw, false>(g, maps, a, st);
 }
 
 }  // namespace mxmoe
