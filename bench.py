@@ -399,9 +399,35 @@ def run_ours(args):
         mx.moe_check(ws, stream)
         return [s_.elapsed_time(e_) for s_, e_ in zip(starts, ends)], mx.moe_profile_read()
 
+    def timed_graph_pass():
+        """The same step captured once as a CUDA graph and replayed K times, L2
+        flushed (eagerly) before each replay."""
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream, capture_error_mode="thread_local"):
+            step()
+        with torch.cuda.stream(stream):
+            for _ in range(2):
+                flush_l2()
+                graph.replay()
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        with torch.cuda.stream(stream):
+            for i in range(args.steps):
+                flush_l2()
+                starts[i].record(stream)
+                graph.replay()
+                ends[i].record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        mx.moe_check(ws, stream)
+        return [s_.elapsed_time(e_) for s_, e_ in zip(starts, ends)]
+
     with ClockSampler(local) as clocks:
         step_ms, _ = timed_pass(False)
         prof_step_ms, per_kernel = timed_pass(True)
+        graph_ms = timed_graph_pass()
     probe = fp4_mma_probe(mx, ws, stream, mx.moe_device_sm_count())
     ms_local = statistics.mean(step_ms)
     ms = max_over_ranks(world, ms_local)
@@ -477,6 +503,11 @@ def run_ours(args):
         "roofline": roof,
         "roofline_other": other_roof,
         "kernels_ms": kern_ms,
+        "step_us": {"mean": ms_local * 1e3, "median": statistics.median(step_ms) * 1e3,
+                    "min": min(step_ms) * 1e3},
+        "graph_step_us": {"mean": statistics.mean(graph_ms) * 1e3,
+                          "median": statistics.median(graph_ms) * 1e3,
+                          "min": min(graph_ms) * 1e3},
         "profiled_ms_per_step": statistics.mean(prof_step_ms),
         "clocks": clocks.summary(),
         "gpu_launches": KERNELS_PER_STEP * args.steps,   # in the headline timed pass

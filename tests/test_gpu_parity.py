@@ -209,6 +209,36 @@ def test_forward_is_repeatable_and_host_path_matches(layers):
     assert normwise_rel_err(oracle.bf16_bits_to_f64(c), oracle.bf16_bits_to_f64(a)) <= 1e-3
 
 
+def test_cuda_graph_replay_matches_eager(layers):
+    """pre_dispatch + forward captured as one CUDA graph (the calls neither
+    synchronise nor allocate) and replayed: same intermediate codes as an eager run,
+    same output up to the order of the fp32 reductions."""
+    layer, W = layers("zipf")
+    w = layer.w
+    x = synth.hidden_bf16(w)
+    ids, tw = synth.routing(w)
+    eager = layer.run(x, ids, tw)
+    inter_e = mx.moe_read_intermediate(layer.dims, layer.ws, w.T)
+    xd, idd, twd = to_dev(x), to_dev(ids), to_dev(tw)
+    out = torch.empty((w.T, w.H), dtype=torch.bfloat16, device=device())
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s, capture_error_mode="thread_local"):
+        mx.moe_pre_dispatch(layer.dims, xd, idd, twd, w.T, layer.ws, s)
+        mx.moe_forward(layer.dims, layer.prepared, layer.ws, out, w.T, s)
+    for _ in range(3):
+        out.fill_(float("nan"))
+        with torch.cuda.stream(s):
+            g.replay()
+        s.synchronize()
+        mx.moe_check(layer.ws, s)
+        got = out.view(torch.int16).cpu().numpy().view(np.uint16)
+        assert normwise_rel_err(oracle.bf16_bits_to_f64(got), oracle.bf16_bits_to_f64(eager)) <= 1e-3
+    inter_g = mx.moe_read_intermediate(layer.dims, layer.ws, w.T)
+    assert np.array_equal(inter_g["h_codes"], inter_e["h_codes"])
+    assert np.array_equal(inter_g["h_scales"], inter_e["h_scales"])
+
+
 def test_forward_twice_on_one_pre_dispatch(layers):
     layer, W = layers("ragged")
     w = layer.w
