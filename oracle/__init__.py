@@ -61,6 +61,13 @@ def lib():
         l.oracle_moe.argtypes = [ctypes.POINTER(Shape)] + [vp] * 15 + [ci]
         l.oracle_moe.restype = i64
         l.oracle_moe_down.argtypes = [ctypes.POINTER(Shape)] + [vp] * 8 + [ci]
+        l.oracle_e4m3_value.argtypes = [ci]
+        l.oracle_e4m3_value.restype = ctypes.c_double
+        l.oracle_mxfp8_exponent.argtypes = [ctypes.c_double]
+        l.oracle_mxfp8_exponent.restype = ci
+        l.oracle_e4m3_encode.argtypes = [ctypes.c_double]
+        l.oracle_e4m3_encode.restype = ci
+        l.oracle_mxfp8_quantize_bf16.argtypes = [vp, i64, i64, vp, vp, ci]
         _lib = l
     return _lib
 
@@ -118,6 +125,36 @@ def dequantize(codes: np.ndarray, sf: np.ndarray) -> np.ndarray:
     out = np.empty((rows, half * 2), np.float64)
     lib().oracle_dequantize(_p(codes), _p(sf), rows, half * 2, _p(out))
     return out
+
+
+def e4m3_value(code: int) -> float:
+    return float(lib().oracle_e4m3_value(int(code)))
+
+
+def mxfp8_exponent(amax: float) -> int:
+    return int(lib().oracle_mxfp8_exponent(float(amax)))
+
+
+def e4m3_encode(q: float) -> int:
+    return int(lib().oracle_e4m3_encode(float(q)))
+
+
+def mxfp8_quantize_bf16(bits: np.ndarray, nthreads: int | None = None):
+    """bf16 bits [rows, K] -> (E4M3 codes [rows, K] uint8, scale bytes [rows, K/32] uint8)."""
+    bits = np.ascontiguousarray(bits, dtype=np.uint16)
+    rows, K = bits.shape
+    q = np.zeros((rows, K), np.uint8)
+    sf = np.zeros((rows, K // 32), np.uint8)
+    lib().oracle_mxfp8_quantize_bf16(_p(bits), rows, K, _p(q), _p(sf), nthreads or threads())
+    return q, sf
+
+
+def mxfp8_packed_scales(sf: np.ndarray) -> np.ndarray:
+    """Scale bytes [rows, K/32] -> packed int32 [rows, K/128] (groups 4j..4j+3 in bytes 0..3)."""
+    rows, kc = sf.shape
+    assert kc % 4 == 0
+    b = sf.astype(np.uint32).reshape(rows, kc // 4, 4)
+    return (b[..., 0] | (b[..., 1] << 8) | (b[..., 2] << 16) | (b[..., 3] << 24)).astype(np.uint32)
 
 
 def interleave_source_rows(I: int) -> np.ndarray:

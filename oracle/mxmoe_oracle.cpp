@@ -383,4 +383,94 @@ void oracle_moe_down(const oracle_shape* s, const int32_t* ids, const float* tw,
                      nthreads);
 }
 
+// ---------------------------------------------------------------------------
+// MXFP8 producer (SGLang PR #48424, section "DeepGEMM producers write
+// FlashInfer's 128x4 scale layout"): a producer hands its consumer an MXFP8 pair,
+// FP8 values plus one power-of-two scale per 32 elements, the scales either
+// packed four to an int32 along K or in the 4-D [ceil(rows/128), K/128, 32, 4]
+// int32 layout (byte order R9), with padded rows' scales zero.
+// Readings where the page is silent:
+//   R13 E4M3: sign bit, 4 exponent bits (bias 7), 3 mantissa bits; exponent
+//       field 0 holds the subnormals m/8 * 2^-6; codes 0x7F and 0xFF are NaN; the
+//       largest finite magnitude is 448 (exponent field 15, mantissa 6).
+//   R14 The scale is 2^e with e the smallest integer such that
+//       amax <= 448 * 2^e (R2 with 448 in place of 6), clamped to [-127, 127];
+//       amax = 0 gives e = -127.  Stored as the UE8M0 byte e + 127.
+//   R15 Each element becomes the E4M3 value nearest to x * 2^-e, a tie going to
+//       the code with even mantissa field; the sign bit follows x.
+//   R16 Packed scales: word j of a row holds groups 4j..4j+3 in its bytes 0..3
+//       (little endian), i.e. the row-major scale bytes read as int32.
+
+// R13: value of one E4M3 code (NaN for 0x7F / 0xFF).
+double oracle_e4m3_value(int code) {
+    const int e = (code >> 3) & 15, m = code & 7;
+    const double sign = (code & 0x80) ? -1.0 : 1.0;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0) return sign * std::ldexp((double)m / 8.0, -6);
+    return sign * std::ldexp(1.0 + (double)m / 8.0, e - 7);
+}
+
+// R14: smallest e with amax <= 448 * 2^e, clamped to [-127, 127].
+int oracle_mxfp8_exponent(double amax) {
+    assert(std::isfinite(amax) && amax >= 0.0);
+    if (amax == 0.0) return -127;
+    int p = 0;
+    (void)std::frexp(amax, &p);  // amax = f * 2^p, f in [0.5, 1)
+    int e = p - 10;              // 448 * 2^(p-10) = 0.4375 * 2^p < amax: too small
+    assert(amax > std::ldexp(448.0, e));
+    while (amax > std::ldexp(448.0, e)) ++e;
+    if (e < -127) e = -127;
+    if (e > 127) e = 127;
+    return e;
+}
+
+// R15: nearest E4M3 code to q (|q| <= 448, exact in double), ties to the even
+// mantissa field.  The grid is uniform within each binade, spacing 2^(E-3)
+// (2^-9 for the subnormals), so rounding the quotient by that spacing to the
+// nearest integer, ties to even, picks the code; a result of 16 spacings is the
+// first code of the next binade.
+int oracle_e4m3_encode(double q) {
+    const int sign = std::signbit(q) ? 0x80 : 0;
+    const double a = std::fabs(q);
+    assert(a <= 448.0);
+    if (a < std::ldexp(1.0, -6)) {
+        const double m = std::nearbyint(a / std::ldexp(1.0, -9));   // 0..8
+        return sign | (int)m;                                       // 8 = smallest normal
+    }
+    int x = 0;
+    (void)std::frexp(a, &x);      // a in [2^(x-1), 2^x)
+    int E = x - 1;                // unbiased exponent, -6..8
+    double r = std::nearbyint(a / std::ldexp(1.0, E - 3));   // 8..16 spacings
+    if (r == 16.0) {
+        ++E;
+        r = 8.0;
+    }
+    assert(E + 7 >= 1 && E + 7 <= 15);
+    const int code = ((E + 7) << 3) | ((int)r - 8);
+    assert(code <= 0x7E);
+    return sign | code;
+}
+
+// bf16 bits [rows, K] -> E4M3 codes [rows, K] and scale bytes [rows, K/32]
+// (R14, R15), one group of 32 at a time.
+void oracle_mxfp8_quantize_bf16(const uint16_t* x, int64_t rows, int64_t K, uint8_t* q,
+                                uint8_t* sf, int nthreads) {
+    assert(K % 32 == 0);
+    parallel_for(rows, nthreads, [&](int64_t r0, int64_t r1) {
+        for (int64_t r = r0; r < r1; ++r)
+            for (int64_t g = 0; g < K / 32; ++g) {
+                double v[32], amax = 0.0;
+                for (int i = 0; i < 32; ++i) {
+                    v[i] = bf16_bits_to_double(x[r * K + g * 32 + i]);
+                    assert(std::isfinite(v[i]));
+                    amax = std::max(amax, std::fabs(v[i]));
+                }
+                const int e = oracle_mxfp8_exponent(amax);
+                for (int i = 0; i < 32; ++i)
+                    q[r * K + g * 32 + i] = (uint8_t)oracle_e4m3_encode(std::ldexp(v[i], -e));
+                sf[r * (K / 32) + g] = (uint8_t)(e + 127);
+            }
+    });
+}
+
 }  // extern "C"

@@ -14,6 +14,8 @@ from fractions import Fraction
 import numpy as np
 import pytest
 
+torch = pytest.importorskip("torch")
+
 import oracle
 import synth
 from tests.helpers import oracle_expert_weights
@@ -386,3 +388,98 @@ def test_threads_do_not_change_results():
     a = oracle.moe(x, ids, tw, *W, nthreads=1)
     b = oracle.moe(x, ids, tw, *W, nthreads=5)
     assert np.array_equal(a["out_f64"], b["out_f64"])
+
+
+# --------------------------------------------------------------------------
+# MXFP8 producer (SGLang PR #48424, "DeepGEMM producers write FlashInfer's 128x4
+# scale layout"): E4M3 values with one UE8M0 scale per 32 elements.
+
+def _e4m3_all_values():
+    return np.array([oracle.e4m3_value(c) for c in range(256)])
+
+
+def test_e4m3_grid_matches_torch_float8():
+    """Every E4M3 code decodes to what PyTorch's float8_e4m3fn type gives it."""
+    ref = torch.arange(256, dtype=torch.int32).to(torch.uint8).view(torch.float8_e4m3fn)
+    ref = ref.to(torch.float64).numpy()
+    got = _e4m3_all_values()
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(got[ok], ref[ok])
+    assert got[0x7E] == 448.0 and np.isnan(got[0x7F]) and got[0x01] == 2.0 ** -9
+
+
+def test_e4m3_encode_matches_torch_and_brute_force():
+    """Round to nearest E4M3, ties to the even mantissa: against PyTorch's cast and a
+    brute-force nearest search, on every exact tie between neighbouring codes, on
+    the codes themselves, on the subnormal range and on random values."""
+    vals = _e4m3_all_values()
+    pos = np.sort(vals[:0x7F])                  # 0 .. 448, finite non-negative
+    # fp32 values (the producer's scaled inputs are bf16 * 2^-e, exact in fp32);
+    # PyTorch casts wider types through fp32, so fp32 inputs make its cast a
+    # single rounding
+    ties = ((pos[1:] + pos[:-1]) / 2).astype(np.float32)
+    rng = np.random.default_rng(21)
+    q = np.concatenate([pos.astype(np.float32), ties, np.nextafter(ties, np.float32(0)),
+                        np.nextafter(ties, np.float32(1e9)),
+                        rng.uniform(0, 448, 4000).astype(np.float32),
+                        rng.uniform(0, 2.0 ** -5, 1000).astype(np.float32),
+                        (2.0 ** rng.uniform(-12, 8.8, 2000)).astype(np.float32)])
+    q = np.clip(q, 0, 448).astype(np.float64)
+    q = np.concatenate([q, -q])
+    got = np.array([oracle.e4m3_encode(v) for v in q])
+    ref = torch.from_numpy(q).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(got, ref)
+    # brute force: nearest finite code, ties to the even code, sign kept
+    cand = np.arange(0x7F)
+    for v, c in zip(q[::7], got[::7]):
+        d = np.abs(vals[cand] - abs(v))
+        best = cand[d == d.min()]
+        want = best[best % 2 == 0][0] if len(best) > 1 else best[0]
+        assert c == (want | (0x80 if np.signbit(v) else 0))
+
+
+def test_mxfp8_exponent_against_definition():
+    rng = np.random.default_rng(22)
+    amaxes = np.concatenate([[0.0, 448.0, 448.0 * (1 + 2.0 ** -20), 224.0, 1.0, 2.0 ** -140],
+                             2.0 ** rng.uniform(-130, 120, 3000)])
+    for a in amaxes:
+        e = oracle.mxfp8_exponent(a)
+        if a == 0:
+            assert e == -127
+            continue
+        # smallest e with a <= 448 * 2^e, within the clamp
+        want = next(k for k in range(-200, 200) if a <= 448.0 * 2.0 ** k)
+        assert e == max(-127, min(127, want))
+
+
+def test_mxfp8_quantize_rows_against_torch_cast():
+    """Whole rows: each group's scale is the definition's, and its elements are
+    PyTorch's E4M3 cast of x * 2^-e; nonzero groups fill the top binade."""
+    rng = np.random.default_rng(23)
+    x = (rng.standard_normal((37, 256)) * 10.0 ** rng.uniform(-4, 4, (37, 1))).astype(np.float32)
+    x[3, 32:64] = 0.0
+    x[5, ::41] *= 300.0
+    bits = (torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy()).view(np.uint16)
+    xb = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    q, sf = oracle.mxfp8_quantize_bf16(bits)
+    g = xb.reshape(37, 8, 32)
+    amax = np.abs(g).max(axis=2)
+    e = sf.astype(np.int64) - 127
+    for r in range(37):
+        for j in range(8):
+            assert e[r, j] == oracle.mxfp8_exponent(amax[r, j])
+            if amax[r, j] > 0:
+                assert 224.0 < amax[r, j] * 2.0 ** -e[r, j] <= 448.0
+    scaled = g * np.ldexp(1.0, -e)[..., None]
+    ref = torch.from_numpy(scaled.reshape(37, 256)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(q, ref)
+    assert np.all(sf[3, 1] == 0)
+
+
+def test_mxfp8_packed_scales_are_row_major_bytes_as_int32():
+    sf = np.arange(3 * 16, dtype=np.uint8).reshape(3, 16)
+    packed = oracle.mxfp8_packed_scales(sf)
+    assert packed.shape == (3, 4)
+    assert packed[1, 2] == (24 | 25 << 8 | 26 << 16 | 27 << 24)   # row 1 = bytes 16..31
+    assert np.array_equal(packed.view(np.uint8).reshape(3, 16), sf)   # little-endian host
