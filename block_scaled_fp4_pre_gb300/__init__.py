@@ -85,6 +85,8 @@ def lib() -> ctypes.CDLL:
             "moe_bucket_noalloc": ([D, vp, vp, i32, vp, vp, vp], i32),
             "moe_debug_wait_probe": ([vp, i64, vp], i32),
             "moe_fp4_mma_probe": ([vp, i32, i32, i32, i64, vp], i32),
+            "moe_mxfp8_scale_bytes": ([i64, i64, i32], ctypes.c_size_t),
+            "moe_mxfp8_quantize": ([vp, i64, i64, vp, vp, i32, i64, vp], i32),
         }
         for name, (args, res) in sigs.items():
             f = getattr(l, name)
@@ -220,6 +222,21 @@ def moe_debug_gate_up(dims: MoeDims, prepared, ws, gate_up, num_tokens: int, str
 
 def moe_debug_wait_probe(ws, limit_ns: int, stream=None) -> None:
     _check(lib().moe_debug_wait_probe(_ptr(ws), int(limit_ns), _stream(stream)))
+
+
+MOE_SF_PACKED = 0
+MOE_SF_128X4 = 1
+
+
+def moe_mxfp8_scale_bytes(rows_cap: int, K: int, layout: int) -> int:
+    return int(lib().moe_mxfp8_scale_bytes(int(rows_cap), int(K), int(layout)))
+
+
+def moe_mxfp8_quantize(x, rows: int, K: int, q, sf, layout: int, rows_cap: int | None = None,
+                       stream=None) -> None:
+    """bf16 rows -> E4M3 values and UE8M0 scales (packed int32 or the 4-D 128x4 layout)."""
+    _check(lib().moe_mxfp8_quantize(_ptr(x), int(rows), int(K), _ptr(q), _ptr(sf), int(layout),
+                                    int(rows if rows_cap is None else rows_cap), _stream(stream)))
 
 
 def moe_fp4_mma_probe(ws, n: int, blocks_per_sm: int, blocks: int, mma_count: int,

@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libmxmoe.so")
 BUILD_DIR = os.path.join(PKG, "_build")
-SOURCES = ["api.cu", "dispatch.cu", "gemm.cu", "noalloc.cu", "peak.cu"]
+SOURCES = ["api.cu", "dispatch.cu", "gemm.cu", "noalloc.cu", "peak.cu", "mxfp8.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler",
          "-fvisibility=hidden", "-I", INCLUDE, "-I", CSRC]

@@ -622,6 +622,32 @@ moe_status moe_debug_wait_probe(void* ws, int64_t limit_ns, void* stream) {
   return MOE_OK;
 }
 
+size_t moe_mxfp8_scale_bytes(int64_t rows_cap, int64_t K, int32_t layout) {
+  if (rows_cap < 0 || K <= 0 || K % 128 || (layout != MOE_SF_PACKED && layout != MOE_SF_128X4))
+    return 0;
+  return mxfp8_scale_bytes(rows_cap, K, layout);
+}
+
+moe_status moe_mxfp8_quantize(const void* x, int64_t rows, int64_t K, void* q, void* sf,
+                              int32_t layout, int64_t rows_cap, void* stream) {
+  constexpr int64_t kMax = (int64_t)1 << 23;
+  if (K <= 0 || K % 128 || K > kMax)
+    return fail(MOE_ERR_INVALID_ARG, "K = %lld: must be a positive multiple of 128, at most 2^23",
+                (long long)K);
+  if (rows < 0 || rows > rows_cap || rows_cap > kMax)
+    return fail(MOE_ERR_INVALID_ARG, "rows = %lld, rows_cap = %lld: need 0 <= rows <= rows_cap <= 2^23",
+                (long long)rows, (long long)rows_cap);
+  if (layout != MOE_SF_PACKED && layout != MOE_SF_128X4)
+    return fail(MOE_ERR_INVALID_ARG, "unknown scale layout %d", layout);
+  if (!sf || !aligned(sf, 16)) return fail(MOE_ERR_INVALID_ARG, "sf must be a 16-byte aligned pointer");
+  if (rows > 0 && (!x || !q || !aligned(x, 16) || !aligned(q, 16)))
+    return fail(MOE_ERR_INVALID_ARG, "x and q must be 16-byte aligned pointers");
+  cudaError_t e = launch_mxfp8_quantize(x, rows, K, q, sf, layout, rows_cap,
+                                        static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "mxfp8 quantize");
+  return MOE_OK;
+}
+
 moe_status moe_fp4_mma_probe(void* ws, int32_t n, int32_t blocks_per_sm, int32_t blocks,
                              int64_t mma_count, void* stream) {
   if (!ws) return fail(MOE_ERR_INVALID_ARG, "workspace is NULL");

@@ -157,6 +157,9 @@ cudaError_t launch_prepare(const Shape& s, const uint8_t* w1c, const uint8_t* w1
 // One block waiting, with the given limit, on an mbarrier no one arrives at and on a
 // counter no one increments, through the same bounded waits as the layer kernel.
 cudaError_t launch_wait_probe(int32_t* flags, unsigned long long limit_ns, cudaStream_t st);
+size_t mxfp8_scale_bytes(int64_t rows_cap, int64_t K, int layout);
+cudaError_t launch_mxfp8_quantize(const void* x, int64_t rows, int64_t K, void* q, void* sf,
+                                  int layout, int64_t rows_cap, cudaStream_t st);
 cudaError_t launch_fp4_mma_probe(int n, int blocks_per_sm, int blocks, long long mma_count,
                                  int32_t* flags, cudaStream_t st);
 

@@ -193,6 +193,34 @@ MXMOE_API moe_status moe_debug_gate_up(const moe_dims *dims, const void *prepare
  * next moe_check returns MOE_ERR_TIMEOUT. */
 MXMOE_API moe_status moe_debug_wait_probe(void *ws_dev, int64_t limit_ns, void *stream);
 
+/* ---- MXFP8 producer ----
+ * SGLang PR #48424, section "DeepGEMM producers write FlashInfer's 128x4 scale
+ * layout": a producer hands a downstream MXFP8 GEMM an FP8 pair, E4M3 values plus one
+ * power-of-two (UE8M0) scale per 32 elements of a row, with the scales either packed
+ * four to an int32 along K or written directly in the 4-D int32 layout
+ * [ceil(rows/128), K/128, 32, 4], and padded rows' scales zeroed, so that the live
+ * rows' scales are a prefix of a buffer sized for more rows.
+ *
+ * x   bf16 [rows, K] row-major, device, 16-byte aligned.
+ * q   E4M3 codes [rows, K] row-major, device, 16-byte aligned (written).
+ * sf  scales, device, 16-byte aligned, moe_mxfp8_scale_bytes(rows_cap, K, layout) bytes:
+ *     MOE_SF_PACKED   int32 [rows_cap, K/128]; word j of a row holds groups 4j..4j+3
+ *                     in its bytes 0..3; rows rows..rows_cap-1 are zeroed.
+ *     MOE_SF_128X4    int32 [ceil(rows_cap/128), K/128, 32, 4]; the byte of (row r,
+ *                     group s) sits at ((r/128)*(K/128) + s/4)*512 + (r%32)*16 +
+ *                     ((r%128)/32)*4 + s%4; every row past `rows` is zeroed.
+ * Each group's scale is 2^e, e the smallest integer with amax <= 448 * 2^e (clamped to
+ * [-127, 127], amax = 0 gives -127), stored as the byte e + 127; each value is the
+ * E4M3 value nearest to x * 2^-e, ties to the even code, sign kept.
+ * 0 <= rows <= rows_cap <= 2^23, K a positive multiple of 128 (at most 2^23); inputs
+ * finite.  Stream-ordered, no allocation, no synchronisation.  MOE_ERR_INVALID_ARG for
+ * bad sizes, an unknown layout, or NULL / misaligned pointers. */
+enum { MOE_SF_PACKED = 0, MOE_SF_128X4 = 1 };
+MXMOE_API size_t moe_mxfp8_scale_bytes(int64_t rows_cap, int64_t K, int32_t sf_layout);
+MXMOE_API moe_status moe_mxfp8_quantize(const void *x, int64_t rows, int64_t K, void *q,
+                                        void *sf, int32_t sf_layout, int64_t rows_cap,
+                                        void *stream);
+
 /* FP4 tensor-core throughput probe (measurement only; the denominator of the
  * layer's compute roofline).  Launches `blocks` blocks of 128 threads on `stream`,
  * blocks_per_sm (1 or 2) of them resident per SM, each of which issues mma_count
