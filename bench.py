@@ -51,6 +51,8 @@ def parse_args():
                    help="override the expert count (small cases for profiler captures)")
     p.add_argument("--tokens", type=int, default=0, help="override the token count")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--dispatch", choices=["bucketed", "pull"], default="bucketed",
+                   help="token rows copied per expert by pre_dispatch, or gathered by the layer")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-sample-tokens", type=int, default=0)
     return p.parse_args()
@@ -260,12 +262,14 @@ def oracle_sample(w: synth.Workload, x, ids, tw, n_tokens: int):
     return tokens, sub, Wc
 
 
-def time_oracle(w, x, ids, tw, n_tokens: int, repeats: int = 1):
+def time_oracle(w, x, ids, tw, n_tokens: int, repeats: int = 1, min_seconds: float = 0.0):
+    """The oracle on the first n_tokens tokens (with all their experts), run `repeats`
+    times, or more until min_seconds of CPU work have been timed (at most 64 runs)."""
     import oracle
 
     tokens, sub, Wc = oracle_sample(w, x, ids, tw, n_tokens)
     times = []
-    for _ in range(repeats):
+    while len(times) < repeats or (sum(times) < min_seconds and len(times) < 64):
         t0 = time.perf_counter()
         oracle.moe(x[tokens], sub, tw[tokens], *Wc)
         times.append(time.perf_counter() - t0)
@@ -342,7 +346,7 @@ def run_reference(args):
         "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": config_dict(w, world),
+        "config": dict(config_dict(w, world), dispatch=args.dispatch),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.threads(),
                          "kind": "oracle",
                          "sample": f"first {len(tokens)} of {w.T} tokens per step, all their experts"},
@@ -387,6 +391,8 @@ def run_ours(args):
     out = torch.empty((w.T, w.H), dtype=torch.bfloat16, device=dev)
     ws = torch.empty(mx.moe_workspace_size(dims), dtype=torch.uint8, device=dev)
     mx.moe_workspace_init(dims, ws, stream)
+    mx.moe_workspace_set_dispatch(ws, mx.MOE_DISPATCH_PULL if args.dispatch == "pull"
+                                  else mx.MOE_DISPATCH_BUCKETED)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     clean = torch.ones(L2_CLEAN_BYTES // 4, dtype=torch.float32, device=dev)
 
@@ -511,11 +517,12 @@ def run_ours(args):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         n = args.cpu_sample_tokens or default_cpu_tokens(w)
-        r = time_oracle(w, x, ids, tw, n)
-        cpu = {"value": r["tokens"] / r["seconds"][0], "unit": "tokens/s", "cores": r["threads"],
+        r = time_oracle(w, x, ids, tw, n, min_seconds=10.0)
+        runs, secs = len(r["seconds"]), sum(r["seconds"])
+        cpu = {"value": r["tokens"] * runs / secs, "unit": "tokens/s", "cores": r["threads"],
                "kind": "oracle",
-               "sample": f"first {r['tokens']} of {w.T} tokens with all {w.k} experts each "
-                         f"({r['seconds'][0]:.1f} s of oracle time)"}
+               "sample": f"first {r['tokens']} of {w.T} tokens with all {w.k} experts each, "
+                         f"{runs} runs ({secs:.1f} s of oracle time)"}
 
     if rank != 0:
         return
@@ -525,7 +532,7 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": ms, "us_per_layer": ms * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "mxfp4 (e2m1 x ue8m0), fp32 accumulate", "data": "synthetic",
-        "config": config_dict(w, world),
+        "config": dict(config_dict(w, world), dispatch=args.dispatch),
         "layer_hbm_tbs": alg["layer_bytes"] / (ms / 1e3) / 1e12,
         "layer_roofline_frac": (alg["layer_bytes"] / (hbm_peak * 1e9)) / (ms / 1e3),
         "touched_experts": alg["touched_experts"],

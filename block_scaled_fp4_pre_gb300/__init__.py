@@ -86,6 +86,7 @@ def lib() -> ctypes.CDLL:
             "moe_debug_wait_probe": ([vp, i64, vp], i32),
             "moe_fp4_mma_probe": ([vp, i32, i32, i32, i64, vp], i32),
             "moe_mxfp8_scale_bytes": ([i64, i64, i32], ctypes.c_size_t),
+            "moe_workspace_set_dispatch": ([vp, i32], i32),
             "moe_mxfp8_quantize": ([vp, i64, i64, vp, vp, i32, i64, vp], i32),
         }
         for name, (args, res) in sigs.items():
@@ -222,6 +223,15 @@ def moe_debug_gate_up(dims: MoeDims, prepared, ws, gate_up, num_tokens: int, str
 
 def moe_debug_wait_probe(ws, limit_ns: int, stream=None) -> None:
     _check(lib().moe_debug_wait_probe(_ptr(ws), int(limit_ns), _stream(stream)))
+
+
+MOE_DISPATCH_BUCKETED = 0
+MOE_DISPATCH_PULL = 1
+
+
+def moe_workspace_set_dispatch(ws, mode: int) -> None:
+    """Bucketed token copies (TMA) or per-token rows gathered by the layer kernel."""
+    _check(lib().moe_workspace_set_dispatch(_ptr(ws), int(mode)))
 
 
 MOE_SF_PACKED = 0

@@ -71,6 +71,8 @@ WsLayout ws_layout(const moe_dims& d) {
   L.off_slot_weight = take((size_t)L.R_cap * 4);
   L.off_xb = take((size_t)L.R_cap * H / 2);
   L.off_xsf = take((size_t)L.R_cap * H / 32);
+  L.off_xq = take((size_t)L.T_cap * H / 2);
+  L.off_xs = take((size_t)L.T_cap * H / 32);
   L.off_hb = take((size_t)L.R_cap * I / 2);
   L.off_hsf = take((size_t)L.R_cap * I / 32);
   L.off_acc = take((size_t)L.T_cap * H * 4);
@@ -99,6 +101,8 @@ WsPtrs ws_ptrs(void* ws, const WsLayout& L) {
   p.slot_weight = reinterpret_cast<float*>(b + L.off_slot_weight);
   p.xb = b + L.off_xb;
   p.xsf = b + L.off_xsf;
+  p.xq = b + L.off_xq;
+  p.xs = b + L.off_xs;
   p.hb = b + L.off_hb;
   p.hsf = b + L.off_hsf;
   p.acc = reinterpret_cast<float*>(b + L.off_acc);
@@ -129,9 +133,17 @@ Shape shape_of(const moe_dims& d) { return Shape{d.hidden, d.inter, d.num_expert
 struct WsState {
   moe_dims dims;
   bool dispatched;
+  int dispatch_mode;   // MOE_DISPATCH_*
 };
 std::mutex g_reg_mu;
 std::map<const void*, WsState> g_registry;
+
+// Dispatch mode of a registered workspace (bucketed copies if unknown).
+int dispatch_mode(const void* ws) {
+  std::lock_guard<std::mutex> lk(g_reg_mu);
+  auto it = g_registry.find(ws);
+  return it == g_registry.end() ? MOE_DISPATCH_BUCKETED : it->second.dispatch_mode;
+}
 
 // Marks the workspace's pre_dispatch as consumed; returns whether it was fresh.
 bool take_dispatch(const void* ws) {
@@ -264,7 +276,7 @@ moe_status pre_dispatch_impl(const moe_dims* d, const void* x, const int32_t* id
   if (e != cudaSuccess) return cuda_fail(e, "bucket kernel");
   {
     ProfScope ps("quantize_scatter", st);
-    e = launch_quantize_scatter(s, x, ids, tw, T, p, st);
+    e = launch_quantize_scatter(s, x, ids, tw, T, p, dispatch_mode(ws) == MOE_DISPATCH_PULL, st);
   }
   if (e != cudaSuccess) return cuda_fail(e, "quantize kernel");
   mark_dispatched(ws);
@@ -287,6 +299,7 @@ LayerLaunch layer_launch(const moe_dims* d, const void* prepared, void* ws, int3
   g.ws = ws_ptrs(ws, L);
   g.gate_up_debug = nullptr;
   g.num_sms = sm_count();
+  g.pull = dispatch_mode(ws) == MOE_DISPATCH_PULL;
   return g;
 }
 
@@ -365,7 +378,20 @@ moe_status moe_workspace_init(const moe_dims* dims, void* ws, size_t ws_bytes, v
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "workspace header");
   std::lock_guard<std::mutex> lk(g_reg_mu);
-  g_registry[ws] = WsState{*dims, false};
+  g_registry[ws] = WsState{*dims, false, MOE_DISPATCH_BUCKETED};
+  return MOE_OK;
+}
+
+moe_status moe_workspace_set_dispatch(void* ws, int32_t mode) {
+  if (!ws) return fail(MOE_ERR_INVALID_ARG, "workspace is NULL");
+  if (mode != MOE_DISPATCH_BUCKETED && mode != MOE_DISPATCH_PULL)
+    return fail(MOE_ERR_INVALID_ARG, "unknown dispatch mode %d", mode);
+  std::lock_guard<std::mutex> lk(g_reg_mu);
+  auto it = g_registry.find(ws);
+  if (it == g_registry.end())
+    return fail(MOE_ERR_WORKSPACE_MISMATCH, "workspace %p was not initialised", ws);
+  it->second.dispatch_mode = mode;
+  it->second.dispatched = false;   // a pre_dispatch in the new mode must come first
   return MOE_OK;
 }
 
@@ -521,7 +547,30 @@ moe_status moe_read_dispatch(const moe_dims* dims, const void* ws, int32_t T, in
     for (int64_t a = 0; a < A; ++a)
       slot_token_host[a] = (assign[a] >= 0 && assign[a] < R) ? st[assign[a]] : -1;
   }
-  if (xc_host || xs_host) {
+  if ((xc_host || xs_host) && dispatch_mode(ws) == MOE_DISPATCH_PULL) {
+    // one row per token; an assignment's row is its token's
+    std::vector<uint8_t> codes((size_t)T * H / 2), sf((size_t)T * H / 32);
+    if (T && (e = cudaMemcpy(codes.data(), b + L.off_xq, codes.size(), cudaMemcpyDeviceToHost)))
+      return cuda_fail(e, "codes read");
+    if (T && (e = cudaMemcpy(sf.data(), b + L.off_xs, sf.size(), cudaMemcpyDeviceToHost)))
+      return cuda_fail(e, "scales read");
+    for (int64_t a = 0; a < A; ++a) {
+      const bool ok = assign[a] >= 0 && assign[a] < R;
+      const int64_t t = a / k;
+      if (xc_host) {
+        if (ok)
+          std::memcpy(xc_host + a * (H / 2), codes.data() + (size_t)t * H / 2, (size_t)H / 2);
+        else
+          std::memset(xc_host + a * (H / 2), 0, (size_t)H / 2);
+      }
+      if (xs_host) {
+        if (ok)
+          std::memcpy(xs_host + a * (H / 32), sf.data() + (size_t)t * H / 32, (size_t)H / 32);
+        else
+          std::memset(xs_host + a * (H / 32), 0, (size_t)H / 32);
+      }
+    }
+  } else if (xc_host || xs_host) {
     std::vector<uint8_t> codes((size_t)R * H / 2), sf((size_t)R * H / 32);
     if (R && (e = cudaMemcpy(codes.data(), b + L.off_xb, codes.size(), cudaMemcpyDeviceToHost)))
       return cuda_fail(e, "codes read");

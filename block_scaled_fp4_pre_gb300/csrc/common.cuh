@@ -67,7 +67,7 @@ struct WsLayout {
   int64_t T_cap, A_cap, R_cap, tiles_cap;
   size_t off_header, off_flags, off_counts, off_seg, off_tiles, off_tile_done, off_assign,
       off_local_rank, off_blk_base, off_tile_start,
-      off_slot_token, off_slot_assign, off_slot_weight, off_xb, off_xsf, off_hb,
+      off_slot_token, off_slot_assign, off_slot_weight, off_xb, off_xsf, off_xq, off_xs, off_hb,
       off_hsf, off_acc, off_stage_x, off_stage_ids, off_stage_w, off_stage_out, total;
 };
 
@@ -86,6 +86,8 @@ struct WsPtrs {
   float* slot_weight;    // [R_cap]
   uint8_t* xb;           // [R_cap, H/2] quantised token rows
   uint8_t* xsf;          // 128x4 blocks of [R_cap, H/32]
+  uint8_t* xq;           // [T_cap, H/2] quantised token rows, one per token (pull dispatch)
+  uint8_t* xs;           // [T_cap, H/32] their scales, row-major (pull dispatch)
   uint8_t* hb;           // [R_cap, I/2] requantised intermediate rows
   uint8_t* hsf;          // 128x4 blocks of [R_cap, I/32]
   float* acc;            // [T_cap, H] fp32 combine accumulator, cleared by pre_dispatch
@@ -141,8 +143,11 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 cudaError_t launch_bucket(const Shape& s, const int32_t* ids, int T, const WsPtrs& ws,
                           cudaStream_t st);
 // Quantise the tokens, give every assignment its row and copy the token there.
+// pull: write each token's row once (xq/xs) instead of copying it to its k rows; the
+// layer kernel then gathers token rows itself.
 cudaError_t launch_quantize_scatter(const Shape& s, const void* x, const int32_t* ids,
-                                    const float* tw, int T, const WsPtrs& ws, cudaStream_t st);
+                                    const float* tw, int T, const WsPtrs& ws, bool pull,
+                                    cudaStream_t st);
 // Rows of all assignments and the per-row tables, without quantising anything.
 cudaError_t launch_assign_slots(const Shape& s, const int32_t* ids, const float* tw, int T,
                                 const WsPtrs& ws, cudaStream_t st);
@@ -181,6 +186,7 @@ struct LayerLaunch {
   WsPtrs ws;
   float* gate_up_debug;      // [T*k, 2I] (num_phases == 1)
   int num_sms;
+  bool pull;                 // gate/up token rows gathered from ws.xq/xs (pull dispatch)
 };
 cudaError_t launch_layer(const LayerLaunch& g, cudaStream_t st);
 

@@ -222,7 +222,8 @@ __global__ void assign_slots_kernel(const int32_t* __restrict__ ids, const float
 __global__ void __launch_bounds__(256) quantize_scatter_kernel(const __nv_bfloat16* __restrict__ x,
                                                                const int32_t* __restrict__ ids,
                                                                const float* __restrict__ tw,
-                                                               int H, int k, int E, WsPtrs ws) {
+                                                               int H, int k, int E, WsPtrs ws,
+                                                               bool pull) {
   extern __shared__ __align__(16) uint8_t qsh[];       // [H/2 codes | H/32 scales]
   __shared__ int32_t slots[32];
   uint8_t* codes_sh = qsh;
@@ -254,11 +255,20 @@ __global__ void __launch_bounds__(256) quantize_scatter_kernel(const __nv_bfloat
     const float inv = ptx::pow2_neg(e);
 #pragma unroll
     for (int i = 0; i < 8; ++i) v[i] *= inv;
-    *reinterpret_cast<uint32_t*>(codes_sh + base / 2) = ptx::e2m1x8(v);
-    if ((tid & 3) == 0) sf_sh[base / 32] = (uint8_t)(e + 127);
+    const uint32_t c8 = ptx::e2m1x8(v);
+    const uint8_t sb = (uint8_t)(e + 127);
+    if (pull) {
+      // the token's one row, gathered by the layer kernel for each of its experts
+      *reinterpret_cast<uint32_t*>(ws.xq + (size_t)t * (H / 2) + base / 2) = c8;
+      if ((tid & 3) == 0) ws.xs[(size_t)t * (H / 32) + base / 32] = sb;
+    } else {
+      *reinterpret_cast<uint32_t*>(codes_sh + base / 2) = c8;
+      if ((tid & 3) == 0) sf_sh[base / 32] = sb;
+    }
   }
   ptx::pdl_wait();
   if (tid < k) slots[tid] = assign_slot(t * k + tid, k, E, ids, tw, ws);
+  if (pull) return;
   __syncthreads();
   const int kc4 = H / 128;
   const size_t row_bytes = (size_t)H / 2;
@@ -392,9 +402,10 @@ cudaError_t launch_bucket(const Shape& s, const int32_t* ids, int T, const WsPtr
 }
 
 cudaError_t launch_quantize_scatter(const Shape& s, const void* x, const int32_t* ids,
-                                    const float* tw, int T, const WsPtrs& ws, cudaStream_t st) {
+                                    const float* tw, int T, const WsPtrs& ws, bool pull,
+                                    cudaStream_t st) {
   return launch_pdl(quantize_scatter_kernel, dim3(T), dim3(256), (size_t)s.H / 2 + s.H / 32, st,
-                    reinterpret_cast<const __nv_bfloat16*>(x), ids, tw, s.H, s.k, s.E, ws);
+                    reinterpret_cast<const __nv_bfloat16*>(x), ids, tw, s.H, s.k, s.E, ws, pull);
 }
 
 cudaError_t launch_assign_slots(const Shape& s, const int32_t* ids, const float* tw, int T,

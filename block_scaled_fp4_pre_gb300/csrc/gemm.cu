@@ -159,7 +159,7 @@ __device__ __forceinline__ void ring_release(uint64_t* empty, int rank) {
 // and adjacent weight slabs (2p, 2p+1) of each item; each block loads half of the
 // token boxes and multicasts them into both, which halves the token rows read
 // from L2.  Block 0 of the pair claims the items and hands each to both blocks.
-template <int MODE, bool PAIR>
+template <int MODE, bool PAIR, bool PULL>
 __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
     moe_layer_kernel(const __grid_constant__ CUtensorMap tmap_w1,
                      const __grid_constant__ CUtensorMap tmap_x,
@@ -245,148 +245,208 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
 
   if (warp == 0) {
     // ------------------------------------------------- scheduler + producer
-    if (lane == 0) {
-      const uint64_t pol_once = ptx::policy_evict_first();
-      const uint64_t pol_shared = ptx::policy_evict_normal();
-      const uint64_t pol_t = ptx::policy_evict_last();
-      const bool scheduler = rank == 0;
-      int stage = 0, r = 0;
-      uint32_t phase = 0, rph = 0;
-      int64_t issued = 0;
-      bool ok = true;
-      // Items are claimed one ahead so that the claim and the table reads of the
-      // next item overlap the loads of the current one.
-      int g = 0;
-      Item it = {};
-      int4 ti = make_int4(0, 0, 0, 0);
-      if (scheduler) {
-        g = atomicAdd(&args.ws.flags[kFlagSched], 1);
-        if (g < total) {
-          it = decode_item(g, n0, m0, m1, E, tile_start);
-          ti = args.ws.tiles[it.tile];
-        }
+    // Lane 0 claims items, hands them on and issues the TMA copies; with PULL the
+    // whole warp also gathers the gate/up token rows of each stage (one row per
+    // token, written once by the quantiser) with per-thread asynchronous copies.
+    const bool leader = lane == 0;
+    const bool scheduler = rank == 0;
+    const uint64_t pol_once = ptx::policy_evict_first();
+    const uint64_t pol_shared = ptx::policy_evict_normal();
+    const uint64_t pol_t = ptx::policy_evict_last();
+    int stage = 0, r = 0;
+    uint32_t phase = 0, rph = 0;
+    int64_t issued = 0;
+    bool ok = true;
+    // Items are claimed one ahead so that the claim and the table reads of the
+    // next item overlap the loads of the current one.
+    int g = 0;
+    Item it = {};
+    int4 ti = make_int4(0, 0, 0, 0);
+    if (leader && scheduler) {
+      g = atomicAdd(&args.ws.flags[kFlagSched], 1);
+      if (g < total) {
+        it = decode_item(g, n0, m0, m1, E, tile_start);
+        ti = args.ws.tiles[it.tile];
       }
-      while (true) {
-        int item;
+    }
+    while (true) {
+      int item = -1;
+      if (leader) {
         if (scheduler) {
           item = g < total ? g : -1;
           if (!ptx::mbar_wait(&tail->ring_empty[r], rph ^ 1u, abort_flag, kWaitLimitNs)) {
             ok = false;
-            break;
-          }
-          const int4 rec = make_int4(item, ti.y, ti.z | (it.mt << 8), it.tile);
-          tail->ring[r] = rec;
-          ptx::mbar_arrive(&tail->ring_full[r]);
-          if (PAIR) {
-            // hand the same item to the second block of the pair
-            ptx::st_cluster_v4(ptx::cluster_addr(&tail->ring[r], 1), rec);
-            ptx::mbar_arrive_cluster(ptx::cluster_addr(&tail->ring_full[r], 1));
+          } else {
+            const int4 rec = make_int4(item, ti.y, ti.z | (it.mt << 8), it.tile);
+            tail->ring[r] = rec;
+            ptx::mbar_arrive(&tail->ring_full[r]);
+            if (PAIR) {
+              // hand the same item to the second block of the pair
+              ptx::st_cluster_v4(ptx::cluster_addr(&tail->ring[r], 1), rec);
+              ptx::mbar_arrive_cluster(ptx::cluster_addr(&tail->ring_full[r], 1));
+            }
           }
         } else {
           // second block of a pair: the item block 0 handed over
           if (!ptx::mbar_wait_cluster(&tail->ring_full[r], rph, abort_flag, kWaitLimitNs)) {
             ok = false;
-            break;
-          }
-          const int4 rec = tail->ring[r];
-          ptx::mbar_arrive_cluster(ptx::cluster_addr(&tail->ring_empty[r], 0));
-          item = rec.x;
-          if (item >= 0) {
-            it.phase = item < n0 ? 0 : 1;
-            it.tile = rec.w;
-            it.mt = rec.z >> 8;
-            it.e = args.ws.tiles[it.tile].x;
-            it.ntiles = tile_start[it.e + 1] - tile_start[it.e];
-            ti = make_int4(it.e, rec.y, rec.z & 0xFF, 0);
+          } else {
+            const int4 rec = tail->ring[r];
+            ptx::mbar_arrive_cluster(ptx::cluster_addr(&tail->ring_empty[r], 0));
+            item = rec.x;
+            if (item >= 0) {
+              it.phase = item < n0 ? 0 : 1;
+              it.tile = rec.w;
+              it.mt = rec.z >> 8;
+              it.e = args.ws.tiles[it.tile].x;
+              it.ntiles = tile_start[it.e + 1] - tile_start[it.e];
+              ti = make_int4(it.e, rec.y, rec.z & 0xFF, 0);
+            }
           }
         }
-        if (++r == kRing) {
-          r = 0;
-          rph ^= 1u;
+      }
+      // the item, to every lane
+      ok = __shfl_sync(kFull, ok ? 1 : 0, 0) != 0;
+      if (!ok) break;
+      item = __shfl_sync(kFull, item, 0);
+      if (++r == kRing) {
+        r = 0;
+        rph ^= 1u;
+      }
+      if (item < 0) break;
+      it.phase = __shfl_sync(kFull, it.phase, 0);
+      it.tile = __shfl_sync(kFull, it.tile, 0);
+      it.mt = __shfl_sync(kFull, it.mt, 0);
+      it.e = __shfl_sync(kFull, it.e, 0);
+      it.ntiles = __shfl_sync(kFull, it.ntiles, 0);
+      ti.y = __shfl_sync(kFull, ti.y, 0);
+      ti.z = __shfl_sync(kFull, ti.z, 0);
+      const int g_next = (leader && scheduler) ? atomicAdd(&args.ws.flags[kFlagSched], 1) : total;
+      Item it_next = {};
+      int4 ti_next = make_int4(0, 0, 0, 0);
+      const PhaseArgs& P = args.ph[it.phase];
+      const CUtensorMap* tw = it.phase ? &tmap_w2 : &tmap_w1;
+      const CUtensorMap* tt = it.phase ? &tmap_h : &tmap_x;
+      // a full tile's token rows in one box (one half-tile box per block of a pair)
+      const CUtensorMap* tt_full = it.phase ? &tmap_h_full : &tmap_x_full;
+      // A slab read by one token tile only is not kept; one shared by several
+      // tiles of the expert stays for them.
+      const uint64_t pol_w = it.ntiles > 1 ? pol_shared : pol_once;
+      const int e = it.e, row0 = ti.y, n = ti.z;
+      const int nb = (n + kBBoxRows - 1) / kBBoxRows;
+      const int mt = it.mt * (PAIR ? 2 : 1) + rank;   // this block's weight slab
+      const int wrow = e * P.rows_per_expert + mt * kBM;
+      const uint8_t* wsf = P.w_sf + ((size_t)(e * P.m_tiles + mt) * P.kc4) * kSFAtomBytes;
+      const uint8_t* tsf = P.t_sf + ((size_t)(row0 / kBN) * P.kc4) * kSFAtomBytes;
+      // Pulled token rows: lane l gathers rows l, l+32, l+64, l+96 of the tile.
+      const bool pulled = PULL && it.phase == 0;
+      int tok[kBN / 32];
+#pragma unroll
+      for (int i = 0; i < kBN / 32; ++i)
+        tok[i] = (pulled && lane + 32 * i < n) ? args.ws.slot_token[row0 + lane + 32 * i] : -1;
+      if (it.phase == 1) {
+        // The down projection reads the intermediate rows that this tile's
+        // gate/up items wrote with ordinary stores.
+        if (leader) {
+          ok = ptx::wait_counter(&args.ws.tile_done[it.tile], slabs0, abort_flag, kWaitLimitNs);
+          if (ok) ptx::fence_proxy_async_global();
         }
-        if (item < 0) break;
-        const int g_next = scheduler ? atomicAdd(&args.ws.flags[kFlagSched], 1) : total;
-        Item it_next = {};
-        int4 ti_next = make_int4(0, 0, 0, 0);
-        const PhaseArgs& P = args.ph[it.phase];
-        const CUtensorMap* tw = it.phase ? &tmap_w2 : &tmap_w1;
-        const CUtensorMap* tt = it.phase ? &tmap_h : &tmap_x;
-        // a full tile's token rows in one box (one half-tile box per block of a pair)
-        const CUtensorMap* tt_full = it.phase ? &tmap_h_full : &tmap_x_full;
-        // A slab read by one token tile only is not kept; one shared by several
-        // tiles of the expert stays for them.
-        const uint64_t pol_w = it.ntiles > 1 ? pol_shared : pol_once;
-        const int e = it.e, row0 = ti.y, n = ti.z;
-        const int nb = (n + kBBoxRows - 1) / kBBoxRows;
-        const int mt = it.mt * (PAIR ? 2 : 1) + rank;   // this block's weight slab
-        const int wrow = e * P.rows_per_expert + mt * kBM;
-        const uint8_t* wsf = P.w_sf + ((size_t)(e * P.m_tiles + mt) * P.kc4) * kSFAtomBytes;
-        const uint8_t* tsf = P.t_sf + ((size_t)(row0 / kBN) * P.kc4) * kSFAtomBytes;
-        if (it.phase == 1) {
-          // The down projection reads the intermediate rows that this tile's
-          // gate/up items wrote with ordinary stores.
-          if (!ptx::wait_counter(&args.ws.tile_done[it.tile], slabs0, abort_flag, kWaitLimitNs)) {
-            ok = false;
-            break;
+        ok = __shfl_sync(kFull, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
+      }
+      for (int kb = 0; kb < P.num_kb; ++kb) {
+        if (leader) ok = ptx::mbar_wait(&tail->empty[stage], phase ^ 1u, abort_flag, kWaitLimitNs);
+        ok = __shfl_sync(kFull, ok ? 1 : 0, 0) != 0;   // the stage is free for every lane
+        if (!ok) break;
+        const int kvalid = min(kBK, P.K - kb * kBK);
+        const int atoms = kvalid / 128;
+        uint64_t* bar = &tail->full[stage];
+        uint8_t* b_dst = smem + kSmemB + (size_t)stage * kBTileBytes;
+        if (pulled) {
+          // Row i of the tile is token tok's codes [kb*128, kb*128 + kvalid/2) in the
+          // 128-byte swizzle (16-byte chunk c of row i at chunk c ^ (i % 8)), and its
+          // scales in the 128x4 blocks the scale copy reads.
+          uint8_t* sf_dst = smem + kSmemSFB + (size_t)stage * kSFStageBytes;
+          // Lane l copies rows l, l+32, l+64, l+96: only live rows cost anything,
+          // which matters for the few-row tiles of decode-sized loads.
+          const int chunks = kvalid / 32;
+#pragma unroll
+          for (int i = 0; i < kBN / 32; ++i) {
+            const int row = lane + 32 * i;
+            if (tok[i] < 0) continue;
+            const uint8_t* src = args.ws.xq + (size_t)tok[i] * (args.H / 2) + (size_t)kb * kBKBytes;
+            uint8_t* dst = b_dst + row * kBKBytes;
+            for (int c = 0; c < chunks; ++c)
+              ptx::cp_async16(dst + ((c ^ (row & 7)) << 4), src + c * 16);
           }
-          ptx::fence_proxy_async_global();
+          // Scales: lane l, row l + 32 i, 4 bytes per 128-element block.
+#pragma unroll
+          for (int i = 0; i < kBN / 32; ++i) {
+            const int row = lane + 32 * i;
+            if (tok[i] < 0) continue;
+            const uint8_t* ssrc = args.ws.xs + (size_t)tok[i] * (args.H / 32) + (size_t)kb * 8;
+            for (int a = 0; a < atoms; ++a)
+              ptx::cp_async4(sf_dst + a * kSFAtomBytes + (row & 31) * 16 + (row >> 5) * 4,
+                             ssrc + a * 4);
+          }
+          ptx::cp_async_arrive(bar);
+          __syncwarp();   // every lane's copies count against the stage before lane 0 arrives
         }
-        for (int kb = 0; kb < P.num_kb; ++kb) {
-          if (!ptx::mbar_wait(&tail->empty[stage], phase ^ 1u, abort_flag, kWaitLimitNs)) {
-            ok = false;
-            break;
-          }
-          const int kvalid = min(kBK, P.K - kb * kBK);
-          const int atoms = kvalid / 128;
-          // every token box lands here: this block's own and, in a pair, the
-          // partner's multicast ones
+        if (leader) {
+          // every byte the TMA lands here: the weight box and scales and, unless
+          // pulled, the token rows (in a pair: this block's and the partner's
+          // multicast ones) and their scales
           const uint32_t bytes =
-              kATileBytes + nb * (kBBoxRows * kBKBytes) + 2u * atoms * kSFAtomBytes;
-          uint64_t* bar = &tail->full[stage];
+              kATileBytes + atoms * kSFAtomBytes +
+              (pulled ? 0u : (uint32_t)(nb * (kBBoxRows * kBKBytes) + atoms * kSFAtomBytes));
           ptx::mbar_arrive_expect_tx(bar, bytes);
           ptx::tma_load_2d(smem + kSmemA + (size_t)stage * kATileBytes, tw, kb * kBKBytes, wrow,
                            bar, pol_w);
           ptx::bulk_load(smem + kSmemSFA + (size_t)stage * kSFStageBytes,
                          wsf + (size_t)kb * 2 * kSFAtomBytes, atoms * kSFAtomBytes, bar, pol_w);
-          uint8_t* b_dst = smem + kSmemB + (size_t)stage * kBTileBytes;
-          if (nb * kBBoxRows == kBN) {
-            if (!PAIR) {
-              ptx::tma_load_2d(b_dst, tt_full, kb * kBKBytes, row0, bar, pol_t);
+          if (!pulled) {
+            if (nb * kBBoxRows == kBN) {
+              if (!PAIR) {
+                ptx::tma_load_2d(b_dst, tt_full, kb * kBKBytes, row0, bar, pol_t);
+              } else {
+                const int half = rank * (kBN / 2);
+                ptx::tma_load_2d_multicast(b_dst + half * kBKBytes, tt_full, kb * kBKBytes,
+                                           row0 + half, bar, kPairMask, pol_t);
+              }
             } else {
-              const int half = rank * (kBN / 2);
-              ptx::tma_load_2d_multicast(b_dst + half * kBKBytes, tt_full, kb * kBKBytes,
-                                         row0 + half, bar, kPairMask, pol_t);
+              for (int j = 0; j < nb; ++j) {
+                uint8_t* dst = b_dst + j * kBBoxRows * kBKBytes;
+                if (!PAIR)
+                  ptx::tma_load_2d(dst, tt, kb * kBKBytes, row0 + j * kBBoxRows, bar, pol_t);
+                else if ((j & 1) == rank)
+                  ptx::tma_load_2d_multicast(dst, tt, kb * kBKBytes, row0 + j * kBBoxRows, bar,
+                                             kPairMask, pol_t);
+              }
             }
-          } else {
-            for (int j = 0; j < nb; ++j) {
-              uint8_t* dst = b_dst + j * kBBoxRows * kBKBytes;
-              if (!PAIR)
-                ptx::tma_load_2d(dst, tt, kb * kBKBytes, row0 + j * kBBoxRows, bar, pol_t);
-              else if ((j & 1) == rank)
-                ptx::tma_load_2d_multicast(dst, tt, kb * kBKBytes, row0 + j * kBBoxRows, bar,
-                                           kPairMask, pol_t);
-            }
-          }
-          ptx::bulk_load(smem + kSmemSFB + (size_t)stage * kSFStageBytes,
-                         tsf + (size_t)kb * 2 * kSFAtomBytes, atoms * kSFAtomBytes, bar, pol_t);
-          ++issued;
-          if (++stage == kStages) {
-            stage = 0;
-            phase ^= 1u;
+            ptx::bulk_load(smem + kSmemSFB + (size_t)stage * kSFStageBytes,
+                           tsf + (size_t)kb * 2 * kSFAtomBytes, atoms * kSFAtomBytes, bar, pol_t);
           }
           if (kb == 0 && g_next < total) {
             it_next = decode_item(g_next, n0, m0, m1, E, tile_start);
             ti_next = args.ws.tiles[it_next.tile];
           }
         }
-        if (!ok) break;
-        g = g_next;
-        it = it_next;
-        ti = ti_next;
+        ++issued;
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
       }
-      if (!ok) atomicOr(&args.ws.flags[0], kErrTimeout);
-      // Drain: every copy this thread issued must have landed before the block
-      // exits (normally they all have, because the MMA consumed them).
+      if (!ok) break;
+      g = g_next;
+      it = it_next;
+      ti = ti_next;
+    }
+    if (leader && !ok) atomicOr(&args.ws.flags[0], kErrTimeout);
+    // Drain: every copy this warp issued must have landed before the block exits
+    // (normally they all have, because the MMA consumed them).
+    if (PULL) ptx::cp_async_wait_all();
+    if (leader) {
       const int64_t first = issued > kStages ? issued - kStages : 0;
       for (int64_t i = first; i < issued; ++i) {
         const int s = (int)(i % kStages);
@@ -415,6 +475,9 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
         const int item = rec.x;
         if (item < 0) break;
         const PhaseArgs& P = args.ph[item < n0 ? 0 : 1];
+        // gate/up token rows gathered by per-thread copies (generic proxy) are read
+        // by the tensor core (async proxy) after each stage's barrier
+        const bool pulled = PULL && item < n0;
         const int n = rec.z & 0xFF;
         const int n_mma = (n + kBBoxRows - 1) / kBBoxRows * kBBoxRows;
         if (!ptx::mbar_wait(&tail->acc_empty, acc_phase ^ 1u, abort_flag, kWaitLimitNs)) {
@@ -428,6 +491,7 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
             break;
           }
           ptx::tc_fence_after();
+          if (pulled) ptx::fence_proxy_async_smem();
           const int kvalid = min(kBK, P.K - kb * kBK);
           const int atoms = kvalid / 128;
           const uint32_t sfa_t = tmem_base + (uint32_t)(kSfTmemBase + sfbuf * 16);
@@ -724,12 +788,12 @@ PhaseArgs phase_args(const uint8_t* w_sf, const uint8_t* t_sf, int rows_per_expe
 // kernel is used.
 constexpr int kPairMinRowsPerExpert = 64;
 
-template <int MODE, bool PAIR>
+template <int MODE, bool PAIR, bool PULL>
 cudaError_t launch_mode(const LayerLaunch& g, const CUtensorMap* maps, const LayerArgs& a,
                         cudaStream_t st) {
   static int grid = 0;   // per instantiation, for the device of the first launch
   if (grid == 0) {
-    cudaError_t err = cudaFuncSetAttribute(moe_layer_kernel<MODE, PAIR>,
+    cudaError_t err = cudaFuncSetAttribute(moe_layer_kernel<MODE, PAIR, PULL>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)kSmemBytes);
     if (err != cudaSuccess) return err;
@@ -739,7 +803,7 @@ cudaError_t launch_mode(const LayerLaunch& g, const CUtensorMap* maps, const Lay
     const int blocks = kBlocksPerSM * g.num_sms;
     grid = blocks;
   }
-  return launch_pdl_cluster(moe_layer_kernel<MODE, PAIR>, dim3(grid), dim3(kThreads), kSmemBytes,
+  return launch_pdl_cluster(moe_layer_kernel<MODE, PAIR, PULL>, dim3(grid), dim3(kThreads), kSmemBytes,
                             PAIR ? 2u : 1u, st, maps[0], maps[1], maps[2], maps[3], maps[4],
                             maps[5], a);
 }
@@ -774,10 +838,14 @@ cudaError_t launch_layer(const LayerLaunch& g, cudaStream_t st) {
   a.ws = g.ws;
   a.gate_up_debug = g.gate_up_debug;
   if (g.num_phases == 2)
-    return pair ? launch_mode<kModeLayer, true>(g, maps, a, st)
-                : launch_mode<kModeLayer, false>(g, maps, a, st);
-  return pair ? launch_mode<kModeRaw, true>(g, maps, a, st)
-              : launch_mode<kModeRaw, false>(g, maps, a, st);
+    return g.pull ? (pair ? launch_mode<kModeLayer, true, true>(g, maps, a, st)
+                          : launch_mode<kModeLayer, false, true>(g, maps, a, st))
+                  : (pair ? launch_mode<kModeLayer, true, false>(g, maps, a, st)
+                          : launch_mode<kModeLayer, false, false>(g, maps, a, st));
+  return g.pull ? (pair ? launch_mode<kModeRaw, true, true>(g, maps, a, st)
+                        : launch_mode<kModeRaw, false, true>(g, maps, a, st))
+                : (pair ? launch_mode<kModeRaw, true, false>(g, maps, a, st)
+                        : launch_mode<kModeRaw, false, false>(g, maps, a, st));
 }
 
 }  // namespace mxmoe

@@ -226,6 +226,26 @@ __device__ __forceinline__ void tma_load_2d_multicast(void* smem_dst, const void
       : "memory");
 }
 
+// Per-thread asynchronous copies global -> shared (no registers involved): 16 bytes
+// (both addresses 16-byte aligned, L2 only) or 4 bytes (4-byte aligned).
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(smem_dst)), "l"(gsrc)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async4(void* smem_dst, const void* gsrc) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(smem_dst)), "l"(gsrc)
+               : "memory");
+}
+// Makes `bar` wait for this thread's earlier cp.async copies: its pending count
+// goes up by one now and back down when they have all landed.
+__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+// Waits for all of this thread's cp.async copies.
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 // Prefetch of a 2-D box into L2 (no shared memory, no completion to wait for).
 __device__ __forceinline__ void tma_prefetch_2d(const void* tmap, int32_t x, int32_t y) {
   asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(

@@ -105,6 +105,19 @@ MXMOE_API size_t moe_workspace_size(const moe_dims *dims);
 MXMOE_API moe_status moe_workspace_init(const moe_dims *dims, void *ws_dev, size_t ws_bytes,
                                         void *stream);
 
+/* How pre_dispatch hands the quantised tokens to the layer (SGLang PR #48424,
+ * Summary: "SIMT dispatch pull for FP4 activations"):
+ *   MOE_DISPATCH_BUCKETED (default after moe_workspace_init): each token's row is
+ *     copied to the row of every one of its assignments, expert-contiguous, and the
+ *     layer loads token tiles from there with TMA.
+ *   MOE_DISPATCH_PULL: each token's row is written once, and the layer gathers its
+ *     experts' token tiles from those rows with asynchronous per-thread copies.
+ * Both give the same results.  Set on an initialised workspace, before the
+ * pre_dispatch whose forward should use it; MOE_ERR_INVALID_ARG for an unknown mode,
+ * MOE_ERR_WORKSPACE_MISMATCH for a workspace moe_workspace_init has not seen. */
+enum { MOE_DISPATCH_BUCKETED = 0, MOE_DISPATCH_PULL = 1 };
+MXMOE_API moe_status moe_workspace_set_dispatch(void *ws_dev, int32_t mode);
+
 /* Quantises row-major fp32 src_dev [rows, K] (K % 32 == 0) to MXFP4 with the rule
  * above: codes_dev [rows, K/2], scales_dev [rows, K/32], both row-major.  A helper
  * for producing canonical MXFP4 weights on the device. */
