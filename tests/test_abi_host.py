@@ -114,3 +114,30 @@ def test_hot_calls_reject_uninitialised_workspace_without_touching_the_gpu(mx):
 def test_binding_has_the_c_names(mx):
     for name in declared_functions():
         assert hasattr(mx, name), name
+
+
+def test_mxfp8_producer_and_dispatch_mode_host_checks(mx):
+    """Sizing of the MXFP8 scale buffers and the argument checks of the producer and of
+    the dispatch-mode setter, all decided on the host before any CUDA call."""
+    lib = mx.lib()
+    # 4-D layout: rows padded to whole 128-row blocks, 512 bytes per block per 128 of K
+    assert mx.moe_mxfp8_scale_bytes(1, 256, mx.MOE_SF_128X4) == 1 * 2 * 512
+    assert mx.moe_mxfp8_scale_bytes(129, 256, mx.MOE_SF_128X4) == 2 * 2 * 512
+    # packed: one int32 per row per 128 of K
+    assert mx.moe_mxfp8_scale_bytes(129, 256, mx.MOE_SF_PACKED) == 129 * 2 * 4
+    assert mx.moe_mxfp8_scale_bytes(10, 100, mx.MOE_SF_PACKED) == 0     # K % 128 != 0
+    assert mx.moe_mxfp8_scale_bytes(10, 256, 9) == 0                     # unknown layout
+    fake = 1 << 20   # 16-byte aligned, never dereferenced: the host checks fail first
+    bad = [
+        (fake, 4, 100, fake, fake, 0, 4),        # K not a multiple of 128
+        (fake, 5, 128, fake, fake, 0, 4),        # rows > rows_cap
+        (fake, -1, 128, fake, fake, 0, 4),       # negative rows
+        (fake, 4, 128, fake, fake, 7, 4),        # unknown layout
+        (fake + 1, 4, 128, fake, fake, 0, 4),    # misaligned input
+        (fake, 4, 128, fake, fake + 8, 1, 4),    # misaligned scales
+    ]
+    for args in bad:
+        assert lib.moe_mxfp8_quantize(*args, None) == mx.MOE_ERR_INVALID_ARG, args
+    assert lib.moe_workspace_set_dispatch(fake, 5) == mx.MOE_ERR_INVALID_ARG
+    assert lib.moe_workspace_set_dispatch(None, 1) == mx.MOE_ERR_INVALID_ARG
+    assert lib.moe_workspace_set_dispatch(fake, 1) == mx.MOE_ERR_WORKSPACE_MISMATCH
