@@ -236,8 +236,14 @@ __global__ void __launch_bounds__(256) quantize_scatter_kernel(const __nv_bfloat
     const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int i = tid; i < H / 4; i += blockDim.x) acc[i] = z;
   }
-  for (int base = tid * 8; base < H; base += blockDim.x * 8) {
-    const uint4 raw = *reinterpret_cast<const uint4*>(x + (size_t)t * H + base);
+  // Every lane of a warp runs every round (the shuffles below need all 32): H is a
+  // multiple of 128, so a round can end mid-warp (H = 384: lanes 16-31 of warp 1 are
+  // past the row); those lanes work on zeros and store nothing.
+  for (int round0 = 0; round0 < H; round0 += blockDim.x * 8) {
+    const int base = round0 + tid * 8;
+    const bool live = base < H;
+    uint4 raw = make_uint4(0u, 0u, 0u, 0u);
+    if (live) raw = *reinterpret_cast<const uint4*>(x + (size_t)t * H + base);
     const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
     float v[8];
 #pragma unroll
@@ -257,6 +263,7 @@ __global__ void __launch_bounds__(256) quantize_scatter_kernel(const __nv_bfloat
     for (int i = 0; i < 8; ++i) v[i] *= inv;
     const uint32_t c8 = ptx::e2m1x8(v);
     const uint8_t sb = (uint8_t)(e + 127);
+    if (!live) continue;
     if (pull) {
       // the token's one row, gathered by the layer kernel for each of its experts
       *reinterpret_cast<uint32_t*>(ws.xq + (size_t)t * (H / 2) + base / 2) = c8;

@@ -32,6 +32,9 @@ SMALL = {
     "zipf": synth.Workload("zipf", T=1024, H=256, I=256, E=32, k=4, routing="zipf",
                            outlier_frac=0.001),
     "top1": synth.Workload("top1", T=96, H=256, I=128, E=1, k=1),
+    # 256 rows per expert (wide tiles) with an odd number of down slabs (H/128 = 3),
+    # so block pairs stay off, and a 128-wide last k-block in the gate/up phase
+    "oddslab": synth.Workload("oddslab", T=512, H=384, I=256, E=4, k=2),
 }
 
 
@@ -172,7 +175,7 @@ def test_gate_up_accumulators(layers, name):
 # --------------------------------------------------------------------------
 # Whole layer
 
-@pytest.mark.parametrize("name", ["tiny", "ragged", "zipf", "top1"])
+@pytest.mark.parametrize("name", ["tiny", "ragged", "zipf", "top1", "oddslab"])
 def test_forward_matches_oracle(layers, name):
     layer, W = layers(name)
     w = layer.w

@@ -29,6 +29,9 @@ SMALL = {
     "ragged": synth.Workload("ragged", T=700, H=512, I=384, E=8, k=2),
     "zipf": synth.Workload("zipf", T=1024, H=256, I=256, E=32, k=4, routing="zipf",
                            outlier_frac=0.001),
+    # a 128-wide last k-block in the gathered gate/up phase (H % 256 == 128), and an
+    # odd number of down slabs (no block pairs)
+    "oddslab": synth.Workload("oddslab", T=512, H=384, I=256, E=4, k=2),
 }
 
 
