@@ -49,6 +49,11 @@ constexpr int kBlocksPerSM = 2;
 constexpr int kTmemCols = 256;             // half of the SM's tensor memory per block
 constexpr int kAccCols = kBN;              // one fp32 accumulator of up to 128 columns
 constexpr int kSfTmemBase = kAccCols;      // scale registers (2 x 16 columns) after it
+// The rest of the block's tensor memory holds a copy of the accumulator's first
+// columns, so that the accumulator can go back to the MMA issuer before the math.
+constexpr int kSpareCol = kSfTmemBase + 32;
+constexpr int kSpareChunks = (kTmemCols - kSpareCol) / 16;   // 6 chunks of 16 columns
+static_assert(kSpareChunks == 6, "tensor memory layout");
 constexpr int kEpiCols = 16;               // accumulator columns per epilogue load
 constexpr int kRing = 8;                   // work items in flight inside a block
 constexpr unsigned kFull = 0xFFFFFFFFu;
@@ -577,28 +582,10 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
       acc_phase ^= 1u;
       ptx::tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16);
-      // Chunks of 16 columns; the load of chunk ci+1 runs during the math of ci.
-      uint32_t ra[kEpiCols], rb[kEpiCols];
-      ptx::tmem_ld16_issue(taddr, ra);
-      ptx::tmem_wait_ld(ra);
-#pragma unroll
-      for (int ci = 0; ci < kBN / kEpiCols; ++ci) {
+      const uint32_t tspare = taddr + (uint32_t)kSpareCol;
+      // The math of one 16-column chunk, wherever its values were read from.
+      auto chunk = [&](const int ci, const float(&v)[kEpiCols]) {
         const int c0 = ci * kEpiCols;
-        if (c0 >= n) break;
-        uint32_t(&cur)[kEpiCols] = (ci & 1) ? rb : ra;
-        uint32_t(&nxt)[kEpiCols] = (ci & 1) ? ra : rb;
-        const bool more = c0 + kEpiCols < n;
-        if (more) {
-          ptx::tmem_ld16_issue(taddr + (uint32_t)(c0 + kEpiCols), nxt);
-        } else {
-          // Every load of this item is done: hand the accumulator back to the MMA
-          // issuer before the last chunk's math, so the next item's MMAs overlap it.
-          ptx::tc_fence_before();
-          ptx::mbar_arrive(&tail->acc_empty);
-        }
-        float v[kEpiCols];
-#pragma unroll
-        for (int j = 0; j < kEpiCols; ++j) v[j] = __uint_as_float(cur[j]);
         const int ncol = min(kEpiCols, n - c0);
         if (MODE == kModeRaw) {
           const int m = mt * kBM + q * 32 + lane;
@@ -699,6 +686,65 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
             if (j < ncol) atomicAdd(args.ws.acc + (size_t)tok * args.H + feat, wt * v[j]);
           }
         }
+      };
+      const int nch = (n + kEpiCols - 1) / kEpiCols;
+      const int ncopy = min(nch, kSpareChunks);
+      // 1. The first ncopy chunks (up to 96 columns) into this block's spare tensor
+      //    memory, two loads in flight.
+#pragma unroll
+      for (int ci = 0; ci < kSpareChunks; ci += 2) {
+        if (ci < ncopy) {
+          uint32_t r0[kEpiCols], r1[kEpiCols];
+          const bool two = ci + 1 < ncopy;
+          ptx::tmem_ld16_issue(taddr + (uint32_t)(ci * kEpiCols), r0);
+          if (two) ptx::tmem_ld16_issue(taddr + (uint32_t)((ci + 1) * kEpiCols), r1);
+          ptx::tmem_wait_ld(r0);
+          if (two) ptx::tmem_wait_ld(r1);
+          ptx::tmem_st16(tspare + (uint32_t)(ci * kEpiCols), r0);
+          if (two) ptx::tmem_st16(tspare + (uint32_t)((ci + 1) * kEpiCols), r1);
+        }
+      }
+      // 2. Columns past the spare area straight from the accumulator.  Once every
+      //    accumulator load is done it goes back to the MMA issuer, so the next
+      //    item's MMAs run during the rest of this item's math.
+#pragma unroll
+      for (int ci = kSpareChunks; ci < kBN / kEpiCols; ++ci) {
+        if (ci < nch) {
+          uint32_t r[kEpiCols];
+          ptx::tmem_ld16_issue(taddr + (uint32_t)(ci * kEpiCols), r);
+          ptx::tmem_wait_ld(r);
+          if (ci + 1 >= nch) {
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(&tail->acc_empty);
+          }
+          float v[kEpiCols];
+#pragma unroll
+          for (int j = 0; j < kEpiCols; ++j) v[j] = __uint_as_float(r[j]);
+          chunk(ci, v);
+        }
+      }
+      if (nch <= kSpareChunks) {
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(&tail->acc_empty);
+      }
+      ptx::tmem_wait_st();
+      // 3. The copied chunks; the load of chunk ci+1 runs during the math of ci.
+      uint32_t ra[kEpiCols], rb[kEpiCols];
+      if (ncopy > 0) {
+        ptx::tmem_ld16_issue(tspare, ra);
+        ptx::tmem_wait_ld(ra);
+      }
+#pragma unroll
+      for (int ci = 0; ci < kSpareChunks; ++ci) {
+        if (ci >= ncopy) break;
+        uint32_t(&cur)[kEpiCols] = (ci & 1) ? rb : ra;
+        uint32_t(&nxt)[kEpiCols] = (ci & 1) ? ra : rb;
+        const bool more = ci + 1 < ncopy;
+        if (more) ptx::tmem_ld16_issue(tspare + (uint32_t)((ci + 1) * kEpiCols), nxt);
+        float v[kEpiCols];
+#pragma unroll
+        for (int j = 0; j < kEpiCols; ++j) v[j] = __uint_as_float(cur[j]);
+        chunk(ci, v);
         if (more) ptx::tmem_wait_ld(nxt);
       }
       if (MODE == kModeLayer && item_phase == 0) {
