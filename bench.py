@@ -229,6 +229,16 @@ def kernel_source_hash() -> str:
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
+def profile_fields(text: str) -> dict:
+    """The `- key: `value`` lines of a profile summary (keys may hold colons)."""
+    vals = {}
+    for line in text.splitlines():
+        if line.startswith("- ") and ":" in line:
+            k, v = line[2:].rsplit(":", 1)
+            vals[k.strip()] = v.strip().strip("`")
+    return vals
+
+
 def recorded_traffic(kernel: str, workload_name: str):
     """DRAM bytes per launch from a committed ncu summary, if it still matches gemm.cu."""
     path = os.path.join(ROOT, "profiles", f"traffic_{kernel}_kernel_{workload_name}.md")
@@ -236,11 +246,7 @@ def recorded_traffic(kernel: str, workload_name: str):
         text = open(path).read()
     except OSError:
         return None
-    vals = {}
-    for line in text.splitlines():
-        if line.startswith("- ") and ":" in line:
-            k, v = line[2:].split(":", 1)
-            vals[k.strip()] = v.strip().strip("`")
+    vals = profile_fields(text)
     if vals.get("gemm.cu sha256[:16]") != kernel_source_hash():
         return None
     try:

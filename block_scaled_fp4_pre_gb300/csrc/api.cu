@@ -457,6 +457,19 @@ moe_status moe_forward(const moe_dims* dims, const void* prepared, void* ws, siz
   return forward_impl(dims, prepared, ws, out, T, static_cast<cudaStream_t>(stream));
 }
 
+// Device address of a host buffer the GPU can access directly (page-locked, e.g.
+// cudaHostAlloc / cudaHostRegister), 16-byte aligned; nullptr otherwise.
+void* device_alias(const void* host) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, host) != cudaSuccess) {
+    (void)cudaGetLastError();   // not a CUDA-known pointer: not an error here
+    return nullptr;
+  }
+  if (a.type != cudaMemoryTypeHost || !a.devicePointer || !aligned(a.devicePointer, 16))
+    return nullptr;
+  return a.devicePointer;
+}
+
 moe_status moe_run_host(const moe_dims* dims, const void* prepared, void* ws, size_t ws_bytes,
                         const void* x_host, const int32_t* ids_host, const float* tw_host,
                         void* out_host, int32_t T, void* stream) {
@@ -473,16 +486,35 @@ moe_status moe_run_host(const moe_dims* dims, const void* prepared, void* ws, si
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const size_t xbytes = (size_t)T * dims->hidden * 2, abytes = (size_t)T * dims->topk * 4;
   cudaError_t e;
-  if ((e = cudaMemcpyAsync(b + L.off_stage_x, x_host, xbytes, cudaMemcpyHostToDevice, st)) ||
-      (e = cudaMemcpyAsync(b + L.off_stage_ids, ids_host, abytes, cudaMemcpyHostToDevice, st)) ||
-      (e = cudaMemcpyAsync(b + L.off_stage_w, tw_host, abytes, cudaMemcpyHostToDevice, st)))
-    return cuda_fail(e, "input copy");
-  s = pre_dispatch_impl(dims, b + L.off_stage_x, reinterpret_cast<int32_t*>(b + L.off_stage_ids),
-                        reinterpret_cast<float*>(b + L.off_stage_w), T, ws, st);
+  // Page-locked inputs are read by the dispatch kernels straight from host memory,
+  // and a page-locked output buffer is written by the bf16 conversion directly;
+  // other buffers go through staging copies.
+  const void* x_dev = device_alias(x_host);
+  const void* ids_dev = device_alias(ids_host);
+  const void* tw_dev = device_alias(tw_host);
+  void* out_dev = device_alias(out_host);
+  if (!x_dev) {
+    if ((e = cudaMemcpyAsync(b + L.off_stage_x, x_host, xbytes, cudaMemcpyHostToDevice, st)))
+      return cuda_fail(e, "input copy");
+    x_dev = b + L.off_stage_x;
+  }
+  if (!ids_dev) {
+    if ((e = cudaMemcpyAsync(b + L.off_stage_ids, ids_host, abytes, cudaMemcpyHostToDevice, st)))
+      return cuda_fail(e, "input copy");
+    ids_dev = b + L.off_stage_ids;
+  }
+  if (!tw_dev) {
+    if ((e = cudaMemcpyAsync(b + L.off_stage_w, tw_host, abytes, cudaMemcpyHostToDevice, st)))
+      return cuda_fail(e, "input copy");
+    tw_dev = b + L.off_stage_w;
+  }
+  s = pre_dispatch_impl(dims, x_dev, static_cast<const int32_t*>(ids_dev),
+                        static_cast<const float*>(tw_dev), T, ws, st);
   if (s) return s;
-  s = forward_impl(dims, prepared, ws, b + L.off_stage_out, T, st);
+  s = forward_impl(dims, prepared, ws, out_dev ? out_dev : b + L.off_stage_out, T, st);
   if (s) return s;
-  if ((e = cudaMemcpyAsync(out_host, b + L.off_stage_out, xbytes, cudaMemcpyDeviceToHost, st)))
+  if (!out_dev &&
+      (e = cudaMemcpyAsync(out_host, b + L.off_stage_out, xbytes, cudaMemcpyDeviceToHost, st)))
     return cuda_fail(e, "output copy");
   if ((e = cudaStreamSynchronize(st))) return cuda_fail(e, "stream synchronize");
   return MOE_OK;

@@ -159,10 +159,12 @@ MXMOE_API moe_status moe_pre_dispatch(const moe_dims *dims, const void *x_dev,
 MXMOE_API moe_status moe_forward(const moe_dims *dims, const void *prepared_dev, void *ws_dev,
                                  size_t ws_bytes, void *out_dev, int32_t num_tokens, void *stream);
 
-/* End-to-end call on HOST buffers: copies x_host (bf16 [T, H]), topk_ids_host and
- * topk_weights_host into staging areas of the workspace, runs moe_pre_dispatch and
- * moe_forward, copies the bf16 result to out_host [T, H] and synchronises the
- * stream.  Pinned host memory gives asynchronous copies. */
+/* End-to-end call on HOST buffers: x_host (bf16 [T, H]), topk_ids_host and
+ * topk_weights_host in, the bf16 result in out_host [T, H]; runs moe_pre_dispatch
+ * and moe_forward and synchronises the stream.  Each page-locked buffer
+ * (cudaHostAlloc, cudaHostRegister; 16-byte aligned) is read or written by the
+ * kernels directly over the host link; any other buffer goes through a staging
+ * area of the workspace with a copy. */
 MXMOE_API moe_status moe_run_host(const moe_dims *dims, const void *prepared_dev, void *ws_dev,
                                   size_t ws_bytes, const void *x_host,
                                   const int32_t *topk_ids_host, const float *topk_weights_host,

@@ -204,12 +204,17 @@ def test_forward_is_repeatable_and_host_path_matches(layers):
     assert np.array_equal(inter_a["h_codes"], inter_b["h_codes"])
     # fp32 reductions in arbitrary order: outputs agree to bf16 rounding
     assert normwise_rel_err(oracle.bf16_bits_to_f64(a), oracle.bf16_bits_to_f64(b)) <= 1e-3
+    # page-locked buffers are accessed in place, pageable ones staged; all and none
+    # page-locked, then a mix
     xh = torch.from_numpy(x.view(np.int16)).pin_memory()
-    out_h = torch.empty((w.T, w.H), dtype=torch.int16).pin_memory()
-    mx.moe_run_host(layer.dims, layer.prepared, layer.ws, xh, torch.from_numpy(ids),
-                    torch.from_numpy(tw), out_h, w.T)
-    c = out_h.numpy().view(np.uint16)
-    assert normwise_rel_err(oracle.bf16_bits_to_f64(c), oracle.bf16_bits_to_f64(a)) <= 1e-3
+    idh, twh = torch.from_numpy(ids).pin_memory(), torch.from_numpy(tw).pin_memory()
+    for args in [(xh, idh, twh, torch.empty((w.T, w.H), dtype=torch.int16).pin_memory()),
+                 (np.ascontiguousarray(x.view(np.int16)), ids, tw, np.zeros((w.T, w.H), np.int16)),
+                 (np.ascontiguousarray(x.view(np.int16)), idh, tw, torch.zeros((w.T, w.H), dtype=torch.int16).pin_memory()),
+                 (xh, ids, twh, np.zeros((w.T, w.H), np.int16))]:
+        mx.moe_run_host(layer.dims, layer.prepared, layer.ws, *args, w.T)
+        c = np.asarray(args[3]).view(np.uint16)
+        assert normwise_rel_err(oracle.bf16_bits_to_f64(c), oracle.bf16_bits_to_f64(a)) <= 1e-3
 
 
 def test_cuda_graph_replay_matches_eager(layers):
