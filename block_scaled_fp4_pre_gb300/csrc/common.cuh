@@ -103,36 +103,21 @@ struct Shape {
 
 // Launch with programmatic stream serialisation: the kernel may start before the
 // previous kernel in the stream finishes and must call ptx::pdl_wait() before it
-// touches that kernel's output.  Blocks form clusters of cluster_x along x
-// (1: no clusters).
+// touches that kernel's output.
 template <typename... KArgs, typename... Args>
-cudaError_t launch_pdl_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
-                               unsigned cluster_x, cudaStream_t st, Args&&... args) {
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t st, Args&&... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[2];
+  cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.numAttrs = 1;
-  if (cluster_x > 1) {
-    attr[1].id = cudaLaunchAttributeClusterDimension;
-    attr[1].val.clusterDim.x = cluster_x;
-    attr[1].val.clusterDim.y = 1;
-    attr[1].val.clusterDim.z = 1;
-    cfg.numAttrs = 2;
-  }
   cfg.attrs = attr;
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
-}
-
-// launch_pdl_cluster without clusters.
-template <typename... KArgs, typename... Args>
-cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
-                       cudaStream_t st, Args&&... args) {
-  return launch_pdl_cluster(kernel, grid, block, smem, 1, st, std::forward<Args>(args)...);
 }
 
 // ---------------------------------------------------------------------------

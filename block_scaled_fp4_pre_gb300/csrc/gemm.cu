@@ -144,27 +144,7 @@ __device__ __forceinline__ float silu_times(float g, float u) {
   return __fdividef(g, 1.0f + __expf(-g)) * u;
 }
 
-// Ring hand-over of work items to the MMA issuer and the epilogue.  In a pair,
-// block 0 writes both blocks' rings and owns the slot-free barrier, on which the
-// second block's readers arrive remotely.
-template <bool PAIR>
-__device__ __forceinline__ bool ring_wait(uint64_t* full, uint32_t parity, volatile int* abort) {
-  return PAIR ? ptx::mbar_wait_cluster(full, parity, abort, kWaitLimitNs)
-              : ptx::mbar_wait(full, parity, abort, kWaitLimitNs);
-}
-template <bool PAIR>
-__device__ __forceinline__ void ring_release(uint64_t* empty, int rank) {
-  if (!PAIR || rank == 0)
-    ptx::mbar_arrive(empty);
-  else
-    ptx::mbar_arrive_cluster(ptx::cluster_addr(empty, 0));
-}
-
-// PAIR: the kernel runs as clusters of two blocks that take the same token tile
-// and adjacent weight slabs (2p, 2p+1) of each item; each block loads half of the
-// token boxes and multicasts them into both, which halves the token rows read
-// from L2.  Block 0 of the pair claims the items and hands each to both blocks.
-template <int MODE, bool PAIR, bool PULL>
+template <int MODE, bool PULL>
 __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
     moe_layer_kernel(const __grid_constant__ CUtensorMap tmap_w1,
                      const __grid_constant__ CUtensorMap tmap_x,
@@ -177,25 +157,19 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   SmemTail* tail = reinterpret_cast<SmemTail*>(smem + kSmemTail);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // Position in the pair (0 without pairing): block 0 schedules, both load.
-  const int rank = PAIR ? (int)ptx::cluster_ctarank() : 0;
-  constexpr uint16_t kPairMask = 0x3;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(&tail->full[s], 1);
-      // a stage is free again once the MMAs of both blocks of a pair have read it
-      // (the partner's token boxes land in this block's stage too)
-      ptx::mbar_init(&tail->empty[s], PAIR ? 2 : 1);
+      ptx::mbar_init(&tail->empty[s], 1);
     }
     ptx::mbar_init(&tail->acc_full, 1);
     ptx::mbar_init(&tail->acc_empty, 128);
     ptx::mbar_init(&tail->mma_done, 1);
     for (int r = 0; r < kRing; ++r) {
       ptx::mbar_init(&tail->ring_full[r], 1);
-      // the MMA thread + 4 epilogue warps (of both blocks of a pair, plus the
-      // second block's producer; only block 0's count is used)
-      ptx::mbar_init(&tail->ring_empty[r], PAIR ? 11 : 5);
+      // the MMA thread + 4 epilogue warps
+      ptx::mbar_init(&tail->ring_empty[r], 5);
     }
     tail->abort = 0;
     ptx::fence_mbar_init();
@@ -212,8 +186,6 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
   }
   ptx::tc_fence_before();
   __syncthreads();
-  // A pair's blocks touch each other's barriers from here on: both must be set up.
-  if (PAIR) ptx::cluster_sync_all();
   ptx::tc_fence_after();
   const uint32_t tmem_base = tail->tmem_base;
   volatile int* abort_flag = &tail->abort;
@@ -223,11 +195,9 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
     // While the token dispatch finishes, pull into L2 the gate/up slab this block
     // most likely takes first when every expert has one token tile (decode-sized
     // loads): item b = (expert b / slabs, slab b % slabs).  Only a hint.
-    // (with pairing: item b/2 = (expert, slab pair), this block's slab of it)
     const PhaseArgs& P = args.ph[0];
-    const int per_e = PAIR ? P.m_tiles / 2 : P.m_tiles;
-    const int b = PAIR ? (int)blockIdx.x / 2 : (int)blockIdx.x;
-    const int e = b / per_e, mt = (b % per_e) * (PAIR ? 2 : 1) + rank;
+    const int b = (int)blockIdx.x;
+    const int e = b / P.m_tiles, mt = b % P.m_tiles;
     for (int kb = 0; kb < P.num_kb; ++kb)
       ptx::tma_prefetch_2d(&tmap_w1, kb * kBKBytes, e * P.rows_per_expert + mt * kBM);
     ptx::bulk_prefetch(P.w_sf + ((size_t)(e * P.m_tiles + mt) * P.kc4) * kSFAtomBytes,
@@ -240,8 +210,8 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
   const int32_t* tile_start = tail->tile_start;
   for (int e = threadIdx.x; e <= E; e += blockDim.x) tail->tile_start[e] = args.ws.tile_start[e];
   __syncthreads();
-  // Items per token tile and phase: one per weight slab, or per slab pair.
-  const int m0 = args.ph[0].m_tiles / (PAIR ? 2 : 1), m1 = args.ph[1].m_tiles / (PAIR ? 2 : 1);
+  // Items per token tile and phase: one per weight slab.
+  const int m0 = args.ph[0].m_tiles, m1 = args.ph[1].m_tiles;
   const int n0 = num_tiles * m0;
   const int total = n0 + (args.num_phases == 2 ? num_tiles * m1 : 0);
   // A tile's intermediate rows are complete once every gate/up slab has stored its
@@ -254,7 +224,6 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
     // whole warp also gathers the gate/up token rows of each stage (one row per
     // token, written once by the quantiser) with per-thread asynchronous copies.
     const bool leader = lane == 0;
-    const bool scheduler = rank == 0;
     const uint64_t pol_once = ptx::policy_evict_first();
     const uint64_t pol_shared = ptx::policy_evict_normal();
     const uint64_t pol_t = ptx::policy_evict_last();
@@ -267,7 +236,7 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
     int g = 0;
     Item it = {};
     int4 ti = make_int4(0, 0, 0, 0);
-    if (leader && scheduler) {
+    if (leader) {
       g = atomicAdd(&args.ws.flags[kFlagSched], 1);
       if (g < total) {
         it = decode_item(g, n0, m0, m1, E, tile_start);
@@ -277,37 +246,12 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
     while (true) {
       int item = -1;
       if (leader) {
-        if (scheduler) {
-          item = g < total ? g : -1;
-          if (!ptx::mbar_wait(&tail->ring_empty[r], rph ^ 1u, abort_flag, kWaitLimitNs)) {
-            ok = false;
-          } else {
-            const int4 rec = make_int4(item, ti.y, ti.z | (it.mt << 8), it.tile);
-            tail->ring[r] = rec;
-            ptx::mbar_arrive(&tail->ring_full[r]);
-            if (PAIR) {
-              // hand the same item to the second block of the pair
-              ptx::st_cluster_v4(ptx::cluster_addr(&tail->ring[r], 1), rec);
-              ptx::mbar_arrive_cluster(ptx::cluster_addr(&tail->ring_full[r], 1));
-            }
-          }
+        item = g < total ? g : -1;
+        if (!ptx::mbar_wait(&tail->ring_empty[r], rph ^ 1u, abort_flag, kWaitLimitNs)) {
+          ok = false;
         } else {
-          // second block of a pair: the item block 0 handed over
-          if (!ptx::mbar_wait_cluster(&tail->ring_full[r], rph, abort_flag, kWaitLimitNs)) {
-            ok = false;
-          } else {
-            const int4 rec = tail->ring[r];
-            ptx::mbar_arrive_cluster(ptx::cluster_addr(&tail->ring_empty[r], 0));
-            item = rec.x;
-            if (item >= 0) {
-              it.phase = item < n0 ? 0 : 1;
-              it.tile = rec.w;
-              it.mt = rec.z >> 8;
-              it.e = args.ws.tiles[it.tile].x;
-              it.ntiles = tile_start[it.e + 1] - tile_start[it.e];
-              ti = make_int4(it.e, rec.y, rec.z & 0xFF, 0);
-            }
-          }
+          tail->ring[r] = make_int4(item, ti.y, ti.z | (it.mt << 8), it.tile);
+          ptx::mbar_arrive(&tail->ring_full[r]);
         }
       }
       // the item, to every lane
@@ -326,20 +270,20 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
       it.ntiles = __shfl_sync(kFull, it.ntiles, 0);
       ti.y = __shfl_sync(kFull, ti.y, 0);
       ti.z = __shfl_sync(kFull, ti.z, 0);
-      const int g_next = (leader && scheduler) ? atomicAdd(&args.ws.flags[kFlagSched], 1) : total;
+      const int g_next = leader ? atomicAdd(&args.ws.flags[kFlagSched], 1) : total;
       Item it_next = {};
       int4 ti_next = make_int4(0, 0, 0, 0);
       const PhaseArgs& P = args.ph[it.phase];
       const CUtensorMap* tw = it.phase ? &tmap_w2 : &tmap_w1;
       const CUtensorMap* tt = it.phase ? &tmap_h : &tmap_x;
-      // a full tile's token rows in one box (one half-tile box per block of a pair)
+      // a full tile's token rows in one box
       const CUtensorMap* tt_full = it.phase ? &tmap_h_full : &tmap_x_full;
       // A slab read by one token tile only is not kept; one shared by several
       // tiles of the expert stays for them.
       const uint64_t pol_w = it.ntiles > 1 ? pol_shared : pol_once;
       const int e = it.e, row0 = ti.y, n = ti.z;
       const int nb = (n + kBBoxRows - 1) / kBBoxRows;
-      const int mt = it.mt * (PAIR ? 2 : 1) + rank;   // this block's weight slab
+      const int mt = it.mt;   // the item's weight slab
       const int wrow = e * P.rows_per_expert + mt * kBM;
       const uint8_t* wsf = P.w_sf + ((size_t)(e * P.m_tiles + mt) * P.kc4) * kSFAtomBytes;
       const uint8_t* tsf = P.t_sf + ((size_t)(row0 / kBN) * P.kc4) * kSFAtomBytes;
@@ -399,8 +343,7 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
         }
         if (leader) {
           // every byte the TMA lands here: the weight box and scales and, unless
-          // pulled, the token rows (in a pair: this block's and the partner's
-          // multicast ones) and their scales
+          // pulled, the token rows and their scales
           const uint32_t bytes =
               kATileBytes + atoms * kSFAtomBytes +
               (pulled ? 0u : (uint32_t)(nb * (kBBoxRows * kBKBytes) + atoms * kSFAtomBytes));
@@ -411,22 +354,11 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
                          wsf + (size_t)kb * 2 * kSFAtomBytes, atoms * kSFAtomBytes, bar, pol_w);
           if (!pulled) {
             if (nb * kBBoxRows == kBN) {
-              if (!PAIR) {
-                ptx::tma_load_2d(b_dst, tt_full, kb * kBKBytes, row0, bar, pol_t);
-              } else {
-                const int half = rank * (kBN / 2);
-                ptx::tma_load_2d_multicast(b_dst + half * kBKBytes, tt_full, kb * kBKBytes,
-                                           row0 + half, bar, kPairMask, pol_t);
-              }
+              ptx::tma_load_2d(b_dst, tt_full, kb * kBKBytes, row0, bar, pol_t);
             } else {
-              for (int j = 0; j < nb; ++j) {
-                uint8_t* dst = b_dst + j * kBBoxRows * kBKBytes;
-                if (!PAIR)
-                  ptx::tma_load_2d(dst, tt, kb * kBKBytes, row0 + j * kBBoxRows, bar, pol_t);
-                else if ((j & 1) == rank)
-                  ptx::tma_load_2d_multicast(dst, tt, kb * kBKBytes, row0 + j * kBBoxRows, bar,
-                                             kPairMask, pol_t);
-              }
+              for (int j = 0; j < nb; ++j)
+                ptx::tma_load_2d(b_dst + j * kBBoxRows * kBKBytes, tt, kb * kBKBytes,
+                                 row0 + j * kBBoxRows, bar, pol_t);
             }
             ptx::bulk_load(smem + kSmemSFB + (size_t)stage * kSFStageBytes,
                            tsf + (size_t)kb * 2 * kSFAtomBytes, atoms * kSFAtomBytes, bar, pol_t);
@@ -467,12 +399,12 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
       uint32_t phase = 0, rph = 0, acc_phase = 0, sfbuf = 0;
       bool ok = true;
       while (true) {
-        if (!ring_wait<PAIR>(&tail->ring_full[r], rph, abort_flag)) {
+        if (!ptx::mbar_wait(&tail->ring_full[r], rph, abort_flag, kWaitLimitNs)) {
           ok = false;
           break;
         }
         const int4 rec = tail->ring[r];
-        ring_release<PAIR>(&tail->ring_empty[r], rank);
+        ptx::mbar_arrive(&tail->ring_empty[r]);
         if (++r == kRing) {
           r = 0;
           rph ^= 1u;
@@ -516,11 +448,7 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
                              ptx::desc_sw128(b_base + s * 32), idesc, sfa_t + (s >> 1) * 4,
                              sfb_t + (s >> 1) * 4, (kb | s) != 0 ? 1u : 0u);
           }
-          // the stage is free once both blocks of a pair have read it
-          if (PAIR)
-            ptx::tc_commit_multicast(&tail->empty[stage], kPairMask);
-          else
-            ptx::tc_commit(&tail->empty[stage]);
+          ptx::tc_commit(&tail->empty[stage]);
           sfbuf ^= 1u;
           if (++stage == kStages) {
             stage = 0;
@@ -545,13 +473,13 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
     int r = 0, xb = 0;
     uint32_t rph = 0, acc_phase = 0;
     while (true) {
-      if (!ring_wait<PAIR>(&tail->ring_full[r], rph, abort_flag)) {
+      if (!ptx::mbar_wait(&tail->ring_full[r], rph, abort_flag, kWaitLimitNs)) {
         if (ep_tid == 0) atomicOr(&args.ws.flags[0], kErrTimeout);
         break;
       }
       const int4 rec = tail->ring[r];
       __syncwarp();
-      if (lane == 0) ring_release<PAIR>(&tail->ring_empty[r], rank);
+      if (lane == 0) ptx::mbar_arrive(&tail->ring_empty[r]);
       if (++r == kRing) {
         r = 0;
         rph ^= 1u;
@@ -559,9 +487,7 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
       const int item = rec.x;
       if (item < 0) break;
       const int item_phase = item < n0 ? 0 : 1;
-      // this block's weight slab of the item (the item names a slab pair when paired)
-      const int row0 = rec.y, n = rec.z & 0xFF, mt = (rec.z >> 8) * (PAIR ? 2 : 1) + rank,
-                item_tile = rec.w;
+      const int row0 = rec.y, n = rec.z & 0xFF, mt = rec.z >> 8, item_tile = rec.w;
       // Row metadata of a down item, read while the MMAs run: lane l holds rows
       // l, l+32, l+64, l+96 of the tile.
       int tok_r[kBN / 32];
@@ -704,28 +630,28 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
           if (two) ptx::tmem_st16(tspare + (uint32_t)((ci + 1) * kEpiCols), r1);
         }
       }
-      // 2. Columns past the spare area straight from the accumulator.  Once every
-      //    accumulator load is done it goes back to the MMA issuer, so the next
-      //    item's MMAs run during the rest of this item's math.
+      // 2. The two chunks past the spare area straight from the accumulator, both
+      //    loaded before any math.  Then the accumulator goes back to the MMA
+      //    issuer, so the next item's MMAs run during this item's math.
+      static_assert(kBN / kEpiCols == kSpareChunks + 2, "two chunks read directly");
+      uint32_t rd[2][kEpiCols];
 #pragma unroll
-      for (int ci = kSpareChunks; ci < kBN / kEpiCols; ++ci) {
-        if (ci < nch) {
-          uint32_t r[kEpiCols];
-          ptx::tmem_ld16_issue(taddr + (uint32_t)(ci * kEpiCols), r);
-          ptx::tmem_wait_ld(r);
-          if (ci + 1 >= nch) {
-            ptx::tc_fence_before();
-            ptx::mbar_arrive(&tail->acc_empty);
-          }
+      for (int d = 0; d < 2; ++d)
+        if (kSpareChunks + d < nch)
+          ptx::tmem_ld16_issue(taddr + (uint32_t)((kSpareChunks + d) * kEpiCols), rd[d]);
+#pragma unroll
+      for (int d = 0; d < 2; ++d)
+        if (kSpareChunks + d < nch) ptx::tmem_wait_ld(rd[d]);
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(&tail->acc_empty);
+#pragma unroll
+      for (int d = 0; d < 2; ++d) {
+        if (kSpareChunks + d < nch) {
           float v[kEpiCols];
 #pragma unroll
-          for (int j = 0; j < kEpiCols; ++j) v[j] = __uint_as_float(r[j]);
-          chunk(ci, v);
+          for (int j = 0; j < kEpiCols; ++j) v[j] = __uint_as_float(rd[d][j]);
+          chunk(kSpareChunks + d, v);
         }
-      }
-      if (nch <= kSpareChunks) {
-        ptx::tc_fence_before();
-        ptx::mbar_arrive(&tail->acc_empty);
       }
       ptx::tmem_wait_st();
       // 3. The copied chunks; the load of chunk ci+1 runs during the math of ci.
@@ -761,9 +687,6 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
 
   ptx::tc_fence_before();
   __syncthreads();
-  // Neither block of a pair leaves while the other may still write into its shared
-  // memory (multicast copies) or arrive on its barriers.
-  if (PAIR) ptx::cluster_sync_all();
   if (warp == 1) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem_base, kTmemCols);
@@ -829,40 +752,29 @@ PhaseArgs phase_args(const uint8_t* w_sf, const uint8_t* t_sf, int rows_per_expe
   return p;
 }
 
-// Pairs pay off once token tiles are wide: below this many assignments per expert
-// on average the token boxes are a small part of each stage and the single-block
-// kernel is used.
-constexpr int kPairMinRowsPerExpert = 64;
-
-template <int MODE, bool PAIR, bool PULL>
+template <int MODE, bool PULL>
 cudaError_t launch_mode(const LayerLaunch& g, const CUtensorMap* maps, const LayerArgs& a,
                         cudaStream_t st) {
   static int grid = 0;   // per instantiation, for the device of the first launch
   if (grid == 0) {
-    cudaError_t err = cudaFuncSetAttribute(moe_layer_kernel<MODE, PAIR, PULL>,
+    cudaError_t err = cudaFuncSetAttribute(moe_layer_kernel<MODE, PULL>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)kSmemBytes);
     if (err != cudaSuccess) return err;
-    // Pairs too: two blocks of each SM, whichever pair they belong to (the
-    // occupancy query for clusters undercounts this; the work queue needs no
-    // particular number of resident blocks anyway).
-    const int blocks = kBlocksPerSM * g.num_sms;
-    grid = blocks;
+    // two blocks on each SM (the work queue needs no particular number of
+    // resident blocks)
+    grid = kBlocksPerSM * g.num_sms;
   }
-  return launch_pdl_cluster(moe_layer_kernel<MODE, PAIR, PULL>, dim3(grid), dim3(kThreads), kSmemBytes,
-                            PAIR ? 2u : 1u, st, maps[0], maps[1], maps[2], maps[3], maps[4],
-                            maps[5], a);
+  return launch_pdl(moe_layer_kernel<MODE, PULL>, dim3(grid), dim3(kThreads), kSmemBytes, st,
+                    maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], a);
 }
 
 }  // namespace
 
 cudaError_t launch_layer(const LayerLaunch& g, cudaStream_t st) {
   const Shape& s = g.shape;
-  // Pairs split each slab count in two: both phases need an even number of slabs.
-  const bool pair = (2 * s.I / kBM) % 2 == 0 && (s.H / kBM) % 2 == 0 &&
-                    (int64_t)g.T * s.k >= (int64_t)kPairMinRowsPerExpert * s.E;
-  // Full token tiles come in one box per block: all 128 rows, or a pair's half.
-  const uint32_t full_rows = pair ? kBN / 2 : kBN;
+  // Full token tiles come in one box of all 128 rows.
+  const uint32_t full_rows = kBN;
   CUtensorMap maps[6];
   cudaError_t err;
   if ((err = make_tmap(&maps[4], g.ws.xb, (uint64_t)s.H / 2, (uint64_t)g.R_cap, full_rows)) ||
@@ -884,14 +796,10 @@ cudaError_t launch_layer(const LayerLaunch& g, cudaStream_t st) {
   a.ws = g.ws;
   a.gate_up_debug = g.gate_up_debug;
   if (g.num_phases == 2)
-    return g.pull ? (pair ? launch_mode<kModeLayer, true, true>(g, maps, a, st)
-                          : launch_mode<kModeLayer, false, true>(g, maps, a, st))
-                  : (pair ? launch_mode<kModeLayer, true, false>(g, maps, a, st)
-                          : launch_mode<kModeLayer, false, false>(g, maps, a, st));
-  return g.pull ? (pair ? launch_mode<kModeRaw, true, true>(g, maps, a, st)
-                        : launch_mode<kModeRaw, false, true>(g, maps, a, st))
-                : (pair ? launch_mode<kModeRaw, true, false>(g, maps, a, st)
-                        : launch_mode<kModeRaw, false, false>(g, maps, a, st));
+    return g.pull ? launch_mode<kModeLayer, true>(g, maps, a, st)
+                  : launch_mode<kModeLayer, false>(g, maps, a, st);
+  return g.pull ? launch_mode<kModeRaw, true>(g, maps, a, st)
+                : launch_mode<kModeRaw, false>(g, maps, a, st);
 }
 
 }  // namespace mxmoe

@@ -76,74 +76,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
-// As mbar_try_wait, with cluster-scope acquire: for phases completed by arrivals
-// from another block of the cluster that released data it wrote into this block's
-// shared memory.
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_addr(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// mbar_wait with cluster-scope acquire (see mbar_try_wait_cluster).
-__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity,
-                                                  volatile int* abort,
-                                                  unsigned long long limit_ns) {
-  if (mbar_try_wait_cluster(bar, parity)) return true;
-  const unsigned long long t0 = globaltimer();
-  while (true) {
-    if (mbar_try_wait_cluster(bar, parity)) return true;
-    if (*abort) return false;
-    if (globaltimer() - t0 > limit_ns) {
-      *abort = 1;
-      return false;
-    }
-  }
-}
-
-// ---- thread-block clusters ----------------------------------------------------
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
-// Address, in the cluster's shared window, of the variable at `p` in the shared
-// memory of block `rank` of this cluster.
-__device__ __forceinline__ uint32_t cluster_addr(const void* p, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr(p)), "r"(rank));
-  return r;
-}
-
-// One arrival on an mbarrier of another block of the cluster, releasing this
-// thread's earlier writes at cluster scope.
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(
-                   bar_cluster_addr)
-               : "memory");
-}
-
-__device__ __forceinline__ void st_cluster_v4(uint32_t cluster_address, int4 v) {
-  asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(cluster_address),
-               "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
-               : "memory");
-}
-
-// Every thread of every block of the cluster (all of them must execute it).
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile(
-      "barrier.cluster.arrive.release.aligned;\n\t"
-      "barrier.cluster.wait.acquire.aligned;" ::
-          : "memory");
-}
-
 // ---- global-memory ordering ---------------------------------------------------
 __device__ __forceinline__ int ld_acquire(const int32_t* p) {
   int v;
@@ -208,21 +140,6 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const void* tmap, in
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_addr(smem_dst)),
       "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(smem_addr(bar)), "l"(policy)
-      : "memory");
-}
-
-// 2-D tiled load of a box into the same shared-memory offset of every block in
-// cta_mask (blocks of this cluster); each destination's mbarrier at `bar`'s offset
-// receives the complete_tx of its copy.
-__device__ __forceinline__ void tma_load_2d_multicast(void* smem_dst, const void* tmap, int32_t x,
-                                                      int32_t y, uint64_t* bar, uint16_t cta_mask,
-                                                      uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster.L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5, %6;" ::"r"(
-          smem_addr(smem_dst)),
-      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(smem_addr(bar)), "h"(cta_mask),
-      "l"(policy)
       : "memory");
 }
 
@@ -296,16 +213,6 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
           smem_addr(bar))
-      : "memory");
-}
-
-// As tc_commit, arriving on the mbarrier at `bar`'s offset in every block of
-// cta_mask (blocks of this cluster).
-__device__ __forceinline__ void tc_commit_multicast(uint64_t* bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(smem_addr(bar)),
-      "h"(cta_mask)
       : "memory");
 }
 
