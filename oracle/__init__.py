@@ -68,6 +68,13 @@ def lib():
         l.oracle_e4m3_encode.argtypes = [ctypes.c_double]
         l.oracle_e4m3_encode.restype = ci
         l.oracle_mxfp8_quantize_bf16.argtypes = [vp, i64, i64, vp, vp, ci]
+        l.oracle_mxfp8_quantize_f32.argtypes = [vp, i64, i64, vp, vp, ci]
+        l.oracle_mxfp8_dequantize.argtypes = [vp, vp, i64, i64, vp]
+        l.oracle_interleave_source_row_gran8.argtypes = [i64, i64]
+        l.oracle_interleave_source_row_gran8.restype = i64
+        l.oracle_moe_w4a8.argtypes = [ctypes.POINTER(Shape)] + [vp] * 15 + [ci]
+        l.oracle_moe_w4a8.restype = i64
+        l.oracle_moe_w4a8_down.argtypes = [ctypes.POINTER(Shape)] + [vp] * 8 + [ci]
         _lib = l
     return _lib
 
@@ -157,9 +164,30 @@ def mxfp8_packed_scales(sf: np.ndarray) -> np.ndarray:
     return (b[..., 0] | (b[..., 1] << 8) | (b[..., 2] << 16) | (b[..., 3] << 24)).astype(np.uint32)
 
 
-def interleave_source_rows(I: int) -> np.ndarray:
-    """src[r] = canonical row of the first weight that lands at prepared row r (gran=16)."""
-    return np.array([lib().oracle_interleave_source_row(r, I) for r in range(2 * I)], np.int64)
+def mxfp8_quantize_f32(x: np.ndarray, nthreads: int | None = None):
+    """fp32 [rows, K] -> (E4M3 codes [rows, K] uint8, scale bytes [rows, K/32] uint8)."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    rows, K = x.shape
+    q = np.zeros((rows, K), np.uint8)
+    sf = np.zeros((rows, K // 32), np.uint8)
+    lib().oracle_mxfp8_quantize_f32(_p(x), rows, K, _p(q), _p(sf), nthreads or threads())
+    return q, sf
+
+
+def mxfp8_dequantize(q: np.ndarray, sf: np.ndarray) -> np.ndarray:
+    q = np.ascontiguousarray(q, np.uint8)
+    sf = np.ascontiguousarray(sf, np.uint8)
+    rows, K = q.shape
+    out = np.zeros((rows, K), np.float64)
+    lib().oracle_mxfp8_dequantize(_p(q), _p(sf), rows, K, _p(out))
+    return out
+
+
+def interleave_source_rows(I: int, gran: int = 16) -> np.ndarray:
+    """src[r] = canonical row of the first weight that lands at prepared row r: gran=16
+    (even/odd, MXFP4 activations) or gran=8 (contiguous, FP8 activations)."""
+    fn = {16: lib().oracle_interleave_source_row, 8: lib().oracle_interleave_source_row_gran8}[gran]
+    return np.array([fn(r, I) for r in range(2 * I)], np.int64)
 
 
 def scale_block_offset(r: int, s: int, Kc: int) -> int:
@@ -225,6 +253,61 @@ def moe(x_bf16, ids, tw, w1_codes, w1_sf, w2_codes, w2_sf, *, want_intermediates
                            _p(res.get("y")), nthreads or threads())
     res["invalid_ids"] = int(bad)
     return res
+
+
+def moe_w4a8(x_bf16, ids, tw, w1_codes, w1_sf, w2_codes, w2_sf, *, want_intermediates: bool = False,
+             want_y: bool = False, nthreads: int | None = None) -> dict:
+    """The fp8xfp4 (W4A8) layer on the same canonical MXFP4 weights as moe(); the
+    quantised activations are E4M3 codes, one byte each: x_codes [T, H], h_codes [A, I]."""
+    x_bf16 = np.ascontiguousarray(x_bf16, np.uint16)
+    ids = np.ascontiguousarray(ids, np.int32)
+    tw = np.ascontiguousarray(tw, np.float32)
+    T, H = x_bf16.shape
+    k = ids.shape[1]
+    E, twoI, _ = w1_codes.shape
+    I = twoI // 2
+    A = T * k
+    arrs = [np.ascontiguousarray(a, np.uint8) for a in (w1_codes, w1_sf, w2_codes, w2_sf)]
+    assert arrs[0].shape == (E, 2 * I, H // 2) and arrs[1].shape == (E, 2 * I, H // 32)
+    assert arrs[2].shape == (E, H, I // 2) and arrs[3].shape == (E, H, I // 32)
+    res = {
+        "out_f64": np.zeros((T, H), np.float64),
+        "out_bf16": np.zeros((T, H), np.uint16),
+        "x_codes": np.zeros((T, H), np.uint8),
+        "x_sf": np.zeros((T, H // 32), np.uint8),
+    }
+    if want_intermediates:
+        res["gate_up"] = np.zeros((A, 2 * I), np.float64)
+        res["h_codes"] = np.zeros((A, I), np.uint8)
+        res["h_sf"] = np.zeros((A, I // 32), np.uint8)
+    if want_y:
+        res["y"] = np.zeros((A, H), np.float64)
+    shape = Shape(T, H, I, E, k)
+    bad = lib().oracle_moe_w4a8(ctypes.byref(shape), _p(x_bf16), _p(ids), _p(tw),
+                                *[_p(a) for a in arrs], _p(res["out_f64"]), _p(res["out_bf16"]),
+                                _p(res["x_codes"]), _p(res["x_sf"]), _p(res.get("gate_up")),
+                                _p(res.get("h_codes")), _p(res.get("h_sf")), _p(res.get("y")),
+                                nthreads or threads())
+    res["invalid_ids"] = int(bad)
+    return res
+
+
+def moe_w4a8_down(ids, tw, w2_codes, w2_sf, h_codes, h_sf, H: int,
+                  nthreads: int | None = None) -> dict:
+    """W4A8 down projection + combine from given MXFP8 intermediate codes [A, I] and
+    scales [A, I/32]."""
+    ids = np.ascontiguousarray(ids, np.int32)
+    tw = np.ascontiguousarray(tw, np.float32)
+    T, k = ids.shape
+    E = w2_codes.shape[0]
+    I = w2_codes.shape[2] * 2
+    out_f64 = np.zeros((T, H), np.float64)
+    out_bf16 = np.zeros((T, H), np.uint16)
+    shape = Shape(T, H, I, E, k)
+    arrs = [np.ascontiguousarray(a, np.uint8) for a in (w2_codes, w2_sf, h_codes, h_sf)]
+    lib().oracle_moe_w4a8_down(ctypes.byref(shape), _p(ids), _p(tw), *[_p(a) for a in arrs],
+                               _p(out_f64), _p(out_bf16), nthreads or threads())
+    return {"out_f64": out_f64, "out_bf16": out_bf16}
 
 
 def moe_down(ids, tw, w2_codes, w2_sf, h_codes, h_sf, H: int, nthreads: int | None = None) -> dict:

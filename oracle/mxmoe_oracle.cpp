@@ -248,10 +248,12 @@ struct oracle_shape {
 // y[a] = dequant(h[a]) . dequant(W2[e])^T for every valid assignment a = t*k+j,
 // then R7.  Used on its own to check the down projection against any given
 // intermediate, and as the tail of oracle_moe.
+static void dequantize_fp8_row(const uint8_t* q, const uint8_t* sf, int64_t K, double* out);
+
 static void down_and_combine(const oracle_shape* s, const int32_t* ids, const float* tw,
                              const uint8_t* w2_codes, const uint8_t* w2_sf, const uint8_t* h_codes,
                              const uint8_t* h_sf, double* y_out, double* out_f64,
-                             uint16_t* out_bf16, int nthreads) {
+                             uint16_t* out_bf16, int nthreads, bool h_fp8 = false) {
     const int64_t T = s->T, H = s->H, I = s->I, E = s->E, k = s->k, A = T * k;
     std::vector<int64_t> counts(E), offsets(E + 1);
     std::vector<int32_t> st(A), sj(A);
@@ -261,8 +263,13 @@ static void down_and_combine(const oracle_shape* s, const int32_t* ids, const fl
     std::vector<double> hdq((size_t)A * I);
     parallel_for(A, nthreads, [&](int64_t a0, int64_t a1) {
         for (int64_t a = a0; a < a1; ++a)
-            if (ids[a] >= 0 && ids[a] < E)
-                oracle_dequantize(h_codes + a * (I / 2), h_sf + a * (I / 32), 1, I, &hdq[(size_t)a * I]);
+            if (ids[a] >= 0 && ids[a] < E) {
+                if (h_fp8)
+                    dequantize_fp8_row(h_codes + a * I, h_sf + a * (I / 32), I, &hdq[(size_t)a * I]);
+                else
+                    oracle_dequantize(h_codes + a * (I / 2), h_sf + a * (I / 32), 1, I,
+                                      &hdq[(size_t)a * I]);
+            }
     });
     for (int64_t e = 0; e < E; ++e) {
         if (counts[e] == 0) continue;
@@ -471,6 +478,142 @@ void oracle_mxfp8_quantize_bf16(const uint16_t* x, int64_t rows, int64_t K, uint
                 sf[r * (K / 32) + g] = (uint8_t)(e + 127);
             }
     });
+}
+
+// ---------------------------------------------------------------------------
+// fp8xfp4 (W4A8) layer: FP8 activations with per-32 scales against the same
+// MXFP4 weights (digest of SGLang PR #37279, items 1-4: mma_type "fp8xfp4", whose
+// pre_dispatch quantises the hidden states to FP8 with quant_group_size=32, and
+// whose first weight interleaves gate/up with gran=8; the W4A8 column of
+// "[deepseek-v4] Bump sgl-deep-gemm ...", Appendix B).
+// Readings where the pages are silent:
+//   R17 Both activation quantisations of this layer (the hidden states and the
+//       SwiGLU output h) are MXFP8 as in R13-R15: E4M3 values, one power-of-two
+//       UE8M0 scale per 32 elements along K.
+//   R18 gran=8 interleave: each chunk of 8 gate rows and the matching 8 up rows
+//       becomes [gate (8), up (8)], i.e. rows [gate 0..7, up 0..7, gate 8..15, ...].
+//   Everything else (R4-R8) is as in the W4A4 layer.
+
+// R18: canonical row of the first weight that lands at prepared row r.
+int64_t oracle_interleave_source_row_gran8(int64_t r, int64_t I) {
+    const int64_t c = r / 16, o = r % 16;
+    return o < 8 ? c * 8 + o : I + c * 8 + (o - 8);
+}
+
+// One group of 32 values -> 32 E4M3 codes and one scale byte (R14, R15).
+static void mxfp8_group(const double* v, uint8_t* q32, uint8_t* sf) {
+    double amax = 0.0;
+    for (int i = 0; i < 32; ++i) {
+        assert(std::isfinite(v[i]));
+        amax = std::max(amax, std::fabs(v[i]));
+    }
+    const int e = oracle_mxfp8_exponent(amax);
+    for (int i = 0; i < 32; ++i) q32[i] = (uint8_t)oracle_e4m3_encode(std::ldexp(v[i], -e));
+    *sf = (uint8_t)(e + 127);
+}
+
+// Row-major fp32 [rows, K] -> E4M3 codes [rows, K], scale bytes [rows, K/32].
+void oracle_mxfp8_quantize_f32(const float* x, int64_t rows, int64_t K, uint8_t* q, uint8_t* sf,
+                               int nthreads) {
+    assert(K % 32 == 0);
+    parallel_for(rows, nthreads, [&](int64_t r0, int64_t r1) {
+        double v[32];
+        for (int64_t r = r0; r < r1; ++r)
+            for (int64_t g = 0; g < K / 32; ++g) {
+                for (int i = 0; i < 32; ++i) v[i] = (double)x[r * K + g * 32 + i];
+                mxfp8_group(v, q + r * K + g * 32, sf + r * (K / 32) + g);
+            }
+    });
+}
+
+static void dequantize_fp8_row(const uint8_t* q, const uint8_t* sf, int64_t K, double* out) {
+    for (int64_t kk = 0; kk < K; ++kk)
+        out[kk] = std::ldexp(oracle_e4m3_value(q[kk]), (int)sf[kk / 32] - 127);
+}
+
+// codes [rows, K] + scales [rows, K/32] -> double values [rows, K].
+void oracle_mxfp8_dequantize(const uint8_t* q, const uint8_t* sf, int64_t rows, int64_t K,
+                             double* out) {
+    for (int64_t r = 0; r < rows; ++r) dequantize_fp8_row(q + r * K, sf + r * (K / 32), K, out + r * K);
+}
+
+// The W4A8 layer; arguments and optional outputs as oracle_moe, except that the
+// quantised activations are E4M3 codes, one byte each: x_q [T, H], h_q [A, I].
+int64_t oracle_moe_w4a8(const oracle_shape* s, const uint16_t* x_bf16, const int32_t* ids,
+                        const float* tw, const uint8_t* w1_codes, const uint8_t* w1_sf,
+                        const uint8_t* w2_codes, const uint8_t* w2_sf, double* out_f64,
+                        uint16_t* out_bf16, uint8_t* x_q_out, uint8_t* x_sf_out,
+                        double* gate_up_out, uint8_t* h_q_out, uint8_t* h_sf_out, double* y_out,
+                        int nthreads) {
+    const int64_t T = s->T, H = s->H, I = s->I, E = s->E, k = s->k, A = T * k;
+    assert(H % 32 == 0 && I % 32 == 0);
+
+    // 1. quantise the hidden states to MXFP8 (pre_dispatch, quant_group_size=32)
+    std::vector<uint8_t> xq((size_t)T * H), xs((size_t)T * H / 32);
+    oracle_mxfp8_quantize_bf16(x_bf16, T, H, xq.data(), xs.data(), nthreads);
+    if (x_q_out) std::memcpy(x_q_out, xq.data(), xq.size());
+    if (x_sf_out) std::memcpy(x_sf_out, xs.data(), xs.size());
+
+    // 2. bucket the assignments by expert
+    std::vector<int64_t> counts(E), offsets(E + 1);
+    std::vector<int32_t> st(A), sj(A);
+    const int64_t bad =
+        oracle_bucket(ids, T, k, E, counts.data(), offsets.data(), st.data(), sj.data());
+
+    std::vector<double> xdq((size_t)T * H);
+    oracle_mxfp8_dequantize(xq.data(), xs.data(), T, H, xdq.data());
+
+    // 3. grouped gate/up projection against the MXFP4 first weight
+    std::vector<double> gu((size_t)A * 2 * I, 0.0);
+    for (int64_t e = 0; e < E; ++e) {
+        if (counts[e] == 0) continue;
+        parallel_for(2 * I, nthreads, [&](int64_t n0, int64_t n1) {
+            std::vector<double> wrow((size_t)H);
+            for (int64_t n = n0; n < n1; ++n) {
+                oracle_dequantize(w1_codes + (e * 2 * I + n) * (H / 2),
+                                  w1_sf + (e * 2 * I + n) * (H / 32), 1, H, wrow.data());
+                for (int64_t p = offsets[e]; p < offsets[e + 1]; ++p) {
+                    const int64_t t = st[p], a = t * k + sj[p];
+                    double acc = 0.0;
+                    for (int64_t kk = 0; kk < H; ++kk) acc += xdq[(size_t)t * H + kk] * wrow[kk];
+                    gu[(size_t)a * 2 * I + n] = acc;
+                }
+            }
+        });
+    }
+    if (gate_up_out) std::memcpy(gate_up_out, gu.data(), sizeof(double) * gu.size());
+
+    // 4-5. SwiGLU (R6) and MXFP8 requantisation of h along I (R17)
+    std::vector<uint8_t> hq((size_t)A * I, 0), hs((size_t)A * I / 32, 0);
+    parallel_for(A, nthreads, [&](int64_t a0, int64_t a1) {
+        std::vector<float> h((size_t)I);
+        for (int64_t a = a0; a < a1; ++a) {
+            if (ids[a] < 0 || ids[a] >= E) continue;
+            for (int64_t i = 0; i < I; ++i) {
+                const double g = gu[(size_t)a * 2 * I + i];
+                const double u = gu[(size_t)a * 2 * I + I + i];
+                h[i] = (float)(g / (1.0 + std::exp(-g)) * u);
+            }
+            oracle_mxfp8_quantize_f32(h.data(), 1, I, &hq[(size_t)a * I], &hs[(size_t)a * I / 32], 1);
+        }
+    });
+    if (h_q_out) std::memcpy(h_q_out, hq.data(), hq.size());
+    if (h_sf_out) std::memcpy(h_sf_out, hs.data(), hs.size());
+
+    // 6-7. grouped down projection (MXFP8 h against the MXFP4 second weight) and
+    // the top-k weighted combine
+    down_and_combine(s, ids, tw, w2_codes, w2_sf, hq.data(), hs.data(), y_out, out_f64, out_bf16,
+                     nthreads, true);
+    return bad;
+}
+
+// W4A8 down projection + combine from caller-given MXFP8 intermediate codes
+// [A, I] and scales [A, I/32].
+void oracle_moe_w4a8_down(const oracle_shape* s, const int32_t* ids, const float* tw,
+                          const uint8_t* w2_codes, const uint8_t* w2_sf, const uint8_t* h_q,
+                          const uint8_t* h_sf, double* out_f64, uint16_t* out_bf16, int nthreads) {
+    down_and_combine(s, ids, tw, w2_codes, w2_sf, h_q, h_sf, nullptr, out_f64, out_bf16, nthreads,
+                     true);
 }
 
 }  // extern "C"
