@@ -38,6 +38,16 @@ L2_CLEAN_BYTES = 256 << 20          # read after the write flush, so that its di
                                     # lines are written back before the timed step
 KERNELS_PER_STEP = 4                # bucket, quantize_scatter, layer (both GEMMs + combine), convert
 METRIC = "W4A4 MoE layer tokens/s (E=256, top-6, T=512; also us/layer and HBM TB/s)"
+METRIC_W4A8 = "W4A8 (fp8xfp4) MoE layer tokens/s (E=256, top-6, T=512; also us/layer and HBM TB/s)"
+
+
+def w4a8(args) -> bool:
+    """fp8xfp4: MXFP8 activations against the same MXFP4 weights."""
+    return args.mma == "fp8xfp4"
+
+
+def metric(args) -> str:
+    return METRIC_W4A8 if w4a8(args) else METRIC
 
 
 def parse_args():
@@ -53,6 +63,8 @@ def parse_args():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--dispatch", choices=["bucketed", "pull"], default="bucketed",
                    help="token rows copied per expert by pre_dispatch, or gathered by the layer")
+    p.add_argument("--mma", choices=["mxf4xmxf4", "fp8xfp4"], default="mxf4xmxf4",
+                   help="activation format: MXFP4 (W4A4, the headline) or MXFP8 (W4A8)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-sample-tokens", type=int, default=0)
     return p.parse_args()
@@ -142,8 +154,9 @@ def touched_experts(ids, E):
     return int(np.count_nonzero(np.bincount(ids.reshape(-1), minlength=E)))
 
 
-def algorithmic(w: synth.Workload, ids) -> dict:
-    """Bytes a perfect implementation must move, and FLOPs."""
+def algorithmic(w: synth.Workload, ids, act_fp8: bool = False) -> dict:
+    """Bytes a perfect implementation must move, and FLOPs.  act_fp8: the token rows
+    are E4M3 (one byte an element) instead of packed E2M1."""
     H, I, k, T = w.H, w.I, w.k, w.T
     A = T * k
     u = touched_experts(ids, w.E)
@@ -154,13 +167,15 @@ def algorithmic(w: synth.Workload, ids) -> dict:
         "layer_bytes": u * (w1 + w2) + 2 * T * H + 2 * T * H + 8 * T * k,
         # layer kernel: every touched expert's weights and the quantised token rows it
         # reads once
-        "layer_kernel_bytes": u * (w1 + w2) + A * (H // 2 + H // 32),
+        "layer_kernel_bytes": u * (w1 + w2) + A * ((H if act_fp8 else H // 2) + H // 32),
         "flops": 6 * A * H * I,
     }
 
 
-# Nominal dense FP4 : bf16 tensor throughput of the part (13.5 : 2.25 PFLOP/s).
+# Nominal dense FP4 : bf16 tensor throughput of the part (13.5 : 2.25 PFLOP/s), and
+# FP8 : bf16 (4.5 : 2.25) for the fp8xfp4 MMAs (kind::mxf8f6f4 runs at the FP8 rate).
 FP4_PER_BF16 = 6.0
+FP8_PER_BF16 = 2.0
 
 
 def fp4_peak_from_bf16(peaks: dict) -> float:
@@ -268,16 +283,18 @@ def oracle_sample(w: synth.Workload, x, ids, tw, n_tokens: int):
     return tokens, sub, Wc
 
 
-def time_oracle(w, x, ids, tw, n_tokens: int, repeats: int = 1, min_seconds: float = 0.0):
+def time_oracle(w, x, ids, tw, n_tokens: int, repeats: int = 1, min_seconds: float = 0.0,
+                act_fp8: bool = False):
     """The oracle on the first n_tokens tokens (with all their experts), run `repeats`
     times, or more until min_seconds of CPU work have been timed (at most 64 runs)."""
     import oracle
 
+    layer = oracle.moe_w4a8 if act_fp8 else oracle.moe
     tokens, sub, Wc = oracle_sample(w, x, ids, tw, n_tokens)
     times = []
     while len(times) < repeats or (sum(times) < min_seconds and len(times) < 64):
         t0 = time.perf_counter()
-        oracle.moe(x[tokens], sub, tw[tokens], *Wc)
+        layer(x[tokens], sub, tw[tokens], *Wc)
         times.append(time.perf_counter() - t0)
     return {"tokens": len(tokens), "seconds": times, "threads": oracle.threads()}
 
@@ -339,20 +356,21 @@ def run_reference(args):
     n = args.cpu_sample_tokens or max(4, default_cpu_tokens(w) // 3)
     import oracle
 
+    layer = oracle.moe_w4a8 if w4a8(args) else oracle.moe
     tokens, sub, Wc = oracle_sample(w, x, ids, tw, n)
     for _ in range(args.warmup):
-        oracle.moe(x[tokens[:2]], sub[:2], tw[tokens[:2]], *Wc)
+        layer(x[tokens[:2]], sub[:2], tw[tokens[:2]], *Wc)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle.moe(x[tokens], sub, tw[tokens], *Wc)
+        layer(x[tokens], sub, tw[tokens], *Wc)
     dt = (time.perf_counter() - t0) / args.steps
     value = len(tokens) / dt
     line = {
-        "impl": "reference", "metric": METRIC, "value": value,
+        "impl": "reference", "metric": metric(args), "value": value,
         "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": dict(config_dict(w, world), dispatch=args.dispatch),
+        "config": dict(config_dict(w, world), dispatch=args.dispatch, mma_type=args.mma),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.threads(),
                          "kind": "oracle",
                          "sample": f"first {len(tokens)} of {w.T} tokens per step, all their experts"},
@@ -379,7 +397,8 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     w = workload(args)
-    dims = mx.make_dims(w.H, w.I, w.E, w.k, w.T)
+    dims = mx.make_dims(w.H, w.I, w.E, w.k, w.T,
+                        mx.MOE_MMA_FP8xFP4 if w4a8(args) else mx.MOE_MMA_MXF4xMXF4)
     stream = torch.cuda.Stream(dev)
 
     t_setup = time.perf_counter()
@@ -469,12 +488,13 @@ def run_ours(args):
         step_ms, _ = timed_pass(False)
         prof_step_ms, per_kernel = timed_pass(True)
         graph_ms = timed_graph_pass()
-    probe = fp4_mma_probe(mx, ws, stream, mx.moe_device_sm_count())
+    # the FP4 MMA probe measures kind::mxf4; it is no roof for the fp8xfp4 MMAs
+    probe = None if w4a8(args) else fp4_mma_probe(mx, ws, stream, mx.moe_device_sm_count())
     ms_local = statistics.mean(step_ms)
     ms = max_over_ranks(world, ms_local)
     value = job_tokens_per_s(world, w.T, ms)
 
-    alg = algorithmic(w, ids)
+    alg = algorithmic(w, ids, w4a8(args))
     peaks, peak_kind = measured_peaks()
     hbm_peak = float(peaks["hbm_gbs"])
     kern_ms = {k: v[0] / max(v[1], 1) for k, v in per_kernel.items()}
@@ -482,8 +502,10 @@ def run_ours(args):
     dom_bytes = alg["layer_kernel_bytes"]
     dom_ms = kern_ms.get(dominant, float("nan"))
     achieved = dom_bytes / (dom_ms / 1e3) / 1e9
-    traffic = recorded_traffic(dominant, w.name)
-    fp4_peak = fp4_peak_from_bf16(peaks)
+    traffic = recorded_traffic(dominant, w.name + ("_fp8xfp4" if w4a8(args) else ""))
+    # the tensor roof of the MMA kind: FP4 rate (mxf4) or FP8 rate (mxf8f6f4)
+    ratio = FP8_PER_BF16 if w4a8(args) else FP4_PER_BF16
+    fp4_peak = fp4_peak_from_bf16(peaks) * ratio / FP4_PER_BF16
     flops_achieved = alg["flops"] / (dom_ms / 1e3) / 1e12
     # The binding roof is the one that allows the longer time.
     t_hbm = dom_bytes / (hbm_peak * 1e9)
@@ -495,7 +517,8 @@ def run_ours(args):
     tensor_roof = {"kernel": dominant, "bound": "tensor", "achieved": flops_achieved,
                    "peak": fp4_peak, "unit": "TFLOP/s", "frac": flops_achieved / fp4_peak,
                    "traffic": traffic, "algorithmic_flops": alg["flops"], "avg_ms": dom_ms,
-                   "peak_kind": f"{peak_kind} bf16 GEMM burst x {FP4_PER_BF16:g} (nominal FP4:bf16)",
+                   "peak_kind": f"{peak_kind} bf16 GEMM burst x {ratio:g} (nominal "
+                                f"{'FP8' if w4a8(args) else 'FP4'}:bf16)",
                    "mma_probe_tflops": probe}
     roof, other_roof = (hbm_roof, tensor_roof) if t_hbm >= t_fp4 else (tensor_roof, hbm_roof)
 
@@ -523,7 +546,7 @@ def run_ours(args):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         n = args.cpu_sample_tokens or default_cpu_tokens(w)
-        r = time_oracle(w, x, ids, tw, n, min_seconds=10.0)
+        r = time_oracle(w, x, ids, tw, n, min_seconds=10.0, act_fp8=w4a8(args))
         runs, secs = len(r["seconds"]), sum(r["seconds"])
         cpu = {"value": r["tokens"] * runs / secs, "unit": "tokens/s", "cores": r["threads"],
                "kind": "oracle",
@@ -533,12 +556,14 @@ def run_ours(args):
     if rank != 0:
         return
     line = {
-        "metric": METRIC,
+        "metric": metric(args),
         "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "us_per_layer": ms * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "mxfp4 (e2m1 x ue8m0), fp32 accumulate", "data": "synthetic",
-        "config": dict(config_dict(w, world), dispatch=args.dispatch),
+        "dtype": ("mxfp4 weights (e2m1 x ue8m0) x mxfp8 activations (e4m3 x ue8m0), fp32 accumulate"
+                  if w4a8(args) else "mxfp4 (e2m1 x ue8m0), fp32 accumulate"),
+        "data": "synthetic",
+        "config": dict(config_dict(w, world), dispatch=args.dispatch, mma_type=args.mma),
         "layer_hbm_tbs": alg["layer_bytes"] / (ms / 1e3) / 1e12,
         "layer_roofline_frac": (alg["layer_bytes"] / (hbm_peak * 1e9)) / (ms / 1e3),
         "touched_experts": alg["touched_experts"],

@@ -18,6 +18,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libmxmoe.so")
 
 MOE_MMA_MXF4xMXF4 = 1
+MOE_MMA_FP8xFP4 = 2
 MOE_OK = 0
 MOE_ERR_INVALID_ARG = 1
 MOE_ERR_UNSUPPORTED = 2
@@ -193,12 +194,17 @@ def moe_check(ws, stream=None) -> None:
     _check(lib().moe_check(_ptr(ws), _stream(stream)))
 
 
+def _act_row_bytes(dims: MoeDims, K: int) -> int:
+    """Bytes of a quantised activation row: E4M3 (fp8xfp4) or packed E2M1."""
+    return K if dims.mma_type == MOE_MMA_FP8xFP4 else K // 2
+
+
 def moe_read_dispatch(dims: MoeDims, ws, num_tokens: int) -> dict:
     T, k, H, E = int(num_tokens), dims.topk, dims.hidden, dims.num_experts
     out = {
         "counts": np.zeros(E, np.int32),
         "assign_slot": np.zeros(T * k, np.int32),
-        "x_codes": np.zeros((T * k, H // 2), np.uint8),
+        "x_codes": np.zeros((T * k, _act_row_bytes(dims, H)), np.uint8),
         "x_scales": np.zeros((T * k, H // 32), np.uint8),
         "slot_token": np.zeros(T * k, np.int32),
     }
@@ -209,7 +215,7 @@ def moe_read_dispatch(dims: MoeDims, ws, num_tokens: int) -> dict:
 
 def moe_read_intermediate(dims: MoeDims, ws, num_tokens: int) -> dict:
     T, k, I = int(num_tokens), dims.topk, dims.inter
-    out = {"h_codes": np.zeros((T * k, I // 2), np.uint8),
+    out = {"h_codes": np.zeros((T * k, _act_row_bytes(dims, I)), np.uint8),
            "h_scales": np.zeros((T * k, I // 32), np.uint8)}
     _check(lib().moe_read_intermediate(ctypes.byref(dims), _ptr(ws), T, _ptr(out["h_codes"]),
                                        _ptr(out["h_scales"])))

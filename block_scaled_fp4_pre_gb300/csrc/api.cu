@@ -43,6 +43,12 @@ bool dims_equal(const moe_dims& a, const moe_dims& b) {
          a.topk == b.topk && a.max_tokens == b.max_tokens && a.mma_type == b.mma_type;
 }
 
+// Bytes of one quantised activation row of K elements: packed E2M1 (two per byte)
+// for mxf4xmxf4, one E4M3 byte each for fp8xfp4.
+int64_t act_row_bytes(const moe_dims& d, int64_t K) {
+  return d.mma_type == MOE_MMA_FP8xFP4 ? K : K / 2;
+}
+
 WsLayout ws_layout(const moe_dims& d) {
   WsLayout L;
   const int64_t H = d.hidden, I = d.inter, E = d.num_experts, k = d.topk;
@@ -69,11 +75,11 @@ WsLayout ws_layout(const moe_dims& d) {
   L.off_slot_token = take((size_t)L.R_cap * 4);
   L.off_slot_assign = take((size_t)L.R_cap * 4);
   L.off_slot_weight = take((size_t)L.R_cap * 4);
-  L.off_xb = take((size_t)L.R_cap * H / 2);
+  L.off_xb = take((size_t)L.R_cap * act_row_bytes(d, H));
   L.off_xsf = take((size_t)L.R_cap * H / 32);
   L.off_xq = take((size_t)L.T_cap * H / 2);
   L.off_xs = take((size_t)L.T_cap * H / 32);
-  L.off_hb = take((size_t)L.R_cap * I / 2);
+  L.off_hb = take((size_t)L.R_cap * act_row_bytes(d, I));
   L.off_hsf = take((size_t)L.R_cap * I / 32);
   L.off_acc = take((size_t)L.T_cap * H * 4);
   L.off_stage_x = take((size_t)L.T_cap * H * 2);
@@ -125,7 +131,9 @@ PrepLayout prep_layout(const moe_dims& d) {
   return P;
 }
 
-Shape shape_of(const moe_dims& d) { return Shape{d.hidden, d.inter, d.num_experts, d.topk}; }
+Shape shape_of(const moe_dims& d) {
+  return Shape{d.hidden, d.inter, d.num_experts, d.topk, d.mma_type == MOE_MMA_FP8xFP4 ? 1 : 0};
+}
 
 // Workspaces initialised by moe_workspace_init, with the dims they were laid out for
 // and whether their accumulator holds a fresh pre_dispatch (cleared rows, no sums
@@ -209,8 +217,9 @@ int sm_count() {
 
 moe_status check_dims(const moe_dims* d) {
   if (!d) return fail(MOE_ERR_INVALID_ARG, "dims is NULL");
-  if (d->mma_type != MOE_MMA_MXF4xMXF4)
-    return fail(MOE_ERR_UNSUPPORTED, "mma_type %d: only MOE_MMA_MXF4xMXF4 (mxf4xmxf4) is built",
+  if (d->mma_type != MOE_MMA_MXF4xMXF4 && d->mma_type != MOE_MMA_FP8xFP4)
+    return fail(MOE_ERR_UNSUPPORTED,
+                "mma_type %d: MOE_MMA_MXF4xMXF4 (mxf4xmxf4) and MOE_MMA_FP8xFP4 (fp8xfp4) are built",
                 d->mma_type);
   if (d->hidden < 256 || d->hidden % 128 != 0 || d->hidden > 65536)
     return fail(MOE_ERR_INVALID_ARG, "hidden %d must be a multiple of 128 in [256, 65536]",
@@ -390,6 +399,8 @@ moe_status moe_workspace_set_dispatch(void* ws, int32_t mode) {
   auto it = g_registry.find(ws);
   if (it == g_registry.end())
     return fail(MOE_ERR_WORKSPACE_MISMATCH, "workspace %p was not initialised", ws);
+  if (mode == MOE_DISPATCH_PULL && it->second.dims.mma_type != MOE_MMA_MXF4xMXF4)
+    return fail(MOE_ERR_UNSUPPORTED, "pull dispatch is built for mxf4xmxf4 only");
   it->second.dispatch_mode = mode;
   it->second.dispatched = false;   // a pre_dispatch in the new mode must come first
   return MOE_OK;
@@ -603,7 +614,8 @@ moe_status moe_read_dispatch(const moe_dims* dims, const void* ws, int32_t T, in
       }
     }
   } else if (xc_host || xs_host) {
-    std::vector<uint8_t> codes((size_t)R * H / 2), sf((size_t)R * H / 32);
+    const size_t rb = (size_t)act_row_bytes(*dims, H);
+    std::vector<uint8_t> codes((size_t)R * rb), sf((size_t)R * H / 32);
     if (R && (e = cudaMemcpy(codes.data(), b + L.off_xb, codes.size(), cudaMemcpyDeviceToHost)))
       return cuda_fail(e, "codes read");
     if (R && (e = cudaMemcpy(sf.data(), b + L.off_xsf, sf.size(), cudaMemcpyDeviceToHost)))
@@ -613,9 +625,9 @@ moe_status moe_read_dispatch(const moe_dims* dims, const void* ws, int32_t T, in
       const bool ok = r >= 0 && r < R;
       if (xc_host) {
         if (ok)
-          std::memcpy(xc_host + a * (H / 2), codes.data() + (size_t)r * H / 2, (size_t)H / 2);
+          std::memcpy(xc_host + a * rb, codes.data() + (size_t)r * rb, rb);
         else
-          std::memset(xc_host + a * (H / 2), 0, (size_t)H / 2);
+          std::memset(xc_host + a * rb, 0, rb);
       }
       if (xs_host)
         for (int g = 0; g < H / 32; ++g)
@@ -645,7 +657,8 @@ moe_status moe_read_intermediate(const moe_dims* dims, const void* ws, int32_t T
     return cuda_fail(e, "seg read");
   const int64_t R = seg[E];
   if (R < 0 || R > L.R_cap) return fail(MOE_ERR_CUDA, "corrupt segment table");
-  std::vector<uint8_t> codes((size_t)R * I / 2), sf((size_t)R * I / 32);
+  const size_t rb = (size_t)act_row_bytes(*dims, I);
+  std::vector<uint8_t> codes((size_t)R * rb), sf((size_t)R * I / 32);
   if (R && (e = cudaMemcpy(codes.data(), b + L.off_hb, codes.size(), cudaMemcpyDeviceToHost)))
     return cuda_fail(e, "codes read");
   if (R && (e = cudaMemcpy(sf.data(), b + L.off_hsf, sf.size(), cudaMemcpyDeviceToHost)))
@@ -655,9 +668,9 @@ moe_status moe_read_intermediate(const moe_dims* dims, const void* ws, int32_t T
     const bool ok = r >= 0 && r < R;
     if (hc_host) {
       if (ok)
-        std::memcpy(hc_host + a * (I / 2), codes.data() + (size_t)r * I / 2, (size_t)I / 2);
+        std::memcpy(hc_host + a * rb, codes.data() + (size_t)r * rb, rb);
       else
-        std::memset(hc_host + a * (I / 2), 0, (size_t)I / 2);
+        std::memset(hc_host + a * rb, 0, rb);
     }
     if (hs_host)
       for (int g = 0; g < I / 32; ++g)

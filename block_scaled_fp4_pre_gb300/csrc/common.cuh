@@ -61,6 +61,18 @@ __host__ __device__ __forceinline__ int gate_up_source_row(int r, int I) {
   return is_up * I + chunk * 16 + (within & 7) * 2 + odd;
 }
 
+// The same under the gran=8 contiguous interleave of FP8 activations: prepared rows
+// [gate 0..7, up 0..7, gate 8..15, up 8..15, ...].
+__host__ __device__ __forceinline__ int gate_up_source_row8(int r, int I) {
+  const int chunk = r >> 4, within = r & 15;
+  return (within >> 3) * I + chunk * 8 + (within & 7);
+}
+
+// Interleave by activation format: gran=8 when f8, else gran=16.
+__host__ __device__ __forceinline__ int gate_up_source_row_for(int r, int I, int f8) {
+  return f8 ? gate_up_source_row8(r, I) : gate_up_source_row(r, I);
+}
+
 // ---------------------------------------------------------------------------
 // Workspace layout (computed on the host from the dims, passed to kernels).
 struct WsLayout {
@@ -84,11 +96,11 @@ struct WsPtrs {
   int32_t* slot_token;   // [R_cap]
   int32_t* slot_assign;  // [R_cap]
   float* slot_weight;    // [R_cap]
-  uint8_t* xb;           // [R_cap, H/2] quantised token rows
+  uint8_t* xb;           // [R_cap, H/2] (FP4) or [R_cap, H] (FP8) quantised token rows
   uint8_t* xsf;          // 128x4 blocks of [R_cap, H/32]
   uint8_t* xq;           // [T_cap, H/2] quantised token rows, one per token (pull dispatch)
   uint8_t* xs;           // [T_cap, H/32] their scales, row-major (pull dispatch)
-  uint8_t* hb;           // [R_cap, I/2] requantised intermediate rows
+  uint8_t* hb;           // [R_cap, I/2] (FP4) or [R_cap, I] (FP8) requantised intermediate rows
   uint8_t* hsf;          // 128x4 blocks of [R_cap, I/32]
   float* acc;            // [T_cap, H] fp32 combine accumulator, cleared by pre_dispatch
 };
@@ -99,6 +111,7 @@ struct PrepLayout {
 
 struct Shape {
   int H, I, E, k;
+  int f8;   // 1: fp8xfp4 (E4M3 activations, gran=8 interleave); 0: mxf4xmxf4
 };
 
 // Launch with programmatic stream serialisation: the kernel may start before the

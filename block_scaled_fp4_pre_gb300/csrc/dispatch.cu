@@ -219,15 +219,20 @@ __global__ void assign_slots_kernel(const int32_t* __restrict__ ids, const float
 // The row is quantised into shared memory (and the token's fp32 combine row
 // cleared) while the bucketing kernel may still be running; the block then waits
 // for it, gives the token's k assignments their rows and copies the row to each.
+// F8: MXFP8 rows (one E4M3 byte per element, scale rule amax <= 448 * 2^e) for
+// fp8xfp4; otherwise MXFP4 rows (packed E2M1, amax <= 6 * 2^e).
+template <bool F8>
 __global__ void __launch_bounds__(256) quantize_scatter_kernel(const __nv_bfloat16* __restrict__ x,
                                                                const int32_t* __restrict__ ids,
                                                                const float* __restrict__ tw,
                                                                int H, int k, int E, WsPtrs ws,
                                                                bool pull) {
-  extern __shared__ __align__(16) uint8_t qsh[];       // [H/2 codes | H/32 scales]
+  constexpr int kBytesPer8 = F8 ? 8 : 4;                // code bytes of 8 elements
+  extern __shared__ __align__(16) uint8_t qsh[];       // [row codes | H/32 scales]
   __shared__ int32_t slots[32];
+  const int row_bytes_q = H / 8 * kBytesPer8;
   uint8_t* codes_sh = qsh;
-  uint8_t* sf_sh = qsh + H / 2;
+  uint8_t* sf_sh = qsh + row_bytes_q;
   const int t = blockIdx.x, tid = threadIdx.x;
   ptx::pdl_launch_dependents();
   {
@@ -257,12 +262,19 @@ __global__ void __launch_bounds__(256) quantize_scatter_kernel(const __nv_bfloat
     for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
     amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
     amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2));
-    const int e = ptx::mx_scale_exponent(amax);
+    const int e = F8 ? ptx::mxfp8_exponent(amax) : ptx::mx_scale_exponent(amax);
     const float inv = ptx::pow2_neg(e);
 #pragma unroll
     for (int i = 0; i < 8; ++i) v[i] *= inv;
-    const uint32_t c8 = ptx::e2m1x8(v);
     const uint8_t sb = (uint8_t)(e + 127);
+    if (F8) {
+      const uint2 c8 = ptx::e4m3x8(v);
+      if (!live) continue;
+      *reinterpret_cast<uint2*>(codes_sh + base) = c8;
+      if ((tid & 3) == 0) sf_sh[base / 32] = sb;
+      continue;
+    }
+    const uint32_t c8 = ptx::e2m1x8(v);
     if (!live) continue;
     if (pull) {
       // the token's one row, gathered by the layer kernel for each of its experts
@@ -278,15 +290,15 @@ __global__ void __launch_bounds__(256) quantize_scatter_kernel(const __nv_bfloat
   if (pull) return;
   __syncthreads();
   const int kc4 = H / 128;
-  const size_t row_bytes = (size_t)H / 2;
+  const size_t row_bytes = (size_t)row_bytes_q;
   for (int j = 0; j < k; ++j) {
     const int slot = slots[j];
     if (slot < 0) continue;
     uint4* dst = reinterpret_cast<uint4*>(ws.xb + (size_t)slot * row_bytes);
-    for (int i = tid; i < H / 32; i += blockDim.x) {   // 16-byte chunks of the code row
+    for (int i = tid; i < row_bytes_q / 16; i += blockDim.x)   // 16-byte chunks of the row
       dst[i] = reinterpret_cast<const uint4*>(codes_sh)[i];
+    for (int i = tid; i < H / 32; i += blockDim.x)
       ws.xsf[sf_atom_offset((size_t)slot, i, kc4)] = sf_sh[i];
-    }
   }
 }
 
@@ -317,7 +329,8 @@ __global__ void quantize_rows_kernel(const float* __restrict__ src, int64_t n_th
   }
 }
 
-// Row copy with the optional gran=16 interleave: 16 bytes per thread.
+// Row copy with the optional gate/up interleave (interleave: 0 none, 16 or 8 the
+// granule): 16 bytes per thread.
 __global__ void copy_rows_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst,
                                  int64_t total_chunks, int chunks_per_row, int rows_per_expert,
                                  int I, int interleave) {
@@ -327,7 +340,7 @@ __global__ void copy_rows_kernel(const uint8_t* __restrict__ src, uint8_t* __res
     const int part = (int)(c % chunks_per_row);
     const int64_t e = row / rows_per_expert;
     const int r = (int)(row % rows_per_expert);
-    const int sr = interleave ? gate_up_source_row(r, I) : r;
+    const int sr = interleave ? gate_up_source_row_for(r, I, interleave == 8) : r;
     const uint4 v = reinterpret_cast<const uint4*>(src + ((size_t)e * rows_per_expert + sr) *
                                                              (size_t)chunks_per_row * 16)[part];
     reinterpret_cast<uint4*>(dst)[c] = v;
@@ -351,7 +364,7 @@ __global__ void scale_blocks_kernel(const uint8_t* __restrict__ src, uint32_t* _
     const int64_t row = rb * 128 + q * 32 + i;          // row over E*rows
     const int64_t e = row / rows_per_expert;
     const int r = (int)(row % rows_per_expert);
-    const int sr = interleave ? gate_up_source_row(r, I) : r;
+    const int sr = interleave ? gate_up_source_row_for(r, I, interleave == 8) : r;
     const uint8_t* s = src + ((size_t)e * rows_per_expert + sr) * (size_t)Kc + 4 * kb;
     dst[w] = (uint32_t)s[0] | ((uint32_t)s[1] << 8) | ((uint32_t)s[2] << 16) |
              ((uint32_t)s[3] << 24);
@@ -411,8 +424,15 @@ cudaError_t launch_bucket(const Shape& s, const int32_t* ids, int T, const WsPtr
 cudaError_t launch_quantize_scatter(const Shape& s, const void* x, const int32_t* ids,
                                     const float* tw, int T, const WsPtrs& ws, bool pull,
                                     cudaStream_t st) {
-  return launch_pdl(quantize_scatter_kernel, dim3(T), dim3(256), (size_t)s.H / 2 + s.H / 32, st,
-                    reinterpret_cast<const __nv_bfloat16*>(x), ids, tw, s.H, s.k, s.E, ws, pull);
+  const size_t smem = (size_t)(s.f8 ? s.H : s.H / 2) + s.H / 32;
+  auto kern = s.f8 ? quantize_scatter_kernel<true> : quantize_scatter_kernel<false>;
+  if (smem > 48 * 1024) {   // wide rows (H up to 65536) need the opt-in limit
+    const cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  return launch_pdl(kern, dim3(T), dim3(256), smem, st, reinterpret_cast<const __nv_bfloat16*>(x),
+                    ids, tw, s.H, s.k, s.E, ws, pull);
 }
 
 cudaError_t launch_assign_slots(const Shape& s, const int32_t* ids, const float* tw, int T,
@@ -446,17 +466,18 @@ cudaError_t launch_prepare(const Shape& s, const uint8_t* w1c, const uint8_t* w1
                            const uint8_t* w2c, const uint8_t* w2s, uint8_t* prep,
                            const PrepLayout& pl, cudaStream_t st) {
   const int64_t E = s.E, H = s.H, I = s.I;
+  const int gran = s.f8 ? 8 : 16;   // gate/up interleave of the activation format
   {  // W1 codes: interleaved rows
     const int cpr = (int)(H / 2 / 16);
     const int64_t total = E * 2 * I * cpr;
     copy_rows_kernel<<<grid_for(total, 256, 16384), 256, 0, st>>>(w1c, prep + pl.off_w1c, total,
-                                                                  cpr, (int)(2 * I), (int)I, 1);
+                                                                  cpr, (int)(2 * I), (int)I, gran);
   }
   {  // W1 scales: interleaved rows, 128x4 blocks
     const int64_t words = E * 2 * I * (H / 32) / 4;
     scale_blocks_kernel<<<grid_for(words, 256, 16384), 256, 0, st>>>(
         w1s, reinterpret_cast<uint32_t*>(prep + pl.off_w1s), words, (int)(2 * I), (int)(H / 32),
-        (int)I, 1);
+        (int)I, gran);
   }
   {  // W2 codes: rows unchanged
     const int cpr = (int)(I / 2 / 16);

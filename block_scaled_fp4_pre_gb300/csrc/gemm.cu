@@ -75,7 +75,7 @@ struct __align__(16) SmemTail {
   // One chunk of intermediate rows, gathered from the four epilogue warps before
   // it is stored: per column, the item's 64 features (32 code bytes) and their two
   // scale bytes.  Double-buffered across chunks.
-  alignas(16) uint8_t hstage[2][kEpiCols][32];
+  alignas(16) uint8_t hstage[2][kEpiCols][64];   // 32 bytes used for E2M1, 64 for E4M3
   uint8_t sstage[2][kEpiCols][2];
   int32_t tile_start[1025];   // first tile of each expert (E <= 1024), see decode_item
 };
@@ -144,7 +144,11 @@ __device__ __forceinline__ float silu_times(float g, float u) {
   return __fdividef(g, 1.0f + __expf(-g)) * u;
 }
 
-template <int MODE, bool PULL>
+// F8: fp8xfp4 -- E4M3 token and intermediate rows (128 elements a k-block), E2M1
+// weights widened to 8-bit containers by their TMA copies (CU_TENSOR_MAP_DATA_TYPE_
+// 16U4_ALIGN16B), kind::mxf8f6f4 MMAs, gran=8 gate/up rows.  Otherwise mxf4xmxf4:
+// packed E2M1 throughout, 256 elements a k-block, kind::mxf4 MMAs, gran=16.
+template <int MODE, bool PULL, bool F8>
 __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
     moe_layer_kernel(const __grid_constant__ CUtensorMap tmap_w1,
                      const __grid_constant__ CUtensorMap tmap_x,
@@ -157,6 +161,7 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   SmemTail* tail = reinterpret_cast<SmemTail*>(smem + kSmemTail);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int kKb = F8 ? 128 : kBK;   // K elements per k-block (128-byte rows either way)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -307,7 +312,7 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
         if (leader) ok = ptx::mbar_wait(&tail->empty[stage], phase ^ 1u, abort_flag, kWaitLimitNs);
         ok = __shfl_sync(kFull, ok ? 1 : 0, 0) != 0;   // the stage is free for every lane
         if (!ok) break;
-        const int kvalid = min(kBK, P.K - kb * kBK);
+        const int kvalid = min(kKb, P.K - kb * kKb);
         const int atoms = kvalid / 128;
         uint64_t* bar = &tail->full[stage];
         uint8_t* b_dst = smem + kSmemB + (size_t)stage * kBTileBytes;
@@ -343,15 +348,18 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
         }
         if (leader) {
           // every byte the TMA lands here: the weight box and scales and, unless
-          // pulled, the token rows and their scales
+          // pulled, the token rows and their scales.  A widened E2M1 box (F8) counts
+          // its packed bytes only: each 16-byte chunk of it gets 8 bytes of data and
+          // 8 that the copy leaves untouched.
           const uint32_t bytes =
-              kATileBytes + atoms * kSFAtomBytes +
+              (F8 ? kATileBytes / 2 : kATileBytes) + atoms * kSFAtomBytes +
               (pulled ? 0u : (uint32_t)(nb * (kBBoxRows * kBKBytes) + atoms * kSFAtomBytes));
           ptx::mbar_arrive_expect_tx(bar, bytes);
           ptx::tma_load_2d(smem + kSmemA + (size_t)stage * kATileBytes, tw, kb * kBKBytes, wrow,
                            bar, pol_w);
           ptx::bulk_load(smem + kSmemSFA + (size_t)stage * kSFStageBytes,
-                         wsf + (size_t)kb * 2 * kSFAtomBytes, atoms * kSFAtomBytes, bar, pol_w);
+                         wsf + (size_t)kb * (kKb / 128) * kSFAtomBytes, atoms * kSFAtomBytes, bar,
+                         pol_w);
           if (!pulled) {
             if (nb * kBBoxRows == kBN) {
               ptx::tma_load_2d(b_dst, tt_full, kb * kBKBytes, row0, bar, pol_t);
@@ -361,7 +369,8 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
                                  row0 + j * kBBoxRows, bar, pol_t);
             }
             ptx::bulk_load(smem + kSmemSFB + (size_t)stage * kSFStageBytes,
-                           tsf + (size_t)kb * 2 * kSFAtomBytes, atoms * kSFAtomBytes, bar, pol_t);
+                           tsf + (size_t)kb * (kKb / 128) * kSFAtomBytes, atoms * kSFAtomBytes,
+                           bar, pol_t);
           }
           if (kb == 0 && g_next < total) {
             it_next = decode_item(g_next, n0, m0, m1, E, tile_start);
@@ -429,7 +438,7 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
           }
           ptx::tc_fence_after();
           if (pulled) ptx::fence_proxy_async_smem();
-          const int kvalid = min(kBK, P.K - kb * kBK);
+          const int kvalid = min(kKb, P.K - kb * kKb);
           const int atoms = kvalid / 128;
           const uint32_t sfa_t = tmem_base + (uint32_t)(kSfTmemBase + sfbuf * 16);
           const uint32_t sfb_t = sfa_t + 8;
@@ -441,12 +450,20 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
           }
           const uint32_t a_base = ptx::smem_addr(smem + kSmemA + (size_t)stage * kATileBytes);
           const uint32_t b_base = ptx::smem_addr(smem + kSmemB + (size_t)stage * kBTileBytes);
-          const int steps = kvalid / 64;
+          // 32 bytes of K per instruction: 64 packed E2M1 elements, or 32 one-byte ones
+          const int steps = kvalid / (F8 ? 32 : 64);
           for (int s = 0; s < steps; ++s) {
-            const uint32_t idesc = ptx::idesc_mxf4(n_mma, (s & 1) * 2);
-            ptx::tc_mma_mxf4(tmem_base, ptx::desc_sw128(a_base + s * 32),
-                             ptx::desc_sw128(b_base + s * 32), idesc, sfa_t + (s >> 1) * 4,
-                             sfb_t + (s >> 1) * 4, (kb | s) != 0 ? 1u : 0u);
+            if (F8) {
+              // one 128-element k-block: one scale atom, scale byte s of each row
+              ptx::tc_mma_f8f4(tmem_base, ptx::desc_sw128(a_base + s * 32),
+                               ptx::desc_sw128(b_base + s * 32), ptx::idesc_f8f4(n_mma, s), sfa_t,
+                               sfb_t, (kb | s) != 0 ? 1u : 0u);
+            } else {
+              const uint32_t idesc = ptx::idesc_mxf4(n_mma, (s & 1) * 2);
+              ptx::tc_mma_mxf4(tmem_base, ptx::desc_sw128(a_base + s * 32),
+                               ptx::desc_sw128(b_base + s * 32), idesc, sfa_t + (s >> 1) * 4,
+                               sfb_t + (s >> 1) * 4, (kb | s) != 0 ? 1u : 0u);
+            }
           }
           ptx::tc_commit(&tail->empty[stage]);
           sfbuf ^= 1u;
@@ -515,7 +532,7 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
         const int ncol = min(kEpiCols, n - c0);
         if (MODE == kModeRaw) {
           const int m = mt * kBM + q * 32 + lane;
-          const int col = gate_up_source_row(m, args.I);
+          const int col = gate_up_source_row_for(m, args.I, F8 ? 1 : 0);
 #pragma unroll
           for (int j = 0; j < kEpiCols; ++j) {
             if (j < ncol) {
@@ -525,7 +542,9 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
           }
         } else if (item_phase == 0) {
           // Rows of this warp: chunk c of 32 interleaved gate/up rows =
-          // [gate even 8 | up even 8 | gate odd 8 | up odd 8] of features c*16..c*16+15.
+          // [gate even 8 | up even 8 | gate odd 8 | up odd 8] of features c*16..c*16+15
+          // (F8, gran=8: [gate 8 | up 8 | gate next 8 | up next 8] of the same features).
+          // Either way lane l and lane l^8 hold the gate and up of one feature.
           // Columns go in pairs: gate lanes (0-7, 16-23) compute column 2p from their
           // gate and the up of lane+8, up lanes (8-15, 24-31) column 2p+1 from their up
           // and the gate of lane-8 -- one exchange, and no lane idles.
@@ -546,7 +565,7 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
           }
           ptx::named_bar_sync(1, 128);
           const int i_kc4 = args.I / 128;
-          const size_t hrow_bytes = (size_t)args.I / 2;
+          const size_t hrow_bytes = F8 ? (size_t)args.I : (size_t)args.I / 2;
           // All shared-memory reads first, then the arithmetic, then the writes: the
           // eight columns' work is independent and overlaps instead of forming one
           // chain through shared memory.
@@ -561,12 +580,28 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
           int ex[kEpiCols / 2];
 #pragma unroll
           for (int p = 0; p < kEpiCols / 2; ++p) {
-            ex[p] = ptx::mx_scale_exponent(amax[p]);
+            ex[p] = F8 ? ptx::mxfp8_exponent(amax[p]) : ptx::mx_scale_exponent(amax[p]);
             const float qv = hv[p] * ptx::pow2_neg(ex[p]);
-            const float qodd = __shfl_down_sync(kFull, qv, 16);
-            code[p] = ptx::e2m1x2(qv, qodd);
+            if (F8) {
+              code[p] = ptx::e4m3x2(qv, 0.f) & 0xFFu;
+            } else {
+              const float qodd = __shfl_down_sync(kFull, qv, 16);
+              code[p] = ptx::e2m1x2(qv, qodd);
+            }
           }
-          if (lane < 16) {
+          if (F8) {
+            // one E4M3 byte per lane and column: feature 16q + (l & 7) + 8 * (l >> 4)
+            // of the item's 64 (lanes 0-7 and 16-23 column 2p, lanes 8-15 and 24-31
+            // column 2p+1)
+            const int f = q * 16 + (lane & 7) + ((lane >> 4) << 3);
+#pragma unroll
+            for (int p = 0; p < kEpiCols / 2; ++p) {
+              const int jc = 2 * p + (up_lane ? 1 : 0);
+              tail->hstage[xb][jc][f] = (uint8_t)code[p];
+              if ((lane & 23) == 0 && (q & 1) == 0)
+                tail->sstage[xb][jc][q >> 1] = (uint8_t)(ex[p] + 127);
+            }
+          } else if (lane < 16) {
             // lanes 0-7 (column 2p) and 8-15 (column 2p+1) each hold one of the 8
             // bytes of features c*16..c*16+15 of their column (c = 4*slab + q)
 #pragma unroll
@@ -579,8 +614,27 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
           }
           ptx::named_bar_sync(1, 128);
           // The chunk's rows, whole: warp q stores columns 4q..4q+3, 16 code bytes a
-          // lane (two lanes fill a row's 32-byte sector) and the two scale bytes.
-          if (lane < 8) {
+          // lane (two lanes fill a row's 32-byte sector; F8: four lanes its 64 bytes)
+          // and the two scale bytes.
+          if (F8) {
+            if (lane < 16) {
+              const int jc = q * 4 + (lane >> 2);
+              if (jc < ncol) {
+                const size_t row = (size_t)row0 + c0 + jc;
+                const uint4 cv =
+                    *reinterpret_cast<const uint4*>(&tail->hstage[xb][jc][(lane & 3) * 16]);
+                *reinterpret_cast<uint4*>(args.ws.hb + row * hrow_bytes + (size_t)mt * 64 +
+                                          (lane & 3) * 16) = cv;
+              }
+            } else if (lane < 20) {
+              const int jc = q * 4 + (lane - 16);
+              if (jc < ncol) {
+                const size_t row = (size_t)row0 + c0 + jc;
+                const uint16_t sv = *reinterpret_cast<const uint16_t*>(&tail->sstage[xb][jc][0]);
+                *reinterpret_cast<uint16_t*>(args.ws.hsf + sf_atom_offset(row, mt * 2, i_kc4)) = sv;
+              }
+            }
+          } else if (lane < 8) {
             const int jc = q * 4 + (lane >> 1);
             if (jc < ncol) {
               const size_t row = (size_t)row0 + c0 + jc;
@@ -740,24 +794,44 @@ cudaError_t make_tmap(CUtensorMap* m, const void* base, uint64_t row_bytes, uint
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-PhaseArgs phase_args(const uint8_t* w_sf, const uint8_t* t_sf, int rows_per_expert, int K) {
+// kb_elems: K elements per k-block (256 for packed E2M1 tokens, 128 for E4M3).
+// Packed E2M1 matrix [rows, K elements] (K/2 bytes a row), read in boxes of 128
+// elements x 128 rows that land one element per byte: each 16 elements' 8 packed
+// bytes followed by 8 unused bytes (CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B), the
+// operand layout of kind::mxf8f6f4 for E2M1; 128-byte swizzle, 16 KiB a box.
+cudaError_t make_tmap_e2m1_wide(CUtensorMap* m, const void* base, uint64_t K, uint64_t rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return cudaErrorNotSupported;
+  const cuuint64_t dims[2] = {K, rows};
+  const cuuint64_t strides[1] = {K / 2};
+  const cuuint32_t box[2] = {128, kBM};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, const_cast<void*>(base),
+                         dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+PhaseArgs phase_args(const uint8_t* w_sf, const uint8_t* t_sf, int rows_per_expert, int K,
+                     int kb_elems) {
   PhaseArgs p;
   p.w_sf = w_sf;
   p.t_sf = t_sf;
   p.rows_per_expert = rows_per_expert;
   p.K = K;
   p.m_tiles = rows_per_expert / kBM;
-  p.num_kb = (K + kBK - 1) / kBK;
+  p.num_kb = (K + kb_elems - 1) / kb_elems;
   p.kc4 = K / 128;
   return p;
 }
 
-template <int MODE, bool PULL>
+template <int MODE, bool PULL, bool F8>
 cudaError_t launch_mode(const LayerLaunch& g, const CUtensorMap* maps, const LayerArgs& a,
                         cudaStream_t st) {
   static int grid = 0;   // per instantiation, for the device of the first launch
   if (grid == 0) {
-    cudaError_t err = cudaFuncSetAttribute(moe_layer_kernel<MODE, PULL>,
+    cudaError_t err = cudaFuncSetAttribute(moe_layer_kernel<MODE, PULL, F8>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)kSmemBytes);
     if (err != cudaSuccess) return err;
@@ -765,7 +839,7 @@ cudaError_t launch_mode(const LayerLaunch& g, const CUtensorMap* maps, const Lay
     // resident blocks)
     grid = kBlocksPerSM * g.num_sms;
   }
-  return launch_pdl(moe_layer_kernel<MODE, PULL>, dim3(grid), dim3(kThreads), kSmemBytes, st,
+  return launch_pdl(moe_layer_kernel<MODE, PULL, F8>, dim3(grid), dim3(kThreads), kSmemBytes, st,
                     maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], a);
 }
 
@@ -773,21 +847,33 @@ cudaError_t launch_mode(const LayerLaunch& g, const CUtensorMap* maps, const Lay
 
 cudaError_t launch_layer(const LayerLaunch& g, cudaStream_t st) {
   const Shape& s = g.shape;
+  const bool f8 = s.f8 != 0;
+  if (f8 && g.pull) return cudaErrorNotSupported;   // pull is built for E2M1 tokens only
+  // Activation rows: packed E2M1 (K/2 bytes) or E4M3 (K bytes).
+  const uint64_t xrow = f8 ? (uint64_t)s.H : (uint64_t)s.H / 2;
+  const uint64_t hrow = f8 ? (uint64_t)s.I : (uint64_t)s.I / 2;
   // Full token tiles come in one box of all 128 rows.
   const uint32_t full_rows = kBN;
   CUtensorMap maps[6];
   cudaError_t err;
-  if ((err = make_tmap(&maps[4], g.ws.xb, (uint64_t)s.H / 2, (uint64_t)g.R_cap, full_rows)) ||
-      (err = make_tmap(&maps[5], g.ws.hb, (uint64_t)s.I / 2, (uint64_t)g.R_cap, full_rows)))
+  if ((err = make_tmap(&maps[4], g.ws.xb, xrow, (uint64_t)g.R_cap, full_rows)) ||
+      (err = make_tmap(&maps[5], g.ws.hb, hrow, (uint64_t)g.R_cap, full_rows)) ||
+      (err = make_tmap(&maps[1], g.ws.xb, xrow, (uint64_t)g.R_cap, kBBoxRows)) ||
+      (err = make_tmap(&maps[3], g.ws.hb, hrow, (uint64_t)g.R_cap, kBBoxRows)))
     return err;
-  if ((err = make_tmap(&maps[0], g.w1_codes, (uint64_t)s.H / 2, (uint64_t)s.E * 2 * s.I, kBM)) ||
-      (err = make_tmap(&maps[1], g.ws.xb, (uint64_t)s.H / 2, (uint64_t)g.R_cap, kBBoxRows)) ||
-      (err = make_tmap(&maps[2], g.w2_codes, (uint64_t)s.I / 2, (uint64_t)s.E * s.H, kBM)) ||
-      (err = make_tmap(&maps[3], g.ws.hb, (uint64_t)s.I / 2, (uint64_t)g.R_cap, kBBoxRows)))
+  if (f8) {
+    // weights widened from packed E2M1 to one element per byte as they land
+    if ((err = make_tmap_e2m1_wide(&maps[0], g.w1_codes, (uint64_t)s.H, (uint64_t)s.E * 2 * s.I)) ||
+        (err = make_tmap_e2m1_wide(&maps[2], g.w2_codes, (uint64_t)s.I, (uint64_t)s.E * s.H)))
+      return err;
+  } else if ((err = make_tmap(&maps[0], g.w1_codes, (uint64_t)s.H / 2, (uint64_t)s.E * 2 * s.I, kBM)) ||
+             (err = make_tmap(&maps[2], g.w2_codes, (uint64_t)s.I / 2, (uint64_t)s.E * s.H, kBM))) {
     return err;
+  }
   LayerArgs a;
-  a.ph[0] = phase_args(g.w1_sf, g.ws.xsf, 2 * s.I, s.H);
-  a.ph[1] = phase_args(g.w2_sf, g.ws.hsf, s.H, s.I);
+  const int kb_elems = f8 ? 128 : kBK;
+  a.ph[0] = phase_args(g.w1_sf, g.ws.xsf, 2 * s.I, s.H, kb_elems);
+  a.ph[1] = phase_args(g.w2_sf, g.ws.hsf, s.H, s.I, kb_elems);
   a.num_phases = g.num_phases;
   a.H = s.H;
   a.I = s.I;
@@ -795,11 +881,14 @@ cudaError_t launch_layer(const LayerLaunch& g, cudaStream_t st) {
   a.E = s.E;
   a.ws = g.ws;
   a.gate_up_debug = g.gate_up_debug;
+  if (f8)
+    return g.num_phases == 2 ? launch_mode<kModeLayer, false, true>(g, maps, a, st)
+                             : launch_mode<kModeRaw, false, true>(g, maps, a, st);
   if (g.num_phases == 2)
-    return g.pull ? launch_mode<kModeLayer, true>(g, maps, a, st)
-                  : launch_mode<kModeLayer, false>(g, maps, a, st);
-  return g.pull ? launch_mode<kModeRaw, true>(g, maps, a, st)
-                : launch_mode<kModeRaw, false>(g, maps, a, st);
+    return g.pull ? launch_mode<kModeLayer, true, false>(g, maps, a, st)
+                  : launch_mode<kModeLayer, false, false>(g, maps, a, st);
+  return g.pull ? launch_mode<kModeRaw, true, false>(g, maps, a, st)
+                : launch_mode<kModeRaw, false, false>(g, maps, a, st);
 }
 
 }  // namespace mxmoe

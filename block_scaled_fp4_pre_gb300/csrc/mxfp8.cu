@@ -26,22 +26,8 @@ constexpr int kColsPerBlock = 128;
 constexpr int kThreads8 = 256;
 constexpr unsigned kFull8 = 0xFFFFFFFFu;
 
-// Smallest e with amax <= 448 * 2^e, clamped below at -127 (fp32 bit arithmetic:
-// amax = 1.m * 2^p needs e >= p - 8, one more when 1.m > 1.75).
-__device__ __forceinline__ int mxfp8_exponent(float amax) {
-  const uint32_t b = __float_as_uint(amax);
-  const int biased = (int)((b >> 23) & 0xFFu);
-  if (biased == 0) return -127;   // zero or subnormal: 448 * 2^-127 already covers it
-  const int e = biased - 135 + (((b & 0x7FFFFFu) > 0x600000u) ? 1 : 0);
-  return e < -127 ? -127 : e;
-}
-
-// Two scaled values (|v| <= 448) to E4M3, round to nearest even; `lo` in bits 0-7.
-__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
-  uint16_t r;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-  return (uint32_t)r;
-}
+using ptx::e4m3x2;
+using ptx::mxfp8_exponent;
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }

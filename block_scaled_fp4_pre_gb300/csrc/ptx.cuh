@@ -236,6 +236,21 @@ __device__ __forceinline__ void tc_mma_mxf4(uint32_t d_tmem, uint64_t adesc, uin
       : "memory");
 }
 
+// D[tmem] (+)= A[smem] * B[smem]^T with A = E2M1 in the 8-bit-container layout that
+// a CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B copy writes, B = E4M3, one UE8M0 scale per
+// 32 elements of K for each (K = 32 per instruction).
+__device__ __forceinline__ void tc_mma_f8f4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, "
+      "[%5], [%6], p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+      : "memory");
+}
+
 // Shared-memory matrix descriptor, K-major, 128-byte swizzle: 8-row x 128-byte
 // atoms stacked every 1024 bytes.
 __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
@@ -259,6 +274,14 @@ __device__ __forceinline__ uint64_t desc_sf(uint32_t saddr) {
 // K-major operands; sf_id picks the byte pair of the scale registers.
 __device__ __forceinline__ uint32_t idesc_mxf4(int N, int sf_id) {
   return ((uint32_t)sf_id << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
+         (1u << 23) | ((uint32_t)(128 >> 4) << 24) | ((uint32_t)sf_id << 29);
+}
+
+// Instruction descriptor of kind::mxf8f6f4 with A = E2M1 (format 5), B = E4M3
+// (format 0), UE8M0 scales, M = 128, K-major operands; sf_id (0..3) picks the scale
+// byte of the four a scale register holds for each row.
+__device__ __forceinline__ uint32_t idesc_f8f4(int N, int sf_id) {
+  return ((uint32_t)sf_id << 4) | (5u << 7) | (0u << 10) | ((uint32_t)(N >> 3) << 17) |
          (1u << 23) | ((uint32_t)(128 >> 4) << 24) | ((uint32_t)sf_id << 29);
 }
 
@@ -387,6 +410,30 @@ __device__ __forceinline__ uint32_t e2m1x2(float a, float b) {
       : "f"(fabsf(b)), "f"(fabsf(a)));
   return ((uint32_t)r & 0xFFu) | ((__float_as_uint(a) >> 31) << 3) |
          ((__float_as_uint(b) >> 31) << 7);
+}
+
+// ---- MXFP8 element math ----------------------------------------------------
+// Smallest e with amax <= 448 * 2^e, clamped below at -127 (fp32 bit arithmetic:
+// amax = 1.m * 2^p needs e >= p - 8, one more when 1.m > 1.75).
+__device__ __forceinline__ int mxfp8_exponent(float amax) {
+  const uint32_t b = __float_as_uint(amax);
+  const int biased = (int)((b >> 23) & 0xFFu);
+  if (biased == 0) return -127;   // zero or subnormal: 448 * 2^-127 already covers it
+  const int e = biased - 135 + (((b & 0x7FFFFFu) > 0x600000u) ? 1 : 0);
+  return e < -127 ? -127 : e;
+}
+
+// Two scaled values (|v| <= 448) to E4M3, round to nearest even; `lo` in bits 0-7.
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return (uint32_t)r;
+}
+
+// Eight scaled values to E4M3 bytes, element i in byte i.
+__device__ __forceinline__ uint2 e4m3x8(const float (&v)[8]) {
+  return make_uint2(e4m3x2(v[0], v[1]) | (e4m3x2(v[2], v[3]) << 16),
+                    e4m3x2(v[4], v[5]) | (e4m3x2(v[6], v[7]) << 16));
 }
 
 }  // namespace ptx

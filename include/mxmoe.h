@@ -55,7 +55,7 @@ typedef int32_t moe_status;
 enum {
     MOE_OK = 0,
     MOE_ERR_INVALID_ARG = 1,         /* null/misaligned pointer, bad size or shape   */
-    MOE_ERR_UNSUPPORTED = 2,         /* mma_type other than MOE_MMA_MXF4xMXF4        */
+    MOE_ERR_UNSUPPORTED = 2,         /* mma_type or mode that is not built           */
     MOE_ERR_WORKSPACE_TOO_SMALL = 3, /* ws_bytes < moe_workspace_size(dims)          */
     MOE_ERR_WORKSPACE_MISMATCH = 4,  /* workspace initialised for other dims/mma    */
     MOE_ERR_CUDA = 5,                /* a CUDA runtime/driver call failed            */
@@ -63,9 +63,16 @@ enum {
     MOE_ERR_TIMEOUT = 7              /* a device wait ran past its limit             */
 };
 
-/* Operand types of the expert GEMMs.  Only MXFP4 x MXFP4 (the pages' "mxf4xmxf4")
- * is built; every other value returns MOE_ERR_UNSUPPORTED. */
-enum { MOE_MMA_MXF4xMXF4 = 1 };
+/* Operand types of the expert GEMMs (digest of PR #37279, items 1-4: the explicit
+ * mma_type):
+ *   MOE_MMA_MXF4xMXF4  "mxf4xmxf4": activations MXFP4 (packed E2M1, UE8M0 per 32),
+ *                      W1 gate/up rows interleaved with gran=16 (even/odd).
+ *   MOE_MMA_FP8xFP4    "fp8xfp4" (W4A8): activations MXFP8 (one E4M3 byte per
+ *                      element, UE8M0 per 32; the scale 2^e with e the smallest
+ *                      integer such that amax <= 448 * 2^e), W1 gate/up rows
+ *                      interleaved with gran=8 ([gate 0..7, up 0..7, gate 8..15, ..]).
+ * The weights are MXFP4 in both.  Every other value returns MOE_ERR_UNSUPPORTED. */
+enum { MOE_MMA_MXF4xMXF4 = 1, MOE_MMA_FP8xFP4 = 2 };
 
 /* Layer dimensions.  hidden H and inter I must be multiples of 128 (H >= 256);
  * 1 <= topk <= min(num_experts, 32); 1 <= num_experts <= 1024;
@@ -114,7 +121,9 @@ MXMOE_API moe_status moe_workspace_init(const moe_dims *dims, void *ws_dev, size
  *     experts' token tiles from those rows with asynchronous per-thread copies.
  * Both give the same results.  Set on an initialised workspace, before the
  * pre_dispatch whose forward should use it; MOE_ERR_INVALID_ARG for an unknown mode,
- * MOE_ERR_WORKSPACE_MISMATCH for a workspace moe_workspace_init has not seen. */
+ * MOE_ERR_WORKSPACE_MISMATCH for a workspace moe_workspace_init has not seen,
+ * MOE_ERR_UNSUPPORTED for MOE_DISPATCH_PULL on an fp8xfp4 workspace (pull is built
+ * for MXFP4 activations only). */
 enum { MOE_DISPATCH_BUCKETED = 0, MOE_DISPATCH_PULL = 1 };
 MXMOE_API moe_status moe_workspace_set_dispatch(void *ws_dev, int32_t mode);
 
@@ -130,7 +139,8 @@ MXMOE_API moe_status moe_quantize_mxfp4(const float *src_dev, int64_t rows, int3
  *   w2_codes_dev [E, H, I/2],  w2_scales_dev [E, H, I/32]
  * Output `prepared_dev` (prepared_bytes >= moe_prepared_weights_size): W1 rows
  * interleaved with gran=16 (each chunk of 16 gate and 16 up rows becomes
- * [gate even, up even, gate odd, up odd]), codes and scales alike, and both
+ * [gate even, up even, gate odd, up odd]; for fp8xfp4 gran=8: [gate 8, up 8]),
+ * codes and scales alike, and both
  * weights' scales in the 128x4 block layout.  Inputs are not modified; the
  * caller may free them afterwards. */
 MXMOE_API moe_status moe_prepare_weights(const moe_dims *dims, const uint8_t *w1_codes_dev,
@@ -138,7 +148,8 @@ MXMOE_API moe_status moe_prepare_weights(const moe_dims *dims, const uint8_t *w1
                                          const uint8_t *w2_scales_dev, void *prepared_dev,
                                          size_t prepared_bytes, void *stream);
 
-/* Quantise-and-bucket (the pages' mega_moe_pre_dispatch, group_size 32).
+/* Quantise-and-bucket (the pages' mega_moe_pre_dispatch, group_size 32): MXFP4 or,
+ * for fp8xfp4, MXFP8 token rows (see MOE_MMA_*).
  *   x_dev            bf16 [num_tokens, H] row-major, finite values
  *   topk_ids_dev     int32 [num_tokens, k]; ids outside [0, E) are skipped and
  *                    raise MOE_ERR_ROUTING at the next moe_check
@@ -152,7 +163,8 @@ MXMOE_API moe_status moe_pre_dispatch(const moe_dims *dims, const void *x_dev,
                                       void *stream);
 
 /* The expert layer on the buffers of the last moe_pre_dispatch on this workspace
- * (same num_tokens): grouped gate/up GEMM with SwiGLU and MXFP4 requantisation,
+ * (same num_tokens): grouped gate/up GEMM with SwiGLU and requantisation to the
+ * activation format of dims->mma_type,
  * grouped down GEMM, top-k weighted combine.  out_dev: bf16 [num_tokens, H].
  * Calling it again without a new moe_pre_dispatch recomputes the same layer (the
  * library then clears the accumulator rows first). */
@@ -180,6 +192,7 @@ MXMOE_API moe_status moe_check(void *ws_dev, void *stream);
  *   counts_host        int32 [E]          tokens routed to each expert
  *   assign_slot_host   int32 [T*k]        workspace row of assignment a (-1: skipped)
  *   x_codes_host       uint8 [T*k, H/2]   quantised token row as stored for assignment a
+ *                                         ([T*k, H]: one E4M3 byte each, for fp8xfp4)
  *   x_scales_host      uint8 [T*k, H/32]
  *   slot_token_host    int32 [T*k]        token recorded in row assign_slot[a] (check) */
 MXMOE_API moe_status moe_read_dispatch(const moe_dims *dims, const void *ws_dev,
@@ -188,6 +201,7 @@ MXMOE_API moe_status moe_read_dispatch(const moe_dims *dims, const void *ws_dev,
                                        uint8_t *x_scales_host, int32_t *slot_token_host);
 
 /*   h_codes_host  uint8 [T*k, I/2]   requantised SwiGLU output of assignment a
+ *                 ([T*k, I] for fp8xfp4)
  *   h_scales_host uint8 [T*k, I/32]                                                   */
 MXMOE_API moe_status moe_read_intermediate(const moe_dims *dims, const void *ws_dev,
                                            int32_t num_tokens, uint8_t *h_codes_host,

@@ -26,10 +26,10 @@ class DeviceLayer:
     """Prepared weights + an initialised workspace for one workload shape."""
 
     def __init__(self, w: synth.Workload, seed: int = 0, max_tokens: int | None = None,
-                 keep_canonical: bool = False):
+                 keep_canonical: bool = False, mma_type: int = mx.MOE_MMA_MXF4xMXF4):
         self.w = w
         self.seed = seed
-        self.dims = mx.make_dims(w.H, w.I, w.E, w.k, max_tokens or w.T)
+        self.dims = mx.make_dims(w.H, w.I, w.E, w.k, max_tokens or w.T, mma_type)
         dev = device()
         can = mxw.quantize_experts(self.dims, lambda e, o: synth.expert_w1_f32(w, e, seed, out=o),
                                    lambda e, o: synth.expert_w2_f32(w, e, seed, out=o), dev)

@@ -56,8 +56,13 @@ def test_header_compiles_as_c():
 def test_dims_validation(mx):
     ok = mx.make_dims(4096, 2048, 256, 6, 512)
     mx.moe_validate_dims(ok)
+    w4a8 = mx.make_dims(4096, 2048, 256, 6, 512, mma_type=mx.MOE_MMA_FP8xFP4)
+    mx.moe_validate_dims(w4a8)
+    # same weights; the E4M3 activation rows take twice the bytes of packed E2M1 rows
+    assert mx.moe_prepared_weights_size(w4a8) == mx.moe_prepared_weights_size(ok)
+    assert mx.moe_workspace_size(w4a8) > mx.moe_workspace_size(ok)
     bad = [
-        (mx.make_dims(4096, 2048, 256, 6, 512, mma_type=2), mx.MOE_ERR_UNSUPPORTED),
+        (mx.make_dims(4096, 2048, 256, 6, 512, mma_type=3), mx.MOE_ERR_UNSUPPORTED),
         (mx.make_dims(4096, 2048, 256, 6, 512, mma_type=0), mx.MOE_ERR_UNSUPPORTED),
         (mx.make_dims(4000, 2048, 256, 6, 512), mx.MOE_ERR_INVALID_ARG),
         (mx.make_dims(128, 2048, 256, 6, 512), mx.MOE_ERR_INVALID_ARG),

@@ -5,6 +5,7 @@ import glob
 import os
 
 import bench
+import synth
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
@@ -28,3 +29,15 @@ def test_committed_traffic_summaries_parse():
             assert got == float(vals["dram bytes per launch"])
         else:
             assert got is None     # counters taken on another version of the kernel
+
+
+def test_algorithmic_bytes_by_activation_format():
+    w = synth.WORKLOADS["layer_T512"]
+    ids, _ = synth.routing(w)
+    a4 = bench.algorithmic(w, ids)
+    a8 = bench.algorithmic(w, ids, act_fp8=True)
+    A = w.T * w.k
+    # same weights and FLOPs; the E4M3 token rows take H/2 more bytes each
+    assert a8["flops"] == a4["flops"] == 6 * A * w.H * w.I
+    assert a8["layer_kernel_bytes"] - a4["layer_kernel_bytes"] == A * (w.H // 2)
+    assert a4["layer_kernel_bytes"] == 256 * 13369344 + A * 2176
