@@ -75,6 +75,11 @@ def lib():
         l.oracle_moe_w4a8.argtypes = [ctypes.POINTER(Shape)] + [vp] * 15 + [ci]
         l.oracle_moe_w4a8.restype = i64
         l.oracle_moe_w4a8_down.argtypes = [ctypes.POINTER(Shape)] + [vp] * 8 + [ci]
+        l.oracle_nvfp4_quantize_f32.argtypes = [vp, i64, i64, vp, vp, ci]
+        l.oracle_nvfp4_quantize_bf16.argtypes = [vp, i64, i64, vp, vp, ci]
+        l.oracle_nvfp4_dequantize.argtypes = [vp, vp, i64, i64, vp]
+        l.oracle_moe_nvf4.argtypes = [ctypes.POINTER(Shape)] + [vp] * 15 + [ci]
+        l.oracle_moe_nvf4.restype = i64
         _lib = l
     return _lib
 
@@ -308,6 +313,71 @@ def moe_w4a8_down(ids, tw, w2_codes, w2_sf, h_codes, h_sf, H: int,
     lib().oracle_moe_w4a8_down(ctypes.byref(shape), _p(ids), _p(tw), *[_p(a) for a in arrs],
                                _p(out_f64), _p(out_bf16), nthreads or threads())
     return {"out_f64": out_f64, "out_bf16": out_bf16}
+
+
+def nvfp4_quantize_f32(x: np.ndarray, nthreads: int | None = None):
+    """fp32 [rows, K] -> (packed E2M1 codes [rows, K/2], E4M3 scale bytes [rows, K/16])."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    rows, K = x.shape
+    codes = np.zeros((rows, K // 2), np.uint8)
+    sf = np.zeros((rows, K // 16), np.uint8)
+    lib().oracle_nvfp4_quantize_f32(_p(x), rows, K, _p(codes), _p(sf), nthreads or threads())
+    return codes, sf
+
+
+def nvfp4_quantize_bf16(bits: np.ndarray, nthreads: int | None = None):
+    bits = np.ascontiguousarray(bits, dtype=np.uint16)
+    rows, K = bits.shape
+    codes = np.zeros((rows, K // 2), np.uint8)
+    sf = np.zeros((rows, K // 16), np.uint8)
+    lib().oracle_nvfp4_quantize_bf16(_p(bits), rows, K, _p(codes), _p(sf), nthreads or threads())
+    return codes, sf
+
+
+def nvfp4_dequantize(codes: np.ndarray, sf: np.ndarray) -> np.ndarray:
+    codes = np.ascontiguousarray(codes, np.uint8)
+    sf = np.ascontiguousarray(sf, np.uint8)
+    rows, half = codes.shape
+    out = np.zeros((rows, 2 * half), np.float64)
+    lib().oracle_nvfp4_dequantize(_p(codes), _p(sf), rows, 2 * half, _p(out))
+    return out
+
+
+def moe_nvf4(x_bf16, ids, tw, w1_codes, w1_sf, w2_codes, w2_sf, *, want_intermediates: bool = False,
+             want_y: bool = False, nthreads: int | None = None) -> dict:
+    """The NVFP4 layer: canonical NVFP4 weights w1_codes [E, 2I, H/2], w1_sf [E, 2I, H/16],
+    w2_codes [E, H, I/2], w2_sf [E, H, I/16] (E4M3 scale bytes, one per 16 elements)."""
+    x_bf16 = np.ascontiguousarray(x_bf16, np.uint16)
+    ids = np.ascontiguousarray(ids, np.int32)
+    tw = np.ascontiguousarray(tw, np.float32)
+    T, H = x_bf16.shape
+    k = ids.shape[1]
+    E, twoI, _ = w1_codes.shape
+    I = twoI // 2
+    A = T * k
+    arrs = [np.ascontiguousarray(a, np.uint8) for a in (w1_codes, w1_sf, w2_codes, w2_sf)]
+    assert arrs[0].shape == (E, 2 * I, H // 2) and arrs[1].shape == (E, 2 * I, H // 16)
+    assert arrs[2].shape == (E, H, I // 2) and arrs[3].shape == (E, H, I // 16)
+    res = {
+        "out_f64": np.zeros((T, H), np.float64),
+        "out_bf16": np.zeros((T, H), np.uint16),
+        "x_codes": np.zeros((T, H // 2), np.uint8),
+        "x_sf": np.zeros((T, H // 16), np.uint8),
+    }
+    if want_intermediates:
+        res["gate_up"] = np.zeros((A, 2 * I), np.float64)
+        res["h_codes"] = np.zeros((A, I // 2), np.uint8)
+        res["h_sf"] = np.zeros((A, I // 16), np.uint8)
+    if want_y:
+        res["y"] = np.zeros((A, H), np.float64)
+    shape = Shape(T, H, I, E, k)
+    bad = lib().oracle_moe_nvf4(ctypes.byref(shape), _p(x_bf16), _p(ids), _p(tw),
+                                *[_p(a) for a in arrs], _p(res["out_f64"]), _p(res["out_bf16"]),
+                                _p(res["x_codes"]), _p(res["x_sf"]), _p(res.get("gate_up")),
+                                _p(res.get("h_codes")), _p(res.get("h_sf")), _p(res.get("y")),
+                                nthreads or threads())
+    res["invalid_ids"] = int(bad)
+    return res
 
 
 def moe_down(ids, tw, w2_codes, w2_sf, h_codes, h_sf, H: int, nthreads: int | None = None) -> dict:

@@ -616,4 +616,185 @@ void oracle_moe_w4a8_down(const oracle_shape* s, const int32_t* ids, const float
                      true);
 }
 
+// ---------------------------------------------------------------------------
+// NVFP4 layer (digest of SGLang PR #37279: the motivation "nvfp4 megamoe support";
+// the pages give no arithmetic for it).  Readings, each the plainest one:
+//   R19 NVFP4 element format: E2M1 codes as R1, packed as R1, with one scale per 16
+//       elements along K; the scale is an unsigned E4M3 value (R13 without the sign),
+//       stored as its byte.  No second, per-tensor scale: the pages give none, so
+//       every quantised value is code value x block scale.
+//   R20 Block scale: s = the E4M3 value nearest to fp32(amax / 6) (ties to even,
+//       saturating at 448), amax over the 16 elements.  Element: q = fp32(x / s)
+//       (correctly rounded fp32 division), then the nearest E2M1 value, ties to the
+//       even code, saturating at 6; the sign bit follows x.  A scale of zero (all 16
+//       values below the smallest E4M3 step) makes every code a signed zero.
+//   R21 Activations (hidden states and the SwiGLU output h) and both weights use
+//       R19/R20; the first weight's gate/up rows use the gran=16 interleave of FP4
+//       activations.  Bucketing, SwiGLU (R6) and combine (R7) as before.
+
+// R20 on one group of 16 fp32 values: 8 packed code bytes and one scale byte.
+static void nvfp4_group(const float* v, uint8_t* codes8, uint8_t* sf) {
+    float amax = 0.0f;
+    for (int i = 0; i < 16; ++i) {
+        assert(std::isfinite(v[i]));
+        amax = std::max(amax, std::fabs(v[i]));
+    }
+    const float target = amax / 6.0f;                       // fp32, correctly rounded
+    const int sbyte = oracle_e4m3_encode(std::min((double)target, 448.0)) & 0x7F;
+    const double s = oracle_e4m3_value(sbyte);
+    int c[16];
+    for (int i = 0; i < 16; ++i) {
+        const int sign = std::signbit(v[i]) ? 8 : 0;
+        if (s == 0.0) {
+            c[i] = sign;
+            continue;
+        }
+        const float q = v[i] / (float)s;                     // fp32, correctly rounded
+        const double a = std::min((double)std::fabs(q), 6.0);
+        c[i] = (oracle_e2m1_encode(a) & 7) | sign;
+    }
+    for (int i = 0; i < 8; ++i) codes8[i] = (uint8_t)(c[2 * i] | (c[2 * i + 1] << 4));
+    *sf = (uint8_t)sbyte;
+}
+
+// Row-major fp32 [rows, K] -> codes [rows, K/2], scale bytes [rows, K/16].
+void oracle_nvfp4_quantize_f32(const float* x, int64_t rows, int64_t K, uint8_t* codes,
+                               uint8_t* sf, int nthreads) {
+    assert(K % 16 == 0);
+    parallel_for(rows, nthreads, [&](int64_t r0, int64_t r1) {
+        for (int64_t r = r0; r < r1; ++r)
+            for (int64_t g = 0; g < K / 16; ++g)
+                nvfp4_group(x + r * K + g * 16, codes + r * (K / 2) + g * 8, sf + r * (K / 16) + g);
+    });
+}
+
+// bf16 bits [rows, K] -> codes, scales (bf16 widens exactly to fp32).
+void oracle_nvfp4_quantize_bf16(const uint16_t* x, int64_t rows, int64_t K, uint8_t* codes,
+                                uint8_t* sf, int nthreads) {
+    assert(K % 16 == 0);
+    parallel_for(rows, nthreads, [&](int64_t r0, int64_t r1) {
+        float v[16];
+        for (int64_t r = r0; r < r1; ++r)
+            for (int64_t g = 0; g < K / 16; ++g) {
+                for (int i = 0; i < 16; ++i) v[i] = (float)bf16_bits_to_double(x[r * K + g * 16 + i]);
+                nvfp4_group(v, codes + r * (K / 2) + g * 8, sf + r * (K / 16) + g);
+            }
+    });
+}
+
+static void dequantize_nvfp4_row(const uint8_t* codes, const uint8_t* sf, int64_t K, double* out) {
+    for (int64_t kk = 0; kk < K; ++kk) {
+        const uint8_t byte = codes[kk / 2];
+        const int code = (kk % 2 == 0) ? (byte & 0xF) : (byte >> 4);
+        out[kk] = oracle_e2m1_value(code) * oracle_e4m3_value(sf[kk / 16] & 0x7F);
+    }
+}
+
+void oracle_nvfp4_dequantize(const uint8_t* codes, const uint8_t* sf, int64_t rows, int64_t K,
+                             double* out) {
+    for (int64_t r = 0; r < rows; ++r)
+        dequantize_nvfp4_row(codes + r * (K / 2), sf + r * (K / 16), K, out + r * K);
+}
+
+// The NVFP4 layer; arguments as oracle_moe, with every scale array one E4M3 byte per
+// 16 elements: w1_sf [E, 2I, H/16], w2_sf [E, H, I/16], x_sf [T, H/16], h_sf [A, I/16].
+int64_t oracle_moe_nvf4(const oracle_shape* s, const uint16_t* x_bf16, const int32_t* ids,
+                        const float* tw, const uint8_t* w1_codes, const uint8_t* w1_sf,
+                        const uint8_t* w2_codes, const uint8_t* w2_sf, double* out_f64,
+                        uint16_t* out_bf16, uint8_t* x_codes_out, uint8_t* x_sf_out,
+                        double* gate_up_out, uint8_t* h_codes_out, uint8_t* h_sf_out,
+                        double* y_out, int nthreads) {
+    const int64_t T = s->T, H = s->H, I = s->I, E = s->E, k = s->k, A = T * k;
+    assert(H % 16 == 0 && I % 16 == 0);
+
+    // 1. quantise the hidden states (R20)
+    std::vector<uint8_t> xc((size_t)T * H / 2), xs((size_t)T * H / 16);
+    oracle_nvfp4_quantize_bf16(x_bf16, T, H, xc.data(), xs.data(), nthreads);
+    if (x_codes_out) std::memcpy(x_codes_out, xc.data(), xc.size());
+    if (x_sf_out) std::memcpy(x_sf_out, xs.data(), xs.size());
+
+    // 2. bucket
+    std::vector<int64_t> counts(E), offsets(E + 1);
+    std::vector<int32_t> st(A), sj(A);
+    const int64_t bad =
+        oracle_bucket(ids, T, k, E, counts.data(), offsets.data(), st.data(), sj.data());
+    std::vector<double> xdq((size_t)T * H);
+    oracle_nvfp4_dequantize(xc.data(), xs.data(), T, H, xdq.data());
+
+    // 3. grouped gate/up projection
+    std::vector<double> gu((size_t)A * 2 * I, 0.0);
+    for (int64_t e = 0; e < E; ++e) {
+        if (counts[e] == 0) continue;
+        parallel_for(2 * I, nthreads, [&](int64_t n0, int64_t n1) {
+            std::vector<double> wrow((size_t)H);
+            for (int64_t n = n0; n < n1; ++n) {
+                dequantize_nvfp4_row(w1_codes + (e * 2 * I + n) * (H / 2),
+                                     w1_sf + (e * 2 * I + n) * (H / 16), H, wrow.data());
+                for (int64_t p = offsets[e]; p < offsets[e + 1]; ++p) {
+                    const int64_t t = st[p], a = t * k + sj[p];
+                    double acc = 0.0;
+                    for (int64_t kk = 0; kk < H; ++kk) acc += xdq[(size_t)t * H + kk] * wrow[kk];
+                    gu[(size_t)a * 2 * I + n] = acc;
+                }
+            }
+        });
+    }
+    if (gate_up_out) std::memcpy(gate_up_out, gu.data(), sizeof(double) * gu.size());
+
+    // 4-5. SwiGLU (R6) and NVFP4 requantisation of h (R20)
+    std::vector<uint8_t> hc((size_t)A * I / 2, 0), hs((size_t)A * I / 16, 0);
+    parallel_for(A, nthreads, [&](int64_t a0, int64_t a1) {
+        std::vector<float> h((size_t)I);
+        for (int64_t a = a0; a < a1; ++a) {
+            if (ids[a] < 0 || ids[a] >= E) continue;
+            for (int64_t i = 0; i < I; ++i) {
+                const double g = gu[(size_t)a * 2 * I + i];
+                const double u = gu[(size_t)a * 2 * I + I + i];
+                h[i] = (float)(g / (1.0 + std::exp(-g)) * u);
+            }
+            oracle_nvfp4_quantize_f32(h.data(), 1, I, &hc[(size_t)a * I / 2], &hs[(size_t)a * I / 16], 1);
+        }
+    });
+    if (h_codes_out) std::memcpy(h_codes_out, hc.data(), hc.size());
+    if (h_sf_out) std::memcpy(h_sf_out, hs.data(), hs.size());
+
+    // 6-7. grouped down projection and combine
+    std::vector<double> y((size_t)A * H, 0.0);
+    std::vector<double> hdq((size_t)A * I);
+    for (int64_t a = 0; a < A; ++a)
+        if (ids[a] >= 0 && ids[a] < E)
+            dequantize_nvfp4_row(&hc[(size_t)a * I / 2], &hs[(size_t)a * I / 16], I, &hdq[(size_t)a * I]);
+    for (int64_t e = 0; e < E; ++e) {
+        if (counts[e] == 0) continue;
+        parallel_for(H, nthreads, [&](int64_t n0, int64_t n1) {
+            std::vector<double> wrow((size_t)I);
+            for (int64_t n = n0; n < n1; ++n) {
+                dequantize_nvfp4_row(w2_codes + (e * H + n) * (I / 2), w2_sf + (e * H + n) * (I / 16),
+                                     I, wrow.data());
+                for (int64_t p = offsets[e]; p < offsets[e + 1]; ++p) {
+                    const int64_t a = (int64_t)st[p] * k + sj[p];
+                    double acc = 0.0;
+                    for (int64_t i = 0; i < I; ++i) acc += hdq[(size_t)a * I + i] * wrow[i];
+                    y[(size_t)a * H + n] = acc;
+                }
+            }
+        });
+    }
+    if (y_out) std::memcpy(y_out, y.data(), sizeof(double) * y.size());
+    parallel_for(T, nthreads, [&](int64_t t0, int64_t t1) {
+        for (int64_t t = t0; t < t1; ++t)
+            for (int64_t n = 0; n < H; ++n) {
+                double acc = 0.0;
+                for (int64_t j = 0; j < k; ++j) {
+                    const int32_t e = ids[t * k + j];
+                    if (e < 0 || e >= E) continue;
+                    acc += (double)tw[t * k + j] * y[(size_t)(t * k + j) * H + n];
+                }
+                if (out_f64) out_f64[t * H + n] = acc;
+                if (out_bf16) out_bf16[t * H + n] = oracle_bf16_round(acc);
+            }
+    });
+    return bad;
+}
+
 }  // extern "C"

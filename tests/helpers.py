@@ -22,6 +22,19 @@ def oracle_expert_weights(w: synth.Workload, experts, seed: int = 0):
     return np.stack(w1c), np.stack(w1s), np.stack(w2c), np.stack(w2s)
 
 
+def oracle_expert_weights_nvf4(w: synth.Workload, experts, seed: int = 0):
+    """As oracle_expert_weights, quantised to NVFP4 (E4M3 scale per 16 elements)."""
+    w1c, w1s, w2c, w2s = [], [], [], []
+    for e in experts:
+        c, s = oracle.nvfp4_quantize_f32(synth.expert_w1_f32(w, int(e), seed))
+        w1c.append(c)
+        w1s.append(s)
+        c, s = oracle.nvfp4_quantize_f32(synth.expert_w2_f32(w, int(e), seed))
+        w2c.append(c)
+        w2s.append(s)
+    return np.stack(w1c), np.stack(w1s), np.stack(w2c), np.stack(w2s)
+
+
 def normwise_rel_err(got, ref) -> float:
     got = np.asarray(got, np.float64)
     ref = np.asarray(ref, np.float64)
