@@ -39,6 +39,7 @@ L2_CLEAN_BYTES = 256 << 20          # read after the write flush, so that its di
 KERNELS_PER_STEP = 4                # bucket, quantize_scatter, layer (both GEMMs + combine), convert
 METRIC = "W4A4 MoE layer tokens/s (E=256, top-6, T=512; also us/layer and HBM TB/s)"
 METRIC_W4A8 = "W4A8 (fp8xfp4) MoE layer tokens/s (E=256, top-6, T=512; also us/layer and HBM TB/s)"
+METRIC_NVF4 = "NVFP4 (nvf4xnvf4) MoE layer tokens/s (E=256, top-6, T=512; also us/layer and HBM TB/s)"
 
 
 def w4a8(args) -> bool:
@@ -46,8 +47,13 @@ def w4a8(args) -> bool:
     return args.mma == "fp8xfp4"
 
 
+def nvf4(args) -> bool:
+    """nvf4xnvf4: NVFP4 weights and activations (E4M3 scale per 16 elements)."""
+    return args.mma == "nvf4xnvf4"
+
+
 def metric(args) -> str:
-    return METRIC_W4A8 if w4a8(args) else METRIC
+    return METRIC_W4A8 if w4a8(args) else METRIC_NVF4 if nvf4(args) else METRIC
 
 
 def parse_args():
@@ -63,8 +69,8 @@ def parse_args():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--dispatch", choices=["bucketed", "pull"], default="bucketed",
                    help="token rows copied per expert by pre_dispatch, or gathered by the layer")
-    p.add_argument("--mma", choices=["mxf4xmxf4", "fp8xfp4"], default="mxf4xmxf4",
-                   help="activation format: MXFP4 (W4A4, the headline) or MXFP8 (W4A8)")
+    p.add_argument("--mma", choices=["mxf4xmxf4", "fp8xfp4", "nvf4xnvf4"], default="mxf4xmxf4",
+                   help="formats: MXFP4 (W4A4, the headline), MXFP8 activations (W4A8) or NVFP4")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-sample-tokens", type=int, default=0)
     return p.parse_args()
@@ -154,20 +160,21 @@ def touched_experts(ids, E):
     return int(np.count_nonzero(np.bincount(ids.reshape(-1), minlength=E)))
 
 
-def algorithmic(w: synth.Workload, ids, act_fp8: bool = False) -> dict:
+def algorithmic(w: synth.Workload, ids, act_fp8: bool = False, sf_group: int = 32) -> dict:
     """Bytes a perfect implementation must move, and FLOPs.  act_fp8: the token rows
-    are E4M3 (one byte an element) instead of packed E2M1."""
+    are E4M3 (one byte an element) instead of packed E2M1; sf_group: elements per
+    scale byte (16 for NVFP4)."""
     H, I, k, T = w.H, w.I, w.k, w.T
     A = T * k
     u = touched_experts(ids, w.E)
-    w1 = 2 * I * H // 2 + 2 * I * H // 32           # gate/up codes + scales per expert
-    w2 = H * I // 2 + H * I // 32                   # down codes + scales per expert
+    w1 = 2 * I * H // 2 + 2 * I * H // sf_group     # gate/up codes + scales per expert
+    w2 = H * I // 2 + H * I // sf_group             # down codes + scales per expert
     return {
         "touched_experts": u,
         "layer_bytes": u * (w1 + w2) + 2 * T * H + 2 * T * H + 8 * T * k,
         # layer kernel: every touched expert's weights and the quantised token rows it
         # reads once
-        "layer_kernel_bytes": u * (w1 + w2) + A * ((H if act_fp8 else H // 2) + H // 32),
+        "layer_kernel_bytes": u * (w1 + w2) + A * ((H if act_fp8 else H // 2) + H // sf_group),
         "flops": 6 * A * H * I,
     }
 
@@ -273,24 +280,25 @@ def recorded_traffic(kernel: str, workload_name: str):
 # ---------------------------------------------------------------------------
 # CPU oracle timing (baseline and reference arm)
 
-def oracle_sample(w: synth.Workload, x, ids, tw, n_tokens: int):
+def oracle_sample(w: synth.Workload, x, ids, tw, n_tokens: int, nv: bool = False):
     import oracle
-    from tests.helpers import compact_problem, oracle_expert_weights
+    from tests.helpers import compact_problem, oracle_expert_weights, oracle_expert_weights_nvf4
 
     tokens = np.arange(min(n_tokens, w.T))
     sub, experts = compact_problem(ids, tokens)
-    Wc = oracle_expert_weights(w, experts)          # offline weight preparation, untimed
+    # offline weight preparation, untimed
+    Wc = (oracle_expert_weights_nvf4 if nv else oracle_expert_weights)(w, experts)
     return tokens, sub, Wc
 
 
 def time_oracle(w, x, ids, tw, n_tokens: int, repeats: int = 1, min_seconds: float = 0.0,
-                act_fp8: bool = False):
+                act_fp8: bool = False, nv: bool = False):
     """The oracle on the first n_tokens tokens (with all their experts), run `repeats`
     times, or more until min_seconds of CPU work have been timed (at most 64 runs)."""
     import oracle
 
-    layer = oracle.moe_w4a8 if act_fp8 else oracle.moe
-    tokens, sub, Wc = oracle_sample(w, x, ids, tw, n_tokens)
+    layer = oracle.moe_w4a8 if act_fp8 else oracle.moe_nvf4 if nv else oracle.moe
+    tokens, sub, Wc = oracle_sample(w, x, ids, tw, n_tokens, nv)
     times = []
     while len(times) < repeats or (sum(times) < min_seconds and len(times) < 64):
         t0 = time.perf_counter()
@@ -356,8 +364,8 @@ def run_reference(args):
     n = args.cpu_sample_tokens or max(4, default_cpu_tokens(w) // 3)
     import oracle
 
-    layer = oracle.moe_w4a8 if w4a8(args) else oracle.moe
-    tokens, sub, Wc = oracle_sample(w, x, ids, tw, n)
+    layer = oracle.moe_w4a8 if w4a8(args) else oracle.moe_nvf4 if nvf4(args) else oracle.moe
+    tokens, sub, Wc = oracle_sample(w, x, ids, tw, n, nvf4(args))
     for _ in range(args.warmup):
         layer(x[tokens[:2]], sub[:2], tw[tokens[:2]], *Wc)
     t0 = time.perf_counter()
@@ -398,7 +406,8 @@ def run_ours(args):
     torch.cuda.set_device(dev)
     w = workload(args)
     dims = mx.make_dims(w.H, w.I, w.E, w.k, w.T,
-                        mx.MOE_MMA_FP8xFP4 if w4a8(args) else mx.MOE_MMA_MXF4xMXF4)
+                        mx.MOE_MMA_FP8xFP4 if w4a8(args) else
+                        mx.MOE_MMA_NVF4xNVF4 if nvf4(args) else mx.MOE_MMA_MXF4xMXF4)
     stream = torch.cuda.Stream(dev)
 
     t_setup = time.perf_counter()
@@ -488,13 +497,14 @@ def run_ours(args):
         step_ms, _ = timed_pass(False)
         prof_step_ms, per_kernel = timed_pass(True)
         graph_ms = timed_graph_pass()
-    # the FP4 MMA probe measures kind::mxf4; it is no roof for the fp8xfp4 MMAs
-    probe = None if w4a8(args) else fp4_mma_probe(mx, ws, stream, mx.moe_device_sm_count())
+    # the FP4 MMA probe measures kind::mxf4; it is no roof for the other MMA kinds
+    probe = None if args.mma != "mxf4xmxf4" else fp4_mma_probe(mx, ws, stream,
+                                                               mx.moe_device_sm_count())
     ms_local = statistics.mean(step_ms)
     ms = max_over_ranks(world, ms_local)
     value = job_tokens_per_s(world, w.T, ms)
 
-    alg = algorithmic(w, ids, w4a8(args))
+    alg = algorithmic(w, ids, w4a8(args), 16 if nvf4(args) else 32)
     peaks, peak_kind = measured_peaks()
     hbm_peak = float(peaks["hbm_gbs"])
     kern_ms = {k: v[0] / max(v[1], 1) for k, v in per_kernel.items()}
@@ -502,7 +512,7 @@ def run_ours(args):
     dom_bytes = alg["layer_kernel_bytes"]
     dom_ms = kern_ms.get(dominant, float("nan"))
     achieved = dom_bytes / (dom_ms / 1e3) / 1e9
-    traffic = recorded_traffic(dominant, w.name + ("_fp8xfp4" if w4a8(args) else ""))
+    traffic = recorded_traffic(dominant, w.name + ("" if args.mma == "mxf4xmxf4" else "_" + args.mma))
     # the tensor roof of the MMA kind: FP4 rate (mxf4) or FP8 rate (mxf8f6f4)
     ratio = FP8_PER_BF16 if w4a8(args) else FP4_PER_BF16
     fp4_peak = fp4_peak_from_bf16(peaks) * ratio / FP4_PER_BF16
@@ -546,7 +556,7 @@ def run_ours(args):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         n = args.cpu_sample_tokens or default_cpu_tokens(w)
-        r = time_oracle(w, x, ids, tw, n, min_seconds=10.0, act_fp8=w4a8(args))
+        r = time_oracle(w, x, ids, tw, n, min_seconds=10.0, act_fp8=w4a8(args), nv=nvf4(args))
         runs, secs = len(r["seconds"]), sum(r["seconds"])
         cpu = {"value": r["tokens"] * runs / secs, "unit": "tokens/s", "cores": r["threads"],
                "kind": "oracle",
@@ -561,7 +571,9 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": ms, "us_per_layer": ms * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": ("mxfp4 weights (e2m1 x ue8m0) x mxfp8 activations (e4m3 x ue8m0), fp32 accumulate"
-                  if w4a8(args) else "mxfp4 (e2m1 x ue8m0), fp32 accumulate"),
+                  if w4a8(args) else
+                  "nvfp4 (e2m1 x ue4m3 per 16), fp32 accumulate" if nvf4(args) else
+                  "mxfp4 (e2m1 x ue8m0), fp32 accumulate"),
         "data": "synthetic",
         "config": dict(config_dict(w, world), dispatch=args.dispatch, mma_type=args.mma),
         "layer_hbm_tbs": alg["layer_bytes"] / (ms / 1e3) / 1e12,

@@ -19,6 +19,7 @@ LIB_PATH = os.path.join(_HERE, "libmxmoe.so")
 
 MOE_MMA_MXF4xMXF4 = 1
 MOE_MMA_FP8xFP4 = 2
+MOE_MMA_NVF4xNVF4 = 3
 MOE_OK = 0
 MOE_ERR_INVALID_ARG = 1
 MOE_ERR_UNSUPPORTED = 2
@@ -71,6 +72,7 @@ def lib() -> ctypes.CDLL:
             "moe_workspace_size": ([D], sz),
             "moe_workspace_init": ([D, vp, sz, vp], i32),
             "moe_quantize_mxfp4": ([vp, i64, i32, vp, vp, vp], i32),
+            "moe_quantize_nvfp4": ([vp, i64, i32, vp, vp, vp], i32),
             "moe_prepare_weights": ([D, vp, vp, vp, vp, vp, sz, vp], i32),
             "moe_pre_dispatch": ([D, vp, vp, vp, i32, vp, sz, vp], i32),
             "moe_forward": ([D, vp, vp, sz, vp, i32, vp], i32),
@@ -165,6 +167,16 @@ def moe_quantize_mxfp4(src, codes, scales, stream=None) -> None:
     _check(lib().moe_quantize_mxfp4(_ptr(src), rows, K, _ptr(codes), _ptr(scales), _stream(stream)))
 
 
+def moe_quantize_nvfp4(src, codes, scales, stream=None) -> None:
+    rows, K = src.shape
+    _check(lib().moe_quantize_nvfp4(_ptr(src), rows, K, _ptr(codes), _ptr(scales), _stream(stream)))
+
+
+def sf_group(dims: MoeDims) -> int:
+    """Elements per scale: 16 for nvf4xnvf4, 32 otherwise."""
+    return 16 if dims.mma_type == MOE_MMA_NVF4xNVF4 else 32
+
+
 def moe_prepare_weights(dims: MoeDims, w1_codes, w1_scales, w2_codes, w2_scales, prepared,
                         stream=None) -> None:
     _check(lib().moe_prepare_weights(ctypes.byref(dims), _ptr(w1_codes), _ptr(w1_scales),
@@ -205,7 +217,7 @@ def moe_read_dispatch(dims: MoeDims, ws, num_tokens: int) -> dict:
         "counts": np.zeros(E, np.int32),
         "assign_slot": np.zeros(T * k, np.int32),
         "x_codes": np.zeros((T * k, _act_row_bytes(dims, H)), np.uint8),
-        "x_scales": np.zeros((T * k, H // 32), np.uint8),
+        "x_scales": np.zeros((T * k, H // sf_group(dims)), np.uint8),
         "slot_token": np.zeros(T * k, np.int32),
     }
     _check(lib().moe_read_dispatch(ctypes.byref(dims), _ptr(ws), T, *[_ptr(out[n]) for n in
@@ -216,7 +228,7 @@ def moe_read_dispatch(dims: MoeDims, ws, num_tokens: int) -> dict:
 def moe_read_intermediate(dims: MoeDims, ws, num_tokens: int) -> dict:
     T, k, I = int(num_tokens), dims.topk, dims.inter
     out = {"h_codes": np.zeros((T * k, _act_row_bytes(dims, I)), np.uint8),
-           "h_scales": np.zeros((T * k, I // 32), np.uint8)}
+           "h_scales": np.zeros((T * k, I // sf_group(dims)), np.uint8)}
     _check(lib().moe_read_intermediate(ctypes.byref(dims), _ptr(ws), T, _ptr(out["h_codes"]),
                                        _ptr(out["h_scales"])))
     return out

@@ -49,6 +49,12 @@ int64_t act_row_bytes(const moe_dims& d, int64_t K) {
   return d.mma_type == MOE_MMA_FP8xFP4 ? K : K / 2;
 }
 
+// Scale bytes of one row of K elements: one E4M3 byte per 16 for nvf4xnvf4, one
+// UE8M0 byte per 32 otherwise.
+int64_t sf_row_bytes(const moe_dims& d, int64_t K) {
+  return d.mma_type == MOE_MMA_NVF4xNVF4 ? K / 16 : K / 32;
+}
+
 WsLayout ws_layout(const moe_dims& d) {
   WsLayout L;
   const int64_t H = d.hidden, I = d.inter, E = d.num_experts, k = d.topk;
@@ -76,11 +82,11 @@ WsLayout ws_layout(const moe_dims& d) {
   L.off_slot_assign = take((size_t)L.R_cap * 4);
   L.off_slot_weight = take((size_t)L.R_cap * 4);
   L.off_xb = take((size_t)L.R_cap * act_row_bytes(d, H));
-  L.off_xsf = take((size_t)L.R_cap * H / 32);
+  L.off_xsf = take((size_t)L.R_cap * sf_row_bytes(d, H));
   L.off_xq = take((size_t)L.T_cap * H / 2);
   L.off_xs = take((size_t)L.T_cap * H / 32);
   L.off_hb = take((size_t)L.R_cap * act_row_bytes(d, I));
-  L.off_hsf = take((size_t)L.R_cap * I / 32);
+  L.off_hsf = take((size_t)L.R_cap * sf_row_bytes(d, I));
   L.off_acc = take((size_t)L.T_cap * H * 4);
   L.off_stage_x = take((size_t)L.T_cap * H * 2);
   L.off_stage_ids = take((size_t)L.A_cap * 4);
@@ -122,17 +128,18 @@ PrepLayout prep_layout(const moe_dims& d) {
   P.off_w1c = o;
   o = align_up(o + E * 2 * I * H / 2, kAlign);
   P.off_w1s = o;
-  o = align_up(o + E * 2 * I * H / 32, kAlign);
+  o = align_up(o + E * 2 * I * (size_t)sf_row_bytes(d, (int64_t)H), kAlign);
   P.off_w2c = o;
   o = align_up(o + E * H * I / 2, kAlign);
   P.off_w2s = o;
-  o = align_up(o + E * H * I / 32, kAlign);
+  o = align_up(o + E * H * (size_t)sf_row_bytes(d, (int64_t)I), kAlign);
   P.total = o;
   return P;
 }
 
 Shape shape_of(const moe_dims& d) {
-  return Shape{d.hidden, d.inter, d.num_experts, d.topk, d.mma_type == MOE_MMA_FP8xFP4 ? 1 : 0};
+  return Shape{d.hidden, d.inter, d.num_experts, d.topk, d.mma_type == MOE_MMA_FP8xFP4 ? 1 : 0,
+               d.mma_type == MOE_MMA_NVF4xNVF4 ? 1 : 0};
 }
 
 // Workspaces initialised by moe_workspace_init, with the dims they were laid out for
@@ -217,9 +224,10 @@ int sm_count() {
 
 moe_status check_dims(const moe_dims* d) {
   if (!d) return fail(MOE_ERR_INVALID_ARG, "dims is NULL");
-  if (d->mma_type != MOE_MMA_MXF4xMXF4 && d->mma_type != MOE_MMA_FP8xFP4)
+  if (d->mma_type != MOE_MMA_MXF4xMXF4 && d->mma_type != MOE_MMA_FP8xFP4 &&
+      d->mma_type != MOE_MMA_NVF4xNVF4)
     return fail(MOE_ERR_UNSUPPORTED,
-                "mma_type %d: MOE_MMA_MXF4xMXF4 (mxf4xmxf4) and MOE_MMA_FP8xFP4 (fp8xfp4) are built",
+                "mma_type %d: MOE_MMA_MXF4xMXF4, MOE_MMA_FP8xFP4 and MOE_MMA_NVF4xNVF4 are built",
                 d->mma_type);
   if (d->hidden < 256 || d->hidden % 128 != 0 || d->hidden > 65536)
     return fail(MOE_ERR_INVALID_ARG, "hidden %d must be a multiple of 128 in [256, 65536]",
@@ -421,6 +429,21 @@ moe_status moe_quantize_mxfp4(const float* src, int64_t rows, int32_t K, uint8_t
   return MOE_OK;
 }
 
+moe_status moe_quantize_nvfp4(const float* src, int64_t rows, int32_t K, uint8_t* codes,
+                              uint8_t* scales, void* stream) {
+  if (rows < 0 || K <= 0 || K % 16 != 0)
+    return fail(MOE_ERR_INVALID_ARG, "rows %lld / K %d: need rows >= 0 and K %% 16 == 0",
+                (long long)rows, K);
+  if (rows == 0) return MOE_OK;
+  if (!src || !codes || !scales) return fail(MOE_ERR_INVALID_ARG, "NULL pointer");
+  if (!aligned(src, 16) || !aligned(codes, 4))
+    return fail(MOE_ERR_INVALID_ARG, "src must be 16-byte and codes 4-byte aligned");
+  cudaError_t e =
+      launch_quantize_rows_nv(src, rows, K, codes, scales, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "quantize kernel");
+  return MOE_OK;
+}
+
 moe_status moe_prepare_weights(const moe_dims* dims, const uint8_t* w1c, const uint8_t* w1s,
                                const uint8_t* w2c, const uint8_t* w2s, void* prepared,
                                size_t prepared_bytes, void* stream) {
@@ -615,7 +638,8 @@ moe_status moe_read_dispatch(const moe_dims* dims, const void* ws, int32_t T, in
     }
   } else if (xc_host || xs_host) {
     const size_t rb = (size_t)act_row_bytes(*dims, H);
-    std::vector<uint8_t> codes((size_t)R * rb), sf((size_t)R * H / 32);
+    const int sfb = (int)sf_row_bytes(*dims, H);
+    std::vector<uint8_t> codes((size_t)R * rb), sf((size_t)R * sfb);
     if (R && (e = cudaMemcpy(codes.data(), b + L.off_xb, codes.size(), cudaMemcpyDeviceToHost)))
       return cuda_fail(e, "codes read");
     if (R && (e = cudaMemcpy(sf.data(), b + L.off_xsf, sf.size(), cudaMemcpyDeviceToHost)))
@@ -630,8 +654,8 @@ moe_status moe_read_dispatch(const moe_dims* dims, const void* ws, int32_t T, in
           std::memset(xc_host + a * rb, 0, rb);
       }
       if (xs_host)
-        for (int g = 0; g < H / 32; ++g)
-          xs_host[a * (H / 32) + g] = ok ? sf[sf_atom_offset((size_t)r, g, H / 128)] : 0;
+        for (int g = 0; g < sfb; ++g)
+          xs_host[a * sfb + g] = ok ? sf[sf_atom_offset((size_t)r, g, sfb / 4)] : 0;
     }
   }
   return MOE_OK;
@@ -658,7 +682,8 @@ moe_status moe_read_intermediate(const moe_dims* dims, const void* ws, int32_t T
   const int64_t R = seg[E];
   if (R < 0 || R > L.R_cap) return fail(MOE_ERR_CUDA, "corrupt segment table");
   const size_t rb = (size_t)act_row_bytes(*dims, I);
-  std::vector<uint8_t> codes((size_t)R * rb), sf((size_t)R * I / 32);
+  const int sfb = (int)sf_row_bytes(*dims, I);
+  std::vector<uint8_t> codes((size_t)R * rb), sf((size_t)R * sfb);
   if (R && (e = cudaMemcpy(codes.data(), b + L.off_hb, codes.size(), cudaMemcpyDeviceToHost)))
     return cuda_fail(e, "codes read");
   if (R && (e = cudaMemcpy(sf.data(), b + L.off_hsf, sf.size(), cudaMemcpyDeviceToHost)))
@@ -673,8 +698,8 @@ moe_status moe_read_intermediate(const moe_dims* dims, const void* ws, int32_t T
         std::memset(hc_host + a * rb, 0, rb);
     }
     if (hs_host)
-      for (int g = 0; g < I / 32; ++g)
-        hs_host[a * (I / 32) + g] = ok ? sf[sf_atom_offset((size_t)r, g, I / 128)] : 0;
+      for (int g = 0; g < sfb; ++g)
+        hs_host[a * sfb + g] = ok ? sf[sf_atom_offset((size_t)r, g, sfb / 4)] : 0;
   }
   return MOE_OK;
 }

@@ -97,11 +97,11 @@ struct WsPtrs {
   int32_t* slot_assign;  // [R_cap]
   float* slot_weight;    // [R_cap]
   uint8_t* xb;           // [R_cap, H/2] (FP4) or [R_cap, H] (FP8) quantised token rows
-  uint8_t* xsf;          // 128x4 blocks of [R_cap, H/32]
+  uint8_t* xsf;          // 128x4 blocks of [R_cap, H/32] (H/16 for NVFP4)
   uint8_t* xq;           // [T_cap, H/2] quantised token rows, one per token (pull dispatch)
   uint8_t* xs;           // [T_cap, H/32] their scales, row-major (pull dispatch)
   uint8_t* hb;           // [R_cap, I/2] (FP4) or [R_cap, I] (FP8) requantised intermediate rows
-  uint8_t* hsf;          // 128x4 blocks of [R_cap, I/32]
+  uint8_t* hsf;          // 128x4 blocks of [R_cap, I/32] (I/16 for NVFP4)
   float* acc;            // [T_cap, H] fp32 combine accumulator, cleared by pre_dispatch
 };
 
@@ -111,8 +111,12 @@ struct PrepLayout {
 
 struct Shape {
   int H, I, E, k;
-  int f8;   // 1: fp8xfp4 (E4M3 activations, gran=8 interleave); 0: mxf4xmxf4
+  int f8;   // 1: fp8xfp4 (E4M3 activations, gran=8 interleave)
+  int nv;   // 1: nvf4xnvf4 (E4M3 scale per 16 elements); both 0: mxf4xmxf4
 };
+
+// Elements per scale of the format: 16 (NVFP4) or 32 (MXFP4, MXFP8).
+__host__ __device__ __forceinline__ int sf_group(const Shape& s) { return s.nv ? 16 : 32; }
 
 // Launch with programmatic stream serialisation: the kernel may start before the
 // previous kernel in the stream finishes and must call ptx::pdl_wait() before it
@@ -152,6 +156,9 @@ cudaError_t launch_assign_slots(const Shape& s, const int32_t* ids, const float*
 // acc [n] fp32 -> out [n] bf16 (round to nearest even).
 cudaError_t launch_convert_out(const float* acc, void* out, int64_t n, cudaStream_t st);
 cudaError_t launch_quantize_rows(const float* src, int64_t rows, int K, uint8_t* codes,
+                                 uint8_t* sf, cudaStream_t st);
+// fp32 rows -> NVFP4 codes and E4M3 scales (one per 16 elements).
+cudaError_t launch_quantize_rows_nv(const float* src, int64_t rows, int K, uint8_t* codes,
                                  uint8_t* sf, cudaStream_t st);
 cudaError_t launch_prepare(const Shape& s, const uint8_t* w1c, const uint8_t* w1s,
                            const uint8_t* w2c, const uint8_t* w2s, uint8_t* prep,

@@ -219,16 +219,22 @@ __global__ void assign_slots_kernel(const int32_t* __restrict__ ids, const float
 // The row is quantised into shared memory (and the token's fp32 combine row
 // cleared) while the bucketing kernel may still be running; the block then waits
 // for it, gives the token's k assignments their rows and copies the row to each.
-// F8: MXFP8 rows (one E4M3 byte per element, scale rule amax <= 448 * 2^e) for
-// fp8xfp4; otherwise MXFP4 rows (packed E2M1, amax <= 6 * 2^e).
-template <bool F8>
+// Token row formats of pre_dispatch.
+enum TokenFormat { kTokMxfp4 = 0, kTokMxfp8 = 1, kTokNvfp4 = 2 };
+
+// FMT kTokMxfp8: one E4M3 byte per element, scale rule amax <= 448 * 2^e (fp8xfp4);
+// kTokNvfp4: packed E2M1 with an E4M3 scale per 16 elements (nvf4xnvf4); kTokMxfp4:
+// packed E2M1, amax <= 6 * 2^e per 32.
+template <int FMT>
 __global__ void __launch_bounds__(256) quantize_scatter_kernel(const __nv_bfloat16* __restrict__ x,
                                                                const int32_t* __restrict__ ids,
                                                                const float* __restrict__ tw,
                                                                int H, int k, int E, WsPtrs ws,
                                                                bool pull) {
+  constexpr bool F8 = FMT == kTokMxfp8, NV = FMT == kTokNvfp4;
   constexpr int kBytesPer8 = F8 ? 8 : 4;                // code bytes of 8 elements
-  extern __shared__ __align__(16) uint8_t qsh[];       // [row codes | H/32 scales]
+  constexpr int kGroup = NV ? 16 : 32;                  // elements per scale
+  extern __shared__ __align__(16) uint8_t qsh[];       // [row codes | H/kGroup scales]
   __shared__ int32_t slots[32];
   const int row_bytes_q = H / 8 * kBytesPer8;
   uint8_t* codes_sh = qsh;
@@ -261,6 +267,19 @@ __global__ void __launch_bounds__(256) quantize_scatter_kernel(const __nv_bfloat
 #pragma unroll
     for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
     amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
+    if (NV) {
+      // 16-element group = this lane and its neighbour: scale = E4M3(amax / 6),
+      // elements fp32(x / scale) (signed zeros when the scale is zero)
+      const uint32_t sb = ptx::nvfp4_scale_byte(amax);
+      const float sc = ptx::ue4m3_value(sb);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = sc > 0.f ? __fdiv_rn(v[i], sc) : copysignf(0.f, v[i]);
+      const uint32_t c8 = ptx::e2m1x8(v);
+      if (!live) continue;
+      *reinterpret_cast<uint32_t*>(codes_sh + base / 2) = c8;
+      if ((tid & 1) == 0) sf_sh[base / 16] = (uint8_t)sb;
+      continue;
+    }
     amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2));
     const int e = F8 ? ptx::mxfp8_exponent(amax) : ptx::mx_scale_exponent(amax);
     const float inv = ptx::pow2_neg(e);
@@ -289,7 +308,8 @@ __global__ void __launch_bounds__(256) quantize_scatter_kernel(const __nv_bfloat
   if (tid < k) slots[tid] = assign_slot(t * k + tid, k, E, ids, tw, ws);
   if (pull) return;
   __syncthreads();
-  const int kc4 = H / 128;
+  const int nsf = H / kGroup;      // scale bytes of a row
+  const int kc4 = nsf / 4;
   const size_t row_bytes = (size_t)row_bytes_q;
   for (int j = 0; j < k; ++j) {
     const int slot = slots[j];
@@ -297,7 +317,7 @@ __global__ void __launch_bounds__(256) quantize_scatter_kernel(const __nv_bfloat
     uint4* dst = reinterpret_cast<uint4*>(ws.xb + (size_t)slot * row_bytes);
     for (int i = tid; i < row_bytes_q / 16; i += blockDim.x)   // 16-byte chunks of the row
       dst[i] = reinterpret_cast<const uint4*>(codes_sh)[i];
-    for (int i = tid; i < H / 32; i += blockDim.x)
+    for (int i = tid; i < nsf; i += blockDim.x)
       ws.xsf[sf_atom_offset((size_t)slot, i, kc4)] = sf_sh[i];
   }
 }
@@ -326,6 +346,32 @@ __global__ void quantize_rows_kernel(const float* __restrict__ src, int64_t n_th
   if (i < n_threads) {
     reinterpret_cast<uint32_t*>(codes)[ic] = c;
     if ((ic & 3) == 0) sf[elem / 32] = (uint8_t)(e + 127);
+  }
+}
+
+// fp32 rows -> canonical NVFP4 codes/scales (one E4M3 scale per 16 elements).  A
+// thread owns 8 elements; a lane pair shares a group.
+__global__ void quantize_rows_nv_kernel(const float* __restrict__ src, int64_t n_threads,
+                                        uint8_t* __restrict__ codes, uint8_t* __restrict__ sf) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  // n_threads is even, so a lane pair is wholly in range or wholly past the end
+  const int64_t ic = i < n_threads ? i : n_threads - 1;
+  const int64_t elem = ic * 8;
+  const float4 a = *reinterpret_cast<const float4*>(src + elem);
+  const float4 b = *reinterpret_cast<const float4*>(src + elem + 4);
+  float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  float amax = 0.f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(v[j]));
+  amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
+  const uint32_t sb = ptx::nvfp4_scale_byte(amax);
+  const float sc = ptx::ue4m3_value(sb);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) v[j] = sc > 0.f ? __fdiv_rn(v[j], sc) : copysignf(0.f, v[j]);
+  const uint32_t c = ptx::e2m1x8(v);
+  if (i < n_threads) {
+    reinterpret_cast<uint32_t*>(codes)[ic] = c;
+    if ((ic & 1) == 0) sf[elem / 16] = (uint8_t)sb;
   }
 }
 
@@ -424,8 +470,10 @@ cudaError_t launch_bucket(const Shape& s, const int32_t* ids, int T, const WsPtr
 cudaError_t launch_quantize_scatter(const Shape& s, const void* x, const int32_t* ids,
                                     const float* tw, int T, const WsPtrs& ws, bool pull,
                                     cudaStream_t st) {
-  const size_t smem = (size_t)(s.f8 ? s.H : s.H / 2) + s.H / 32;
-  auto kern = s.f8 ? quantize_scatter_kernel<true> : quantize_scatter_kernel<false>;
+  const size_t smem = (size_t)(s.f8 ? s.H : s.H / 2) + s.H / sf_group(s);
+  auto kern = s.f8   ? quantize_scatter_kernel<kTokMxfp8>
+              : s.nv ? quantize_scatter_kernel<kTokNvfp4>
+                     : quantize_scatter_kernel<kTokMxfp4>;
   if (smem > 48 * 1024) {   // wide rows (H up to 65536) need the opt-in limit
     const cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -462,6 +510,15 @@ cudaError_t launch_quantize_rows(const float* src, int64_t rows, int K, uint8_t*
   return cudaGetLastError();
 }
 
+cudaError_t launch_quantize_rows_nv(const float* src, int64_t rows, int K, uint8_t* codes,
+                                    uint8_t* sf, cudaStream_t st) {
+  const int64_t n_threads = rows * (int64_t)K / 8;
+  const int64_t blocks = (n_threads + 255) / 256;
+  if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+  quantize_rows_nv_kernel<<<(unsigned)blocks, 256, 0, st>>>(src, n_threads, codes, sf);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_prepare(const Shape& s, const uint8_t* w1c, const uint8_t* w1s,
                            const uint8_t* w2c, const uint8_t* w2s, uint8_t* prep,
                            const PrepLayout& pl, cudaStream_t st) {
@@ -474,10 +531,10 @@ cudaError_t launch_prepare(const Shape& s, const uint8_t* w1c, const uint8_t* w1
                                                                   cpr, (int)(2 * I), (int)I, gran);
   }
   {  // W1 scales: interleaved rows, 128x4 blocks
-    const int64_t words = E * 2 * I * (H / 32) / 4;
+    const int64_t words = E * 2 * I * (H / sf_group(s)) / 4;
     scale_blocks_kernel<<<grid_for(words, 256, 16384), 256, 0, st>>>(
-        w1s, reinterpret_cast<uint32_t*>(prep + pl.off_w1s), words, (int)(2 * I), (int)(H / 32),
-        (int)I, gran);
+        w1s, reinterpret_cast<uint32_t*>(prep + pl.off_w1s), words, (int)(2 * I),
+        (int)(H / sf_group(s)), (int)I, gran);
   }
   {  // W2 codes: rows unchanged
     const int cpr = (int)(I / 2 / 16);
@@ -486,10 +543,10 @@ cudaError_t launch_prepare(const Shape& s, const uint8_t* w1c, const uint8_t* w1
                                                                   cpr, (int)H, (int)I, 0);
   }
   {  // W2 scales: 128x4 blocks
-    const int64_t words = E * H * (I / 32) / 4;
+    const int64_t words = E * H * (I / sf_group(s)) / 4;
     scale_blocks_kernel<<<grid_for(words, 256, 16384), 256, 0, st>>>(
-        w2s, reinterpret_cast<uint32_t*>(prep + pl.off_w2s), words, (int)H, (int)(I / 32), (int)I,
-        0);
+        w2s, reinterpret_cast<uint32_t*>(prep + pl.off_w2s), words, (int)H,
+        (int)(I / sf_group(s)), (int)I, 0);
   }
   return cudaGetLastError();
 }

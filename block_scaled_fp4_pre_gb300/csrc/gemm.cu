@@ -48,18 +48,27 @@ constexpr int kThreads = 192;
 constexpr int kBlocksPerSM = 2;
 constexpr int kTmemCols = 256;             // half of the SM's tensor memory per block
 constexpr int kAccCols = kBN;              // one fp32 accumulator of up to 128 columns
-constexpr int kSfTmemBase = kAccCols;      // scale registers (2 x 16 columns) after it
-// The rest of the block's tensor memory holds a copy of the accumulator's first
-// columns, so that the accumulator can go back to the MMA issuer before the math.
-constexpr int kSpareCol = kSfTmemBase + 32;
-constexpr int kSpareChunks = (kTmemCols - kSpareCol) / 16;   // 6 chunks of 16 columns
-static_assert(kSpareChunks == 6, "tensor memory layout");
+constexpr int kSfTmemBase = kAccCols;      // two buffers of scale registers after it
+
+// Tensor-memory columns after the accumulator: two buffers of scale registers (A then
+// B; 8 columns an operand, 16 for NVFP4's four scale blocks per k-block), then spare
+// columns that hold a copy of the accumulator's first chunks, so that the accumulator
+// can go back to the MMA issuer before the math.
+template <bool NV>
+struct TmemMap {
+  static constexpr int kSfCols = NV ? 32 : 16;                // one buffer, A and B
+  static constexpr int kSpareCol = kSfTmemBase + 2 * kSfCols;
+  static constexpr int kSpareChunks = (kTmemCols - kSpareCol) / 16;
+};
+static_assert(TmemMap<false>::kSpareChunks == 6 && TmemMap<true>::kSpareChunks == 4,
+              "tensor memory layout");
 constexpr int kEpiCols = 16;               // accumulator columns per epilogue load
 constexpr int kRing = 8;                   // work items in flight inside a block
 constexpr unsigned kFull = 0xFFFFFFFFu;
 
 enum LayerMode { kModeLayer = 0, kModeRaw = 1 };
 
+template <bool NV>
 struct __align__(16) SmemTail {
   uint64_t full[kStages];
   uint64_t empty[kStages];
@@ -76,16 +85,28 @@ struct __align__(16) SmemTail {
   // it is stored: per column, the item's 64 features (32 code bytes) and their two
   // scale bytes.  Double-buffered across chunks.
   alignas(16) uint8_t hstage[2][kEpiCols][64];   // 32 bytes used for E2M1, 64 for E4M3
-  uint8_t sstage[2][kEpiCols][2];
-  int32_t tile_start[1025];   // first tile of each expert (E <= 1024), see decode_item
+  alignas(4) uint8_t sstage[2][kEpiCols][4];      // 2 scale bytes a column (4: NVFP4)
+  // first tile of each expert (E <= 1024), see decode_item; NVFP4 stages take the
+  // room, so that kernel reads the table from global memory
+  int32_t tile_start[NV ? 1 : 1025];
 };
 
-constexpr size_t kSmemA = 0;
-constexpr size_t kSmemB = kSmemA + (size_t)kStages * kATileBytes;
-constexpr size_t kSmemSFA = kSmemB + (size_t)kStages * kBTileBytes;
-constexpr size_t kSmemSFB = kSmemSFA + (size_t)kStages * kSFStageBytes;
-constexpr size_t kSmemTail = kSmemSFB + (size_t)kStages * kSFStageBytes;
-constexpr size_t kSmemBytes = kSmemTail + sizeof(SmemTail) + 1024;  // + alignment slack
+// Shared-memory map: kStages x (weight box, token boxes, both operands' scale
+// blocks: 2 per k-block, 4 for NVFP4), then the tail.
+template <bool NV>
+struct SmemMap {
+  static constexpr size_t kSF = (size_t)(NV ? 4 : 2) * kSFAtomBytes;
+  static constexpr size_t kA = 0;
+  static constexpr size_t kB = kA + (size_t)kStages * kATileBytes;
+  static constexpr size_t kSFA = kB + (size_t)kStages * kBTileBytes;
+  static constexpr size_t kSFB = kSFA + (size_t)kStages * kSF;
+  static constexpr size_t kTail = kSFB + (size_t)kStages * kSF;
+  static constexpr size_t kBytes = kTail + sizeof(SmemTail<NV>) + 1024;  // + alignment slack
+};
+// two blocks per SM (228 KiB of shared memory, 1 KiB of it reserved per block)
+static_assert(2 * (SmemMap<false>::kBytes + 1024) <= 228 * 1024 &&
+                  2 * (SmemMap<true>::kBytes + 1024) <= 228 * 1024,
+              "two blocks per SM");
 
 struct PhaseArgs {
   const uint8_t* w_sf;   // weight scale blocks
@@ -93,8 +114,8 @@ struct PhaseArgs {
   int rows_per_expert;   // 2I (gate/up) or H (down)
   int K;                 // H (gate/up) or I (down)
   int m_tiles;           // rows_per_expert / 128
-  int num_kb;            // k-blocks of 256 elements (the last may be 128 wide)
-  int kc4;               // K / 128: scale blocks per 128-row group
+  int num_kb;            // k-blocks of 256 elements (the last may be 128 wide; F8: 128)
+  int kc4;               // scale blocks per 128-row group: K/128 (K/64 for NVFP4)
 };
 
 struct LayerArgs {
@@ -148,7 +169,9 @@ __device__ __forceinline__ float silu_times(float g, float u) {
 // weights widened to 8-bit containers by their TMA copies (CU_TENSOR_MAP_DATA_TYPE_
 // 16U4_ALIGN16B), kind::mxf8f6f4 MMAs, gran=8 gate/up rows.  Otherwise mxf4xmxf4:
 // packed E2M1 throughout, 256 elements a k-block, kind::mxf4 MMAs, gran=16.
-template <int MODE, bool PULL, bool F8>
+// NV: nvf4xnvf4 -- as mxf4xmxf4 with one E4M3 scale per 16 elements (four scale
+// blocks per k-block and operand), kind::mxf4nvf4 MMAs, NVFP4 requantisation.
+template <int MODE, bool PULL, bool F8, bool NV>
 __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
     moe_layer_kernel(const __grid_constant__ CUtensorMap tmap_w1,
                      const __grid_constant__ CUtensorMap tmap_x,
@@ -159,9 +182,12 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  SmemTail* tail = reinterpret_cast<SmemTail*>(smem + kSmemTail);
+  using SM = SmemMap<NV>;
+  using TM = TmemMap<NV>;
+  SmemTail<NV>* tail = reinterpret_cast<SmemTail<NV>*>(smem + SM::kTail);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr int kKb = F8 ? 128 : kBK;   // K elements per k-block (128-byte rows either way)
+  constexpr int kAtomK = NV ? 64 : 128; // K elements of one scale block (4 scales a row)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -212,8 +238,9 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
 
   const int num_tiles = args.ws.flags[kFlagTiles];
   const int E = args.E;
-  const int32_t* tile_start = tail->tile_start;
-  for (int e = threadIdx.x; e <= E; e += blockDim.x) tail->tile_start[e] = args.ws.tile_start[e];
+  const int32_t* tile_start = NV ? args.ws.tile_start : tail->tile_start;
+  if (!NV)
+    for (int e = threadIdx.x; e <= E; e += blockDim.x) tail->tile_start[e] = args.ws.tile_start[e];
   __syncthreads();
   // Items per token tile and phase: one per weight slab.
   const int m0 = args.ph[0].m_tiles, m1 = args.ph[1].m_tiles;
@@ -313,14 +340,14 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
         ok = __shfl_sync(kFull, ok ? 1 : 0, 0) != 0;   // the stage is free for every lane
         if (!ok) break;
         const int kvalid = min(kKb, P.K - kb * kKb);
-        const int atoms = kvalid / 128;
+        const int atoms = kvalid / kAtomK;
         uint64_t* bar = &tail->full[stage];
-        uint8_t* b_dst = smem + kSmemB + (size_t)stage * kBTileBytes;
+        uint8_t* b_dst = smem + SM::kB + (size_t)stage * kBTileBytes;
         if (pulled) {
           // Row i of the tile is token tok's codes [kb*128, kb*128 + kvalid/2) in the
           // 128-byte swizzle (16-byte chunk c of row i at chunk c ^ (i % 8)), and its
           // scales in the 128x4 blocks the scale copy reads.
-          uint8_t* sf_dst = smem + kSmemSFB + (size_t)stage * kSFStageBytes;
+          uint8_t* sf_dst = smem + SM::kSFB + (size_t)stage * SM::kSF;
           // Lane l copies rows l, l+32, l+64, l+96: only live rows cost anything,
           // which matters for the few-row tiles of decode-sized loads.
           const int chunks = kvalid / 32;
@@ -355,11 +382,11 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
               (F8 ? kATileBytes / 2 : kATileBytes) + atoms * kSFAtomBytes +
               (pulled ? 0u : (uint32_t)(nb * (kBBoxRows * kBKBytes) + atoms * kSFAtomBytes));
           ptx::mbar_arrive_expect_tx(bar, bytes);
-          ptx::tma_load_2d(smem + kSmemA + (size_t)stage * kATileBytes, tw, kb * kBKBytes, wrow,
+          ptx::tma_load_2d(smem + SM::kA + (size_t)stage * kATileBytes, tw, kb * kBKBytes, wrow,
                            bar, pol_w);
-          ptx::bulk_load(smem + kSmemSFA + (size_t)stage * kSFStageBytes,
-                         wsf + (size_t)kb * (kKb / 128) * kSFAtomBytes, atoms * kSFAtomBytes, bar,
-                         pol_w);
+          ptx::bulk_load(smem + SM::kSFA + (size_t)stage * SM::kSF,
+                         wsf + (size_t)kb * (kKb / kAtomK) * kSFAtomBytes, atoms * kSFAtomBytes,
+                         bar, pol_w);
           if (!pulled) {
             if (nb * kBBoxRows == kBN) {
               ptx::tma_load_2d(b_dst, tt_full, kb * kBKBytes, row0, bar, pol_t);
@@ -368,8 +395,8 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
                 ptx::tma_load_2d(b_dst + j * kBBoxRows * kBKBytes, tt, kb * kBKBytes,
                                  row0 + j * kBBoxRows, bar, pol_t);
             }
-            ptx::bulk_load(smem + kSmemSFB + (size_t)stage * kSFStageBytes,
-                           tsf + (size_t)kb * (kKb / 128) * kSFAtomBytes, atoms * kSFAtomBytes,
+            ptx::bulk_load(smem + SM::kSFB + (size_t)stage * SM::kSF,
+                           tsf + (size_t)kb * (kKb / kAtomK) * kSFAtomBytes, atoms * kSFAtomBytes,
                            bar, pol_t);
           }
           if (kb == 0 && g_next < total) {
@@ -439,21 +466,26 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
           ptx::tc_fence_after();
           if (pulled) ptx::fence_proxy_async_smem();
           const int kvalid = min(kKb, P.K - kb * kKb);
-          const int atoms = kvalid / 128;
-          const uint32_t sfa_t = tmem_base + (uint32_t)(kSfTmemBase + sfbuf * 16);
-          const uint32_t sfb_t = sfa_t + 8;
-          const uint32_t sa = ptx::smem_addr(smem + kSmemSFA + (size_t)stage * kSFStageBytes);
-          const uint32_t sb = ptx::smem_addr(smem + kSmemSFB + (size_t)stage * kSFStageBytes);
+          const int atoms = kvalid / kAtomK;
+          const uint32_t sfa_t = tmem_base + (uint32_t)(kSfTmemBase + sfbuf * TM::kSfCols);
+          const uint32_t sfb_t = sfa_t + TM::kSfCols / 2;
+          const uint32_t sa = ptx::smem_addr(smem + SM::kSFA + (size_t)stage * SM::kSF);
+          const uint32_t sb = ptx::smem_addr(smem + SM::kSFB + (size_t)stage * SM::kSF);
           for (int a = 0; a < atoms; ++a) {
             ptx::tc_cp_sf(sfa_t + a * 4, ptx::desc_sf(sa + a * kSFAtomBytes));
             ptx::tc_cp_sf(sfb_t + a * 4, ptx::desc_sf(sb + a * kSFAtomBytes));
           }
-          const uint32_t a_base = ptx::smem_addr(smem + kSmemA + (size_t)stage * kATileBytes);
-          const uint32_t b_base = ptx::smem_addr(smem + kSmemB + (size_t)stage * kBTileBytes);
+          const uint32_t a_base = ptx::smem_addr(smem + SM::kA + (size_t)stage * kATileBytes);
+          const uint32_t b_base = ptx::smem_addr(smem + SM::kB + (size_t)stage * kBTileBytes);
           // 32 bytes of K per instruction: 64 packed E2M1 elements, or 32 one-byte ones
           const int steps = kvalid / (F8 ? 32 : 64);
           for (int s = 0; s < steps; ++s) {
-            if (F8) {
+            if (NV) {
+              // step s (64 elements) takes scale block s whole: four E4M3 scales a row
+              ptx::tc_mma_nvf4(tmem_base, ptx::desc_sw128(a_base + s * 32),
+                               ptx::desc_sw128(b_base + s * 32), ptx::idesc_nvf4(n_mma),
+                               sfa_t + s * 4, sfb_t + s * 4, (kb | s) != 0 ? 1u : 0u);
+            } else if (F8) {
               // one 128-element k-block: one scale atom, scale byte s of each row
               ptx::tc_mma_f8f4(tmem_base, ptx::desc_sw128(a_base + s * 32),
                                ptx::desc_sw128(b_base + s * 32), ptx::idesc_f8f4(n_mma, s), sfa_t,
@@ -525,7 +557,7 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
       acc_phase ^= 1u;
       ptx::tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16);
-      const uint32_t tspare = taddr + (uint32_t)kSpareCol;
+      const uint32_t tspare = taddr + (uint32_t)TM::kSpareCol;
       // The math of one 16-column chunk, wherever its values were read from.
       auto chunk = [&](const int ci, const float(&v)[kEpiCols]) {
         const int c0 = ci * kEpiCols;
@@ -564,7 +596,7 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
             if ((lane & 23) == 0) tail->xchg[xb][q][2 * p + (up_lane ? 1 : 0)] = a;  // lanes 0, 8
           }
           ptx::named_bar_sync(1, 128);
-          const int i_kc4 = args.I / 128;
+          const int i_kc4 = args.I / kAtomK;   // scale blocks of an intermediate row
           const size_t hrow_bytes = F8 ? (size_t)args.I : (size_t)args.I / 2;
           // All shared-memory reads first, then the arithmetic, then the writes: the
           // eight columns' work is independent and overlaps instead of forming one
@@ -573,15 +605,25 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
 #pragma unroll
           for (int p = 0; p < kEpiCols / 2; ++p) {
             const int jc = 2 * p + (up_lane ? 1 : 0);  // this lane's column
-            // 32-feature group = this warp's 16 features + the partner warp's 16.
-            amax[p] = fmaxf(tail->xchg[xb][q][jc], tail->xchg[xb][q ^ 1][jc]);
+            // 32-feature group = this warp's 16 features + the partner warp's 16
+            // (NVFP4: the 16-feature group is this warp's alone)
+            amax[p] = NV ? tail->xchg[xb][q][jc]
+                         : fmaxf(tail->xchg[xb][q][jc], tail->xchg[xb][q ^ 1][jc]);
           }
           uint32_t code[kEpiCols / 2];
           int ex[kEpiCols / 2];
 #pragma unroll
           for (int p = 0; p < kEpiCols / 2; ++p) {
-            ex[p] = F8 ? ptx::mxfp8_exponent(amax[p]) : ptx::mx_scale_exponent(amax[p]);
-            const float qv = hv[p] * ptx::pow2_neg(ex[p]);
+            float qv;
+            if (NV) {
+              // E4M3 scale of amax/6 (kept as its byte in ex), element h / scale
+              ex[p] = (int)ptx::nvfp4_scale_byte(amax[p]);
+              const float sc = ptx::ue4m3_value((uint32_t)ex[p]);
+              qv = sc > 0.f ? __fdiv_rn(hv[p], sc) : copysignf(0.f, hv[p]);
+            } else {
+              ex[p] = F8 ? ptx::mxfp8_exponent(amax[p]) : ptx::mx_scale_exponent(amax[p]);
+              qv = hv[p] * ptx::pow2_neg(ex[p]);
+            }
             if (F8) {
               code[p] = ptx::e4m3x2(qv, 0.f) & 0xFFu;
             } else {
@@ -608,8 +650,11 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
             for (int p = 0; p < kEpiCols / 2; ++p) {
               const int jc = 2 * p + (up_lane ? 1 : 0);
               tail->hstage[xb][jc][q * 8 + (lane & 7)] = (uint8_t)code[p];
-              if ((lane & 7) == 0 && (q & 1) == 0)
+              if (NV) {
+                if ((lane & 7) == 0) tail->sstage[xb][jc][q] = (uint8_t)ex[p];
+              } else if ((lane & 7) == 0 && (q & 1) == 0) {
                 tail->sstage[xb][jc][q >> 1] = (uint8_t)(ex[p] + 127);
+              }
             }
           }
           ptx::named_bar_sync(1, 128);
@@ -646,8 +691,13 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
             const int jc = q * 4 + (lane - 8);
             if (jc < ncol) {
               const size_t row = (size_t)row0 + c0 + jc;
-              const uint16_t sv = *reinterpret_cast<const uint16_t*>(&tail->sstage[xb][jc][0]);
-              *reinterpret_cast<uint16_t*>(args.ws.hsf + sf_atom_offset(row, mt * 2, i_kc4)) = sv;
+              if (NV) {   // the item's four scale bytes: one 32-bit word of a scale block
+                const uint32_t sv = *reinterpret_cast<const uint32_t*>(&tail->sstage[xb][jc][0]);
+                *reinterpret_cast<uint32_t*>(args.ws.hsf + sf_atom_offset(row, mt * 4, i_kc4)) = sv;
+              } else {
+                const uint16_t sv = *reinterpret_cast<const uint16_t*>(&tail->sstage[xb][jc][0]);
+                *reinterpret_cast<uint16_t*>(args.ws.hsf + sf_atom_offset(row, mt * 2, i_kc4)) = sv;
+              }
             }
           }
           xb ^= 1;
@@ -668,9 +718,10 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
         }
       };
       const int nch = (n + kEpiCols - 1) / kEpiCols;
+      constexpr int kSpareChunks = TM::kSpareChunks;   // 6, or 4 for NVFP4
       const int ncopy = min(nch, kSpareChunks);
-      // 1. The first ncopy chunks (up to 96 columns) into this block's spare tensor
-      //    memory, two loads in flight.
+      // 1. The first ncopy chunks (up to 96 columns, 64 for NVFP4) into this block's
+      //    spare tensor memory, two loads in flight.
 #pragma unroll
       for (int ci = 0; ci < kSpareChunks; ci += 2) {
         if (ci < ncopy) {
@@ -684,27 +735,49 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
           if (two) ptx::tmem_st16(tspare + (uint32_t)((ci + 1) * kEpiCols), r1);
         }
       }
-      // 2. The two chunks past the spare area straight from the accumulator, both
-      //    loaded before any math.  Then the accumulator goes back to the MMA
-      //    issuer, so the next item's MMAs run during this item's math.
-      static_assert(kBN / kEpiCols == kSpareChunks + 2, "two chunks read directly");
+      // 2. The chunks past the spare area straight from the accumulator: any before
+      //    the last two one at a time (NVFP4's smaller spare area), then the last two
+      //    both loaded before any math.  Once every accumulator load is done it goes
+      //    back to the MMA issuer, so the next item's MMAs run during this item's math.
+      constexpr int kLastTwo = kBN / kEpiCols - 2;
+      static_assert(kSpareChunks <= kLastTwo, "tensor memory layout");
+      bool released = false;
+#pragma unroll
+      for (int ci = kSpareChunks; ci < kLastTwo; ++ci) {
+        if (ci < nch) {
+          uint32_t r[kEpiCols];
+          ptx::tmem_ld16_issue(taddr + (uint32_t)(ci * kEpiCols), r);
+          ptx::tmem_wait_ld(r);
+          if (ci + 1 >= nch) {
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(&tail->acc_empty);
+            released = true;
+          }
+          float v[kEpiCols];
+#pragma unroll
+          for (int j = 0; j < kEpiCols; ++j) v[j] = __uint_as_float(r[j]);
+          chunk(ci, v);
+        }
+      }
       uint32_t rd[2][kEpiCols];
 #pragma unroll
       for (int d = 0; d < 2; ++d)
-        if (kSpareChunks + d < nch)
-          ptx::tmem_ld16_issue(taddr + (uint32_t)((kSpareChunks + d) * kEpiCols), rd[d]);
+        if (kLastTwo + d < nch)
+          ptx::tmem_ld16_issue(taddr + (uint32_t)((kLastTwo + d) * kEpiCols), rd[d]);
 #pragma unroll
       for (int d = 0; d < 2; ++d)
-        if (kSpareChunks + d < nch) ptx::tmem_wait_ld(rd[d]);
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(&tail->acc_empty);
+        if (kLastTwo + d < nch) ptx::tmem_wait_ld(rd[d]);
+      if (!released) {
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(&tail->acc_empty);
+      }
 #pragma unroll
       for (int d = 0; d < 2; ++d) {
-        if (kSpareChunks + d < nch) {
+        if (kLastTwo + d < nch) {
           float v[kEpiCols];
 #pragma unroll
           for (int j = 0; j < kEpiCols; ++j) v[j] = __uint_as_float(rd[d][j]);
-          chunk(kSpareChunks + d, v);
+          chunk(kLastTwo + d, v);
         }
       }
       ptx::tmem_wait_st();
@@ -813,8 +886,9 @@ cudaError_t make_tmap_e2m1_wide(CUtensorMap* m, const void* base, uint64_t K, ui
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// atom_k: K elements of one 128x4 scale block (128, or 64 for NVFP4's scale per 16).
 PhaseArgs phase_args(const uint8_t* w_sf, const uint8_t* t_sf, int rows_per_expert, int K,
-                     int kb_elems) {
+                     int kb_elems, int atom_k) {
   PhaseArgs p;
   p.w_sf = w_sf;
   p.t_sf = t_sf;
@@ -822,16 +896,17 @@ PhaseArgs phase_args(const uint8_t* w_sf, const uint8_t* t_sf, int rows_per_expe
   p.K = K;
   p.m_tiles = rows_per_expert / kBM;
   p.num_kb = (K + kb_elems - 1) / kb_elems;
-  p.kc4 = K / 128;
+  p.kc4 = K / atom_k;
   return p;
 }
 
-template <int MODE, bool PULL, bool F8>
+template <int MODE, bool PULL, bool F8, bool NV>
 cudaError_t launch_mode(const LayerLaunch& g, const CUtensorMap* maps, const LayerArgs& a,
                         cudaStream_t st) {
+  constexpr size_t kSmemBytes = SmemMap<NV>::kBytes;
   static int grid = 0;   // per instantiation, for the device of the first launch
   if (grid == 0) {
-    cudaError_t err = cudaFuncSetAttribute(moe_layer_kernel<MODE, PULL, F8>,
+    cudaError_t err = cudaFuncSetAttribute(moe_layer_kernel<MODE, PULL, F8, NV>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)kSmemBytes);
     if (err != cudaSuccess) return err;
@@ -839,7 +914,7 @@ cudaError_t launch_mode(const LayerLaunch& g, const CUtensorMap* maps, const Lay
     // resident blocks)
     grid = kBlocksPerSM * g.num_sms;
   }
-  return launch_pdl(moe_layer_kernel<MODE, PULL, F8>, dim3(grid), dim3(kThreads), kSmemBytes, st,
+  return launch_pdl(moe_layer_kernel<MODE, PULL, F8, NV>, dim3(grid), dim3(kThreads), kSmemBytes, st,
                     maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], a);
 }
 
@@ -847,8 +922,8 @@ cudaError_t launch_mode(const LayerLaunch& g, const CUtensorMap* maps, const Lay
 
 cudaError_t launch_layer(const LayerLaunch& g, cudaStream_t st) {
   const Shape& s = g.shape;
-  const bool f8 = s.f8 != 0;
-  if (f8 && g.pull) return cudaErrorNotSupported;   // pull is built for E2M1 tokens only
+  const bool f8 = s.f8 != 0, nv = s.nv != 0;
+  if ((f8 || nv) && g.pull) return cudaErrorNotSupported;   // pull: MXFP4 tokens only
   // Activation rows: packed E2M1 (K/2 bytes) or E4M3 (K bytes).
   const uint64_t xrow = f8 ? (uint64_t)s.H : (uint64_t)s.H / 2;
   const uint64_t hrow = f8 ? (uint64_t)s.I : (uint64_t)s.I / 2;
@@ -872,8 +947,9 @@ cudaError_t launch_layer(const LayerLaunch& g, cudaStream_t st) {
   }
   LayerArgs a;
   const int kb_elems = f8 ? 128 : kBK;
-  a.ph[0] = phase_args(g.w1_sf, g.ws.xsf, 2 * s.I, s.H, kb_elems);
-  a.ph[1] = phase_args(g.w2_sf, g.ws.hsf, s.H, s.I, kb_elems);
+  const int atom_k = nv ? 64 : 128;
+  a.ph[0] = phase_args(g.w1_sf, g.ws.xsf, 2 * s.I, s.H, kb_elems, atom_k);
+  a.ph[1] = phase_args(g.w2_sf, g.ws.hsf, s.H, s.I, kb_elems, atom_k);
   a.num_phases = g.num_phases;
   a.H = s.H;
   a.I = s.I;
@@ -882,13 +958,16 @@ cudaError_t launch_layer(const LayerLaunch& g, cudaStream_t st) {
   a.ws = g.ws;
   a.gate_up_debug = g.gate_up_debug;
   if (f8)
-    return g.num_phases == 2 ? launch_mode<kModeLayer, false, true>(g, maps, a, st)
-                             : launch_mode<kModeRaw, false, true>(g, maps, a, st);
+    return g.num_phases == 2 ? launch_mode<kModeLayer, false, true, false>(g, maps, a, st)
+                             : launch_mode<kModeRaw, false, true, false>(g, maps, a, st);
+  if (nv)
+    return g.num_phases == 2 ? launch_mode<kModeLayer, false, false, true>(g, maps, a, st)
+                             : launch_mode<kModeRaw, false, false, true>(g, maps, a, st);
   if (g.num_phases == 2)
-    return g.pull ? launch_mode<kModeLayer, true, false>(g, maps, a, st)
-                  : launch_mode<kModeLayer, false, false>(g, maps, a, st);
-  return g.pull ? launch_mode<kModeRaw, true, false>(g, maps, a, st)
-                : launch_mode<kModeRaw, false, false>(g, maps, a, st);
+    return g.pull ? launch_mode<kModeLayer, true, false, false>(g, maps, a, st)
+                  : launch_mode<kModeLayer, false, false, false>(g, maps, a, st);
+  return g.pull ? launch_mode<kModeRaw, true, false, false>(g, maps, a, st)
+                : launch_mode<kModeRaw, false, false, false>(g, maps, a, st);
 }
 
 }  // namespace mxmoe

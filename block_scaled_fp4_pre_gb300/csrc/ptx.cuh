@@ -436,5 +436,40 @@ __device__ __forceinline__ uint2 e4m3x8(const float (&v)[8]) {
                     e4m3x2(v[4], v[5]) | (e4m3x2(v[6], v[7]) << 16));
 }
 
+// ---- NVFP4 element math ------------------------------------------------------
+// Value of an unsigned E4M3 byte (sign bit ignored): exponent field 0 holds m/8 *
+// 2^-6, otherwise (1 + m/8) * 2^(e-7); built from the fields, exact in fp32.
+__device__ __forceinline__ float ue4m3_value(uint32_t b) {
+  const uint32_t e = (b >> 3) & 15u, m = b & 7u;
+  return e == 0 ? (float)m * 0.001953125f : __uint_as_float(((e + 120u) << 23) | (m << 20));
+}
+
+// NVFP4 block scale of a 16-element group: the E4M3 byte nearest to amax / 6
+// (correctly rounded fp32 division, then round to nearest even, saturating at 448).
+__device__ __forceinline__ uint32_t nvfp4_scale_byte(float amax) {
+  return e4m3x2(__fdiv_rn(amax, 6.0f), 0.f) & 0x7Fu;
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T, packed E2M1 operands with one UE4M3 scale per 16
+// elements of K for each (K = 64 per instruction: four scales, one 32-bit scale word).
+__device__ __forceinline__ void tc_mma_nvf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, "
+      "[%5], [%6], p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+      : "memory");
+}
+
+// Instruction descriptor of kind::mxf4nvf4 with E2M1 A and B, UE4M3 scales (scale
+// type bit 23 clear), M = 128, K-major operands; the four scales of a step fill the
+// whole scale word, so both scale ids are 0.
+__device__ __forceinline__ uint32_t idesc_nvf4(int N) {
+  return (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+}
+
 }  // namespace ptx
 }  // namespace mxmoe

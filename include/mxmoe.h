@@ -71,8 +71,13 @@ enum {
  *                      element, UE8M0 per 32; the scale 2^e with e the smallest
  *                      integer such that amax <= 448 * 2^e), W1 gate/up rows
  *                      interleaved with gran=8 ([gate 0..7, up 0..7, gate 8..15, ..]).
- * The weights are MXFP4 in both.  Every other value returns MOE_ERR_UNSUPPORTED. */
-enum { MOE_MMA_MXF4xMXF4 = 1, MOE_MMA_FP8xFP4 = 2 };
+ *   MOE_MMA_NVF4xNVF4  NVFP4 throughout: packed E2M1 activations and weights with one
+ *                      unsigned E4M3 scale per 16 elements (the E4M3 value nearest
+ *                      to amax/6; elements fp32(x / scale) rounded to E2M1, ties to
+ *                      even, saturating at 6; no per-tensor scale), gran=16.
+ * The weights are MXFP4 in the first two (NVFP4 in the third: see
+ * moe_quantize_nvfp4).  Every other value returns MOE_ERR_UNSUPPORTED. */
+enum { MOE_MMA_MXF4xMXF4 = 1, MOE_MMA_FP8xFP4 = 2, MOE_MMA_NVF4xNVF4 = 3 };
 
 /* Layer dimensions.  hidden H and inter I must be multiples of 128 (H >= 256);
  * 1 <= topk <= min(num_experts, 32); 1 <= num_experts <= 1024;
@@ -122,8 +127,8 @@ MXMOE_API moe_status moe_workspace_init(const moe_dims *dims, void *ws_dev, size
  * Both give the same results.  Set on an initialised workspace, before the
  * pre_dispatch whose forward should use it; MOE_ERR_INVALID_ARG for an unknown mode,
  * MOE_ERR_WORKSPACE_MISMATCH for a workspace moe_workspace_init has not seen,
- * MOE_ERR_UNSUPPORTED for MOE_DISPATCH_PULL on an fp8xfp4 workspace (pull is built
- * for MXFP4 activations only). */
+ * MOE_ERR_UNSUPPORTED for MOE_DISPATCH_PULL on an fp8xfp4 or nvf4xnvf4 workspace
+ * (pull is built for MXFP4 activations only). */
 enum { MOE_DISPATCH_BUCKETED = 0, MOE_DISPATCH_PULL = 1 };
 MXMOE_API moe_status moe_workspace_set_dispatch(void *ws_dev, int32_t mode);
 
@@ -133,10 +138,17 @@ MXMOE_API moe_status moe_workspace_set_dispatch(void *ws_dev, int32_t mode);
 MXMOE_API moe_status moe_quantize_mxfp4(const float *src_dev, int64_t rows, int32_t K,
                                         uint8_t *codes_dev, uint8_t *scales_dev, void *stream);
 
+/* As moe_quantize_mxfp4 for NVFP4 (K % 16 == 0): codes_dev [rows, K/2], scales_dev
+ * [rows, K/16] one E4M3 byte per 16 elements, with the rule of MOE_MMA_NVF4xNVF4.
+ * Canonical NVFP4 weights for moe_prepare_weights under that mma_type. */
+MXMOE_API moe_status moe_quantize_nvfp4(const float *src_dev, int64_t rows, int32_t K,
+                                        uint8_t *codes_dev, uint8_t *scales_dev, void *stream);
+
 /* Weight transform (the pages' transform_weights_for_mega_moe with mma_type
  * mxf4xmxf4).  Inputs are canonical MXFP4, row-major:
  *   w1_codes_dev [E, 2I, H/2], w1_scales_dev [E, 2I, H/32]   gate rows 0..I-1, up rows I..2I-1
  *   w2_codes_dev [E, H, I/2],  w2_scales_dev [E, H, I/32]
+ *   (NVFP4 for nvf4xnvf4: scales [E, 2I, H/16] and [E, H, I/16], E4M3 bytes)
  * Output `prepared_dev` (prepared_bytes >= moe_prepared_weights_size): W1 rows
  * interleaved with gran=16 (each chunk of 16 gate and 16 up rows becomes
  * [gate even, up even, gate odd, up odd]; for fp8xfp4 gran=8: [gate 8, up 8]),
@@ -193,7 +205,7 @@ MXMOE_API moe_status moe_check(void *ws_dev, void *stream);
  *   assign_slot_host   int32 [T*k]        workspace row of assignment a (-1: skipped)
  *   x_codes_host       uint8 [T*k, H/2]   quantised token row as stored for assignment a
  *                                         ([T*k, H]: one E4M3 byte each, for fp8xfp4)
- *   x_scales_host      uint8 [T*k, H/32]
+ *   x_scales_host      uint8 [T*k, H/32]   ([T*k, H/16] E4M3 bytes for nvf4xnvf4)
  *   slot_token_host    int32 [T*k]        token recorded in row assign_slot[a] (check) */
 MXMOE_API moe_status moe_read_dispatch(const moe_dims *dims, const void *ws_dev,
                                        int32_t num_tokens, int32_t *counts_host,
@@ -202,6 +214,7 @@ MXMOE_API moe_status moe_read_dispatch(const moe_dims *dims, const void *ws_dev,
 
 /*   h_codes_host  uint8 [T*k, I/2]   requantised SwiGLU output of assignment a
  *                 ([T*k, I] for fp8xfp4)
+ *   h_scales_host uint8 [T*k, I/32]  ([T*k, I/16] for nvf4xnvf4)
  *   h_scales_host uint8 [T*k, I/32]                                                   */
 MXMOE_API moe_status moe_read_intermediate(const moe_dims *dims, const void *ws_dev,
                                            int32_t num_tokens, uint8_t *h_codes_host,

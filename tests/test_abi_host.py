@@ -61,8 +61,14 @@ def test_dims_validation(mx):
     # same weights; the E4M3 activation rows take twice the bytes of packed E2M1 rows
     assert mx.moe_prepared_weights_size(w4a8) == mx.moe_prepared_weights_size(ok)
     assert mx.moe_workspace_size(w4a8) > mx.moe_workspace_size(ok)
+    nv = mx.make_dims(4096, 2048, 256, 6, 512, mma_type=mx.MOE_MMA_NVF4xNVF4)
+    mx.moe_validate_dims(nv)
+    # NVFP4: the same codes, twice the scale bytes (one per 16 elements)
+    E, H, I = 256, 4096, 2048
+    scales4 = E * 2 * I * H // 32 + E * H * I // 32
+    assert mx.moe_prepared_weights_size(nv) - mx.moe_prepared_weights_size(ok) == scales4
     bad = [
-        (mx.make_dims(4096, 2048, 256, 6, 512, mma_type=3), mx.MOE_ERR_UNSUPPORTED),
+        (mx.make_dims(4096, 2048, 256, 6, 512, mma_type=4), mx.MOE_ERR_UNSUPPORTED),
         (mx.make_dims(4096, 2048, 256, 6, 512, mma_type=0), mx.MOE_ERR_UNSUPPORTED),
         (mx.make_dims(4000, 2048, 256, 6, 512), mx.MOE_ERR_INVALID_ARG),
         (mx.make_dims(128, 2048, 256, 6, 512), mx.MOE_ERR_INVALID_ARG),
