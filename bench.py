@@ -59,8 +59,8 @@ def metric(args) -> str:
 def parse_args():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=20)
-    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default="layer_T512", choices=sorted(synth.WORKLOADS))
     p.add_argument("--experts", type=int, default=0,
@@ -292,7 +292,7 @@ def oracle_sample(w: synth.Workload, x, ids, tw, n_tokens: int, nv: bool = False
 
 
 def time_oracle(w, x, ids, tw, n_tokens: int, repeats: int = 1, min_seconds: float = 0.0,
-                act_fp8: bool = False, nv: bool = False):
+                act_fp8: bool = False, nv: bool = False, nthreads: int | None = None):
     """The oracle on the first n_tokens tokens (with all their experts), run `repeats`
     times, or more until min_seconds of CPU work have been timed (at most 64 runs)."""
     import oracle
@@ -302,9 +302,9 @@ def time_oracle(w, x, ids, tw, n_tokens: int, repeats: int = 1, min_seconds: flo
     times = []
     while len(times) < repeats or (sum(times) < min_seconds and len(times) < 64):
         t0 = time.perf_counter()
-        layer(x[tokens], sub, tw[tokens], *Wc)
+        layer(x[tokens], sub, tw[tokens], *Wc, nthreads=nthreads)
         times.append(time.perf_counter() - t0)
-    return {"tokens": len(tokens), "seconds": times, "threads": oracle.threads()}
+    return {"tokens": len(tokens), "seconds": times, "threads": nthreads or oracle.threads()}
 
 
 def default_cpu_tokens(w):
@@ -562,6 +562,14 @@ def run_ours(args):
                "kind": "oracle",
                "sample": f"first {r['tokens']} of {w.T} tokens with all {w.k} experts each, "
                          f"{runs} runs ({secs:.1f} s of oracle time)"}
+        # the same oracle on one thread, on a third of the sample
+        r1 = time_oracle(w, x, ids, tw, max(2, n // 3), min_seconds=5.0, act_fp8=w4a8(args),
+                         nv=nvf4(args), nthreads=1)
+        runs1, secs1 = len(r1["seconds"]), sum(r1["seconds"])
+        cpu["single_thread"] = {"value": r1["tokens"] * runs1 / secs1, "unit": "tokens/s",
+                                "cores": 1,
+                                "sample": f"first {r1['tokens']} tokens, {runs1} runs "
+                                          f"({secs1:.1f} s)"}
 
     if rank != 0:
         return
