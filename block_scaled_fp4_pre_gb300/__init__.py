@@ -90,6 +90,7 @@ def lib() -> ctypes.CDLL:
             "moe_fp4_mma_probe": ([vp, i32, i32, i32, i64, vp], i32),
             "moe_mxfp8_scale_bytes": ([i64, i64, i32], ctypes.c_size_t),
             "moe_workspace_set_dispatch": ([vp, i32], i32),
+            "moe_workspace_set_tiles": ([vp, i32], i32),
             "moe_mxfp8_quantize": ([vp, i64, i64, vp, vp, i32, i64, vp], i32),
         }
         for name, (args, res) in sigs.items():
@@ -245,11 +246,19 @@ def moe_debug_wait_probe(ws, limit_ns: int, stream=None) -> None:
 
 MOE_DISPATCH_BUCKETED = 0
 MOE_DISPATCH_PULL = 1
+MOE_TILES_AUTO = 0
+MOE_TILES_WIDE = 1
+MOE_TILES_NARROW = 2
 
 
 def moe_workspace_set_dispatch(ws, mode: int) -> None:
     """Bucketed token copies (TMA) or per-token rows gathered by the layer kernel."""
     _check(lib().moe_workspace_set_dispatch(_ptr(ws), int(mode)))
+
+
+def moe_workspace_set_tiles(ws, mode: int) -> None:
+    """Token tiles of 128 rows (wide), 32 rows (narrow) or chosen per dispatch (auto)."""
+    _check(lib().moe_workspace_set_tiles(_ptr(ws), int(mode)))
 
 
 MOE_SF_PACKED = 0

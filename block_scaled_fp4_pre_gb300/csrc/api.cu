@@ -61,7 +61,7 @@ WsLayout ws_layout(const moe_dims& d) {
   L.T_cap = d.max_tokens;
   L.A_cap = L.T_cap * k;
   L.R_cap = (int64_t)align_up((size_t)L.A_cap, kBN) + (int64_t)kBN * E;
-  L.tiles_cap = L.A_cap / kBN + E + 1;
+  L.tiles_cap = L.A_cap / kBNNarrow + E + 1;   // enough for narrow tiles too
   size_t o = 0;
   auto take = [&](size_t bytes) {
     const size_t at = o;
@@ -82,11 +82,12 @@ WsLayout ws_layout(const moe_dims& d) {
   L.off_slot_assign = take((size_t)L.R_cap * 4);
   L.off_slot_weight = take((size_t)L.R_cap * 4);
   L.off_xb = take((size_t)L.R_cap * act_row_bytes(d, H));
-  L.off_xsf = take((size_t)L.R_cap * sf_row_bytes(d, H));
+  // scale blocks of wide tiles, or of narrow ones (a quarter of each block used)
+  L.off_xsf = take((size_t)L.R_cap * sf_row_bytes(d, H) * 4);
   L.off_xq = take((size_t)L.T_cap * H / 2);
   L.off_xs = take((size_t)L.T_cap * H / 32);
   L.off_hb = take((size_t)L.R_cap * act_row_bytes(d, I));
-  L.off_hsf = take((size_t)L.R_cap * sf_row_bytes(d, I));
+  L.off_hsf = take((size_t)L.R_cap * sf_row_bytes(d, I) * 4);
   L.off_acc = take((size_t)L.T_cap * H * 4);
   L.off_stage_x = take((size_t)L.T_cap * H * 2);
   L.off_stage_ids = take((size_t)L.A_cap * 4);
@@ -149,6 +150,8 @@ struct WsState {
   moe_dims dims;
   bool dispatched;
   int dispatch_mode;   // MOE_DISPATCH_*
+  int tile_mode;       // MOE_TILES_*
+  bool narrow;         // the last pre_dispatch's choice of 32-row token tiles
 };
 std::mutex g_reg_mu;
 std::map<const void*, WsState> g_registry;
@@ -170,10 +173,35 @@ bool take_dispatch(const void* ws) {
   return fresh;
 }
 
-void mark_dispatched(const void* ws) {
+void mark_dispatched(const void* ws, bool narrow) {
   std::lock_guard<std::mutex> lk(g_reg_mu);
   auto it = g_registry.find(ws);
-  if (it != g_registry.end()) it->second.dispatched = true;
+  if (it != g_registry.end()) {
+    it->second.dispatched = true;
+    it->second.narrow = narrow;
+  }
+}
+
+// Tile choice of a workspace's last pre_dispatch (wide if unknown).
+bool narrow_tiles(const void* ws) {
+  std::lock_guard<std::mutex> lk(g_reg_mu);
+  auto it = g_registry.find(ws);
+  return it != g_registry.end() && it->second.narrow;
+}
+
+int tile_mode(const void* ws) {
+  std::lock_guard<std::mutex> lk(g_reg_mu);
+  auto it = g_registry.find(ws);
+  return it == g_registry.end() ? MOE_TILES_AUTO : it->second.tile_mode;
+}
+
+// Narrow tiles when asked for, or (auto) when the experts average at most 16 rows:
+// decode-sized loads, where no tile needs more than a few of the 32 rows.  The pull
+// dispatch gathers into wide tiles only.
+bool choose_narrow(const moe_dims& d, int32_t T, int mode, bool pull) {
+  if (pull || mode == MOE_TILES_WIDE) return false;
+  if (mode == MOE_TILES_NARROW) return true;
+  return (int64_t)T * d.topk <= (int64_t)16 * d.num_experts;
 }
 
 // Timing hooks.
@@ -285,18 +313,20 @@ moe_status pre_dispatch_impl(const moe_dims* d, const void* x, const int32_t* id
   const WsLayout L = ws_layout(*d);
   const WsPtrs p = ws_ptrs(ws, L);
   const Shape s = shape_of(*d);
+  const bool pull = dispatch_mode(ws) == MOE_DISPATCH_PULL;
+  const bool narrow = choose_narrow(*d, T, tile_mode(ws), pull);
   cudaError_t e;
   {
     ProfScope ps("bucket", st);
-    e = launch_bucket(s, ids, T, p, st);
+    e = launch_bucket(s, ids, T, p, narrow ? kBNNarrow : kBN, st);
   }
   if (e != cudaSuccess) return cuda_fail(e, "bucket kernel");
   {
     ProfScope ps("quantize_scatter", st);
-    e = launch_quantize_scatter(s, x, ids, tw, T, p, dispatch_mode(ws) == MOE_DISPATCH_PULL, st);
+    e = launch_quantize_scatter(s, x, ids, tw, T, p, pull, narrow, st);
   }
   if (e != cudaSuccess) return cuda_fail(e, "quantize kernel");
-  mark_dispatched(ws);
+  mark_dispatched(ws, narrow);
   return MOE_OK;
 }
 
@@ -317,6 +347,7 @@ LayerLaunch layer_launch(const moe_dims* d, const void* prepared, void* ws, int3
   g.gate_up_debug = nullptr;
   g.num_sms = sm_count();
   g.pull = dispatch_mode(ws) == MOE_DISPATCH_PULL;
+  g.narrow = narrow_tiles(ws);
   return g;
 }
 
@@ -395,7 +426,7 @@ moe_status moe_workspace_init(const moe_dims* dims, void* ws, size_t ws_bytes, v
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "workspace header");
   std::lock_guard<std::mutex> lk(g_reg_mu);
-  g_registry[ws] = WsState{*dims, false, MOE_DISPATCH_BUCKETED};
+  g_registry[ws] = WsState{*dims, false, MOE_DISPATCH_BUCKETED, MOE_TILES_AUTO, false};
   return MOE_OK;
 }
 
@@ -410,6 +441,19 @@ moe_status moe_workspace_set_dispatch(void* ws, int32_t mode) {
   if (mode == MOE_DISPATCH_PULL && it->second.dims.mma_type != MOE_MMA_MXF4xMXF4)
     return fail(MOE_ERR_UNSUPPORTED, "pull dispatch is built for mxf4xmxf4 only");
   it->second.dispatch_mode = mode;
+  it->second.dispatched = false;   // a pre_dispatch in the new mode must come first
+  return MOE_OK;
+}
+
+moe_status moe_workspace_set_tiles(void* ws, int32_t mode) {
+  if (!ws) return fail(MOE_ERR_INVALID_ARG, "workspace is NULL");
+  if (mode != MOE_TILES_AUTO && mode != MOE_TILES_WIDE && mode != MOE_TILES_NARROW)
+    return fail(MOE_ERR_INVALID_ARG, "unknown tile mode %d", mode);
+  std::lock_guard<std::mutex> lk(g_reg_mu);
+  auto it = g_registry.find(ws);
+  if (it == g_registry.end())
+    return fail(MOE_ERR_WORKSPACE_MISMATCH, "workspace %p was not initialised", ws);
+  it->second.tile_mode = mode;
   it->second.dispatched = false;   // a pre_dispatch in the new mode must come first
   return MOE_OK;
 }
@@ -639,7 +683,8 @@ moe_status moe_read_dispatch(const moe_dims* dims, const void* ws, int32_t T, in
   } else if (xc_host || xs_host) {
     const size_t rb = (size_t)act_row_bytes(*dims, H);
     const int sfb = (int)sf_row_bytes(*dims, H);
-    std::vector<uint8_t> codes((size_t)R * rb), sf((size_t)R * sfb);
+    const bool narrow = narrow_tiles(ws);
+    std::vector<uint8_t> codes((size_t)R * rb), sf((size_t)R * sfb * (narrow ? 4 : 1));
     if (R && (e = cudaMemcpy(codes.data(), b + L.off_xb, codes.size(), cudaMemcpyDeviceToHost)))
       return cuda_fail(e, "codes read");
     if (R && (e = cudaMemcpy(sf.data(), b + L.off_xsf, sf.size(), cudaMemcpyDeviceToHost)))
@@ -655,7 +700,7 @@ moe_status moe_read_dispatch(const moe_dims* dims, const void* ws, int32_t T, in
       }
       if (xs_host)
         for (int g = 0; g < sfb; ++g)
-          xs_host[a * sfb + g] = ok ? sf[sf_atom_offset((size_t)r, g, sfb / 4)] : 0;
+          xs_host[a * sfb + g] = ok ? sf[sf_tile_offset((size_t)r, g, sfb / 4, narrow)] : 0;
     }
   }
   return MOE_OK;
@@ -683,7 +728,8 @@ moe_status moe_read_intermediate(const moe_dims* dims, const void* ws, int32_t T
   if (R < 0 || R > L.R_cap) return fail(MOE_ERR_CUDA, "corrupt segment table");
   const size_t rb = (size_t)act_row_bytes(*dims, I);
   const int sfb = (int)sf_row_bytes(*dims, I);
-  std::vector<uint8_t> codes((size_t)R * rb), sf((size_t)R * sfb);
+  const bool narrow = narrow_tiles(ws);
+  std::vector<uint8_t> codes((size_t)R * rb), sf((size_t)R * sfb * (narrow ? 4 : 1));
   if (R && (e = cudaMemcpy(codes.data(), b + L.off_hb, codes.size(), cudaMemcpyDeviceToHost)))
     return cuda_fail(e, "codes read");
   if (R && (e = cudaMemcpy(sf.data(), b + L.off_hsf, sf.size(), cudaMemcpyDeviceToHost)))
@@ -699,7 +745,7 @@ moe_status moe_read_intermediate(const moe_dims* dims, const void* ws, int32_t T
     }
     if (hs_host)
       for (int g = 0; g < sfb; ++g)
-        hs_host[a * sfb + g] = ok ? sf[sf_atom_offset((size_t)r, g, sfb / 4)] : 0;
+        hs_host[a * sfb + g] = ok ? sf[sf_tile_offset((size_t)r, g, sfb / 4, narrow)] : 0;
   }
   return MOE_OK;
 }

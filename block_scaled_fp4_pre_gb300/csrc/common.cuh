@@ -23,6 +23,10 @@ constexpr int kBTileBytes = kBN * kBKBytes;   // 16 KiB
 constexpr int kBBoxRows = 32;                 // token rows per TMA box
 constexpr int kSFAtomBytes = 512;             // 128 rows x 4 scale bytes
 constexpr int kSFStageBytes = 2 * kSFAtomBytes;  // 8 scale columns per k-block
+// Narrow tiles for decode-sized loads (few tokens per expert): 32 token rows a tile,
+// expert segments padded to 32 rows, each tile's token scales in 128x4 blocks of its
+// own (its rows in the first quarter of each block).
+constexpr int kBNNarrow = 32;
 
 // Device error bits in ws.flags[0].
 constexpr int kErrRouting = 1;
@@ -71,6 +75,14 @@ __host__ __device__ __forceinline__ int gate_up_source_row8(int r, int I) {
 // Interleave by activation format: gran=8 when f8, else gran=16.
 __host__ __device__ __forceinline__ int gate_up_source_row_for(int r, int I, int f8) {
   return f8 ? gate_up_source_row8(r, I) : gate_up_source_row(r, I);
+}
+
+// Byte of token-side scale (row, scale column s) in a workspace of wide (128-row) or
+// narrow (32-row) tiles: a narrow tile of rows 32t..32t+31 owns its scale blocks,
+// with row r in line r % 32 and the first 4-byte word of it.
+__host__ __device__ __forceinline__ size_t sf_tile_offset(size_t row, int s, int kc4, int narrow) {
+  if (!narrow) return sf_atom_offset(row, s, kc4);
+  return (((row >> 5) * (size_t)kc4 + (size_t)(s >> 2)) << 9) + ((row & 31) << 4) + (size_t)(s & 3);
 }
 
 // ---------------------------------------------------------------------------
@@ -142,14 +154,16 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 // of its launch.
 // Bucketing: per-expert counts and segment starts, the tile list, and each
 // assignment's rank; the quantiser (or launch_assign_slots) turns ranks into rows.
+// tile_rows: kBN (wide tiles) or kBNNarrow.
 cudaError_t launch_bucket(const Shape& s, const int32_t* ids, int T, const WsPtrs& ws,
-                          cudaStream_t st);
+                          int tile_rows, cudaStream_t st);
 // Quantise the tokens, give every assignment its row and copy the token there.
 // pull: write each token's row once (xq/xs) instead of copying it to its k rows; the
 // layer kernel then gathers token rows itself.
+// narrow: token scales in the narrow-tile layout (sf_tile_offset).
 cudaError_t launch_quantize_scatter(const Shape& s, const void* x, const int32_t* ids,
                                     const float* tw, int T, const WsPtrs& ws, bool pull,
-                                    cudaStream_t st);
+                                    bool narrow, cudaStream_t st);
 // Rows of all assignments and the per-row tables, without quantising anything.
 cudaError_t launch_assign_slots(const Shape& s, const int32_t* ids, const float* tw, int T,
                                 const WsPtrs& ws, cudaStream_t st);
@@ -192,6 +206,7 @@ struct LayerLaunch {
   float* gate_up_debug;      // [T*k, 2I] (num_phases == 1)
   int num_sms;
   bool pull;                 // gate/up token rows gathered from ws.xq/xs (pull dispatch)
+  bool narrow;               // 32-row token tiles (the dispatch's choice)
 };
 cudaError_t launch_layer(const LayerLaunch& g, cudaStream_t st);
 

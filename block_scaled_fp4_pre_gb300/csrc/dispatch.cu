@@ -24,7 +24,8 @@ constexpr unsigned kFull = 0xFFFFFFFFu;
 // them advances the warp's count for that expert, and a scan over warps turns the
 // counts into each warp's base.  Each block publishes its per-expert totals; the
 // last block to finish scans them over blocks (bases of later chunks) and over
-// experts (segment starts padded to kBN rows, tile list).  Row of an assignment =
+// experts (segment starts padded to tile_rows -- kBN, or kBNNarrow for narrow tiles --
+// and the tile list).  Row of an assignment =
 // segment start + its chunk's base + its rank in the chunk.
 
 // Lanes whose key equals this lane's key (keys < 2^nbits).
@@ -39,7 +40,7 @@ __device__ __forceinline__ unsigned peers_of(int key, int nbits) {
 }
 
 __global__ void __launch_bounds__(1024) bucket_kernel(const int32_t* __restrict__ ids, int T,
-                                                      int k, int E, WsPtrs ws) {
+                                                      int k, int E, WsPtrs ws, int tile_rows) {
   extern __shared__ int32_t sh[];
   int32_t* cnt = sh;                        // [32][E] per-warp counts, then bases
   int32_t* key_sh = cnt + 32 * E;           // [kBucketChunk] expert id, E if invalid
@@ -144,8 +145,8 @@ __global__ void __launch_bounds__(1024) bucket_kernel(const int32_t* __restrict_
     for (int e0 = 0; e0 < E; e0 += 32) {
       const int e = e0 + lane;
       const int n = e < E ? tot[e] : 0;
-      const int tiles = (n + kBN - 1) / kBN;
-      const int rows = tiles * kBN;
+      const int tiles = (n + tile_rows - 1) / tile_rows;
+      const int rows = tiles * tile_rows;
       int ir = rows, it = tiles;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -174,8 +175,8 @@ __global__ void __launch_bounds__(1024) bucket_kernel(const int32_t* __restrict_
     const int n = tot[e];
     ws.counts[e] = n;
     ws.seg[e] = seg[e];
-    for (int i = 0, r = 0; r < n; ++i, r += kBN) {
-      ws.tiles[tst[e] + i] = make_int4(e, seg[e] + r, min(kBN, n - r), 0);
+    for (int i = 0, r = 0; r < n; ++i, r += tile_rows) {
+      ws.tiles[tst[e] + i] = make_int4(e, seg[e] + r, min(tile_rows, n - r), 0);
       ws.tile_done[tst[e] + i] = 0;
     }
   }
@@ -230,7 +231,7 @@ __global__ void __launch_bounds__(256) quantize_scatter_kernel(const __nv_bfloat
                                                                const int32_t* __restrict__ ids,
                                                                const float* __restrict__ tw,
                                                                int H, int k, int E, WsPtrs ws,
-                                                               bool pull) {
+                                                               bool pull, int narrow) {
   constexpr bool F8 = FMT == kTokMxfp8, NV = FMT == kTokNvfp4;
   constexpr int kBytesPer8 = F8 ? 8 : 4;                // code bytes of 8 elements
   constexpr int kGroup = NV ? 16 : 32;                  // elements per scale
@@ -318,7 +319,7 @@ __global__ void __launch_bounds__(256) quantize_scatter_kernel(const __nv_bfloat
     for (int i = tid; i < row_bytes_q / 16; i += blockDim.x)   // 16-byte chunks of the row
       dst[i] = reinterpret_cast<const uint4*>(codes_sh)[i];
     for (int i = tid; i < nsf; i += blockDim.x)
-      ws.xsf[sf_atom_offset((size_t)slot, i, kc4)] = sf_sh[i];
+      ws.xsf[sf_tile_offset((size_t)slot, i, kc4, narrow)] = sf_sh[i];
   }
 }
 
@@ -457,19 +458,20 @@ unsigned grid_for(int64_t work, int block, int64_t cap) {
 }  // namespace
 
 cudaError_t launch_bucket(const Shape& s, const int32_t* ids, int T, const WsPtrs& ws,
-                          cudaStream_t st) {
+                          int tile_rows, cudaStream_t st) {
   const size_t smem = ((size_t)35 * s.E + kBucketChunk + 2) * sizeof(int32_t);
   cudaError_t err = cudaFuncSetAttribute(bucket_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
   if (err != cudaSuccess) return err;
   const int A = T * s.k;
-  bucket_kernel<<<(A + kBucketChunk - 1) / kBucketChunk, 1024, smem, st>>>(ids, T, s.k, s.E, ws);
+  bucket_kernel<<<(A + kBucketChunk - 1) / kBucketChunk, 1024, smem, st>>>(ids, T, s.k, s.E, ws,
+                                                                            tile_rows);
   return cudaGetLastError();
 }
 
 cudaError_t launch_quantize_scatter(const Shape& s, const void* x, const int32_t* ids,
                                     const float* tw, int T, const WsPtrs& ws, bool pull,
-                                    cudaStream_t st) {
+                                    bool narrow, cudaStream_t st) {
   const size_t smem = (size_t)(s.f8 ? s.H : s.H / 2) + s.H / sf_group(s);
   auto kern = s.f8   ? quantize_scatter_kernel<kTokMxfp8>
               : s.nv ? quantize_scatter_kernel<kTokNvfp4>
@@ -480,7 +482,7 @@ cudaError_t launch_quantize_scatter(const Shape& s, const void* x, const int32_t
     if (e != cudaSuccess) return e;
   }
   return launch_pdl(kern, dim3(T), dim3(256), smem, st, reinterpret_cast<const __nv_bfloat16*>(x),
-                    ids, tw, s.H, s.k, s.E, ws, pull);
+                    ids, tw, s.H, s.k, s.E, ws, pull, narrow ? 1 : 0);
 }
 
 cudaError_t launch_assign_slots(const Shape& s, const int32_t* ids, const float* tw, int T,

@@ -43,7 +43,9 @@
 namespace mxmoe {
 namespace {
 
-constexpr int kStages = 3;
+constexpr int kStages = 3;                 // wide token tiles
+constexpr int kStagesNarrow = 4;           // narrow (32-row) token tiles
+constexpr int kMaxStages = kStagesNarrow;
 constexpr int kThreads = 192;
 constexpr int kBlocksPerSM = 2;
 constexpr int kTmemCols = 256;             // half of the SM's tensor memory per block
@@ -70,8 +72,8 @@ enum LayerMode { kModeLayer = 0, kModeRaw = 1 };
 
 template <bool NV>
 struct __align__(16) SmemTail {
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
   uint64_t acc_full;
   uint64_t acc_empty;
   uint64_t mma_done;
@@ -91,22 +93,24 @@ struct __align__(16) SmemTail {
   int32_t tile_start[NV ? 1 : 1025];
 };
 
-// Shared-memory map: kStages x (weight box, token boxes, both operands' scale
-// blocks: 2 per k-block, 4 for NVFP4), then the tail.
-template <bool NV>
+// Shared-memory map: kSt stages x (weight box, token boxes, both operands' scale
+// blocks: 2 per k-block, 4 for NVFP4), then the tail.  Narrow tiles need a quarter
+// of the token room, which pays for a fourth stage.
+template <bool NV, bool NARROW>
 struct SmemMap {
+  static constexpr int kSt = NARROW ? kStagesNarrow : kStages;
+  static constexpr int kBRows = NARROW ? kBNNarrow : kBN;        // token rows a stage holds
+  static constexpr size_t kBSlot = (size_t)kBRows * kBKBytes;
   static constexpr size_t kSF = (size_t)(NV ? 4 : 2) * kSFAtomBytes;
   static constexpr size_t kA = 0;
-  static constexpr size_t kB = kA + (size_t)kStages * kATileBytes;
-  static constexpr size_t kSFA = kB + (size_t)kStages * kBTileBytes;
-  static constexpr size_t kSFB = kSFA + (size_t)kStages * kSF;
-  static constexpr size_t kTail = kSFB + (size_t)kStages * kSF;
+  static constexpr size_t kB = kA + (size_t)kSt * kATileBytes;
+  static constexpr size_t kSFA = kB + (size_t)kSt * kBSlot;
+  static constexpr size_t kSFB = kSFA + (size_t)kSt * kSF;
+  static constexpr size_t kTail = kSFB + (size_t)kSt * kSF;
   static constexpr size_t kBytes = kTail + sizeof(SmemTail<NV>) + 1024;  // + alignment slack
+  // two blocks per SM (228 KiB of shared memory, 1 KiB of it reserved per block)
+  static_assert(2 * (kBytes + 1024) <= 228 * 1024, "two blocks per SM");
 };
-// two blocks per SM (228 KiB of shared memory, 1 KiB of it reserved per block)
-static_assert(2 * (SmemMap<false>::kBytes + 1024) <= 228 * 1024 &&
-                  2 * (SmemMap<true>::kBytes + 1024) <= 228 * 1024,
-              "two blocks per SM");
 
 struct PhaseArgs {
   const uint8_t* w_sf;   // weight scale blocks
@@ -171,7 +175,8 @@ __device__ __forceinline__ float silu_times(float g, float u) {
 // packed E2M1 throughout, 256 elements a k-block, kind::mxf4 MMAs, gran=16.
 // NV: nvf4xnvf4 -- as mxf4xmxf4 with one E4M3 scale per 16 elements (four scale
 // blocks per k-block and operand), kind::mxf4nvf4 MMAs, NVFP4 requantisation.
-template <int MODE, bool PULL, bool F8, bool NV>
+// NARROW: 32-row token tiles (a quarter of the token room, four stages).
+template <int MODE, bool PULL, bool F8, bool NV, bool NARROW>
 __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
     moe_layer_kernel(const __grid_constant__ CUtensorMap tmap_w1,
                      const __grid_constant__ CUtensorMap tmap_x,
@@ -182,7 +187,8 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  using SM = SmemMap<NV>;
+  using SM = SmemMap<NV, NARROW>;
+  constexpr int kSt = SM::kSt;
   using TM = TmemMap<NV>;
   SmemTail<NV>* tail = reinterpret_cast<SmemTail<NV>*>(smem + SM::kTail);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -190,7 +196,7 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
   constexpr int kAtomK = NV ? 64 : 128; // K elements of one scale block (4 scales a row)
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kSt; ++s) {
       ptx::mbar_init(&tail->full[s], 1);
       ptx::mbar_init(&tail->empty[s], 1);
     }
@@ -318,7 +324,8 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
       const int mt = it.mt;   // the item's weight slab
       const int wrow = e * P.rows_per_expert + mt * kBM;
       const uint8_t* wsf = P.w_sf + ((size_t)(e * P.m_tiles + mt) * P.kc4) * kSFAtomBytes;
-      const uint8_t* tsf = P.t_sf + ((size_t)(row0 / kBN) * P.kc4) * kSFAtomBytes;
+      // the tile's token scale blocks (each narrow tile has blocks of its own)
+      const uint8_t* tsf = P.t_sf + ((size_t)(row0 / SM::kBRows) * P.kc4) * kSFAtomBytes;
       // Pulled token rows: lane l gathers rows l, l+32, l+64, l+96 of the tile.
       const bool pulled = PULL && it.phase == 0;
       int tok[kBN / 32];
@@ -342,7 +349,7 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
         const int kvalid = min(kKb, P.K - kb * kKb);
         const int atoms = kvalid / kAtomK;
         uint64_t* bar = &tail->full[stage];
-        uint8_t* b_dst = smem + SM::kB + (size_t)stage * kBTileBytes;
+        uint8_t* b_dst = smem + SM::kB + (size_t)stage * SM::kBSlot;
         if (pulled) {
           // Row i of the tile is token tok's codes [kb*128, kb*128 + kvalid/2) in the
           // 128-byte swizzle (16-byte chunk c of row i at chunk c ^ (i % 8)), and its
@@ -388,7 +395,7 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
                          wsf + (size_t)kb * (kKb / kAtomK) * kSFAtomBytes, atoms * kSFAtomBytes,
                          bar, pol_w);
           if (!pulled) {
-            if (nb * kBBoxRows == kBN) {
+            if (nb * kBBoxRows == SM::kBRows) {
               ptx::tma_load_2d(b_dst, tt_full, kb * kBKBytes, row0, bar, pol_t);
             } else {
               for (int j = 0; j < nb; ++j)
@@ -405,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
           }
         }
         ++issued;
-        if (++stage == kStages) {
+        if (++stage == kSt) {
           stage = 0;
           phase ^= 1u;
         }
@@ -420,10 +427,10 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
     // (normally they all have, because the MMA consumed them).
     if (PULL) ptx::cp_async_wait_all();
     if (leader) {
-      const int64_t first = issued > kStages ? issued - kStages : 0;
+      const int64_t first = issued > kSt ? issued - kSt : 0;
       for (int64_t i = first; i < issued; ++i) {
-        const int s = (int)(i % kStages);
-        const uint32_t par = (uint32_t)((i / kStages) & 1);
+        const int s = (int)(i % kSt);
+        const uint32_t par = (uint32_t)((i / kSt) & 1);
         int never = 0;
         ptx::mbar_wait(&tail->full[s], par, &never, kWaitLimitNs);
       }
@@ -476,7 +483,7 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
             ptx::tc_cp_sf(sfb_t + a * 4, ptx::desc_sf(sb + a * kSFAtomBytes));
           }
           const uint32_t a_base = ptx::smem_addr(smem + SM::kA + (size_t)stage * kATileBytes);
-          const uint32_t b_base = ptx::smem_addr(smem + SM::kB + (size_t)stage * kBTileBytes);
+          const uint32_t b_base = ptx::smem_addr(smem + SM::kB + (size_t)stage * SM::kBSlot);
           // 32 bytes of K per instruction: 64 packed E2M1 elements, or 32 one-byte ones
           const int steps = kvalid / (F8 ? 32 : 64);
           for (int s = 0; s < steps; ++s) {
@@ -499,7 +506,7 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
           }
           ptx::tc_commit(&tail->empty[stage]);
           sfbuf ^= 1u;
-          if (++stage == kStages) {
+          if (++stage == kSt) {
             stage = 0;
             phase ^= 1u;
           }
@@ -676,7 +683,8 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
               if (jc < ncol) {
                 const size_t row = (size_t)row0 + c0 + jc;
                 const uint16_t sv = *reinterpret_cast<const uint16_t*>(&tail->sstage[xb][jc][0]);
-                *reinterpret_cast<uint16_t*>(args.ws.hsf + sf_atom_offset(row, mt * 2, i_kc4)) = sv;
+                *reinterpret_cast<uint16_t*>(args.ws.hsf +
+                                             sf_tile_offset(row, mt * 2, i_kc4, NARROW)) = sv;
               }
             }
           } else if (lane < 8) {
@@ -693,10 +701,12 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
               const size_t row = (size_t)row0 + c0 + jc;
               if (NV) {   // the item's four scale bytes: one 32-bit word of a scale block
                 const uint32_t sv = *reinterpret_cast<const uint32_t*>(&tail->sstage[xb][jc][0]);
-                *reinterpret_cast<uint32_t*>(args.ws.hsf + sf_atom_offset(row, mt * 4, i_kc4)) = sv;
+                *reinterpret_cast<uint32_t*>(args.ws.hsf +
+                                             sf_tile_offset(row, mt * 4, i_kc4, NARROW)) = sv;
               } else {
                 const uint16_t sv = *reinterpret_cast<const uint16_t*>(&tail->sstage[xb][jc][0]);
-                *reinterpret_cast<uint16_t*>(args.ws.hsf + sf_atom_offset(row, mt * 2, i_kc4)) = sv;
+                *reinterpret_cast<uint16_t*>(args.ws.hsf +
+                                             sf_tile_offset(row, mt * 2, i_kc4, NARROW)) = sv;
               }
             }
           }
@@ -900,13 +910,13 @@ PhaseArgs phase_args(const uint8_t* w_sf, const uint8_t* t_sf, int rows_per_expe
   return p;
 }
 
-template <int MODE, bool PULL, bool F8, bool NV>
+template <int MODE, bool PULL, bool F8, bool NV, bool NARROW>
 cudaError_t launch_mode(const LayerLaunch& g, const CUtensorMap* maps, const LayerArgs& a,
                         cudaStream_t st) {
-  constexpr size_t kSmemBytes = SmemMap<NV>::kBytes;
+  constexpr size_t kSmemBytes = SmemMap<NV, NARROW>::kBytes;
   static int grid = 0;   // per instantiation, for the device of the first launch
   if (grid == 0) {
-    cudaError_t err = cudaFuncSetAttribute(moe_layer_kernel<MODE, PULL, F8, NV>,
+    cudaError_t err = cudaFuncSetAttribute(moe_layer_kernel<MODE, PULL, F8, NV, NARROW>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)kSmemBytes);
     if (err != cudaSuccess) return err;
@@ -914,7 +924,8 @@ cudaError_t launch_mode(const LayerLaunch& g, const CUtensorMap* maps, const Lay
     // resident blocks)
     grid = kBlocksPerSM * g.num_sms;
   }
-  return launch_pdl(moe_layer_kernel<MODE, PULL, F8, NV>, dim3(grid), dim3(kThreads), kSmemBytes, st,
+  return launch_pdl(moe_layer_kernel<MODE, PULL, F8, NV, NARROW>, dim3(grid), dim3(kThreads),
+                    kSmemBytes, st,
                     maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], a);
 }
 
@@ -927,8 +938,9 @@ cudaError_t launch_layer(const LayerLaunch& g, cudaStream_t st) {
   // Activation rows: packed E2M1 (K/2 bytes) or E4M3 (K bytes).
   const uint64_t xrow = f8 ? (uint64_t)s.H : (uint64_t)s.H / 2;
   const uint64_t hrow = f8 ? (uint64_t)s.I : (uint64_t)s.I / 2;
-  // Full token tiles come in one box of all 128 rows.
-  const uint32_t full_rows = kBN;
+  // Full token tiles come in one box of all their rows (128, or 32 when narrow).
+  const bool narrow = g.narrow && !g.pull;
+  const uint32_t full_rows = narrow ? kBNNarrow : kBN;
   CUtensorMap maps[6];
   cudaError_t err;
   if ((err = make_tmap(&maps[4], g.ws.xb, xrow, (uint64_t)g.R_cap, full_rows)) ||
@@ -957,17 +969,28 @@ cudaError_t launch_layer(const LayerLaunch& g, cudaStream_t st) {
   a.E = s.E;
   a.ws = g.ws;
   a.gate_up_debug = g.gate_up_debug;
+  const bool layer = g.num_phases == 2;
+  if (g.pull)
+    return layer ? launch_mode<kModeLayer, true, false, false, false>(g, maps, a, st)
+                 : launch_mode<kModeRaw, true, false, false, false>(g, maps, a, st);
+  if (narrow) {
+    if (f8)
+      return layer ? launch_mode<kModeLayer, false, true, false, true>(g, maps, a, st)
+                   : launch_mode<kModeRaw, false, true, false, true>(g, maps, a, st);
+    if (nv)
+      return layer ? launch_mode<kModeLayer, false, false, true, true>(g, maps, a, st)
+                   : launch_mode<kModeRaw, false, false, true, true>(g, maps, a, st);
+    return layer ? launch_mode<kModeLayer, false, false, false, true>(g, maps, a, st)
+                 : launch_mode<kModeRaw, false, false, false, true>(g, maps, a, st);
+  }
   if (f8)
-    return g.num_phases == 2 ? launch_mode<kModeLayer, false, true, false>(g, maps, a, st)
-                             : launch_mode<kModeRaw, false, true, false>(g, maps, a, st);
+    return layer ? launch_mode<kModeLayer, false, true, false, false>(g, maps, a, st)
+                 : launch_mode<kModeRaw, false, true, false, false>(g, maps, a, st);
   if (nv)
-    return g.num_phases == 2 ? launch_mode<kModeLayer, false, false, true>(g, maps, a, st)
-                             : launch_mode<kModeRaw, false, false, true>(g, maps, a, st);
-  if (g.num_phases == 2)
-    return g.pull ? launch_mode<kModeLayer, true, false, false>(g, maps, a, st)
-                  : launch_mode<kModeLayer, false, false, false>(g, maps, a, st);
-  return g.pull ? launch_mode<kModeRaw, true, false, false>(g, maps, a, st)
-                : launch_mode<kModeRaw, false, false, false>(g, maps, a, st);
+    return layer ? launch_mode<kModeLayer, false, false, true, false>(g, maps, a, st)
+                 : launch_mode<kModeRaw, false, false, true, false>(g, maps, a, st);
+  return layer ? launch_mode<kModeLayer, false, false, false, false>(g, maps, a, st)
+               : launch_mode<kModeRaw, false, false, false, false>(g, maps, a, st);
 }
 
 }  // namespace mxmoe

@@ -117,7 +117,7 @@ extern "C" moe_status moe_bucket_noalloc(const moe_dims* dims, const int32_t* to
   p.slot_assign = reinterpret_cast<int32_t*>(base + kOffSlotAssign);
   p.slot_weight = reinterpret_cast<float*>(base + kOffSlotWeight);
   const Shape shape{dims->hidden, dims->inter, dims->num_experts, dims->topk};
-  e = launch_bucket(shape, topk_ids_dev, num_tokens, p, st);
+  e = launch_bucket(shape, topk_ids_dev, num_tokens, p, kBN, st);
   if (e != cudaSuccess) return fail(MOE_ERR_CUDA, cudaGetErrorString(e));
   e = launch_assign_slots(shape, topk_ids_dev, topk_weights_dev, num_tokens, p, st);
   if (e != cudaSuccess) return fail(MOE_ERR_CUDA, cudaGetErrorString(e));

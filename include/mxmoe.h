@@ -132,6 +132,20 @@ MXMOE_API moe_status moe_workspace_init(const moe_dims *dims, void *ws_dev, size
 enum { MOE_DISPATCH_BUCKETED = 0, MOE_DISPATCH_PULL = 1 };
 MXMOE_API moe_status moe_workspace_set_dispatch(void *ws_dev, int32_t mode);
 
+/* Token tiles of the grouped GEMMs:
+ *   MOE_TILES_WIDE:   up to 128 token rows a tile, expert segments padded to 128 rows.
+ *   MOE_TILES_NARROW: up to 32 rows a tile (segments padded to 32); the layer then
+ *                     keeps four stages of operands in flight instead of three,
+ *                     which pays when experts hold few tokens (decode-sized loads).
+ *   MOE_TILES_AUTO (default after moe_workspace_init): narrow when num_tokens * k <=
+ *                     16 * num_experts, else wide.
+ * The choice is made at each moe_pre_dispatch and holds for the forward that
+ * follows; results are the same either way up to fp32 summation order.  The pull
+ * dispatch always uses wide tiles.  MOE_ERR_INVALID_ARG for an unknown mode,
+ * MOE_ERR_WORKSPACE_MISMATCH for a workspace moe_workspace_init has not seen. */
+enum { MOE_TILES_AUTO = 0, MOE_TILES_WIDE = 1, MOE_TILES_NARROW = 2 };
+MXMOE_API moe_status moe_workspace_set_tiles(void *ws_dev, int32_t mode);
+
 /* Quantises row-major fp32 src_dev [rows, K] (K % 32 == 0) to MXFP4 with the rule
  * above: codes_dev [rows, K/2], scales_dev [rows, K/32], both row-major.  A helper
  * for producing canonical MXFP4 weights on the device. */
