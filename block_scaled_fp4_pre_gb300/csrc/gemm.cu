@@ -45,7 +45,8 @@ namespace {
 
 constexpr int kStages = 3;                 // wide token tiles
 constexpr int kStagesNarrow = 4;           // narrow (32-row) token tiles
-constexpr int kMaxStages = kStagesNarrow;
+constexpr int kStagesNarrowF8 = 5;         // narrow, E4M3 tokens: one scale block a stage
+constexpr int kMaxStages = kStagesNarrowF8;
 constexpr int kThreads = 192;
 constexpr int kBlocksPerSM = 2;
 constexpr int kTmemCols = 256;             // half of the SM's tensor memory per block
@@ -70,7 +71,8 @@ constexpr unsigned kFull = 0xFFFFFFFFu;
 
 enum LayerMode { kModeLayer = 0, kModeRaw = 1 };
 
-template <bool NV>
+// GLOBAL_TILES: the expert tile table stays in global memory (stage room is short).
+template <bool GLOBAL_TILES>
 struct __align__(16) SmemTail {
   uint64_t full[kMaxStages];
   uint64_t empty[kMaxStages];
@@ -88,26 +90,28 @@ struct __align__(16) SmemTail {
   // scale bytes.  Double-buffered across chunks.
   alignas(16) uint8_t hstage[2][kEpiCols][64];   // 32 bytes used for E2M1, 64 for E4M3
   alignas(4) uint8_t sstage[2][kEpiCols][4];      // 2 scale bytes a column (4: NVFP4)
-  // first tile of each expert (E <= 1024), see decode_item; NVFP4 stages take the
-  // room, so that kernel reads the table from global memory
-  int32_t tile_start[NV ? 1 : 1025];
+  // first tile of each expert (E <= 1024), see decode_item
+  int32_t tile_start[GLOBAL_TILES ? 1 : 1025];
 };
 
 // Shared-memory map: kSt stages x (weight box, token boxes, both operands' scale
-// blocks: 2 per k-block, 4 for NVFP4), then the tail.  Narrow tiles need a quarter
-// of the token room, which pays for a fourth stage.
-template <bool NV, bool NARROW>
+// blocks: 2 per k-block, 4 for NVFP4, 1 for the 128-element k-blocks of E4M3 tokens),
+// then the tail.  Narrow tiles need a quarter of the token room, which pays for a
+// fourth stage (a fifth with E4M3 tokens, whose weight boxes carry half the bytes).
+template <bool NV, bool NARROW, bool F8>
 struct SmemMap {
-  static constexpr int kSt = NARROW ? kStagesNarrow : kStages;
+  static constexpr int kSt = NARROW ? (F8 ? kStagesNarrowF8 : kStagesNarrow) : kStages;
   static constexpr int kBRows = NARROW ? kBNNarrow : kBN;        // token rows a stage holds
   static constexpr size_t kBSlot = (size_t)kBRows * kBKBytes;
-  static constexpr size_t kSF = (size_t)(NV ? 4 : 2) * kSFAtomBytes;
+  static constexpr size_t kSF = (size_t)(NV ? 4 : F8 ? 1 : 2) * kSFAtomBytes;
   static constexpr size_t kA = 0;
   static constexpr size_t kB = kA + (size_t)kSt * kATileBytes;
   static constexpr size_t kSFA = kB + (size_t)kSt * kBSlot;
   static constexpr size_t kSFB = kSFA + (size_t)kSt * kSF;
   static constexpr size_t kTail = kSFB + (size_t)kSt * kSF;
-  static constexpr size_t kBytes = kTail + sizeof(SmemTail<NV>) + 1024;  // + alignment slack
+  // NVFP4's scale blocks and the fifth narrow E4M3 stage take the tile table's room
+  static constexpr bool kGlobalTiles = NV || (NARROW && F8);
+  static constexpr size_t kBytes = kTail + sizeof(SmemTail<kGlobalTiles>) + 1024;  // + slack
   // two blocks per SM (228 KiB of shared memory, 1 KiB of it reserved per block)
   static_assert(2 * (kBytes + 1024) <= 228 * 1024, "two blocks per SM");
 };
@@ -187,10 +191,10 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  using SM = SmemMap<NV, NARROW>;
+  using SM = SmemMap<NV, NARROW, F8>;
   constexpr int kSt = SM::kSt;
   using TM = TmemMap<NV>;
-  SmemTail<NV>* tail = reinterpret_cast<SmemTail<NV>*>(smem + SM::kTail);
+  SmemTail<SM::kGlobalTiles>* tail = reinterpret_cast<SmemTail<SM::kGlobalTiles>*>(smem + SM::kTail);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr int kKb = F8 ? 128 : kBK;   // K elements per k-block (128-byte rows either way)
   constexpr int kAtomK = NV ? 64 : 128; // K elements of one scale block (4 scales a row)
@@ -244,8 +248,8 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
 
   const int num_tiles = args.ws.flags[kFlagTiles];
   const int E = args.E;
-  const int32_t* tile_start = NV ? args.ws.tile_start : tail->tile_start;
-  if (!NV)
+  const int32_t* tile_start = SM::kGlobalTiles ? args.ws.tile_start : tail->tile_start;
+  if (!SM::kGlobalTiles)
     for (int e = threadIdx.x; e <= E; e += blockDim.x) tail->tile_start[e] = args.ws.tile_start[e];
   __syncthreads();
   // Items per token tile and phase: one per weight slab.
@@ -913,7 +917,7 @@ PhaseArgs phase_args(const uint8_t* w_sf, const uint8_t* t_sf, int rows_per_expe
 template <int MODE, bool PULL, bool F8, bool NV, bool NARROW>
 cudaError_t launch_mode(const LayerLaunch& g, const CUtensorMap* maps, const LayerArgs& a,
                         cudaStream_t st) {
-  constexpr size_t kSmemBytes = SmemMap<NV, NARROW>::kBytes;
+  constexpr size_t kSmemBytes = SmemMap<NV, NARROW, F8>::kBytes;
   static int grid = 0;   // per instantiation, for the device of the first launch
   if (grid == 0) {
     cudaError_t err = cudaFuncSetAttribute(moe_layer_kernel<MODE, PULL, F8, NV, NARROW>,
