@@ -69,6 +69,8 @@ def parse_args():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--dispatch", choices=["bucketed", "pull"], default="bucketed",
                    help="token rows copied per expert by pre_dispatch, or gathered by the layer")
+    p.add_argument("--tiles", choices=["auto", "wide", "narrow"], default="auto",
+                   help="token tiles: 128 rows (wide), 32 rows (narrow) or the layer's choice")
     p.add_argument("--mma", choices=["mxf4xmxf4", "fp8xfp4", "nvf4xnvf4"], default="mxf4xmxf4",
                    help="formats: MXFP4 (W4A4, the headline), MXFP8 activations (W4A8) or NVFP4")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -425,6 +427,8 @@ def run_ours(args):
     out = torch.empty((w.T, w.H), dtype=torch.bfloat16, device=dev)
     ws = torch.empty(mx.moe_workspace_size(dims), dtype=torch.uint8, device=dev)
     mx.moe_workspace_init(dims, ws, stream)
+    mx.moe_workspace_set_tiles(ws, {"auto": mx.MOE_TILES_AUTO, "wide": mx.MOE_TILES_WIDE,
+                                    "narrow": mx.MOE_TILES_NARROW}[args.tiles])
     mx.moe_workspace_set_dispatch(ws, mx.MOE_DISPATCH_PULL if args.dispatch == "pull"
                                   else mx.MOE_DISPATCH_BUCKETED)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -583,7 +587,8 @@ def run_ours(args):
                   "nvfp4 (e2m1 x ue4m3 per 16), fp32 accumulate" if nvf4(args) else
                   "mxfp4 (e2m1 x ue8m0), fp32 accumulate"),
         "data": "synthetic",
-        "config": dict(config_dict(w, world), dispatch=args.dispatch, mma_type=args.mma),
+        "config": dict(config_dict(w, world), dispatch=args.dispatch, mma_type=args.mma,
+                       tiles=args.tiles),
         "layer_hbm_tbs": alg["layer_bytes"] / (ms / 1e3) / 1e12,
         "layer_roofline_frac": (alg["layer_bytes"] / (hbm_peak * 1e9)) / (ms / 1e3),
         "touched_experts": alg["touched_experts"],
