@@ -105,3 +105,43 @@ def test_invalid_ids_skipped_and_reported(mma):
     assert ref["invalid_ids"] == 2
     assert normwise_rel_err(oracle.bf16_bits_to_f64(_bits(out)), ref["out_f64"]) <= 2e-3
     mx.moe_check(layer.ws)   # the flag was read and cleared
+
+
+@pytest.mark.parametrize("mma", list(MMAS))
+def test_largest_hidden_size(mma):
+    """hidden = 65536, the largest the ABI takes: 32 quantiser rounds per token row
+    (and, for E4M3 rows, the opt-in shared-memory limit of the quantiser)."""
+    w = synth.Workload("wideH", T=24, H=65536, I=128, E=3, k=2)
+    layer = DeviceLayer(w, mma_type=MMAS[mma])
+    layer_fn, weights = ORACLE[mma]
+    x = synth.hidden_bf16(w)
+    ids, tw = synth.routing(w)
+    got = layer.run(x, ids, tw)
+    ref = layer_fn(x, ids, tw, *weights(w, range(w.E)))
+    d = mx.moe_read_dispatch(layer.dims, layer.ws, w.T)
+    assert np.array_equal(d["x_codes"], np.repeat(ref["x_codes"], w.k, axis=0))
+    assert np.array_equal(d["x_scales"], np.repeat(ref["x_sf"], w.k, axis=0))
+    assert normwise_rel_err(oracle.bf16_bits_to_f64(got), ref["out_f64"]) <= 2e-3
+
+
+def test_largest_token_count():
+    """num_tokens = max_tokens = 65536 on a small layer: 262144 assignments, 32
+    bucketing chunks; bucketing checked whole, outputs on sampled tokens."""
+    w = synth.Workload("maxT", T=65536, H=256, I=128, E=64, k=4, routing="zipf")
+    layer = DeviceLayer(w)
+    x = synth.hidden_bf16(w)
+    ids, tw = synth.routing(w)
+    got = layer.run(x, ids, tw)
+    d = mx.moe_read_dispatch(layer.dims, layer.ws, w.T)
+    counts, offsets, st, sj, bad = oracle.bucket(ids, w.E)
+    assert bad == 0 and np.array_equal(d["counts"], counts)
+    slot = d["assign_slot"]
+    for e in range(w.E):
+        a_sorted = st[offsets[e]:offsets[e + 1]].astype(np.int64) * w.k + sj[offsets[e]:offsets[e + 1]]
+        assert np.all(np.diff(slot[a_sorted]) == 1)
+    from tests.helpers import compact_problem
+    rng = np.random.default_rng(41)
+    tokens = np.unique(np.concatenate([[0, w.T - 1], rng.choice(w.T, 30, replace=False)]))
+    sub_ids, experts = compact_problem(ids, tokens)
+    ref = oracle.moe(x[tokens], sub_ids, tw[tokens], *oracle_expert_weights(w, experts))
+    assert normwise_rel_err(oracle.bf16_bits_to_f64(got[tokens]), ref["out_f64"]) <= 2e-3
