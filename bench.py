@@ -69,8 +69,8 @@ def parse_args():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--dispatch", choices=["bucketed", "pull"], default="bucketed",
                    help="token rows copied per expert by pre_dispatch, or gathered by the layer")
-    p.add_argument("--tiles", choices=["auto", "wide", "narrow"], default="auto",
-                   help="token tiles: 128 rows (wide), 32 rows (narrow) or the layer's choice")
+    p.add_argument("--tiles", choices=["auto", "wide", "medium", "narrow"], default="auto",
+                   help="token tiles: 128 rows (wide), 64 (medium), 32 (narrow) or the layer's choice")
     p.add_argument("--mma", choices=["mxf4xmxf4", "fp8xfp4", "nvf4xnvf4"], default="mxf4xmxf4",
                    help="formats: MXFP4 (W4A4, the headline), MXFP8 activations (W4A8) or NVFP4")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -428,6 +428,7 @@ def run_ours(args):
     ws = torch.empty(mx.moe_workspace_size(dims), dtype=torch.uint8, device=dev)
     mx.moe_workspace_init(dims, ws, stream)
     mx.moe_workspace_set_tiles(ws, {"auto": mx.MOE_TILES_AUTO, "wide": mx.MOE_TILES_WIDE,
+                                    "medium": mx.MOE_TILES_MEDIUM,
                                     "narrow": mx.MOE_TILES_NARROW}[args.tiles])
     mx.moe_workspace_set_dispatch(ws, mx.MOE_DISPATCH_PULL if args.dispatch == "pull"
                                   else mx.MOE_DISPATCH_BUCKETED)

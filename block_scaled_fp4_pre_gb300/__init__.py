@@ -249,6 +249,7 @@ MOE_DISPATCH_PULL = 1
 MOE_TILES_AUTO = 0
 MOE_TILES_WIDE = 1
 MOE_TILES_NARROW = 2
+MOE_TILES_MEDIUM = 3
 
 
 def moe_workspace_set_dispatch(ws, mode: int) -> None:
@@ -257,7 +258,7 @@ def moe_workspace_set_dispatch(ws, mode: int) -> None:
 
 
 def moe_workspace_set_tiles(ws, mode: int) -> None:
-    """Token tiles of 128 rows (wide), 32 rows (narrow) or chosen per dispatch (auto)."""
+    """Token tiles of 128 rows (wide), 64 (medium), 32 (narrow) or chosen per dispatch (auto)."""
     _check(lib().moe_workspace_set_tiles(_ptr(ws), int(mode)))
 
 

@@ -151,7 +151,7 @@ struct WsState {
   bool dispatched;
   int dispatch_mode;   // MOE_DISPATCH_*
   int tile_mode;       // MOE_TILES_*
-  bool narrow;         // the last pre_dispatch's choice of 32-row token tiles
+  int tile_rows;       // the last pre_dispatch's token rows a tile (32, 64 or 128)
 };
 std::mutex g_reg_mu;
 std::map<const void*, WsState> g_registry;
@@ -173,20 +173,20 @@ bool take_dispatch(const void* ws) {
   return fresh;
 }
 
-void mark_dispatched(const void* ws, bool narrow) {
+void mark_dispatched(const void* ws, int tile_rows) {
   std::lock_guard<std::mutex> lk(g_reg_mu);
   auto it = g_registry.find(ws);
   if (it != g_registry.end()) {
     it->second.dispatched = true;
-    it->second.narrow = narrow;
+    it->second.tile_rows = tile_rows;
   }
 }
 
-// Tile choice of a workspace's last pre_dispatch (wide if unknown).
-bool narrow_tiles(const void* ws) {
+// Token rows a tile of a workspace's last pre_dispatch (128 if unknown).
+int tile_rows_of(const void* ws) {
   std::lock_guard<std::mutex> lk(g_reg_mu);
   auto it = g_registry.find(ws);
-  return it != g_registry.end() && it->second.narrow;
+  return it == g_registry.end() ? kBN : it->second.tile_rows;
 }
 
 int tile_mode(const void* ws) {
@@ -195,13 +195,17 @@ int tile_mode(const void* ws) {
   return it == g_registry.end() ? MOE_TILES_AUTO : it->second.tile_mode;
 }
 
-// Narrow tiles when asked for, or (auto) when the experts average at most 16 rows:
-// decode-sized loads, where no tile needs more than a few of the 32 rows.  The pull
-// dispatch gathers into wide tiles only.
-bool choose_narrow(const moe_dims& d, int32_t T, int mode, bool pull) {
-  if (pull || mode == MOE_TILES_WIDE) return false;
-  if (mode == MOE_TILES_NARROW) return true;
-  return (int64_t)T * d.topk <= (int64_t)16 * d.num_experts;
+// Token rows a tile: as asked for, or (auto) by the experts' average rows: up to 16,
+// 32-row tiles (decode-sized loads); up to 64, 64-row tiles; else 128.  Smaller tiles
+// keep more weight bytes in flight but stream an expert's weights once per tile, so
+// each size wins where few experts need more than one tile.  The pull dispatch
+// gathers into 128-row tiles only.
+int choose_tile_rows(const moe_dims& d, int32_t T, int mode, bool pull) {
+  if (pull || mode == MOE_TILES_WIDE) return kBN;
+  if (mode == MOE_TILES_NARROW) return kBNNarrow;
+  if (mode == MOE_TILES_MEDIUM) return kBNMedium;
+  const int64_t rows = (int64_t)T * d.topk, E = d.num_experts;
+  return rows <= 16 * E ? kBNNarrow : rows <= 64 * E ? kBNMedium : kBN;
 }
 
 // Timing hooks.
@@ -314,19 +318,19 @@ moe_status pre_dispatch_impl(const moe_dims* d, const void* x, const int32_t* id
   const WsPtrs p = ws_ptrs(ws, L);
   const Shape s = shape_of(*d);
   const bool pull = dispatch_mode(ws) == MOE_DISPATCH_PULL;
-  const bool narrow = choose_narrow(*d, T, tile_mode(ws), pull);
+  const int tile_rows = choose_tile_rows(*d, T, tile_mode(ws), pull);
   cudaError_t e;
   {
     ProfScope ps("bucket", st);
-    e = launch_bucket(s, ids, T, p, narrow ? kBNNarrow : kBN, st);
+    e = launch_bucket(s, ids, T, p, tile_rows, st);
   }
   if (e != cudaSuccess) return cuda_fail(e, "bucket kernel");
   {
     ProfScope ps("quantize_scatter", st);
-    e = launch_quantize_scatter(s, x, ids, tw, T, p, pull, narrow, st);
+    e = launch_quantize_scatter(s, x, ids, tw, T, p, pull, tile_rows, st);
   }
   if (e != cudaSuccess) return cuda_fail(e, "quantize kernel");
-  mark_dispatched(ws, narrow);
+  mark_dispatched(ws, tile_rows);
   return MOE_OK;
 }
 
@@ -347,7 +351,7 @@ LayerLaunch layer_launch(const moe_dims* d, const void* prepared, void* ws, int3
   g.gate_up_debug = nullptr;
   g.num_sms = sm_count();
   g.pull = dispatch_mode(ws) == MOE_DISPATCH_PULL;
-  g.narrow = narrow_tiles(ws);
+  g.tile_rows = tile_rows_of(ws);
   return g;
 }
 
@@ -426,7 +430,7 @@ moe_status moe_workspace_init(const moe_dims* dims, void* ws, size_t ws_bytes, v
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "workspace header");
   std::lock_guard<std::mutex> lk(g_reg_mu);
-  g_registry[ws] = WsState{*dims, false, MOE_DISPATCH_BUCKETED, MOE_TILES_AUTO, false};
+  g_registry[ws] = WsState{*dims, false, MOE_DISPATCH_BUCKETED, MOE_TILES_AUTO, kBN};
   return MOE_OK;
 }
 
@@ -447,7 +451,8 @@ moe_status moe_workspace_set_dispatch(void* ws, int32_t mode) {
 
 moe_status moe_workspace_set_tiles(void* ws, int32_t mode) {
   if (!ws) return fail(MOE_ERR_INVALID_ARG, "workspace is NULL");
-  if (mode != MOE_TILES_AUTO && mode != MOE_TILES_WIDE && mode != MOE_TILES_NARROW)
+  if (mode != MOE_TILES_AUTO && mode != MOE_TILES_WIDE && mode != MOE_TILES_NARROW &&
+      mode != MOE_TILES_MEDIUM)
     return fail(MOE_ERR_INVALID_ARG, "unknown tile mode %d", mode);
   std::lock_guard<std::mutex> lk(g_reg_mu);
   auto it = g_registry.find(ws);
@@ -683,8 +688,8 @@ moe_status moe_read_dispatch(const moe_dims* dims, const void* ws, int32_t T, in
   } else if (xc_host || xs_host) {
     const size_t rb = (size_t)act_row_bytes(*dims, H);
     const int sfb = (int)sf_row_bytes(*dims, H);
-    const bool narrow = narrow_tiles(ws);
-    std::vector<uint8_t> codes((size_t)R * rb), sf((size_t)R * sfb * (narrow ? 4 : 1));
+    const int tr = tile_rows_of(ws);
+    std::vector<uint8_t> codes((size_t)R * rb), sf((size_t)R * sfb * (kBN / tr));
     if (R && (e = cudaMemcpy(codes.data(), b + L.off_xb, codes.size(), cudaMemcpyDeviceToHost)))
       return cuda_fail(e, "codes read");
     if (R && (e = cudaMemcpy(sf.data(), b + L.off_xsf, sf.size(), cudaMemcpyDeviceToHost)))
@@ -700,7 +705,7 @@ moe_status moe_read_dispatch(const moe_dims* dims, const void* ws, int32_t T, in
       }
       if (xs_host)
         for (int g = 0; g < sfb; ++g)
-          xs_host[a * sfb + g] = ok ? sf[sf_tile_offset((size_t)r, g, sfb / 4, narrow)] : 0;
+          xs_host[a * sfb + g] = ok ? sf[sf_tile_offset((size_t)r, g, sfb / 4, tr)] : 0;
     }
   }
   return MOE_OK;
@@ -728,8 +733,8 @@ moe_status moe_read_intermediate(const moe_dims* dims, const void* ws, int32_t T
   if (R < 0 || R > L.R_cap) return fail(MOE_ERR_CUDA, "corrupt segment table");
   const size_t rb = (size_t)act_row_bytes(*dims, I);
   const int sfb = (int)sf_row_bytes(*dims, I);
-  const bool narrow = narrow_tiles(ws);
-  std::vector<uint8_t> codes((size_t)R * rb), sf((size_t)R * sfb * (narrow ? 4 : 1));
+  const int tr = tile_rows_of(ws);
+  std::vector<uint8_t> codes((size_t)R * rb), sf((size_t)R * sfb * (kBN / tr));
   if (R && (e = cudaMemcpy(codes.data(), b + L.off_hb, codes.size(), cudaMemcpyDeviceToHost)))
     return cuda_fail(e, "codes read");
   if (R && (e = cudaMemcpy(sf.data(), b + L.off_hsf, sf.size(), cudaMemcpyDeviceToHost)))
@@ -745,7 +750,7 @@ moe_status moe_read_intermediate(const moe_dims* dims, const void* ws, int32_t T
     }
     if (hs_host)
       for (int g = 0; g < sfb; ++g)
-        hs_host[a * sfb + g] = ok ? sf[sf_tile_offset((size_t)r, g, sfb / 4, narrow)] : 0;
+        hs_host[a * sfb + g] = ok ? sf[sf_tile_offset((size_t)r, g, sfb / 4, tr)] : 0;
   }
   return MOE_OK;
 }

@@ -23,10 +23,11 @@ constexpr int kBTileBytes = kBN * kBKBytes;   // 16 KiB
 constexpr int kBBoxRows = 32;                 // token rows per TMA box
 constexpr int kSFAtomBytes = 512;             // 128 rows x 4 scale bytes
 constexpr int kSFStageBytes = 2 * kSFAtomBytes;  // 8 scale columns per k-block
-// Narrow tiles for decode-sized loads (few tokens per expert): 32 token rows a tile,
-// expert segments padded to 32 rows, each tile's token scales in 128x4 blocks of its
-// own (its rows in the first quarter of each block).
+// Narrower token tiles for lighter loads: 32 (decode-sized) or 64 token rows a tile,
+// expert segments padded to that many rows, each tile's token scales in 128x4 blocks
+// of its own (its rows in the first quarter or half of each block).
 constexpr int kBNNarrow = 32;
+constexpr int kBNMedium = 64;
 
 // Device error bits in ws.flags[0].
 constexpr int kErrRouting = 1;
@@ -77,12 +78,14 @@ __host__ __device__ __forceinline__ int gate_up_source_row_for(int r, int I, int
   return f8 ? gate_up_source_row8(r, I) : gate_up_source_row(r, I);
 }
 
-// Byte of token-side scale (row, scale column s) in a workspace of wide (128-row) or
-// narrow (32-row) tiles: a narrow tile of rows 32t..32t+31 owns its scale blocks,
-// with row r in line r % 32 and the first 4-byte word of it.
-__host__ __device__ __forceinline__ size_t sf_tile_offset(size_t row, int s, int kc4, int narrow) {
-  if (!narrow) return sf_atom_offset(row, s, kc4);
-  return (((row >> 5) * (size_t)kc4 + (size_t)(s >> 2)) << 9) + ((row & 31) << 4) + (size_t)(s & 3);
+// Byte of token-side scale (row, scale column s) in a workspace of tiles of tile_rows
+// rows (32, 64 or 128): the tile of rows tile_rows*t.. owns its scale blocks, with its
+// row r in line r % 32, 4-byte word r / 32.  For 128-row tiles this is sf_atom_offset.
+__host__ __device__ __forceinline__ size_t sf_tile_offset(size_t row, int s, int kc4,
+                                                          int tile_rows) {
+  const size_t tile = row / (size_t)tile_rows, r = row % (size_t)tile_rows;
+  return ((tile * (size_t)kc4 + (size_t)(s >> 2)) << 9) + ((r & 31) << 4) + ((r >> 5) << 2) +
+         (size_t)(s & 3);
 }
 
 // ---------------------------------------------------------------------------
@@ -154,16 +157,16 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 // of its launch.
 // Bucketing: per-expert counts and segment starts, the tile list, and each
 // assignment's rank; the quantiser (or launch_assign_slots) turns ranks into rows.
-// tile_rows: kBN (wide tiles) or kBNNarrow.
+// tile_rows: kBN (wide tiles), kBNMedium or kBNNarrow.
 cudaError_t launch_bucket(const Shape& s, const int32_t* ids, int T, const WsPtrs& ws,
                           int tile_rows, cudaStream_t st);
 // Quantise the tokens, give every assignment its row and copy the token there.
 // pull: write each token's row once (xq/xs) instead of copying it to its k rows; the
 // layer kernel then gathers token rows itself.
-// narrow: token scales in the narrow-tile layout (sf_tile_offset).
+// tile_rows: token scales in the layout of tiles of that many rows (sf_tile_offset).
 cudaError_t launch_quantize_scatter(const Shape& s, const void* x, const int32_t* ids,
                                     const float* tw, int T, const WsPtrs& ws, bool pull,
-                                    bool narrow, cudaStream_t st);
+                                    int tile_rows, cudaStream_t st);
 // Rows of all assignments and the per-row tables, without quantising anything.
 cudaError_t launch_assign_slots(const Shape& s, const int32_t* ids, const float* tw, int T,
                                 const WsPtrs& ws, cudaStream_t st);
@@ -206,7 +209,7 @@ struct LayerLaunch {
   float* gate_up_debug;      // [T*k, 2I] (num_phases == 1)
   int num_sms;
   bool pull;                 // gate/up token rows gathered from ws.xq/xs (pull dispatch)
-  bool narrow;               // 32-row token tiles (the dispatch's choice)
+  int tile_rows;             // token rows a tile: 32, 64 or 128 (the dispatch's choice)
 };
 cudaError_t launch_layer(const LayerLaunch& g, cudaStream_t st);
 

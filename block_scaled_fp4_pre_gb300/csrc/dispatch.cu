@@ -24,8 +24,8 @@ constexpr unsigned kFull = 0xFFFFFFFFu;
 // them advances the warp's count for that expert, and a scan over warps turns the
 // counts into each warp's base.  Each block publishes its per-expert totals; the
 // last block to finish scans them over blocks (bases of later chunks) and over
-// experts (segment starts padded to tile_rows -- kBN, or kBNNarrow for narrow tiles --
-// and the tile list).  Row of an assignment =
+// experts (segment starts padded to tile_rows -- kBN, kBNMedium or kBNNarrow -- and
+// the tile list).  Row of an assignment =
 // segment start + its chunk's base + its rank in the chunk.
 
 // Lanes whose key equals this lane's key (keys < 2^nbits): one ballot per bit, which
@@ -254,7 +254,7 @@ __global__ void __launch_bounds__(256) quantize_scatter_kernel(const __nv_bfloat
                                                                const int32_t* __restrict__ ids,
                                                                const float* __restrict__ tw,
                                                                int H, int k, int E, WsPtrs ws,
-                                                               bool pull, int narrow) {
+                                                               bool pull, int tile_rows) {
   constexpr bool F8 = FMT == kTokMxfp8, NV = FMT == kTokNvfp4;
   constexpr int kBytesPer8 = F8 ? 8 : 4;                // code bytes of 8 elements
   constexpr int kGroup = NV ? 16 : 32;                  // elements per scale
@@ -342,7 +342,7 @@ __global__ void __launch_bounds__(256) quantize_scatter_kernel(const __nv_bfloat
     for (int i = tid; i < row_bytes_q / 16; i += blockDim.x)   // 16-byte chunks of the row
       dst[i] = reinterpret_cast<const uint4*>(codes_sh)[i];
     for (int i = tid; i < nsf; i += blockDim.x)
-      ws.xsf[sf_tile_offset((size_t)slot, i, kc4, narrow)] = sf_sh[i];
+      ws.xsf[sf_tile_offset((size_t)slot, i, kc4, tile_rows)] = sf_sh[i];
   }
 }
 
@@ -494,7 +494,7 @@ cudaError_t launch_bucket(const Shape& s, const int32_t* ids, int T, const WsPtr
 
 cudaError_t launch_quantize_scatter(const Shape& s, const void* x, const int32_t* ids,
                                     const float* tw, int T, const WsPtrs& ws, bool pull,
-                                    bool narrow, cudaStream_t st) {
+                                    int tile_rows, cudaStream_t st) {
   const size_t smem = (size_t)(s.f8 ? s.H : s.H / 2) + s.H / sf_group(s);
   auto kern = s.f8   ? quantize_scatter_kernel<kTokMxfp8>
               : s.nv ? quantize_scatter_kernel<kTokNvfp4>
@@ -505,7 +505,7 @@ cudaError_t launch_quantize_scatter(const Shape& s, const void* x, const int32_t
     if (e != cudaSuccess) return e;
   }
   return launch_pdl(kern, dim3(T), dim3(256), smem, st, reinterpret_cast<const __nv_bfloat16*>(x),
-                    ids, tw, s.H, s.k, s.E, ws, pull, narrow ? 1 : 0);
+                    ids, tw, s.H, s.k, s.E, ws, pull, tile_rows);
 }
 
 cudaError_t launch_assign_slots(const Shape& s, const int32_t* ids, const float* tw, int T,

@@ -44,8 +44,8 @@ namespace mxmoe {
 namespace {
 
 constexpr int kStages = 3;                 // wide token tiles
-constexpr int kStagesNarrow = 4;           // narrow (32-row) token tiles
-constexpr int kStagesNarrowF8 = 5;         // narrow, E4M3 tokens: one scale block a stage
+constexpr int kStagesNarrow = 4;           // 32- and 64-row token tiles
+constexpr int kStagesNarrowF8 = 5;         // 32-row tiles, E4M3 tokens: one scale block a stage
 constexpr int kMaxStages = kStagesNarrowF8;
 constexpr int kThreads = 192;
 constexpr int kBlocksPerSM = 2;
@@ -96,12 +96,16 @@ struct __align__(16) SmemTail {
 
 // Shared-memory map: kSt stages x (weight box, token boxes, both operands' scale
 // blocks: 2 per k-block, 4 for NVFP4, 1 for the 128-element k-blocks of E4M3 tokens),
-// then the tail.  Narrow tiles need a quarter of the token room, which pays for a
-// fourth stage (a fifth with E4M3 tokens, whose weight boxes carry half the bytes).
-template <bool NV, bool NARROW, bool F8>
+// then the tail.  Tiles of 32 or 64 rows need a quarter or half of the token room,
+// which pays for a fourth stage (a fifth for 32-row tiles of E4M3 tokens, whose weight
+// boxes carry half the bytes; NVFP4's larger scale blocks leave 64-row tiles at three).
+template <bool NV, int TROWS, bool F8>
 struct SmemMap {
-  static constexpr int kSt = NARROW ? (F8 ? kStagesNarrowF8 : kStagesNarrow) : kStages;
-  static constexpr int kBRows = NARROW ? kBNNarrow : kBN;        // token rows a stage holds
+  static constexpr int kSt = TROWS == kBN                 ? kStages
+                             : TROWS == kBNNarrow && F8    ? kStagesNarrowF8
+                             : TROWS == kBNMedium && NV    ? kStages
+                                                           : kStagesNarrow;
+  static constexpr int kBRows = TROWS;                           // token rows a stage holds
   static constexpr size_t kBSlot = (size_t)kBRows * kBKBytes;
   static constexpr size_t kSF = (size_t)(NV ? 4 : F8 ? 1 : 2) * kSFAtomBytes;
   static constexpr size_t kA = 0;
@@ -109,8 +113,8 @@ struct SmemMap {
   static constexpr size_t kSFA = kB + (size_t)kSt * kBSlot;
   static constexpr size_t kSFB = kSFA + (size_t)kSt * kSF;
   static constexpr size_t kTail = kSFB + (size_t)kSt * kSF;
-  // NVFP4's scale blocks and the fifth narrow E4M3 stage take the tile table's room
-  static constexpr bool kGlobalTiles = NV || (NARROW && F8);
+  // NVFP4's scale blocks and the fifth 32-row E4M3 stage take the tile table's room
+  static constexpr bool kGlobalTiles = NV || (TROWS == kBNNarrow && F8);
   static constexpr size_t kBytes = kTail + sizeof(SmemTail<kGlobalTiles>) + 1024;  // + slack
   // two blocks per SM (228 KiB of shared memory, 1 KiB of it reserved per block)
   static_assert(2 * (kBytes + 1024) <= 228 * 1024, "two blocks per SM");
@@ -179,8 +183,8 @@ __device__ __forceinline__ float silu_times(float g, float u) {
 // packed E2M1 throughout, 256 elements a k-block, kind::mxf4 MMAs, gran=16.
 // NV: nvf4xnvf4 -- as mxf4xmxf4 with one E4M3 scale per 16 elements (four scale
 // blocks per k-block and operand), kind::mxf4nvf4 MMAs, NVFP4 requantisation.
-// NARROW: 32-row token tiles (a quarter of the token room, four stages).
-template <int MODE, bool PULL, bool F8, bool NV, bool NARROW>
+// TROWS: token rows a tile (128, or 64 / 32 for lighter loads, with more stages).
+template <int MODE, bool PULL, bool F8, bool NV, int TROWS>
 __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
     moe_layer_kernel(const __grid_constant__ CUtensorMap tmap_w1,
                      const __grid_constant__ CUtensorMap tmap_x,
@@ -191,7 +195,7 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  using SM = SmemMap<NV, NARROW, F8>;
+  using SM = SmemMap<NV, TROWS, F8>;
   constexpr int kSt = SM::kSt;
   using TM = TmemMap<NV>;
   SmemTail<SM::kGlobalTiles>* tail = reinterpret_cast<SmemTail<SM::kGlobalTiles>*>(smem + SM::kTail);
@@ -328,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
       const int mt = it.mt;   // the item's weight slab
       const int wrow = e * P.rows_per_expert + mt * kBM;
       const uint8_t* wsf = P.w_sf + ((size_t)(e * P.m_tiles + mt) * P.kc4) * kSFAtomBytes;
-      // the tile's token scale blocks (each narrow tile has blocks of its own)
+      // the tile's token scale blocks (each tile has blocks of its own)
       const uint8_t* tsf = P.t_sf + ((size_t)(row0 / SM::kBRows) * P.kc4) * kSFAtomBytes;
       // Pulled token rows: lane l gathers rows l, l+32, l+64, l+96 of the tile.
       const bool pulled = PULL && it.phase == 0;
@@ -688,7 +692,7 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
                 const size_t row = (size_t)row0 + c0 + jc;
                 const uint16_t sv = *reinterpret_cast<const uint16_t*>(&tail->sstage[xb][jc][0]);
                 *reinterpret_cast<uint16_t*>(args.ws.hsf +
-                                             sf_tile_offset(row, mt * 2, i_kc4, NARROW)) = sv;
+                                             sf_tile_offset(row, mt * 2, i_kc4, TROWS)) = sv;
               }
             }
           } else if (lane < 8) {
@@ -706,11 +710,11 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
               if (NV) {   // the item's four scale bytes: one 32-bit word of a scale block
                 const uint32_t sv = *reinterpret_cast<const uint32_t*>(&tail->sstage[xb][jc][0]);
                 *reinterpret_cast<uint32_t*>(args.ws.hsf +
-                                             sf_tile_offset(row, mt * 4, i_kc4, NARROW)) = sv;
+                                             sf_tile_offset(row, mt * 4, i_kc4, TROWS)) = sv;
               } else {
                 const uint16_t sv = *reinterpret_cast<const uint16_t*>(&tail->sstage[xb][jc][0]);
                 *reinterpret_cast<uint16_t*>(args.ws.hsf +
-                                             sf_tile_offset(row, mt * 2, i_kc4, NARROW)) = sv;
+                                             sf_tile_offset(row, mt * 2, i_kc4, TROWS)) = sv;
               }
             }
           }
@@ -914,13 +918,13 @@ PhaseArgs phase_args(const uint8_t* w_sf, const uint8_t* t_sf, int rows_per_expe
   return p;
 }
 
-template <int MODE, bool PULL, bool F8, bool NV, bool NARROW>
+template <int MODE, bool PULL, bool F8, bool NV, int TROWS>
 cudaError_t launch_mode(const LayerLaunch& g, const CUtensorMap* maps, const LayerArgs& a,
                         cudaStream_t st) {
-  constexpr size_t kSmemBytes = SmemMap<NV, NARROW, F8>::kBytes;
+  constexpr size_t kSmemBytes = SmemMap<NV, TROWS, F8>::kBytes;
   static int grid = 0;   // per instantiation, for the device of the first launch
   if (grid == 0) {
-    cudaError_t err = cudaFuncSetAttribute(moe_layer_kernel<MODE, PULL, F8, NV, NARROW>,
+    cudaError_t err = cudaFuncSetAttribute(moe_layer_kernel<MODE, PULL, F8, NV, TROWS>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)kSmemBytes);
     if (err != cudaSuccess) return err;
@@ -928,9 +932,23 @@ cudaError_t launch_mode(const LayerLaunch& g, const CUtensorMap* maps, const Lay
     // resident blocks)
     grid = kBlocksPerSM * g.num_sms;
   }
-  return launch_pdl(moe_layer_kernel<MODE, PULL, F8, NV, NARROW>, dim3(grid), dim3(kThreads),
+  return launch_pdl(moe_layer_kernel<MODE, PULL, F8, NV, TROWS>, dim3(grid), dim3(kThreads),
                     kSmemBytes, st,
                     maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], a);
+}
+
+// The format's instantiation for tiles of TROWS rows.
+template <int TROWS>
+cudaError_t launch_fmt(const LayerLaunch& g, const CUtensorMap* maps, const LayerArgs& a,
+                       cudaStream_t st, bool layer, bool f8, bool nv) {
+  if (f8)
+    return layer ? launch_mode<kModeLayer, false, true, false, TROWS>(g, maps, a, st)
+                 : launch_mode<kModeRaw, false, true, false, TROWS>(g, maps, a, st);
+  if (nv)
+    return layer ? launch_mode<kModeLayer, false, false, true, TROWS>(g, maps, a, st)
+                 : launch_mode<kModeRaw, false, false, true, TROWS>(g, maps, a, st);
+  return layer ? launch_mode<kModeLayer, false, false, false, TROWS>(g, maps, a, st)
+               : launch_mode<kModeRaw, false, false, false, TROWS>(g, maps, a, st);
 }
 
 }  // namespace
@@ -942,9 +960,10 @@ cudaError_t launch_layer(const LayerLaunch& g, cudaStream_t st) {
   // Activation rows: packed E2M1 (K/2 bytes) or E4M3 (K bytes).
   const uint64_t xrow = f8 ? (uint64_t)s.H : (uint64_t)s.H / 2;
   const uint64_t hrow = f8 ? (uint64_t)s.I : (uint64_t)s.I / 2;
-  // Full token tiles come in one box of all their rows (128, or 32 when narrow).
-  const bool narrow = g.narrow && !g.pull;
-  const uint32_t full_rows = narrow ? kBNNarrow : kBN;
+  // Full token tiles come in one box of all their rows (128, 64 or 32).
+  const int trows = g.pull ? kBN : g.tile_rows;
+  if (trows != kBN && trows != kBNMedium && trows != kBNNarrow) return cudaErrorInvalidValue;
+  const uint32_t full_rows = (uint32_t)trows;
   CUtensorMap maps[6];
   cudaError_t err;
   if ((err = make_tmap(&maps[4], g.ws.xb, xrow, (uint64_t)g.R_cap, full_rows)) ||
@@ -975,26 +994,11 @@ cudaError_t launch_layer(const LayerLaunch& g, cudaStream_t st) {
   a.gate_up_debug = g.gate_up_debug;
   const bool layer = g.num_phases == 2;
   if (g.pull)
-    return layer ? launch_mode<kModeLayer, true, false, false, false>(g, maps, a, st)
-                 : launch_mode<kModeRaw, true, false, false, false>(g, maps, a, st);
-  if (narrow) {
-    if (f8)
-      return layer ? launch_mode<kModeLayer, false, true, false, true>(g, maps, a, st)
-                   : launch_mode<kModeRaw, false, true, false, true>(g, maps, a, st);
-    if (nv)
-      return layer ? launch_mode<kModeLayer, false, false, true, true>(g, maps, a, st)
-                   : launch_mode<kModeRaw, false, false, true, true>(g, maps, a, st);
-    return layer ? launch_mode<kModeLayer, false, false, false, true>(g, maps, a, st)
-                 : launch_mode<kModeRaw, false, false, false, true>(g, maps, a, st);
-  }
-  if (f8)
-    return layer ? launch_mode<kModeLayer, false, true, false, false>(g, maps, a, st)
-                 : launch_mode<kModeRaw, false, true, false, false>(g, maps, a, st);
-  if (nv)
-    return layer ? launch_mode<kModeLayer, false, false, true, false>(g, maps, a, st)
-                 : launch_mode<kModeRaw, false, false, true, false>(g, maps, a, st);
-  return layer ? launch_mode<kModeLayer, false, false, false, false>(g, maps, a, st)
-               : launch_mode<kModeRaw, false, false, false, false>(g, maps, a, st);
+    return layer ? launch_mode<kModeLayer, true, false, false, kBN>(g, maps, a, st)
+                 : launch_mode<kModeRaw, true, false, false, kBN>(g, maps, a, st);
+  if (trows == kBNNarrow) return launch_fmt<kBNNarrow>(g, maps, a, st, layer, f8, nv);
+  if (trows == kBNMedium) return launch_fmt<kBNMedium>(g, maps, a, st, layer, f8, nv);
+  return launch_fmt<kBN>(g, maps, a, st, layer, f8, nv);
 }
 
 }  // namespace mxmoe

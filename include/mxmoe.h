@@ -137,13 +137,15 @@ MXMOE_API moe_status moe_workspace_set_dispatch(void *ws_dev, int32_t mode);
  *   MOE_TILES_NARROW: up to 32 rows a tile (segments padded to 32); the layer then
  *                     keeps four stages of operands in flight instead of three,
  *                     which pays when experts hold few tokens (decode-sized loads).
+ *   MOE_TILES_MEDIUM: up to 64 rows a tile (segments padded to 64), four stages where
+ *                     shared memory allows (three for nvf4xnvf4).
  *   MOE_TILES_AUTO (default after moe_workspace_init): narrow when num_tokens * k <=
- *                     16 * num_experts, else wide.
+ *                     16 * num_experts, medium when <= 64 * num_experts, else wide.
  * The choice is made at each moe_pre_dispatch and holds for the forward that
  * follows; results are the same either way up to fp32 summation order.  The pull
  * dispatch always uses wide tiles.  MOE_ERR_INVALID_ARG for an unknown mode,
  * MOE_ERR_WORKSPACE_MISMATCH for a workspace moe_workspace_init has not seen. */
-enum { MOE_TILES_AUTO = 0, MOE_TILES_WIDE = 1, MOE_TILES_NARROW = 2 };
+enum { MOE_TILES_AUTO = 0, MOE_TILES_WIDE = 1, MOE_TILES_NARROW = 2, MOE_TILES_MEDIUM = 3 };
 MXMOE_API moe_status moe_workspace_set_tiles(void *ws_dev, int32_t mode);
 
 /* Quantises row-major fp32 src_dev [rows, K] (K % 32 == 0) to MXFP4 with the rule

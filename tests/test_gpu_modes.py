@@ -66,7 +66,7 @@ def test_graph_replay_and_host_path(mma):
     assert normwise_rel_err(oracle.bf16_bits_to_f64(oh.numpy().view(np.uint16)), ref["out_f64"]) <= 2e-3
 
 
-@pytest.mark.parametrize("tiles", [mx.MOE_TILES_NARROW, mx.MOE_TILES_WIDE])
+@pytest.mark.parametrize("tiles", [mx.MOE_TILES_NARROW, mx.MOE_TILES_MEDIUM, mx.MOE_TILES_WIDE])
 @pytest.mark.parametrize("mma", list(MMAS))
 def test_edge_token_counts_and_one_expert(mma, tiles):
     layer, layer_fn, Wts = _setup(mma)

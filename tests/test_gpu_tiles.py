@@ -1,6 +1,7 @@
-"""Narrow (32-row) against wide (128-row) token tiles, for every mma type.
+"""Narrow (32-row) and medium (64-row) against wide (128-row) token tiles, for every
+mma type.
 
-Narrow tiles change how token rows are grouped into MMA operands and how many stages
+Smaller tiles change how token rows are grouped into MMA operands and how many stages
 the layer keeps in flight, not what it computes: each output column's K reduction is
 the same, so the gate/up accumulators and the requantised intermediate must be
 bit-identical, the outputs equal up to the order of the fp32 combine reductions, and
@@ -41,7 +42,7 @@ def test_narrow_tiles_match_wide_tiles(name, mma):
     x = synth.hidden_bf16(w)
     ids, tw = synth.routing(w)
     res = {}
-    for mode in (mx.MOE_TILES_WIDE, mx.MOE_TILES_NARROW):
+    for mode in (mx.MOE_TILES_WIDE, mx.MOE_TILES_MEDIUM, mx.MOE_TILES_NARROW):
         mx.moe_workspace_set_tiles(layer.ws, mode)
         mx.moe_pre_dispatch(layer.dims, to_dev(x), to_dev(ids), to_dev(tw), w.T, layer.ws)
         gu = torch.full((w.T * w.k, 2 * w.I), float("nan"), dtype=torch.float32, device=device())
@@ -51,16 +52,18 @@ def test_narrow_tiles_match_wide_tiles(name, mma):
         res[mode] = (gu.cpu().numpy(), got, mx.moe_read_intermediate(layer.dims, layer.ws, w.T),
                      mx.moe_read_dispatch(layer.dims, layer.ws, w.T))
     gw, ow, iw, dw = res[mx.MOE_TILES_WIDE]
-    gn, on, inn, dn = res[mx.MOE_TILES_NARROW]
-    assert np.array_equal(gn, gw)
-    assert np.array_equal(inn["h_codes"], iw["h_codes"])
-    assert np.array_equal(inn["h_scales"], iw["h_scales"])
-    assert np.array_equal(dn["x_codes"], dw["x_codes"]) and np.array_equal(dn["x_scales"], dw["x_scales"])
-    assert np.array_equal(dn["counts"], dw["counts"])
-    assert normwise_rel_err(oracle.bf16_bits_to_f64(on), oracle.bf16_bits_to_f64(ow)) <= 1e-3
     layer_fn, weights = ORACLE[mma]
     ref = layer_fn(x, ids, tw, *weights(w, range(w.E)))
-    assert normwise_rel_err(oracle.bf16_bits_to_f64(on), ref["out_f64"]) <= 2e-3
+    for mode in (mx.MOE_TILES_MEDIUM, mx.MOE_TILES_NARROW):
+        gn, on, inn, dn = res[mode]
+        assert np.array_equal(gn, gw)
+        assert np.array_equal(inn["h_codes"], iw["h_codes"])
+        assert np.array_equal(inn["h_scales"], iw["h_scales"])
+        assert np.array_equal(dn["x_codes"], dw["x_codes"])
+        assert np.array_equal(dn["x_scales"], dw["x_scales"])
+        assert np.array_equal(dn["counts"], dw["counts"])
+        assert normwise_rel_err(oracle.bf16_bits_to_f64(on), oracle.bf16_bits_to_f64(ow)) <= 1e-3
+        assert normwise_rel_err(oracle.bf16_bits_to_f64(on), ref["out_f64"]) <= 2e-3
 
 
 def test_tile_mode_argument_checks():
