@@ -321,7 +321,8 @@ MXMOE_API int32_t moe_device_sm_count(void);
  *   assign_slot_dev  int32 [T*k]  row of assignment t*k+j in the expert-grouped order
  *                                 (experts' rows start at multiples of 128, tokens
  *                                 ascending inside an expert; -1 for ids outside [0, E))
- * -- the values moe_pre_dispatch stores in a workspace (see moe_read_dispatch).
+ * -- the values moe_pre_dispatch stores in a workspace set to MOE_TILES_WIDE (see
+ * moe_read_dispatch).
  * The kernel's other buffers live in a static device array of the library, about
  * 0.5 MiB, which every GPU that loads the library holds until the process exits.
  * Limits: num_experts <= 256 and num_tokens * topk <= 8192; larger sizes return

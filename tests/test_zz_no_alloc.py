@@ -31,6 +31,8 @@ def _dev(a):
 def _existing_path(dims, ws, ids, tw):
     T = ids.shape[0]
     x = torch.zeros((T, dims.hidden), dtype=torch.bfloat16, device="cuda")
+    # moe_bucket_noalloc lays rows out in 128-row tiles; pre_dispatch then must too
+    mx.moe_workspace_set_tiles(ws, mx.MOE_TILES_WIDE)
     mx.moe_pre_dispatch(dims, x, _dev(ids), _dev(tw), T, ws)
     d = mx.moe_read_dispatch(dims, ws, T)
     return d["counts"], d["assign_slot"]
