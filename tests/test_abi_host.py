@@ -152,3 +152,22 @@ def test_mxfp8_producer_and_dispatch_mode_host_checks(mx):
     assert lib.moe_workspace_set_dispatch(fake, 5) == mx.MOE_ERR_INVALID_ARG
     assert lib.moe_workspace_set_dispatch(None, 1) == mx.MOE_ERR_INVALID_ARG
     assert lib.moe_workspace_set_dispatch(fake, 1) == mx.MOE_ERR_WORKSPACE_MISMATCH
+
+
+def test_tile_mode_and_nvfp4_quantiser_host_checks(mx):
+    """The tile-mode setter and the NVFP4 weight quantiser reject bad arguments on the
+    host, before any CUDA call."""
+    lib = mx.lib()
+    fake = 1 << 20
+    assert lib.moe_workspace_set_tiles(fake, 9) == mx.MOE_ERR_INVALID_ARG
+    assert lib.moe_workspace_set_tiles(None, mx.MOE_TILES_NARROW) == mx.MOE_ERR_INVALID_ARG
+    assert lib.moe_workspace_set_tiles(fake, mx.MOE_TILES_MEDIUM) == mx.MOE_ERR_WORKSPACE_MISMATCH
+    for rows, K, src in ((4, 24, fake), (-1, 32, fake), (4, 32, fake + 4)):
+        assert lib.moe_quantize_nvfp4(src, rows, K, fake, fake, None) == mx.MOE_ERR_INVALID_ARG
+    assert lib.moe_quantize_nvfp4(fake, 0, 32, fake, fake, None) == mx.MOE_OK   # no rows: no-op
+    # the three mma types' workspaces: E4M3 rows take more room, NVFP4 scales twice
+    # the bytes of MXFP4's; all accept the same dims otherwise
+    sizes = [mx.moe_workspace_size(mx.make_dims(4096, 2048, 256, 6, 512, m))
+             for m in (mx.MOE_MMA_MXF4xMXF4, mx.MOE_MMA_FP8xFP4, mx.MOE_MMA_NVF4xNVF4)]
+    assert all(v > 0 for v in sizes)
+    assert sizes[1] > sizes[0] and sizes[2] > sizes[0]
