@@ -107,7 +107,7 @@ MXMOE_API size_t moe_prepared_weights_size(const moe_dims *dims);
 
 /* Bytes of the workspace for dims->max_tokens tokens; 0 for bad dims.  Host only.
  * (The pages' symmetric buffer sized by num_max_tokens_per_rank, one per
- * mma_type; this build is single-GPU, so it is plain device memory.) */
+ * mma_type; this library runs on one GPU, so it is plain device memory.) */
 MXMOE_API size_t moe_workspace_size(const moe_dims *dims);
 
 /* Initialises a workspace: clears it and records dims and mma_type in its header
