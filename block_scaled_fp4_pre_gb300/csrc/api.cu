@@ -122,25 +122,27 @@ WsPtrs ws_ptrs(void* ws, const WsLayout& L) {
   return p;
 }
 
+Shape shape_of(const moe_dims& d) {
+  return Shape{d.hidden, d.inter, d.num_experts, d.topk, d.mma_type == MOE_MMA_FP8xFP4 ? 1 : 0,
+               d.mma_type == MOE_MMA_NVF4xNVF4 ? 1 : 0};
+}
+
+// Codes in k-block tiles (weight_code_bytes), then the scales in 128x4 blocks.
 PrepLayout prep_layout(const moe_dims& d) {
   PrepLayout P;
   const size_t H = d.hidden, I = d.inter, E = d.num_experts;
+  const Shape s = shape_of(d);
   size_t o = 0;
   P.off_w1c = o;
-  o = align_up(o + E * 2 * I * H / 2, kAlign);
+  o = align_up(o + (size_t)weight_code_bytes(s, (int64_t)(E * 2 * I), (int64_t)H), kAlign);
   P.off_w1s = o;
   o = align_up(o + E * 2 * I * (size_t)sf_row_bytes(d, (int64_t)H), kAlign);
   P.off_w2c = o;
-  o = align_up(o + E * H * I / 2, kAlign);
+  o = align_up(o + (size_t)weight_code_bytes(s, (int64_t)(E * H), (int64_t)I), kAlign);
   P.off_w2s = o;
   o = align_up(o + E * H * (size_t)sf_row_bytes(d, (int64_t)I), kAlign);
   P.total = o;
   return P;
-}
-
-Shape shape_of(const moe_dims& d) {
-  return Shape{d.hidden, d.inter, d.num_experts, d.topk, d.mma_type == MOE_MMA_FP8xFP4 ? 1 : 0,
-               d.mma_type == MOE_MMA_NVF4xNVF4 ? 1 : 0};
 }
 
 // Workspaces initialised by moe_workspace_init, with the dims they were laid out for

@@ -133,6 +133,24 @@ struct Shape {
 // Elements per scale of the format: 16 (NVFP4) or 32 (MXFP4, MXFP8).
 __host__ __device__ __forceinline__ int sf_group(const Shape& s) { return s.nv ? 16 : 32; }
 
+// Prepared weight codes are stored in k-block tiles: the 128 rows of one weight slab
+// over one k-block are contiguous, row after row, so each TMA box of the layer
+// kernel reads one contiguous 16 KiB (8 KiB for fp8xfp4) run of memory.  A tile row
+// holds one k-block's packed E2M1 bytes: 128 (256 elements) or, for fp8xfp4, whose
+// k-blocks are 128 elements, 64.  Byte j of weight row R of a matrix with K elements
+// a row sits at ((R / 128 * num_kb + j / kb_bytes) * 128 + R % 128) * kb_bytes +
+// j % kb_bytes; a last k-block shorter than the others is zero-padded to full width.
+__host__ __device__ __forceinline__ int weight_kb_bytes(const Shape& s) { return s.f8 ? 64 : 128; }
+__host__ __device__ __forceinline__ int64_t weight_num_kb(const Shape& s, int64_t K) {
+  const int64_t elems = 2 * (int64_t)weight_kb_bytes(s);
+  return (K + elems - 1) / elems;
+}
+// Bytes of the tiled codes of `rows` weight rows (a multiple of 128) of K elements.
+__host__ __device__ __forceinline__ int64_t weight_code_bytes(const Shape& s, int64_t rows,
+                                                              int64_t K) {
+  return rows * weight_num_kb(s, K) * weight_kb_bytes(s);
+}
+
 // Launch with programmatic stream serialisation: the kernel may start before the
 // previous kernel in the stream finishes and must call ptx::pdl_wait() before it
 // touches that kernel's output.

@@ -399,20 +399,29 @@ __global__ void quantize_rows_nv_kernel(const float* __restrict__ src, int64_t n
   }
 }
 
-// Row copy with the optional gate/up interleave (interleave: 0 none, 16 or 8 the
-// granule): 16 bytes per thread.
-__global__ void copy_rows_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst,
-                                 int64_t total_chunks, int chunks_per_row, int rows_per_expert,
-                                 int I, int interleave) {
+// Canonical codes [E*rows, row_bytes] -> k-block tiles (the layout of
+// weight_code_bytes), with the optional gate/up interleave (interleave: 0 none, 16 or
+// 8 the granule): 16 bytes per thread, written in tile order.  Bytes past a row's
+// end (a short last k-block) are zero.
+__global__ void tile_codes_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst,
+                                  int64_t total_chunks, int row_bytes, int kb_bytes, int num_kb,
+                                  int rows_per_expert, int I, int interleave) {
+  const int cpr = kb_bytes / 16;   // 16-byte chunks a tile row
   for (int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; c < total_chunks;
        c += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t row = c / chunks_per_row;
-    const int part = (int)(c % chunks_per_row);
+    const int part = (int)(c % cpr);
+    const int64_t trow = c / cpr;                     // tile row, over all tiles
+    const int64_t tile = trow >> 7;
+    const int kb = (int)(tile % num_kb);
+    const int64_t row = (tile / num_kb) * 128 + (trow & 127);   // weight row over E*rows
     const int64_t e = row / rows_per_expert;
     const int r = (int)(row % rows_per_expert);
     const int sr = interleave ? gate_up_source_row_for(r, I, interleave == 8) : r;
-    const uint4 v = reinterpret_cast<const uint4*>(src + ((size_t)e * rows_per_expert + sr) *
-                                                             (size_t)chunks_per_row * 16)[part];
+    const int j = kb * kb_bytes + part * 16;          // byte of the row
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (j < row_bytes)
+      v = *reinterpret_cast<const uint4*>(src + ((size_t)e * rows_per_expert + sr) *
+                                                    (size_t)row_bytes + j);
     reinterpret_cast<uint4*>(dst)[c] = v;
   }
 }
@@ -549,11 +558,12 @@ cudaError_t launch_prepare(const Shape& s, const uint8_t* w1c, const uint8_t* w1
                            const PrepLayout& pl, cudaStream_t st) {
   const int64_t E = s.E, H = s.H, I = s.I;
   const int gran = s.f8 ? 8 : 16;   // gate/up interleave of the activation format
-  {  // W1 codes: interleaved rows
-    const int cpr = (int)(H / 2 / 16);
-    const int64_t total = E * 2 * I * cpr;
-    copy_rows_kernel<<<grid_for(total, 256, 16384), 256, 0, st>>>(w1c, prep + pl.off_w1c, total,
-                                                                  cpr, (int)(2 * I), (int)I, gran);
+  const int kbb = weight_kb_bytes(s);
+  {  // W1 codes: interleaved rows, k-block tiles
+    const int64_t total = weight_code_bytes(s, E * 2 * I, H) / 16;
+    tile_codes_kernel<<<grid_for(total, 256, 16384), 256, 0, st>>>(
+        w1c, prep + pl.off_w1c, total, (int)(H / 2), kbb, (int)weight_num_kb(s, H), (int)(2 * I),
+        (int)I, gran);
   }
   {  // W1 scales: interleaved rows, 128x4 blocks
     const int64_t words = E * 2 * I * (H / sf_group(s)) / 4;
@@ -561,11 +571,11 @@ cudaError_t launch_prepare(const Shape& s, const uint8_t* w1c, const uint8_t* w1
         w1s, reinterpret_cast<uint32_t*>(prep + pl.off_w1s), words, (int)(2 * I),
         (int)(H / sf_group(s)), (int)I, gran);
   }
-  {  // W2 codes: rows unchanged
-    const int cpr = (int)(I / 2 / 16);
-    const int64_t total = E * H * cpr;
-    copy_rows_kernel<<<grid_for(total, 256, 16384), 256, 0, st>>>(w2c, prep + pl.off_w2c, total,
-                                                                  cpr, (int)H, (int)I, 0);
+  {  // W2 codes: rows unchanged, k-block tiles
+    const int64_t total = weight_code_bytes(s, E * H, I) / 16;
+    tile_codes_kernel<<<grid_for(total, 256, 16384), 256, 0, st>>>(
+        w2c, prep + pl.off_w2c, total, (int)(I / 2), kbb, (int)weight_num_kb(s, I), (int)H,
+        (int)I, 0);
   }
   {  // W2 scales: 128x4 blocks
     const int64_t words = E * H * (I / sf_group(s)) / 4;

@@ -244,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
     const int b = (int)blockIdx.x;
     const int e = b / P.m_tiles, mt = b % P.m_tiles;
     for (int kb = 0; kb < P.num_kb; ++kb)
-      ptx::tma_prefetch_2d(&tmap_w1, kb * kBKBytes, e * P.rows_per_expert + mt * kBM);
+      ptx::tma_prefetch_2d(&tmap_w1, 0, ((e * P.m_tiles + mt) * P.num_kb + kb) * kBM);
     ptx::bulk_prefetch(P.w_sf + ((size_t)(e * P.m_tiles + mt) * P.kc4) * kSFAtomBytes,
                        (uint32_t)P.kc4 * kSFAtomBytes);
   }
@@ -330,8 +330,8 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
       const int e = it.e, row0 = ti.y, n = ti.z;
       const int nb = (n + kBBoxRows - 1) / kBBoxRows;
       const int mt = it.mt;   // the item's weight slab
-      const int wrow = e * P.rows_per_expert + mt * kBM;
-      const uint8_t* wsf = P.w_sf + ((size_t)(e * P.m_tiles + mt) * P.kc4) * kSFAtomBytes;
+      const int wslab = e * P.m_tiles + mt;   // weight slab over all experts
+      const uint8_t* wsf = P.w_sf + ((size_t)wslab * P.kc4) * kSFAtomBytes;
       // the tile's token scale blocks (each tile has blocks of its own)
       const uint8_t* tsf = P.t_sf + ((size_t)(row0 / SM::kBRows) * P.kc4) * kSFAtomBytes;
       // Pulled token rows: lane l gathers rows l, l+32, l+64, l+96 of the tile.
@@ -397,8 +397,8 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
               (F8 ? kATileBytes / 2 : kATileBytes) + atoms * kSFAtomBytes +
               (pulled ? 0u : (uint32_t)(nb * (kBBoxRows * kBKBytes) + atoms * kSFAtomBytes));
           ptx::mbar_arrive_expect_tx(bar, bytes);
-          ptx::tma_load_2d(smem + SM::kA + (size_t)stage * kATileBytes, tw, kb * kBKBytes, wrow,
-                           bar, pol_w);
+          ptx::tma_load_2d(smem + SM::kA + (size_t)stage * kATileBytes, tw, 0,
+                           (wslab * P.num_kb + kb) * kBM, bar, pol_w);
           ptx::bulk_load(smem + SM::kSFA + (size_t)stage * SM::kSF,
                          wsf + (size_t)kb * (kKb / kAtomK) * kSFAtomBytes, atoms * kSFAtomBytes,
                          bar, pol_w);
@@ -964,6 +964,12 @@ cudaError_t launch_layer(const LayerLaunch& g, cudaStream_t st) {
   const int trows = g.pull ? kBN : g.tile_rows;
   if (trows != kBN && trows != kBNMedium && trows != kBNNarrow) return cudaErrorInvalidValue;
   const uint32_t full_rows = (uint32_t)trows;
+  // Weight codes are in k-block tiles: a map row is one slab row's k-block, and the
+  // 128 rows of slab w's k-block kb are map rows (w * num_kb + kb) * 128 onwards.
+  const uint64_t w1_rows = (uint64_t)s.E * 2 * s.I * weight_num_kb(s, s.H);
+  const uint64_t w2_rows = (uint64_t)s.E * s.H * weight_num_kb(s, s.I);
+  // TMA row coordinates are 32-bit signed (W1 codes above 256 GiB would overflow them)
+  if (w1_rows > 0x7FFFFFFFull || w2_rows > 0x7FFFFFFFull) return cudaErrorInvalidValue;
   CUtensorMap maps[6];
   cudaError_t err;
   if ((err = make_tmap(&maps[4], g.ws.xb, xrow, (uint64_t)g.R_cap, full_rows)) ||
@@ -973,11 +979,11 @@ cudaError_t launch_layer(const LayerLaunch& g, cudaStream_t st) {
     return err;
   if (f8) {
     // weights widened from packed E2M1 to one element per byte as they land
-    if ((err = make_tmap_e2m1_wide(&maps[0], g.w1_codes, (uint64_t)s.H, (uint64_t)s.E * 2 * s.I)) ||
-        (err = make_tmap_e2m1_wide(&maps[2], g.w2_codes, (uint64_t)s.I, (uint64_t)s.E * s.H)))
+    if ((err = make_tmap_e2m1_wide(&maps[0], g.w1_codes, 2 * (uint64_t)weight_kb_bytes(s), w1_rows)) ||
+        (err = make_tmap_e2m1_wide(&maps[2], g.w2_codes, 2 * (uint64_t)weight_kb_bytes(s), w2_rows)))
       return err;
-  } else if ((err = make_tmap(&maps[0], g.w1_codes, (uint64_t)s.H / 2, (uint64_t)s.E * 2 * s.I, kBM)) ||
-             (err = make_tmap(&maps[2], g.w2_codes, (uint64_t)s.I / 2, (uint64_t)s.E * s.H, kBM))) {
+  } else if ((err = make_tmap(&maps[0], g.w1_codes, kBKBytes, w1_rows, kBM)) ||
+             (err = make_tmap(&maps[2], g.w2_codes, kBKBytes, w2_rows, kBM))) {
     return err;
   }
   LayerArgs a;

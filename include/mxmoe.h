@@ -101,8 +101,10 @@ MXMOE_API const char *moe_status_string(moe_status s);
 MXMOE_API moe_status moe_validate_dims(const moe_dims *dims);
 
 /* Bytes of the prepared-weight blob moe_prepare_weights writes; 0 for bad dims.
- * Equal to the canonical MXFP4 bytes of both weights (rounded up to 1 KiB per
- * section).  Host only. */
+ * Equal to the canonical bytes of both weights (each of the four sections rounded
+ * up to 1 KiB) when K (hidden for W1, inter for W2) is a whole number of k-blocks
+ * (256 elements; 128 for MOE_MMA_FP8xFP4); otherwise each code row is padded to
+ * whole k-blocks.  Host only. */
 MXMOE_API size_t moe_prepared_weights_size(const moe_dims *dims);
 
 /* Bytes of the workspace for dims->max_tokens tokens; 0 for bad dims.  Host only.
@@ -168,9 +170,13 @@ MXMOE_API moe_status moe_quantize_nvfp4(const float *src_dev, int64_t rows, int3
  * Output `prepared_dev` (prepared_bytes >= moe_prepared_weights_size): W1 rows
  * interleaved with gran=16 (each chunk of 16 gate and 16 up rows becomes
  * [gate even, up even, gate odd, up odd]; for fp8xfp4 gran=8: [gate 8, up 8]),
- * codes and scales alike, and both
- * weights' scales in the 128x4 block layout.  Inputs are not modified; the
- * caller may free them afterwards. */
+ * codes and scales alike.  Sections, each 1 KiB-aligned: W1 codes, W1 scales, W2
+ * codes, W2 scales.  Codes are stored in k-block tiles, so that one weight slab's
+ * k-block is one contiguous run: with kb = 128 bytes (64 for fp8xfp4) and
+ * nkb = ceil(K / (2 kb)), byte j of row R (rows over all experts) sits at
+ * ((R / 128 * nkb + j / kb) * 128 + R % 128) * kb + j % kb, and the bytes past a
+ * row's end in a short last k-block are zero.  Scales are in the 128x4 block
+ * layout.  Inputs are not modified; the caller may free them afterwards. */
 MXMOE_API moe_status moe_prepare_weights(const moe_dims *dims, const uint8_t *w1_codes_dev,
                                          const uint8_t *w1_scales_dev, const uint8_t *w2_codes_dev,
                                          const uint8_t *w2_scales_dev, void *prepared_dev,

@@ -50,3 +50,13 @@ def compact_problem(ids: np.ndarray, tokens):
     remap = {int(e): i for i, e in enumerate(experts)}
     new = np.vectorize(lambda e: remap.get(int(e), -1))(sub).astype(np.int32)
     return new, experts
+
+
+def untile_codes(flat: np.ndarray, rows: int, K: int, kb_bytes: int = 128) -> np.ndarray:
+    """Row-major [rows, K/2] codes from the library's k-block tiles: the 128 rows of a
+    weight slab over one k-block of kb_bytes packed bytes are contiguous, and a short
+    last k-block is zero-padded to full width (asserted here)."""
+    nkb = -(-K // (2 * kb_bytes))
+    t = flat.reshape(rows // 128, nkb, 128, kb_bytes).transpose(0, 2, 1, 3).reshape(rows, nkb * kb_bytes)
+    assert not t[:, K // 2:].any(), "padding of the last k-block is not zero"
+    return t[:, :K // 2]

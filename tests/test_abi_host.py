@@ -7,6 +7,7 @@ import os
 import re
 import subprocess
 
+import numpy as np
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -92,6 +93,37 @@ def test_prepared_size_is_canonical_mxfp4_bytes(mx):
     # gate/up [E, 2I, H] + down [E, H, I] at 4 bits plus one byte per 32 elements
     assert mx.moe_prepared_weights_size(d) == 256 * (2 * 2048 * 4096 + 4096 * 2048) * 17 // 32
     assert mx.moe_prepared_weights_size(d) == 3_422_552_064
+
+
+def test_prepared_size_pads_a_short_last_k_block(mx):
+    """Codes are stored in k-block tiles of 256 elements (128 for fp8xfp4); a K that
+    ends in half a k-block is padded to a whole one, scales are not."""
+    def align(v):
+        return (v + 1023) // 1024 * 1024
+
+    H, I, E = 384, 384, 2
+    w1c, w2c = E * 2 * I * 2 * 128, E * H * 2 * 128     # two k-blocks of 128 bytes a row
+    w1s, w2s = E * 2 * I * H // 32, E * H * I // 32
+    want = align(align(align(align(w1c) + w1s) + w2c) + w2s)
+    assert mx.moe_prepared_weights_size(mx.make_dims(H, I, E, 2, 64)) == want
+    # fp8xfp4 k-blocks are 128 elements: 384 is three whole ones, no padding
+    want8 = align(align(align(align(E * 2 * I * H // 2) + w1s) + E * H * I // 2) + w2s)
+    assert mx.moe_prepared_weights_size(mx.make_dims(H, I, E, 2, 64, mx.MOE_MMA_FP8xFP4)) == want8
+
+
+def test_untile_codes_follows_the_byte_formula():
+    """The tests' untiling against the per-byte position of the k-block tile layout:
+    byte j of row R at ((R // 128 * nkb + j // kb) * 128 + R % 128) * kb + j % kb."""
+    from tests.helpers import untile_codes
+    rng = np.random.default_rng(3)
+    for rows, K, kb in ((256, 384, 128), (128, 256, 64), (384, 128, 128)):
+        nkb = -(-K // (2 * kb))
+        codes = rng.integers(0, 256, size=(rows, K // 2), dtype=np.uint8)
+        flat = np.zeros(rows * nkb * kb, np.uint8)
+        for R in range(rows):
+            for j in range(K // 2):
+                flat[((R // 128 * nkb + j // kb) * 128 + R % 128) * kb + j % kb] = codes[R, j]
+        assert np.array_equal(untile_codes(flat, rows, K, kb), codes)
 
 
 def test_workspace_size_grows_with_capacity(mx):

@@ -18,7 +18,8 @@ import block_scaled_fp4_pre_gb300 as mx  # noqa: E402
 import oracle  # noqa: E402
 import synth  # noqa: E402
 from tests.gpu_common import DeviceLayer, compare_full, device, to_dev  # noqa: E402
-from tests.helpers import compact_problem, normwise_rel_err, oracle_expert_weights  # noqa: E402
+from tests.helpers import (compact_problem, normwise_rel_err, oracle_expert_weights,  # noqa: E402
+                           untile_codes)
 
 pytestmark = pytest.mark.gpu
 
@@ -106,14 +107,14 @@ def test_weights_quantised_and_prepared_bit_exact(layers, name):
     w1c_p = W[0][:, src, :]
     w1s_p = W[1][:, src, :]
     off = 0
-    n = E * 2 * I * H // 2
-    assert np.array_equal(blob[off:off + n], w1c_p.reshape(-1))
+    n = E * 2 * I * -(-H // 256) * 128
+    assert np.array_equal(untile_codes(blob[off:off + n], E * 2 * I, H), w1c_p.reshape(E * 2 * I, -1))
     off = (off + n + 1023) // 1024 * 1024
     n = E * 2 * I * H // 32
     assert np.array_equal(blob[off:off + n], oracle.scale_block_layout(w1s_p.reshape(E * 2 * I, -1)))
     off = (off + n + 1023) // 1024 * 1024
-    n = E * H * I // 2
-    assert np.array_equal(blob[off:off + n], W[2].reshape(-1))
+    n = E * H * -(-I // 256) * 128
+    assert np.array_equal(untile_codes(blob[off:off + n], E * H, I), W[2].reshape(E * H, -1))
     off = (off + n + 1023) // 1024 * 1024
     n = E * H * I // 32
     assert np.array_equal(blob[off:off + n], oracle.scale_block_layout(W[3].reshape(E * H, -1)))
