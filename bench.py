@@ -69,11 +69,14 @@ def parse_args():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--dispatch", choices=["bucketed", "pull"], default="bucketed",
                    help="token rows copied per expert by pre_dispatch, or gathered by the layer")
-    p.add_argument("--tiles", choices=["auto", "wide", "medium", "narrow"], default="auto",
-                   help="token tiles: 128 rows (wide), 64 (medium), 32 (narrow) or the layer's choice")
+    p.add_argument("--tiles", choices=["auto", "wide", "medium", "narrow", "pair"], default="auto",
+                   help="token tiles: 128 rows (wide), 64 (medium), 32 (narrow), 256 on SM pairs "
+                        "(pair) or the layer's choice")
     p.add_argument("--mma", choices=["mxf4xmxf4", "fp8xfp4", "nvf4xnvf4"], default="mxf4xmxf4",
                    help="formats: MXFP4 (W4A4, the headline), MXFP8 activations (W4A8) or NVFP4")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-workloads", action="store_true",
+                   help="skip the other DeepSeek-V4-Flash configurations (the `workloads` object)")
     p.add_argument("--cpu-sample-tokens", type=int, default=0)
     return p.parse_args()
 
@@ -104,8 +107,9 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, interval_ms: int = 20):
         self.gpu = gpu_index
+        self.interval_ms = interval_ms   # short: the timed passes last tens of milliseconds
         self.proc = None
         self.lines = []
 
@@ -113,7 +117,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200", "-i", str(self.gpu)], stdout=subprocess.PIPE,
+                 "-lms", str(self.interval_ms), "-i", str(self.gpu)], stdout=subprocess.PIPE,
                 stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -181,6 +185,13 @@ def algorithmic(w: synth.Workload, ids, act_fp8: bool = False, sf_group: int = 3
     }
 
 
+# The part's nominal HBM3e bandwidth (GB/s), the denominator the target at T=512 names
+# (>= 75% of about 8 TB/s); reported beside the fraction of the measured copy peak.
+NOMINAL_HBM_GBS = 8000.0
+# The DeepSeek-V4-Flash configurations besides the headline one, measured on the same
+# prepared weights (they share H, I and E) and reported in the `workloads` object.
+OTHER_WORKLOADS = ("decode_T64", "prefill_T4096", "prefill_T16384_zipf")
+
 # Nominal dense FP4 : bf16 tensor throughput of the part (13.5 : 2.25 PFLOP/s), and
 # FP8 : bf16 (4.5 : 2.25) for the fp8xfp4 MMAs (kind::mxf8f6f4 runs at the FP8 rate).
 FP4_PER_BF16 = 6.0
@@ -200,22 +211,32 @@ def fp4_mma_probe(mx, ws, stream, n_sms: int) -> dict:
 
     out = {}
     count = 1 << 18
-    for n, bps in ((128, 2), (256, 1)):
-        blocks = n_sms * bps
-        flop = blocks * count * 2.0 * 128 * n * 64
+
+    def best_ms(launch):
         best = float("inf")
         with torch.cuda.stream(stream):
-            mx.moe_fp4_mma_probe(ws, n, bps, blocks, count, stream)
+            launch()
             for _ in range(3):
                 a = torch.cuda.Event(enable_timing=True)
                 b = torch.cuda.Event(enable_timing=True)
                 a.record(stream)
-                mx.moe_fp4_mma_probe(ws, n, bps, blocks, count, stream)
+                launch()
                 b.record(stream)
                 b.synchronize()
                 best = min(best, a.elapsed_time(b))
         mx.moe_check(ws, stream)
-        out[f"n{n}_x{bps}"] = flop / (best / 1e3) / 1e12
+        return best
+
+    # single-CTA M=128 forms (2 or 1 blocks an SM)
+    for n, bps in ((128, 2), (256, 1)):
+        blocks = n_sms * bps
+        ms = best_ms(lambda: mx.moe_fp4_mma_probe(ws, n, bps, blocks, count, stream))
+        out[f"n{n}_x{bps}"] = blocks * count * 2.0 * 128 * n * 64 / (ms / 1e3) / 1e12
+    # the two-SM M=256 form (cta_group::2), one pair of CTAs per two SMs
+    pairs = n_sms // 2
+    for n in (256,):
+        ms = best_ms(lambda: mx.moe_fp4_mma_probe_pair(ws, n, pairs, count, stream))
+        out[f"m256_n{n}_pair"] = pairs * count * 2.0 * 256 * n * 64 / (ms / 1e3) / 1e12
     return out
 
 
@@ -397,6 +418,95 @@ def config_dict(w, world):
                   "flush's dirty lines drain before the step); weights are 26x the L2"}
 
 
+def measure_other_workload(mx, dev, stream, w: synth.Workload, prepared, args, flush_l2,
+                           hbm_peak: float, fp4_peak: float, probe_best) -> dict:
+    """One more layer configuration on the already prepared weights: the same step
+    (pre_dispatch + forward), L2 flushed before each, CUDA events on the launch stream;
+    a second pass with the library's per-kernel events gives the layer kernel's time."""
+    import torch
+
+    dims = mx.make_dims(w.H, w.I, w.E, w.k, w.T,
+                        mx.MOE_MMA_FP8xFP4 if w4a8(args) else
+                        mx.MOE_MMA_NVF4xNVF4 if nvf4(args) else mx.MOE_MMA_MXF4xMXF4)
+    x = synth.hidden_bf16(w)
+    ids, tw = synth.routing(w)
+    xd = torch.from_numpy(x.view(np.int16)).to(dev)
+    idd = torch.from_numpy(ids).to(dev)
+    twd = torch.from_numpy(tw).to(dev)
+    out = torch.empty((w.T, w.H), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(mx.moe_workspace_size(dims), dtype=torch.uint8, device=dev)
+    mx.moe_workspace_init(dims, ws, stream)
+    mx.moe_workspace_set_tiles(ws, tile_modes(mx)[args.tiles])
+    mx.moe_workspace_set_dispatch(ws, mx.MOE_DISPATCH_PULL if args.dispatch == "pull"
+                                  else mx.MOE_DISPATCH_BUCKETED)
+
+    def step():
+        mx.moe_pre_dispatch(dims, xd, idd, twd, w.T, ws, stream)
+        mx.moe_forward(dims, prepared, ws, out, w.T, stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, min(args.warmup, 5))):
+            flush_l2()
+            step()
+    mx.moe_check(ws, stream)
+    steps = max(3, args.steps)
+
+    def timed(profile: bool):
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        mx.moe_profile_reset()
+        torch.cuda.synchronize(dev)
+        with torch.cuda.stream(stream):
+            mx.moe_profile_enable(profile)
+            for i in range(steps):
+                flush_l2()
+                starts[i].record(stream)
+                step()
+                ends[i].record(stream)
+            mx.moe_profile_enable(False)
+        torch.cuda.synchronize(dev)
+        mx.moe_check(ws, stream)
+        return [a.elapsed_time(b) for a, b in zip(starts, ends)], mx.moe_profile_read()
+
+    step_ms, _ = timed(False)
+    _, per_kernel = timed(True)
+    kern_ms = {k: v[0] / max(v[1], 1) for k, v in per_kernel.items()}
+    ms = statistics.mean(step_ms)
+    alg = algorithmic(w, ids, w4a8(args), 16 if nvf4(args) else 32)
+    lay_ms = kern_ms.get("layer", float("nan"))
+    achieved = alg["layer_kernel_bytes"] / (lay_ms / 1e3) / 1e9
+    tflops = alg["flops"] / (lay_ms / 1e3) / 1e12
+    name = w.name + ("" if args.mma == "mxf4xmxf4" else "_" + args.mma)
+    traffic = recorded_traffic("layer", name)
+    res = {
+        "tokens": w.T, "routing": w.routing, "us_per_layer": ms * 1e3,
+        "tokens_per_s": w.T / (ms / 1e3), "steps": steps,
+        "step_us_min": min(step_ms) * 1e3,
+        "kernels_ms": kern_ms,
+        "touched_experts": alg["touched_experts"],
+        "layer_kernel": {
+            "avg_ms": lay_ms,
+            "algorithmic_bytes": alg["layer_kernel_bytes"],
+            "hbm_GBs": achieved, "hbm_frac": achieved / hbm_peak,
+            "hbm_frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS,
+            "algorithmic_flops": alg["flops"], "tflops": tflops,
+            "tensor_frac": tflops / fp4_peak,
+            "tensor_frac_of_mma_probe": (tflops / probe_best) if probe_best else None,
+            "traffic": traffic,
+            "traffic_over_algorithmic": (traffic / alg["layer_kernel_bytes"]) if traffic else None,
+        },
+    }
+    del ws, xd, idd, twd, out
+    torch.cuda.empty_cache()
+    return res
+
+
+def tile_modes(mx) -> dict:
+    return {"auto": mx.MOE_TILES_AUTO, "wide": mx.MOE_TILES_WIDE,
+            "medium": mx.MOE_TILES_MEDIUM, "narrow": mx.MOE_TILES_NARROW,
+            "pair": mx.MOE_TILES_PAIR}
+
+
 def run_ours(args):
     import torch
 
@@ -427,9 +537,7 @@ def run_ours(args):
     out = torch.empty((w.T, w.H), dtype=torch.bfloat16, device=dev)
     ws = torch.empty(mx.moe_workspace_size(dims), dtype=torch.uint8, device=dev)
     mx.moe_workspace_init(dims, ws, stream)
-    mx.moe_workspace_set_tiles(ws, {"auto": mx.MOE_TILES_AUTO, "wide": mx.MOE_TILES_WIDE,
-                                    "medium": mx.MOE_TILES_MEDIUM,
-                                    "narrow": mx.MOE_TILES_NARROW}[args.tiles])
+    mx.moe_workspace_set_tiles(ws, tile_modes(mx)[args.tiles])
     mx.moe_workspace_set_dispatch(ws, mx.MOE_DISPATCH_PULL if args.dispatch == "pull"
                                   else mx.MOE_DISPATCH_BUCKETED)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -535,7 +643,21 @@ def run_ours(args):
                    "peak_kind": f"{peak_kind} bf16 GEMM burst x {ratio:g} (nominal "
                                 f"{'FP8' if w4a8(args) else 'FP4'}:bf16)",
                    "mma_probe_tflops": probe}
+    hbm_roof["frac_of_nominal_8tbs"] = achieved / NOMINAL_HBM_GBS
     roof, other_roof = (hbm_roof, tensor_roof) if t_hbm >= t_fp4 else (tensor_roof, hbm_roof)
+
+    # The other DeepSeek-V4-Flash configurations, on the same prepared weights.
+    workloads = None
+    if not args.no_workloads and rank == 0 and args.workload == "layer_T512" and \
+            not (args.experts or args.tokens):
+        probe_best = max(probe.values()) if probe else None
+        workloads = {}
+        with ClockSampler(local) as wclocks:
+            for name in OTHER_WORKLOADS:
+                workloads[name] = measure_other_workload(
+                    mx, dev, stream, synth.WORKLOADS[name], prepared, args, flush_l2,
+                    hbm_peak, fp4_peak, probe_best)
+        workloads["clocks"] = wclocks.summary()
 
     e2e = None
     if not args.no_e2e:
@@ -607,6 +729,8 @@ def run_ours(args):
         "gpu_launches": KERNELS_PER_STEP * args.steps,   # in the headline timed pass
         "setup_s": setup_s,
     }
+    if workloads is not None:
+        line["workloads"] = workloads
     if e2e is not None:
         line["e2e"] = e2e
     if cpu is not None:

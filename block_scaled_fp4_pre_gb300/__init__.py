@@ -88,6 +88,7 @@ def lib() -> ctypes.CDLL:
             "moe_bucket_noalloc": ([D, vp, vp, i32, vp, vp, vp], i32),
             "moe_debug_wait_probe": ([vp, i64, vp], i32),
             "moe_fp4_mma_probe": ([vp, i32, i32, i32, i64, vp], i32),
+            "moe_fp4_mma_probe_pair": ([vp, i32, i32, i64, vp], i32),
             "moe_mxfp8_scale_bytes": ([i64, i64, i32], ctypes.c_size_t),
             "moe_workspace_set_dispatch": ([vp, i32], i32),
             "moe_workspace_set_tiles": ([vp, i32], i32),
@@ -250,6 +251,7 @@ MOE_TILES_AUTO = 0
 MOE_TILES_WIDE = 1
 MOE_TILES_NARROW = 2
 MOE_TILES_MEDIUM = 3
+MOE_TILES_PAIR = 4
 
 
 def moe_workspace_set_dispatch(ws, mode: int) -> None:
@@ -281,6 +283,12 @@ def moe_fp4_mma_probe(ws, n: int, blocks_per_sm: int, blocks: int, mma_count: in
                       stream=None) -> None:
     _check(lib().moe_fp4_mma_probe(_ptr(ws), int(n), int(blocks_per_sm), int(blocks),
                                    int(mma_count), _stream(stream)))
+
+
+def moe_fp4_mma_probe_pair(ws, n: int, pairs: int, mma_count: int, stream=None) -> None:
+    """The probe's M=256 form across SM pairs (tcgen05 cta_group::2)."""
+    _check(lib().moe_fp4_mma_probe_pair(_ptr(ws), int(n), int(pairs), int(mma_count),
+                                        _stream(stream)))
 
 
 def moe_profile_enable(on: bool) -> None:

@@ -1,7 +1,7 @@
 """Build libmxmoe.so (sm_103a) in-tree with nvcc.
 
-Three translation units compile in parallel and link into one shared library that
-uses the shared CUDA runtime (the same libcudart.so.13 PyTorch loads).
+The translation units in SOURCES compile in parallel and link into one shared
+library that uses the shared CUDA runtime (the same libcudart.so.13 PyTorch loads).
 """
 from __future__ import annotations
 
@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libmxmoe.so")
 BUILD_DIR = os.path.join(PKG, "_build")
-SOURCES = ["api.cu", "dispatch.cu", "gemm.cu", "noalloc.cu", "peak.cu", "mxfp8.cu"]
+SOURCES = ["api.cu", "dispatch.cu", "gemm.cu", "pair.cu", "noalloc.cu", "peak.cu", "mxfp8.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler",
          "-fvisibility=hidden", "-I", INCLUDE, "-I", CSRC]

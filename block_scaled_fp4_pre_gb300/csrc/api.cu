@@ -203,11 +203,21 @@ int tile_mode(const void* ws) {
 // each size wins where few experts need more than one tile.  The pull dispatch
 // gathers into 128-row tiles only.
 int choose_tile_rows(const moe_dims& d, int32_t T, int mode, bool pull) {
+  const bool pair_ok = !pull && pair_shape_ok(shape_of(d));
   if (pull || mode == MOE_TILES_WIDE) return kBN;
   if (mode == MOE_TILES_NARROW) return kBNNarrow;
   if (mode == MOE_TILES_MEDIUM) return kBNMedium;
+  if (mode == MOE_TILES_PAIR) return pair_ok ? kBNPair : kBN;
   const int64_t rows = (int64_t)T * d.topk, E = d.num_experts;
   return rows <= 16 * E ? kBNNarrow : rows <= 64 * E ? kBNMedium : kBN;
+}
+
+// Token rows of a 128x4 scale block's tile in the layout of a dispatch with tiles of
+// tile_rows rows (pair tiles are two whole 128-row blocks).
+int sf_layout_rows(int tile_rows) { return tile_rows > kBN ? kBN : tile_rows; }
+
+cudaError_t launch_any_layer(const LayerLaunch& g, cudaStream_t st) {
+  return g.tile_rows == kBNPair ? launch_layer_pair(g, st) : launch_layer(g, st);
 }
 
 // Timing hooks.
@@ -329,7 +339,7 @@ moe_status pre_dispatch_impl(const moe_dims* d, const void* x, const int32_t* id
   if (e != cudaSuccess) return cuda_fail(e, "bucket kernel");
   {
     ProfScope ps("quantize_scatter", st);
-    e = launch_quantize_scatter(s, x, ids, tw, T, p, pull, tile_rows, st);
+    e = launch_quantize_scatter(s, x, ids, tw, T, p, pull, sf_layout_rows(tile_rows), st);
   }
   if (e != cudaSuccess) return cuda_fail(e, "quantize kernel");
   mark_dispatched(ws, tile_rows);
@@ -370,7 +380,7 @@ moe_status forward_impl(const moe_dims* d, const void* prepared, void* ws, void*
   }
   {
     ProfScope ps("layer", st);
-    e = launch_layer(g, st);
+    e = launch_any_layer(g, st);
   }
   if (e != cudaSuccess) return cuda_fail(e, "layer kernel");
   {
@@ -454,7 +464,7 @@ moe_status moe_workspace_set_dispatch(void* ws, int32_t mode) {
 moe_status moe_workspace_set_tiles(void* ws, int32_t mode) {
   if (!ws) return fail(MOE_ERR_INVALID_ARG, "workspace is NULL");
   if (mode != MOE_TILES_AUTO && mode != MOE_TILES_WIDE && mode != MOE_TILES_NARROW &&
-      mode != MOE_TILES_MEDIUM)
+      mode != MOE_TILES_MEDIUM && mode != MOE_TILES_PAIR)
     return fail(MOE_ERR_INVALID_ARG, "unknown tile mode %d", mode);
   std::lock_guard<std::mutex> lk(g_reg_mu);
   auto it = g_registry.find(ws);
@@ -690,7 +700,7 @@ moe_status moe_read_dispatch(const moe_dims* dims, const void* ws, int32_t T, in
   } else if (xc_host || xs_host) {
     const size_t rb = (size_t)act_row_bytes(*dims, H);
     const int sfb = (int)sf_row_bytes(*dims, H);
-    const int tr = tile_rows_of(ws);
+    const int tr = sf_layout_rows(tile_rows_of(ws));
     std::vector<uint8_t> codes((size_t)R * rb), sf((size_t)R * sfb * (kBN / tr));
     if (R && (e = cudaMemcpy(codes.data(), b + L.off_xb, codes.size(), cudaMemcpyDeviceToHost)))
       return cuda_fail(e, "codes read");
@@ -735,7 +745,7 @@ moe_status moe_read_intermediate(const moe_dims* dims, const void* ws, int32_t T
   if (R < 0 || R > L.R_cap) return fail(MOE_ERR_CUDA, "corrupt segment table");
   const size_t rb = (size_t)act_row_bytes(*dims, I);
   const int sfb = (int)sf_row_bytes(*dims, I);
-  const int tr = tile_rows_of(ws);
+  const int tr = sf_layout_rows(tile_rows_of(ws));
   std::vector<uint8_t> codes((size_t)R * rb), sf((size_t)R * sfb * (kBN / tr));
   if (R && (e = cudaMemcpy(codes.data(), b + L.off_hb, codes.size(), cudaMemcpyDeviceToHost)))
     return cuda_fail(e, "codes read");
@@ -770,7 +780,7 @@ moe_status moe_debug_gate_up(const moe_dims* dims, const void* prepared, void* w
   if (g.num_sms <= 0) return fail(MOE_ERR_CUDA, "no CUDA device");
   g.num_phases = 1;
   g.gate_up_debug = gate_up;
-  cudaError_t e = launch_layer(g, static_cast<cudaStream_t>(stream));
+  cudaError_t e = launch_any_layer(g, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "gate/up GEMM (raw)");
   return MOE_OK;
 }
@@ -803,8 +813,10 @@ size_t moe_mxfp8_scale_bytes(int64_t rows_cap, int64_t K, int32_t layout) {
 moe_status moe_mxfp8_quantize(const void* x, int64_t rows, int64_t K, void* q, void* sf,
                               int32_t layout, int64_t rows_cap, void* stream) {
   constexpr int64_t kMax = (int64_t)1 << 23;
-  if (K <= 0 || K % 128 || K > kMax)
-    return fail(MOE_ERR_INVALID_ARG, "K = %lld: must be a positive multiple of 128, at most 2^23",
+  constexpr int64_t kMaxK = (int64_t)65535 * 128;   // one grid row of blocks per 128 columns
+  if (K <= 0 || K % 128 || K > kMaxK)
+    return fail(MOE_ERR_INVALID_ARG,
+                "K = %lld: must be a positive multiple of 128, at most 65535 * 128",
                 (long long)K);
   if (rows < 0 || rows > rows_cap || rows_cap > kMax)
     return fail(MOE_ERR_INVALID_ARG, "rows = %lld, rows_cap = %lld: need 0 <= rows <= rows_cap <= 2^23",
@@ -845,6 +857,30 @@ moe_status moe_fp4_mma_probe(void* ws, int32_t n, int32_t blocks_per_sm, int32_t
   cudaError_t e = launch_fp4_mma_probe(n, blocks_per_sm, blocks, (long long)mma_count, flags,
                                        static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "fp4 mma probe");
+  return MOE_OK;
+}
+
+moe_status moe_fp4_mma_probe_pair(void* ws, int32_t n, int32_t pairs, int64_t mma_count,
+                                  void* stream) {
+  if (!ws) return fail(MOE_ERR_INVALID_ARG, "workspace is NULL");
+  if (n < 32 || n > 256 || n % 32 != 0)
+    return fail(MOE_ERR_INVALID_ARG, "n = %d: must be a multiple of 32 in [32, 256]", n);
+  if (pairs < 1 || pairs > 32768)
+    return fail(MOE_ERR_INVALID_ARG, "pairs = %d outside [1, 32768]", pairs);
+  if (mma_count < 1 || mma_count > ((int64_t)1 << 20))
+    return fail(MOE_ERR_INVALID_ARG, "mma_count = %lld outside [1, 2^20]", (long long)mma_count);
+  moe_dims d;
+  {
+    std::lock_guard<std::mutex> lk(g_reg_mu);
+    auto it = g_registry.find(ws);
+    if (it == g_registry.end())
+      return fail(MOE_ERR_WORKSPACE_MISMATCH, "workspace %p was not initialised", ws);
+    d = it->second.dims;
+  }
+  int32_t* flags = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ws) + ws_layout(d).off_flags);
+  cudaError_t e = launch_fp4_mma_probe_pair(n, pairs, (long long)mma_count, flags,
+                                            static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "fp4 mma pair probe");
   return MOE_OK;
 }
 

@@ -28,6 +28,9 @@ constexpr int kSFStageBytes = 2 * kSFAtomBytes;  // 8 scale columns per k-block
 // of its own (its rows in the first quarter or half of each block).
 constexpr int kBNNarrow = 32;
 constexpr int kBNMedium = 64;
+// Token tiles of the pair kernel (two SMs share each item, tcgen05 cta_group::2): up
+// to 256 rows, two 128x4 scale blocks; expert segments padded to kBN rows.
+constexpr int kBNPair = 256;
 
 // Device error bits in ws.flags[0].
 constexpr int kErrRouting = 1;
@@ -175,7 +178,7 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 // of its launch.
 // Bucketing: per-expert counts and segment starts, the tile list, and each
 // assignment's rank; the quantiser (or launch_assign_slots) turns ranks into rows.
-// tile_rows: kBN (wide tiles), kBNMedium or kBNNarrow.
+// tile_rows: kBN (wide tiles), kBNMedium, kBNNarrow or kBNPair.
 cudaError_t launch_bucket(const Shape& s, const int32_t* ids, int T, const WsPtrs& ws,
                           int tile_rows, cudaStream_t st);
 // Quantise the tokens, give every assignment its row and copy the token there.
@@ -207,6 +210,9 @@ cudaError_t launch_mxfp8_quantize(const void* x, int64_t rows, int64_t K, void* 
                                   int layout, int64_t rows_cap, cudaStream_t st);
 cudaError_t launch_fp4_mma_probe(int n, int blocks_per_sm, int blocks, long long mma_count,
                                  int32_t* flags, cudaStream_t st);
+// M=256 across SM pairs (2-CTA clusters, tcgen05 cta_group::2), `pairs` clusters.
+cudaError_t launch_fp4_mma_probe_pair(int n, int pairs, long long mma_count, int32_t* flags,
+                                      cudaStream_t st);
 
 // Records the message moe_last_error() returns on this thread.
 void set_last_error(const char* msg);
@@ -227,8 +233,12 @@ struct LayerLaunch {
   float* gate_up_debug;      // [T*k, 2I] (num_phases == 1)
   int num_sms;
   bool pull;                 // gate/up token rows gathered from ws.xq/xs (pull dispatch)
-  int tile_rows;             // token rows a tile: 32, 64 or 128 (the dispatch's choice)
+  int tile_rows;             // token rows a tile: 32, 64, 128 or kBNPair (the dispatch's choice)
 };
 cudaError_t launch_layer(const LayerLaunch& g, cudaStream_t st);
+// The layer on SM pairs (pair.cu): kBNPair-row token tiles, mxf4xmxf4 only, bucketed
+// dispatch; pair_shape_ok says whether the shape allows it (H and 2I multiples of 256).
+bool pair_shape_ok(const Shape& s);
+cudaError_t launch_layer_pair(const LayerLaunch& g, cudaStream_t st);
 
 }  // namespace mxmoe

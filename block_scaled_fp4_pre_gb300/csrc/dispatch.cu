@@ -24,8 +24,8 @@ constexpr unsigned kFull = 0xFFFFFFFFu;
 // them advances the warp's count for that expert, and a scan over warps turns the
 // counts into each warp's base.  Each block publishes its per-expert totals; the
 // last block to finish scans them over blocks (bases of later chunks) and over
-// experts (segment starts padded to tile_rows -- kBN, kBNMedium or kBNNarrow -- and
-// the tile list).  Row of an assignment =
+// experts (segment starts padded to tile_rows -- kBN, kBNMedium or kBNNarrow; to kBN
+// for the pair kernel's kBNPair-row tiles -- and the tile list).  Row of an assignment =
 // segment start + its chunk's base + its rank in the chunk.
 
 // Lanes whose key equals this lane's key (keys < 2^nbits): one ballot per bit, which
@@ -61,6 +61,9 @@ __global__ void __launch_bounds__(1024) bucket_kernel(const int32_t* __restrict_
   const int w0 = min(len, warp * per), w1 = min(len, w0 + per);
   int nbits = 1;
   while ((1 << nbits) <= E + 1) ++nbits;  // keys 0..E+1
+  // Segments are padded to whole tiles, or (tiles of two 128-row scale blocks) to
+  // whole 128-row blocks, so that every tile starts at row 0 of a scale block.
+  const int seg_pad = tile_rows > kBN ? kBN : tile_rows;
 
   for (int i = tid; i < 32 * E; i += blockDim.x) cnt[i] = 0;
   for (int i = tid; i < len; i += blockDim.x) {
@@ -149,7 +152,7 @@ __global__ void __launch_bounds__(1024) bucket_kernel(const int32_t* __restrict_
     const int e = warp * 32 + lane;
     const int n = e < E ? tot[e] : 0;
     tiles = (n + tile_rows - 1) / tile_rows;
-    rows = tiles * tile_rows;
+    rows = (n + seg_pad - 1) / seg_pad * seg_pad;
     ir = rows;
     it = tiles;
 #pragma unroll

@@ -37,8 +37,8 @@ __global__ void __launch_bounds__(kThreads8)
                           uint8_t* __restrict__ q, uint8_t* __restrict__ sf, int layout) {
   __shared__ alignas(16) uint8_t atom[kRowsPerBlock * 4];   // this block's 128 x 4 scales
   const int t = threadIdx.x;
-  const int64_t kc = blockIdx.x;                  // 128-element column block
-  const int64_t r0 = (int64_t)blockIdx.y * kRowsPerBlock;
+  const int64_t kc = blockIdx.y;                  // 128-element column block
+  const int64_t r0 = (int64_t)blockIdx.x * kRowsPerBlock;
   reinterpret_cast<uint16_t*>(atom)[t] = 0;       // padded rows keep zero scales
   __syncthreads();
   const int c = t & 15;                           // 8-element piece of the row segment
@@ -87,7 +87,7 @@ __global__ void __launch_bounds__(kThreads8)
   __syncthreads();
   if (layout == MOE_SF_128X4) {
     if (t < 32)
-      reinterpret_cast<uint4*>(sf + ((uint64_t)blockIdx.y * (K / kColsPerBlock) + kc) * 512)[t] =
+      reinterpret_cast<uint4*>(sf + ((uint64_t)blockIdx.x * (K / kColsPerBlock) + kc) * 512)[t] =
           reinterpret_cast<const uint4*>(atom)[t];
   } else if (t < kRowsPerBlock && r0 + t < rows) {
     reinterpret_cast<uint32_t*>(sf)[(r0 + t) * (K / kColsPerBlock) + kc] =
@@ -116,7 +116,10 @@ cudaError_t launch_mxfp8_quantize(const void* x, int64_t rows, int64_t K, void* 
     if (e != cudaSuccess) return e;
   }
   if (rows == 0) return cudaSuccess;
-  const dim3 grid((unsigned)(K / kColsPerBlock), (unsigned)((rows + kRowsPerBlock - 1) / kRowsPerBlock));
+  // Row blocks on x (up to 2^23 / 128 = 65536 of them, past grid.y's limit), column
+  // blocks on y (K / 128 <= 65535, checked by the caller).
+  const dim3 grid((unsigned)((rows + kRowsPerBlock - 1) / kRowsPerBlock), (unsigned)(K / kColsPerBlock));
+  if (grid.y > 65535u) return cudaErrorInvalidValue;
   mxfp8_quantize_kernel<<<grid, kThreads8, 0, st>>>(static_cast<const uint16_t*>(x), rows, K,
                                                     static_cast<uint8_t*>(q),
                                                     static_cast<uint8_t*>(sf), layout);

@@ -46,22 +46,49 @@ static __device__ __align__(256) unsigned char g_bucket_scratch[kScratchBytes];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
+// Per device: the array's device address and the context it was looked up in.  A
+// device reset (cudaDeviceReset) or a rebuilt primary context reloads the module, so
+// the address is looked up again whenever the current context is not the recorded one.
 unsigned char* g_scratch_dev[kMaxDevices] = {};
+void* g_scratch_ctx[kMaxDevices] = {};
+
+typedef int (*CtxGetCurrentFn)(void**);   // cuCtxGetCurrent, through the runtime's entry point
+
+// The current driver context (nullptr if it cannot be read).
+void* current_context() {
+  static CtxGetCurrentFn fn = nullptr;
+  static bool looked = false;
+  if (!looked) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(p);
+    looked = true;
+  }
+  void* ctx = nullptr;
+  if (!fn || fn(&ctx) != 0) return nullptr;
+  return ctx;
+}
 
 // Device address of g_bucket_scratch on the current device.  In host code the
 // array's name is only a host-side stand-in, so the address must come from
-// cudaGetSymbolAddress, once per device, with that device current.
+// cudaGetSymbolAddress, with that device current: once per device and context (the
+// first call on a device, or the first after its context was rebuilt).
 cudaError_t scratch_address(unsigned char** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lk(g_mu);
-  if (!g_scratch_dev[dev]) {
+  void* ctx = current_context();
+  if (!g_scratch_dev[dev] || ctx == nullptr || ctx != g_scratch_ctx[dev]) {
     void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_bucket_scratch);
+    e = cudaGetSymbolAddress(&p, g_bucket_scratch);   // makes the device's context current
     if (e != cudaSuccess) return e;
     g_scratch_dev[dev] = static_cast<unsigned char*>(p);
+    g_scratch_ctx[dev] = current_context();
   }
   *out = g_scratch_dev[dev];
   return cudaSuccess;
@@ -80,8 +107,15 @@ extern "C" moe_status moe_bucket_noalloc(const moe_dims* dims, const int32_t* to
                                          int32_t* counts_dev, int32_t* assign_slot_dev,
                                          void* stream) {
   using namespace mxmoe;
-  moe_status s = moe_validate_dims(dims);
-  if (s != MOE_OK) return s;
+  // Bucketing reads only the expert count, top-k and mma_type of the dims.
+  if (!dims) return fail(MOE_ERR_INVALID_ARG, "moe_bucket_noalloc: dims is NULL");
+  if (dims->mma_type != MOE_MMA_MXF4xMXF4 && dims->mma_type != MOE_MMA_FP8xFP4 &&
+      dims->mma_type != MOE_MMA_NVF4xNVF4)
+    return fail(MOE_ERR_UNSUPPORTED, "moe_bucket_noalloc: unknown mma_type");
+  if (dims->num_experts < 1)
+    return fail(MOE_ERR_INVALID_ARG, "moe_bucket_noalloc: num_experts < 1");
+  if (dims->topk < 1 || dims->topk > 32 || dims->topk > dims->num_experts)
+    return fail(MOE_ERR_INVALID_ARG, "moe_bucket_noalloc: topk outside [1, min(num_experts, 32)]");
   if (num_tokens < 0) return fail(MOE_ERR_INVALID_ARG, "num_tokens < 0");
   if (dims->num_experts > kMaxExperts)
     return fail(MOE_ERR_INVALID_ARG, "moe_bucket_noalloc: num_experts above its limit of 256");

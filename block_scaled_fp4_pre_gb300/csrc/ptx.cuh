@@ -358,6 +358,90 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// ---- CTA pairs (2-CTA clusters, tcgen05 cta_group::2) -------------------------
+// A pair's leader (rank 0) issues the MMAs; each MMA spans both CTAs' shared memory
+// (A: 128 rows each, B: N/2 rows each, at the same offsets) and writes each CTA's
+// 128 accumulator rows into that CTA's tensor memory.
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Address of the same shared variable in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+// Every thread of both CTAs: release this CTA's earlier shared-memory writes, wait
+// for all threads of the cluster (a hardware barrier, like __syncthreads).
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+// Arrives once on an mbarrier given by its shared::cluster address (either CTA).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster)
+               : "memory");
+}
+// One warp of each CTA of the pair, together: the same columns in both CTAs.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_addr(dst_smem)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+// Leader only: each CTA's 32-row x 16-byte scale block (same shared offset) into that
+// CTA's tensor memory (same address), replicated into all four lane quarters.
+__device__ __forceinline__ void tc_cp_sf_pair(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+               : "memory");
+}
+// Leader only: D (+)= A * B^T with M = 256 across the pair (see above), MXFP4 operands
+// and UE8M0 scales; each CTA's tensor memory holds its rows' scales and all N of B's.
+__device__ __forceinline__ void tc_mma_mxf4_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                                 uint32_t idesc, uint32_t sfa_tmem,
+                                                 uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%5], "
+      "[%6], p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+      : "memory");
+}
+// Leader only: arrives once on the mbarrier at a shared::cluster address (this CTA's
+// or the peer's) when the pair's earlier tcgen05 operations issued here complete.
+__device__ __forceinline__ void tc_commit_pair(uint32_t bar_cluster) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          bar_cluster)
+      : "memory");
+}
+// 2-D tiled load into this CTA's shared memory whose completion (bytes) is signalled
+// on an mbarrier of either CTA of the pair (given by its shared::cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(void* smem_dst, const void* tmap, int32_t x,
+                                                 int32_t y, uint32_t bar_cluster, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::"
+      "bytes.L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_addr(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar_cluster), "l"(policy)
+      : "memory");
+}
+// Instruction descriptor of kind::mxf4 (E2M1 A and B, UE8M0 scales, K-major) for an
+// M-row (128 or, across a pair, 256) by N MMA; sf_id picks the scale byte pair.
+__device__ __forceinline__ uint32_t idesc_mxf4_m(int M, int N, int sf_id) {
+  return ((uint32_t)sf_id << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
+         (1u << 23) | ((uint32_t)(M >> 4) << 24) | ((uint32_t)sf_id << 29);
+}
+
 // ---- MXFP4 element math ----------------------------------------------------
 // Smallest e with amax <= 6 * 2^e, clamped below at -127 (finite fp32 gives e <= 126).
 // amax = 1.m * 2^p: 6 * 2^e = 1.5 * 2^(e+2), so e = p - 2 when 1.m <= 1.5, else p - 1.

@@ -141,13 +141,19 @@ MXMOE_API moe_status moe_workspace_set_dispatch(void *ws_dev, int32_t mode);
  *                     which pays when experts hold few tokens (decode-sized loads).
  *   MOE_TILES_MEDIUM: up to 64 rows a tile (segments padded to 64), four stages where
  *                     shared memory allows (three for nvf4xnvf4).
+ *   MOE_TILES_PAIR:   up to 256 rows a tile (segments padded to 128), each item of the
+ *                     layer run by two SMs together (a 2-CTA cluster issuing M=256
+ *                     tcgen05 MMAs over both SMs' shared memory: twice the FLOPs per
+ *                     staged operand byte).  mxf4xmxf4 with the bucketed dispatch and
+ *                     H a multiple of 256 only; otherwise it falls back to wide tiles.
  *   MOE_TILES_AUTO (default after moe_workspace_init): narrow when num_tokens * k <=
  *                     16 * num_experts, medium when <= 64 * num_experts, else wide.
  * The choice is made at each moe_pre_dispatch and holds for the forward that
  * follows; results are the same either way up to fp32 summation order.  The pull
  * dispatch always uses wide tiles.  MOE_ERR_INVALID_ARG for an unknown mode,
  * MOE_ERR_WORKSPACE_MISMATCH for a workspace moe_workspace_init has not seen. */
-enum { MOE_TILES_AUTO = 0, MOE_TILES_WIDE = 1, MOE_TILES_NARROW = 2, MOE_TILES_MEDIUM = 3 };
+enum { MOE_TILES_AUTO = 0, MOE_TILES_WIDE = 1, MOE_TILES_NARROW = 2, MOE_TILES_MEDIUM = 3,
+       MOE_TILES_PAIR = 4 };
 MXMOE_API moe_status moe_workspace_set_tiles(void *ws_dev, int32_t mode);
 
 /* Quantises row-major fp32 src_dev [rows, K] (K % 32 == 0) to MXFP4 with the rule
@@ -200,6 +206,19 @@ MXMOE_API moe_status moe_pre_dispatch(const moe_dims *dims, const void *x_dev,
  * (same num_tokens): grouped gate/up GEMM with SwiGLU and requantisation to the
  * activation format of dims->mma_type,
  * grouped down GEMM, top-k weighted combine.  out_dev: bf16 [num_tokens, H].
+ * Defined by: the digest of PR #37279, section 实现拆解 item 3 (_run_mega_routed, the
+ * routed forward: pre_dispatch into the per-mma_type buffer, then the fused mega-MoE
+ * kernel with activation "swiglu"), and "[deepseek-v4] Bump sgl-deep-gemm for packed
+ * FP4xFP4 mega-MoE (W4A4)", Appendix B (that fused kernel: both expert GEMMs and the
+ * combine in one launch, streaming every touched expert's packed FP4 weights).
+ *   dims        the dims the workspace was initialised with (else
+ *               MOE_ERR_WORKSPACE_MISMATCH)
+ *   prepared_dev  the blob moe_prepare_weights wrote for these dims, 256-byte aligned
+ *   ws_dev, ws_bytes  the workspace and its size in bytes (checked against
+ *               moe_workspace_size; too small: MOE_ERR_WORKSPACE_TOO_SMALL)
+ *   num_tokens  as passed to the last moe_pre_dispatch; 0 is a no-op
+ * The workspace's fp32 accumulator and intermediate rows are overwritten; the
+ * prepared weights are only read.
  * Calling it again without a new moe_pre_dispatch recomputes the same layer (the
  * library then clears the accumulator rows first). */
 MXMOE_API moe_status moe_forward(const moe_dims *dims, const void *prepared_dev, void *ws_dev,
@@ -276,7 +295,8 @@ MXMOE_API moe_status moe_debug_wait_probe(void *ws_dev, int64_t limit_ns, void *
  * Each group's scale is 2^e, e the smallest integer with amax <= 448 * 2^e (clamped to
  * [-127, 127], amax = 0 gives -127), stored as the byte e + 127; each value is the
  * E4M3 value nearest to x * 2^-e, ties to the even code, sign kept.
- * 0 <= rows <= rows_cap <= 2^23, K a positive multiple of 128 (at most 2^23); inputs
+ * 0 <= rows <= rows_cap <= 2^23, K a positive multiple of 128 (at most 65535 * 128 =
+ * 8388480); inputs
  * finite.  Stream-ordered, no allocation, no synchronisation.  MOE_ERR_INVALID_ARG for
  * bad sizes, an unknown layout, or NULL / misaligned pointers. */
 enum { MOE_SF_PACKED = 0, MOE_SF_128X4 = 1 };
@@ -299,6 +319,16 @@ MXMOE_API moe_status moe_mxfp8_quantize(const void *x, int64_t rows, int64_t K, 
  * Appendix B (Compute SOL of the layer kernel). */
 MXMOE_API moe_status moe_fp4_mma_probe(void *ws_dev, int32_t n, int32_t blocks_per_sm,
                                        int32_t blocks, int64_t mma_count, void *stream);
+
+/* The probe's two-SM form: `pairs` clusters of two CTAs (one per SM), each pair's
+ * leader issuing mma_count MXFP4 MMAs of shape M=256 x N=n x K=64 (tcgen05
+ * cta_group::2: 128 of the 256 rows, and n/2 of B's rows, in each CTA's shared memory;
+ * each CTA's accumulator rows in its own tensor memory).  n a multiple of 32 in
+ * [32, 256]; 1 <= pairs <= 32768; 1 <= mma_count <= 2^20.  The work is
+ * pairs * mma_count * 2*256*n*64 FLOP.  Errors and the timeout flag as for
+ * moe_fp4_mma_probe.  Same page and section. */
+MXMOE_API moe_status moe_fp4_mma_probe_pair(void *ws_dev, int32_t n, int32_t pairs,
+                                            int64_t mma_count, void *stream);
 
 /* ---- timing hooks ----
  * When enabled, moe_pre_dispatch and moe_forward record CUDA events around each
@@ -331,11 +361,16 @@ MXMOE_API int32_t moe_device_sm_count(void);
  * moe_read_dispatch).
  * The kernel's other buffers live in a static device array of the library, about
  * 0.5 MiB, which every GPU that loads the library holds until the process exits.
+ * Ids outside [0, E) are skipped: their assign_slot entry is -1 and they are not
+ * counted, so the sum of counts_dev falls short of T*k by their number (no flag is
+ * kept for them; moe_check does not see this call).
  * Limits: num_experts <= 256 and num_tokens * topk <= 8192; larger sizes return
- * MOE_ERR_INVALID_ARG without launching.  dims->max_tokens is not used.
+ * MOE_ERR_INVALID_ARG without launching.  Only dims->num_experts, dims->topk
+ * (1 <= topk <= min(num_experts, 32)) and dims->mma_type (a built type) are read;
+ * hidden, inter and max_tokens are not used or checked.
  * The first call on a device looks up the array's device address (once per
- * device, with that device current); make that first call before any stream
- * capture.  All calls share the array and it keeps the previous call's contents
+ * device and context, with that device current; again after a device reset);
+ * make that first call before any stream capture.  All calls share the array and it keeps the previous call's contents
  * (the error flags are cleared on every call); calls that overlap on the GPU --
  * on different streams or from different host threads -- race on it, so
  * serialise them.  Allocates nothing: no cudaMalloc, no cudaFree. */

@@ -9,7 +9,8 @@ import block_scaled_fp4_pre_gb300 as mx
 from block_scaled_fp4_pre_gb300 import weights as mxw
 import oracle
 import synth
-from tests.helpers import normwise_rel_err, oracle_expert_weights
+from tests.helpers import (compact_problem, normwise_rel_err, oracle_expert_weights,
+                           oracle_expert_weights_nvf4)
 
 
 def device():
@@ -87,3 +88,109 @@ def compare_full(layer: DeviceLayer, x_bits, ids, tw, got_bf16, oracle_weights):
         "flips_one_step": one_step,
         "ref": ref,
     }
+
+
+def flip_stats8(got_q, got_sf, ref_q, ref_sf):
+    """Fraction of intermediate elements whose MXFP8 value differs from the oracle's,
+    and whether each difference (where the scale agrees) is one E4M3 step."""
+    gd = oracle.mxfp8_dequantize(got_q, got_sf)
+    rd = oracle.mxfp8_dequantize(ref_q, ref_sf)
+    diff = gd != rd
+    same_scale = np.repeat(got_sf == ref_sf, 32, axis=1)
+    # E4M3 magnitudes are ordered like their 7-bit codes: one step = codes 1 apart
+    mg, mr = (got_q & 0x7F).astype(int), (ref_q & 0x7F).astype(int)
+    sign_ok = ((got_q ^ ref_q) & 0x80 == 0) | (mg == 0) | (mr == 0)
+    one = (np.abs(mg - mr) <= 1) & sign_ok
+    return float(diff.mean()) if diff.size else 0.0, bool(np.all(one[diff & same_scale]))
+
+
+def flip_stats_nv(got_c, got_s, ref_c, ref_s):
+    """Fraction of intermediate elements whose NVFP4 value differs from the oracle's,
+    and whether each difference (where the scale agrees) is one E2M1 step."""
+    gd = oracle.nvfp4_dequantize(got_c, got_s)
+    rd = oracle.nvfp4_dequantize(ref_c, ref_s)
+    diff = gd != rd
+    same = np.repeat(got_s == ref_s, 16, axis=1)
+
+    def mags(c):
+        lo, hi = c & 7, (c >> 4) & 7
+        return np.stack([lo, hi], axis=-1).reshape(c.shape[0], -1).astype(int)
+
+    one = np.abs(mags(got_c) - mags(ref_c)) <= 1
+    return float(diff.mean()) if diff.size else 0.0, bool(np.all(one[diff & same]))
+
+
+# Per activation format: the oracle's layer, its token quantiser, the intermediate
+# comparison and the oracle-side weights.
+FORMATS = {
+    "mxf4": dict(layer=oracle.moe, quant=oracle.quantize_bf16, flips=flip_stats,
+                 weights=oracle_expert_weights),
+    "w4a8": dict(layer=oracle.moe_w4a8, quant=oracle.mxfp8_quantize_bf16, flips=flip_stats8,
+                 weights=oracle_expert_weights),
+    "nvf4": dict(layer=oracle.moe_nvf4, quant=oracle.nvfp4_quantize_bf16, flips=flip_stats_nv,
+                 weights=oracle_expert_weights_nvf4),
+}
+
+
+def sampled_tokens(w: synth.Workload, ids: np.ndarray, n: int, seed: int) -> np.ndarray:
+    """First and last token, n - 2 drawn at random, and (skewed routing) the last token
+    routed to the most popular expert, whose tiles are the most numerous."""
+    rng = np.random.default_rng(seed)
+    tokens = np.concatenate([[0, w.T - 1], rng.choice(w.T, max(0, n - 2), replace=False)])
+    if w.routing == "zipf":
+        tokens = np.append(tokens, np.nonzero((ids == 0).any(1))[0][-1])
+    return np.unique(tokens)
+
+
+def full_size_check(layer: DeviceLayer, w: synth.Workload, fmt: str, tokens=None,
+                    n_sample: int = 16, seed: int = 13, weight_cache: dict | None = None) -> dict:
+    """A DeepSeek-V4-Flash-sized layer in the benchmark's launch configuration against
+    the oracle:
+      - bucketing (counts, every assignment's token) and every stored token row's
+        codes and scales bit-exact against the oracle's quantiser;
+      - the intermediate codes of the checked tokens' assignments: at most 0.1% of
+        elements differ from the oracle's, each by one grid step;
+      - those tokens' outputs within 2e-3 normwise of the oracle's (before its bf16
+        rounding), and every output finite.
+    tokens: the tokens to check (default: sampled_tokens).  weight_cache: oracle-side
+    weights by expert, kept across calls."""
+    F = FORMATS[fmt]
+    x = synth.hidden_bf16(w)
+    ids, tw = synth.routing(w)
+    got = layer.run(x, ids, tw)
+    d = mx.moe_read_dispatch(layer.dims, layer.ws, w.T)
+    counts, _, _, _, bad = oracle.bucket(ids, w.E)
+    assert bad == 0 and np.array_equal(d["counts"], counts)
+    assert np.array_equal(d["slot_token"], np.repeat(np.arange(w.T), w.k))
+    xc, xs = F["quant"](x)
+    assert np.array_equal(d["x_codes"], np.repeat(xc, w.k, axis=0)), "token codes"
+    assert np.array_equal(d["x_scales"], np.repeat(xs, w.k, axis=0)), "token scales"
+    del d
+    if tokens is None:
+        tokens = sampled_tokens(w, ids, n_sample, seed)
+    tokens = np.asarray(tokens)
+    sub_ids, experts = compact_problem(ids, tokens)
+    if weight_cache is None:
+        Wc = F["weights"](w, experts)
+    else:
+        missing = [int(e) for e in experts if int(e) not in weight_cache]
+        if missing:
+            new = F["weights"](w, missing)
+            for i, e in enumerate(missing):
+                weight_cache[e] = tuple(a[i] for a in new)
+        Wc = tuple(np.stack([weight_cache[int(e)][i] for e in experts]) for i in range(4))
+    ref = F["layer"](x[tokens], sub_ids, tw[tokens], *Wc, want_intermediates=True)
+    inter = mx.moe_read_intermediate(layer.dims, layer.ws, w.T)
+    rows = (tokens[:, None] * w.k + np.arange(w.k)[None, :]).reshape(-1)
+    frac, one_step = F["flips"](inter["h_codes"][rows], inter["h_scales"][rows],
+                                ref["h_codes"], ref["h_sf"])
+    g = oracle.bf16_bits_to_f64(got)
+    err = normwise_rel_err(g[tokens], ref["out_f64"])
+    err_bf16 = normwise_rel_err(g[tokens], oracle.bf16_bits_to_f64(ref["out_bf16"]))
+    print(f"{w.name} [{fmt}] tokens checked {len(tokens)}, assignments {len(rows)}, "
+          f"intermediate flip rate {frac:.3e} (one-step: {one_step}), normwise err {err:.3e} "
+          f"(vs bf16-rounded oracle {err_bf16:.3e})")
+    assert frac <= 1e-3 and one_step
+    assert err <= 2e-3
+    assert np.all(np.isfinite(g))
+    return {"flip_frac": frac, "err": err, "err_bf16": err_bf16, "tokens": len(tokens)}

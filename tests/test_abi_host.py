@@ -178,6 +178,10 @@ def test_mxfp8_producer_and_dispatch_mode_host_checks(mx):
         (fake, 4, 128, fake, fake, 7, 4),        # unknown layout
         (fake + 1, 4, 128, fake, fake, 0, 4),    # misaligned input
         (fake, 4, 128, fake, fake + 8, 1, 4),    # misaligned scales
+        # the limits: K past 65535 * 128 (one grid row of blocks per 128 columns) and
+        # rows_cap past 2^23, both refused before any launch
+        (fake, 4, 65536 * 128, fake, fake, 0, 4),
+        (fake, 4, 128, fake, fake, 0, (1 << 23) + 1),
     ]
     for args in bad:
         assert lib.moe_mxfp8_quantize(*args, None) == mx.MOE_ERR_INVALID_ARG, args
@@ -203,3 +207,20 @@ def test_tile_mode_and_nvfp4_quantiser_host_checks(mx):
              for m in (mx.MOE_MMA_MXF4xMXF4, mx.MOE_MMA_FP8xFP4, mx.MOE_MMA_NVF4xNVF4)]
     assert all(v > 0 for v in sizes)
     assert sizes[1] > sizes[0] and sizes[2] > sizes[0]
+
+
+def test_bucket_noalloc_reads_only_experts_topk_and_mma_type(mx):
+    """moe_bucket_noalloc checks only the dims fields bucketing uses; with zero tokens
+    it returns before any CUDA call, so these checks run on the host."""
+    lib = mx.lib()
+    fake = 1 << 20
+    # hidden, inter and max_tokens unused: zero values pass
+    d = mx.make_dims(0, 0, 32, 4, 0)
+    assert lib.moe_bucket_noalloc(d, fake, fake, 0, fake, fake, None) == mx.MOE_OK
+    assert lib.moe_bucket_noalloc(mx.make_dims(0, 0, 4, 8, 0), fake, fake, 0, fake, fake,
+                                  None) == mx.MOE_ERR_INVALID_ARG     # topk > experts
+    assert lib.moe_bucket_noalloc(mx.make_dims(0, 0, 0, 1, 0), fake, fake, 0, fake, fake,
+                                  None) == mx.MOE_ERR_INVALID_ARG     # no experts
+    assert lib.moe_bucket_noalloc(mx.make_dims(0, 0, 32, 4, 0, 9), fake, fake, 0, fake, fake,
+                                  None) == mx.MOE_ERR_UNSUPPORTED     # unknown mma_type
+    assert lib.moe_bucket_noalloc(None, fake, fake, 0, fake, fake, None) == mx.MOE_ERR_INVALID_ARG

@@ -5,7 +5,8 @@ route tokens (runtimes that plan all device buffers ahead of time, threads that
 cannot afford cudaMalloc's device-wide synchronisation): its scratch is a static
 array inside the library.  Here two calls in a row, with different routings, must
 give exactly the counts and assignment rows that moe_pre_dispatch stores in a
-workspace (integer outputs: bit-exact).  This file sorts last so that a run
+workspace, and the ones the oracle's bucketing defines (integer outputs:
+bit-exact).  This file sorts last so that a run
 stopping at the first failure has already run every other test; it also passes
 on its own in a fresh process.
 """
@@ -19,6 +20,7 @@ if not torch.cuda.is_available():
     pytest.skip("needs a CUDA GPU", allow_module_level=True)
 
 import block_scaled_fp4_pre_gb300 as mx  # noqa: E402
+import oracle  # noqa: E402
 import synth  # noqa: E402
 
 pytestmark = pytest.mark.gpu
@@ -47,6 +49,22 @@ def _noalloc_path(dims, ids, tw):
     return counts.cpu().numpy(), slots.cpu().numpy()
 
 
+def _oracle_path(ids, E, tile_rows=128):
+    """Counts and assignment rows from the oracle's bucketing: within an expert the
+    oracle's (token, k index) order, each expert's rows starting at the sum of the
+    earlier experts' counts rounded up to 128-row tiles; -1 for ids outside [0, E)."""
+    T, k = ids.shape
+    counts, offsets, st, sj, bad = oracle.bucket(ids, E)
+    slots = np.full(T * k, -1, np.int64)
+    seg = 0
+    for e in range(E):
+        lo, hi = int(offsets[e]), int(offsets[e + 1])
+        for i in range(lo, hi):
+            slots[int(st[i]) * k + int(sj[i])] = seg + (i - lo)
+        seg += -(-int(counts[e]) // tile_rows) * tile_rows
+    return counts, slots, bad
+
+
 def test_noalloc_bucketing_matches_pre_dispatch_on_two_calls():
     dims = mx.make_dims(256, 128, 32, 4, 2048)
     ws = torch.empty(mx.moe_workspace_size(dims), dtype=torch.uint8, device="cuda")
@@ -66,6 +84,11 @@ def test_noalloc_bucketing_matches_pre_dispatch_on_two_calls():
         ref_counts, ref_slots = _existing_path(dims, ws, ids, tw)
         assert np.array_equal(got_counts, ref_counts)
         assert np.array_equal(got_slots, ref_slots)
+        o_counts, o_slots, o_bad = _oracle_path(ids, dims.num_experts)
+        assert np.array_equal(got_counts, o_counts)
+        assert np.array_equal(got_slots, o_slots)
+        # skipped ids show as -1 rows and as counts summing short of T * k
+        assert int(got_counts.sum()) == ids.size - o_bad
     assert (got_slots == -1).sum() == 2
 
 
