@@ -60,7 +60,10 @@ WsLayout ws_layout(const moe_dims& d) {
   const int64_t H = d.hidden, I = d.inter, E = d.num_experts, k = d.topk;
   L.T_cap = d.max_tokens;
   L.A_cap = L.T_cap * k;
-  L.R_cap = (int64_t)align_up((size_t)L.A_cap, kBN) + (int64_t)kBN * E;
+  // Segments of the pair dispatch take up to 4/3 of their rows plus a 128-row tail
+  // (segment_rows); every other dispatch at most its rows plus 127.
+  L.R_cap = (int64_t)align_up((size_t)((L.A_cap * kPairStride + kBNPair - 1) / kBNPair), kBN) +
+            (int64_t)kBN * E;
   L.tiles_cap = L.A_cap / kBNNarrow + E + 1;   // enough for narrow tiles too
   size_t o = 0;
   auto take = [&](size_t bytes) {
@@ -339,7 +342,7 @@ moe_status pre_dispatch_impl(const moe_dims* d, const void* x, const int32_t* id
   if (e != cudaSuccess) return cuda_fail(e, "bucket kernel");
   {
     ProfScope ps("quantize_scatter", st);
-    e = launch_quantize_scatter(s, x, ids, tw, T, p, pull, sf_layout_rows(tile_rows), st);
+    e = launch_quantize_scatter(s, x, ids, tw, T, p, pull, tile_rows, st);
   }
   if (e != cudaSuccess) return cuda_fail(e, "quantize kernel");
   mark_dispatched(ws, tile_rows);

@@ -29,8 +29,26 @@ constexpr int kSFStageBytes = 2 * kSFAtomBytes;  // 8 scale columns per k-block
 constexpr int kBNNarrow = 32;
 constexpr int kBNMedium = 64;
 // Token tiles of the pair kernel (two SMs share each item, tcgen05 cta_group::2): up
-// to 256 rows, two 128x4 scale blocks; expert segments padded to kBN rows.
-constexpr int kBNPair = 256;
+// to kBNPair rows, each starting at a whole 128-row scale block, so a tile spans
+// kPairStride workspace rows of which it uses kBNPair.
+constexpr int kBNPair = 192;
+constexpr int kPairStride = 256;
+
+// Workspace row, from its expert's segment start, of the expert's r-th assignment
+// under a dispatch with token tiles of tile_rows rows.
+__host__ __device__ __forceinline__ int tile_row_of_rank(int r, int tile_rows) {
+  return tile_rows == kBNPair ? (r / kBNPair) * kPairStride + r % kBNPair : r;
+}
+
+// Workspace rows of an expert segment holding n assignments: whole tiles (tiles of up
+// to 128 rows), or whole kPairStride spans and a last partial tile padded to 128 rows.
+__host__ __device__ __forceinline__ int segment_rows(int n, int tile_rows) {
+  if (tile_rows == kBNPair) {
+    const int rem = n % kBNPair;
+    return n / kBNPair * kPairStride + (rem + kBN - 1) / kBN * kBN;
+  }
+  return (n + tile_rows - 1) / tile_rows * tile_rows;
+}
 
 // Device error bits in ws.flags[0].
 constexpr int kErrRouting = 1;
@@ -184,11 +202,13 @@ cudaError_t launch_bucket(const Shape& s, const int32_t* ids, int T, const WsPtr
 // Quantise the tokens, give every assignment its row and copy the token there.
 // pull: write each token's row once (xq/xs) instead of copying it to its k rows; the
 // layer kernel then gathers token rows itself.
-// tile_rows: token scales in the layout of tiles of that many rows (sf_tile_offset).
+// tile_rows: the dispatch's token tiles (rows from tile_row_of_rank; token scales in the
+// layout of tiles of min(tile_rows, 128) rows, sf_tile_offset).
 cudaError_t launch_quantize_scatter(const Shape& s, const void* x, const int32_t* ids,
                                     const float* tw, int T, const WsPtrs& ws, bool pull,
                                     int tile_rows, cudaStream_t st);
-// Rows of all assignments and the per-row tables, without quantising anything.
+// Rows of all assignments (128-row tiles) and the per-row tables, without quantising
+// anything.
 cudaError_t launch_assign_slots(const Shape& s, const int32_t* ids, const float* tw, int T,
                                 const WsPtrs& ws, cudaStream_t st);
 // acc [n] fp32 -> out [n] bf16 (round to nearest even).

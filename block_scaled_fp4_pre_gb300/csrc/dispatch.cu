@@ -24,9 +24,9 @@ constexpr unsigned kFull = 0xFFFFFFFFu;
 // them advances the warp's count for that expert, and a scan over warps turns the
 // counts into each warp's base.  Each block publishes its per-expert totals; the
 // last block to finish scans them over blocks (bases of later chunks) and over
-// experts (segment starts padded to tile_rows -- kBN, kBNMedium or kBNNarrow; to kBN
-// for the pair kernel's kBNPair-row tiles -- and the tile list).  Row of an assignment =
-// segment start + its chunk's base + its rank in the chunk.
+// experts (segment sizes from segment_rows -- whole tiles of tile_rows rows, or for
+// the pair kernel kPairStride-row spans -- and the tile list).  Row of an assignment =
+// segment start + tile_row_of_rank(its chunk's base + its rank in the chunk).
 
 // Lanes whose key equals this lane's key (keys < 2^nbits): one ballot per bit, which
 // measured faster here than __match_any_sync.
@@ -61,9 +61,6 @@ __global__ void __launch_bounds__(1024) bucket_kernel(const int32_t* __restrict_
   const int w0 = min(len, warp * per), w1 = min(len, w0 + per);
   int nbits = 1;
   while ((1 << nbits) <= E + 1) ++nbits;  // keys 0..E+1
-  // Segments are padded to whole tiles, or (tiles of two 128-row scale blocks) to
-  // whole 128-row blocks, so that every tile starts at row 0 of a scale block.
-  const int seg_pad = tile_rows > kBN ? kBN : tile_rows;
 
   for (int i = tid; i < 32 * E; i += blockDim.x) cnt[i] = 0;
   for (int i = tid; i < len; i += blockDim.x) {
@@ -152,7 +149,7 @@ __global__ void __launch_bounds__(1024) bucket_kernel(const int32_t* __restrict_
     const int e = warp * 32 + lane;
     const int n = e < E ? tot[e] : 0;
     tiles = (n + tile_rows - 1) / tile_rows;
-    rows = (n + seg_pad - 1) / seg_pad * seg_pad;
+    rows = segment_rows(n, tile_rows);   // every tile starts at row 0 of a scale block
     ir = rows;
     it = tiles;
 #pragma unroll
@@ -202,7 +199,8 @@ __global__ void __launch_bounds__(1024) bucket_kernel(const int32_t* __restrict_
     ws.counts[e] = n;
     ws.seg[e] = seg[e];
     for (int i = 0, r = 0; r < n; ++i, r += tile_rows) {
-      ws.tiles[tst[e] + i] = make_int4(e, seg[e] + r, min(tile_rows, n - r), 0);
+      ws.tiles[tst[e] + i] =
+          make_int4(e, seg[e] + tile_row_of_rank(r, tile_rows), min(tile_rows, n - r), 0);
       ws.tile_done[tst[e] + i] = 0;
     }
   }
@@ -218,13 +216,16 @@ __global__ void __launch_bounds__(1024) bucket_kernel(const int32_t* __restrict_
   }
 }
 
-// Row of assignment a (or -1 for an id outside [0, E)), and the per-row tables.
+// Row of assignment a (or -1 for an id outside [0, E)), and the per-row tables, for a
+// dispatch with token tiles of tile_rows rows.
 __device__ __forceinline__ int assign_slot(int a, int k, int E, const int32_t* __restrict__ ids,
-                                           const float* __restrict__ tw, const WsPtrs& ws) {
+                                           const float* __restrict__ tw, const WsPtrs& ws,
+                                           int tile_rows) {
   const int e = ids[a];
   int slot = -1;
   if (e >= 0 && e < E) {
-    slot = ws.seg[e] + ws.blk_base[(size_t)(a / kBucketChunk) * E + e] + ws.local_rank[a];
+    const int rank = ws.blk_base[(size_t)(a / kBucketChunk) * E + e] + ws.local_rank[a];
+    slot = ws.seg[e] + tile_row_of_rank(rank, tile_rows);
     ws.slot_token[slot] = a / k;
     ws.slot_assign[slot] = a;
     ws.slot_weight[slot] = tw[a];
@@ -237,7 +238,7 @@ __global__ void assign_slots_kernel(const int32_t* __restrict__ ids, const float
                                     int A, int k, int E, WsPtrs ws) {
   ptx::pdl_wait();
   for (int a = blockIdx.x * blockDim.x + threadIdx.x; a < A; a += gridDim.x * blockDim.x)
-    assign_slot(a, k, E, ids, tw, ws);
+    assign_slot(a, k, E, ids, tw, ws, kBN);
 }
 
 // ---------------------------------------------------------------------------
@@ -332,11 +333,12 @@ __global__ void __launch_bounds__(256) quantize_scatter_kernel(const __nv_bfloat
     }
   }
   ptx::pdl_wait();
-  if (tid < k) slots[tid] = assign_slot(t * k + tid, k, E, ids, tw, ws);
+  if (tid < k) slots[tid] = assign_slot(t * k + tid, k, E, ids, tw, ws, tile_rows);
   if (pull) return;
   __syncthreads();
   const int nsf = H / kGroup;      // scale bytes of a row
   const int kc4 = nsf / 4;
+  const int sf_rows = tile_rows > kBN ? kBN : tile_rows;   // pair tiles: whole 128-row blocks
   const size_t row_bytes = (size_t)row_bytes_q;
   for (int j = 0; j < k; ++j) {
     const int slot = slots[j];
@@ -345,7 +347,7 @@ __global__ void __launch_bounds__(256) quantize_scatter_kernel(const __nv_bfloat
     for (int i = tid; i < row_bytes_q / 16; i += blockDim.x)   // 16-byte chunks of the row
       dst[i] = reinterpret_cast<const uint4*>(codes_sh)[i];
     for (int i = tid; i < nsf; i += blockDim.x)
-      ws.xsf[sf_tile_offset((size_t)slot, i, kc4, tile_rows)] = sf_sh[i];
+      ws.xsf[sf_tile_offset((size_t)slot, i, kc4, sf_rows)] = sf_sh[i];
   }
 }
 

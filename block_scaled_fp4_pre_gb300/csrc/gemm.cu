@@ -820,9 +820,12 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
       }
       if (MODE == kModeLayer && item_phase == 0) {
         // Publish: this item's intermediate rows (and scales) are written.
-        __threadfence();
+        // The epilogue threads' stores are ordered before the barrier at block scope;
+        // one thread's GPU-scope fence after it then releases them all (fences are
+        // cumulative), instead of every thread waiting out a fence of its own.
         ptx::named_bar_sync(2, 128);
         if (ep_tid == 0) {
+          __threadfence();
           ptx::fence_proxy_async_global();
           atomicAdd(&args.ws.tile_done[item_tile], 1);
         }

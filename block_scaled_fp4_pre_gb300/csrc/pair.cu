@@ -15,15 +15,19 @@
 // operand stream from L2 is bound by the bytes each SM can hold in flight.  Here a
 // 2-CTA cluster on two SMs issues one M=256 MMA over both CTAs' shared memory: each
 // CTA stages its own 128-row weight slab (one of the item's two) and half of a
-// 256-row token tile, and receives 128 x 256 accumulators -- twice the FLOPs per
-// staged byte, with no multicast.
+// 192-row token tile, and receives 128 x 192 accumulators -- 1.6 times the FLOPs per
+// staged byte, with no multicast.  Two 192-column accumulators fit one SM's tensor
+// memory with the scale registers, so an item's MMAs never wait for the previous
+// item's epilogue to read its accumulator.
 //
-// Items are (token tile <= 256 rows, pair of 128-row weight slabs), first every
+// Items are (token tile <= 192 rows, pair of 128-row weight slabs), first every
 // gate/up item, then every down item, each phase expert by expert, slab pair by slab
 // pair, then by the expert's token tiles.  Cluster c takes items c, c + C, c + 2C, ...
 // (C clusters, all resident), so both CTAs of a pair know the sequence without
 // talking; every gate/up item of a tile precedes its down items in every cluster's
 // sequence, so a down item's bounded wait for its tile's intermediate rows ends.
+// Token tiles start at whole 128-row scale blocks (kPairStride-row spans, see
+// tile_row_of_rank), so a tile's token scales are one or two whole blocks.
 //
 // Roles (320 threads, one CTA per SM, one pair per two SMs):
 //   warp 0      lane 0: items into the CTA's ring; TMA loads of this CTA's weight slab,
@@ -34,7 +38,7 @@
 //               lane 0 issues the scale copies and MMAs for the pair and commits them
 //               to the stage, accumulator and exit barriers of both CTAs.
 //   warps 2-9   epilogue: warp w reads lane quarter w % 4 of its CTA's accumulator,
-//               columns [128h, 128h + 128) with h = (w - 2) / 4.
+//               the 16-column chunks c with c % 2 == (w - 2) / 4.
 // Every wait is bounded (kWaitLimitNs); a timeout sets the workspace error flag and
 // each role leaves its loop; both CTAs meet at a cluster barrier before the tensor
 // memory is freed.
@@ -47,22 +51,24 @@
 namespace mxmoe {
 namespace {
 
-constexpr int kStages = 6;
+constexpr int kStages = 7;
 constexpr int kThreads = 320;
 constexpr int kEpiWarps = 8;
 constexpr int kTmemCols = 512;
-constexpr int kAccCols = kBNPair;                 // 128 lanes x up to 256 fp32 columns
-// Scale registers after the accumulator, two buffers: A (this CTA's 128 rows) 4
-// columns per 128-element scale block, B (up to 256 token rows = two 128-row blocks)
-// 8 columns per scale block (block b of rows at +4b).
+constexpr int kAccCols = kBNPair;                 // 128 lanes x up to 192 fp32 columns
+constexpr int kAccBufs = 2;
+// Scale registers after the two accumulators, two buffers: A (this CTA's 128 rows) 4
+// columns per 128-element scale block, B (up to 192 token rows, two 128-row blocks) 8
+// columns per scale block (block b of rows at +4b).
 constexpr int kSfaCols = 8;
 constexpr int kSfCols = kSfaCols + 16;
-constexpr int kSfBase = kAccCols;
-constexpr int kSpareBase = kSfBase + 2 * kSfCols;  // copies of accumulator chunks
+constexpr int kSfBase = kAccBufs * kAccCols;
+static_assert(kSfBase + 2 * kSfCols <= kTmemCols, "tensor memory layout");
 constexpr int kEpiCols = 16;
-constexpr int kSpareChunks = 6;                   // per column half (96 columns)
-static_assert(kSpareBase + 2 * kSpareChunks * kEpiCols <= kTmemCols, "tensor memory layout");
+constexpr int kMaxChunks = kBNPair / kEpiCols;    // 12 column chunks an item
 constexpr int kBoxRows = 16;                      // token rows of a partial-tile TMA box
+constexpr int kHalfRows = kBNPair / 2;            // token rows a CTA stages (full tile)
+constexpr int kBSlot = kHalfRows * kBKBytes;      // 12 KiB
 constexpr int kRing = 8;
 constexpr unsigned kFull = 0xFFFFFFFFu;
 constexpr int kSfaBytes = 2 * kSFAtomBytes;       // one k-block of one 128-row slab
@@ -74,15 +80,15 @@ enum PairMode { kModeLayer = 0, kModeRaw = 1 };
 // scales), then the tail.
 constexpr size_t kSmA = 0;
 constexpr size_t kSmB = kSmA + (size_t)kStages * kATileBytes;
-constexpr size_t kSmSfa = kSmB + (size_t)kStages * kBTileBytes;
+constexpr size_t kSmSfa = kSmB + (size_t)kStages * kBSlot;
 constexpr size_t kSmSfb = kSmSfa + (size_t)kStages * kSfaBytes;
 constexpr size_t kSmTail = kSmSfb + (size_t)kStages * kSfbBytes;
 
 struct __align__(16) PairTail {
   uint64_t full[kStages];    // leader: both CTAs' loads of a stage landed
   uint64_t empty[kStages];   // each CTA: the pair's MMAs are done with its stage
-  uint64_t acc_full;         // each CTA: the item's accumulator is complete
-  uint64_t acc_empty;        // leader: all 16 epilogue warps have read it
+  uint64_t acc_full[kAccBufs];    // each CTA: the item's accumulator is complete
+  uint64_t acc_empty[kAccBufs];   // leader: all 16 epilogue warps have read it
   uint64_t mma_done;         // leader: every MMA it issued has finished
   uint64_t ring_full[kRing];
   uint64_t ring_empty[kRing];
@@ -92,6 +98,7 @@ struct __align__(16) PairTail {
   float xchg[2][2][4][kEpiCols];                 // [half][buffer][quarter][column]
   alignas(16) uint8_t hstage[2][2][kEpiCols][32];
   alignas(4) uint8_t sstage[2][2][kEpiCols][2];
+  int32_t tile_start[1025];  // first tile of each expert (E <= 1024), see decode_pair_item
 };
 constexpr size_t kSmemBytes = kSmTail + sizeof(PairTail) + 1024;   // + alignment slack
 static_assert(kSmemBytes <= 227 * 1024, "one CTA per SM");
@@ -116,7 +123,8 @@ struct PairItem {
 };
 
 // Item g of the phase-major, expert-major, slab-pair-major, tile-minor order;
-// tile_start[e] is expert e's first tile (experts without tokens repeat it).
+// tile_start[e] (shared memory) is expert e's first tile (experts without tokens
+// repeat it).
 __device__ __forceinline__ PairItem decode_pair_item(int g, int n0, int m0, int m1, int E,
                                                      const int32_t* __restrict__ tile_start) {
   PairItem it;
@@ -130,13 +138,13 @@ __device__ __forceinline__ PairItem decode_pair_item(int g, int n0, int m0, int 
   int lo = 0, hi = E - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (__ldg(&tile_start[mid]) * m <= g)
+    if (tile_start[mid] * m <= g)
       lo = mid;
     else
       hi = mid - 1;
   }
-  const int t0 = __ldg(&tile_start[lo]);
-  const int ntiles = __ldg(&tile_start[lo + 1]) - t0;
+  const int t0 = tile_start[lo];
+  const int ntiles = tile_start[lo + 1] - t0;
   it.e = lo;
   const int local = g - t0 * m;
   it.mp = local / ntiles;
@@ -160,10 +168,13 @@ __device__ __forceinline__ uint32_t cluster_count() {
 }
 
 // Tensor maps: weight codes (128-row boxes of k-block tiles), token/intermediate rows
-// (a whole 128-row half-tile, or 16-row boxes), and every scale region viewed as
-// 256-byte rows (4-row boxes: two 512-byte scale blocks).
+// (one map per half-tile height 16, 32, .., 96 rows, so that a stage's token rows are
+// one copy), and every scale region viewed as 256-byte rows (4-row boxes: two
+// 512-byte scale blocks).  Each copy costs the issuing SM's TMA unit about the same
+// whatever its size, so fewer, larger boxes keep more bytes in flight.
+constexpr int kHalfSizes = kHalfRows / kBoxRows;   // 6
 struct PairMaps {
-  CUtensorMap w[2], t128[2], t16[2], wsf[2], tsf[2];
+  CUtensorMap w[2], wsf[2], tsf[2], t[2][kHalfSizes];
 };
 
 template <int MODE>
@@ -183,8 +194,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       ptx::mbar_init(&tail->full[s], 1);
       ptx::mbar_init(&tail->empty[s], 1);
     }
-    ptx::mbar_init(&tail->acc_full, 1);
-    ptx::mbar_init(&tail->acc_empty, 2 * kEpiWarps);
+    for (int b = 0; b < kAccBufs; ++b) {
+      ptx::mbar_init(&tail->acc_full[b], 1);
+      ptx::mbar_init(&tail->acc_empty[b], 2 * kEpiWarps);
+    }
     ptx::mbar_init(&tail->mma_done, 1);
     for (int r = 0; r < kRing; ++r) {
       ptx::mbar_init(&tail->ring_full[r], 1);
@@ -194,8 +207,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     ptx::fence_mbar_init();
     for (int p = 0; p < 2; ++p) {
       ptx::prefetch_tmap(&maps.w[p]);
-      ptx::prefetch_tmap(&maps.t128[p]);
-      ptx::prefetch_tmap(&maps.t16[p]);
+      for (int h = 0; h < kHalfSizes; ++h) ptx::prefetch_tmap(&maps.t[p][h]);
       ptx::prefetch_tmap(&maps.wsf[p]);
       ptx::prefetch_tmap(&maps.tsf[p]);
     }
@@ -216,7 +228,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   const int num_tiles = args.ws.flags[kFlagTiles];
   const int E = args.E;
-  const int32_t* tile_start = args.ws.tile_start;
+  const int32_t* tile_start = tail->tile_start;
+  for (int e = threadIdx.x; e <= E; e += blockDim.x) tail->tile_start[e] = args.ws.tile_start[e];
+  __syncthreads();
   const int m0 = args.ph[0].m_pairs, m1 = args.ph[1].m_pairs;
   const int n0 = num_tiles * m0;
   const int total = n0 + (args.num_phases == 2 ? num_tiles * m1 : 0);
@@ -231,18 +245,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint64_t pol_shared = ptx::policy_evict_normal();
       const uint64_t pol_t = ptx::policy_evict_last();
       const uint32_t full0 = ptx::mapa_shared(ptx::smem_addr(&tail->full[0]), 0);
+      const uint32_t s_a = ptx::smem_addr(smem + kSmA), s_b = ptx::smem_addr(smem + kSmB);
+      const uint32_t s_sfa = ptx::smem_addr(smem + kSmSfa), s_sfb = ptx::smem_addr(smem + kSmSfb);
       int stage = 0, r = 0;
       uint32_t phase = 0, rph = 0;
       int64_t issued = 0;
       bool ok = true;
+      // Items are decoded one ahead: the next item's table reads overlap the loads of
+      // the current one.
+      PairItem it = {};
+      int4 ti = make_int4(0, 0, 0, 0);
+      if (pair < total) {
+        it = decode_pair_item(pair, n0, m0, m1, E, tile_start);
+        ti = args.ws.tiles[it.tile];
+      }
       for (int g = pair;; g += npairs) {
         const bool live = g < total;
-        PairItem it = {};
-        int4 ti = make_int4(0, 0, 0, 0);
-        if (live) {
-          it = decode_pair_item(g, n0, m0, m1, E, tile_start);
-          ti = args.ws.tiles[it.tile];
-        }
         if (!ptx::mbar_wait(&tail->ring_empty[r], rph ^ 1u, abort_flag, kWaitLimitNs)) {
           ok = false;
           break;
@@ -257,7 +275,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (!live) break;
         const PairPhase& P = args.ph[it.phase];
         const int row0 = ti.y, n = ti.z;
-        const int nmma = (n + 31) / 32 * 32;       // MMA N: a multiple of 32, <= 256
+        const int nmma = (n + 31) / 32 * 32;       // MMA N: a multiple of 32, <= 192
         const int half = nmma / 2;                 // token rows this CTA stages
         const int nblk = nmma > kBN ? 2 : 1;       // 128-row token scale blocks
         const int wslab = it.e * (2 * P.m_pairs) + it.mp * 2 + (int)rank;
@@ -265,9 +283,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const CUtensorMap* tw = &maps.w[it.phase];
         const CUtensorMap* twsf = &maps.wsf[it.phase];
         const CUtensorMap* ttsf = &maps.tsf[it.phase];
+        const CUtensorMap* tb = &maps.t[it.phase][half / kBoxRows - 1];   // half rows a box
         // A pair of slabs read by one token tile only is not kept; one shared by
         // several tiles of the expert stays for them.
-        const int ntiles = __ldg(&tile_start[it.e + 1]) - __ldg(&tile_start[it.e]);
+        const int ntiles = tile_start[it.e + 1] - tile_start[it.e];
+        const int g_next = g + npairs;
+        PairItem it_next = {};
+        int4 ti_next = make_int4(0, 0, 0, 0);
         const uint64_t pol_w = ntiles > 1 ? pol_shared : pol_once;
         // Both CTAs' bytes of a stage, all counted on the leader's barrier.
         const uint32_t bytes =
@@ -278,6 +300,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (!ok) break;
           ptx::fence_proxy_async_global();
         }
+        // Coordinates of k-block 0; each k-block adds one tile (128 map rows) to the
+        // weight box, 128 bytes to the token box and two scale blocks (4 rows) to both
+        // scale boxes.
+        int wy = wslab * P.num_kb * kBM;
+        int sfay = wslab * P.kc4 * 2;
+        int sfby = (row0 / kBN) * P.kc4 * 2;
+        int bx = 0;
+        const int sfb_next = P.kc4 * 2;   // the tile's second scale block, in 256-byte rows
         for (int kb = 0; kb < P.num_kb; ++kb) {
           if (!ptx::mbar_wait(&tail->empty[stage], phase ^ 1u, abort_flag, kWaitLimitNs)) {
             ok = false;
@@ -285,23 +315,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           const uint32_t bar = full0 + (uint32_t)stage * 8u;
           if (leader) ptx::mbar_arrive_expect_tx(&tail->full[stage], bytes);
-          ptx::tma_load_2d_pair(smem + kSmA + (size_t)stage * kATileBytes, tw, 0,
-                                (wslab * P.num_kb + kb) * kBM, bar, pol_w);
+          ptx::tma_load_2d_pair(s_a + (uint32_t)stage * kATileBytes, tw, 0, wy, bar, pol_w);
           // the slab's two scale blocks of this k-block: 1 KiB = four 256-byte rows
-          ptx::tma_load_2d_pair(smem + kSmSfa + (size_t)stage * kSfaBytes, twsf, 0,
-                                (wslab * P.kc4 + 2 * kb) * 2, bar, pol_w);
-          uint8_t* b_dst = smem + kSmB + (size_t)stage * kBTileBytes;
-          if (half == kBN) {
-            ptx::tma_load_2d_pair(b_dst, &maps.t128[it.phase], kb * kBKBytes, brow, bar, pol_t);
-          } else {
-            for (int j = 0; j < half / kBoxRows; ++j)
-              ptx::tma_load_2d_pair(b_dst + j * kBoxRows * kBKBytes, &maps.t16[it.phase],
-                                    kb * kBKBytes, brow + j * kBoxRows, bar, pol_t);
-          }
+          ptx::tma_load_2d_pair(s_sfa + (uint32_t)stage * kSfaBytes, twsf, 0, sfay, bar, pol_w);
+          ptx::tma_load_2d_pair(s_b + (uint32_t)stage * kBSlot, tb, bx, brow, bar, pol_t);
           // the whole tile's token scale blocks (every CTA's MMA reads all N columns)
-          for (int b = 0; b < nblk; ++b)
-            ptx::tma_load_2d_pair(smem + kSmSfb + (size_t)stage * kSfbBytes + b * kSfaBytes, ttsf,
-                                  0, ((row0 / kBN + b) * P.kc4 + 2 * kb) * 2, bar, pol_t);
+          const uint32_t d_sfb = s_sfb + (uint32_t)stage * kSfbBytes;
+          ptx::tma_load_2d_pair(d_sfb, ttsf, 0, sfby, bar, pol_t);
+          if (nblk == 2) ptx::tma_load_2d_pair(d_sfb + kSfaBytes, ttsf, 0, sfby + sfb_next, bar, pol_t);
+          wy += kBM;
+          sfay += 4;
+          sfby += 4;
+          bx += kBKBytes;
+          if (kb == 0 && g_next < total) {
+            it_next = decode_pair_item(g_next, n0, m0, m1, E, tile_start);
+            ti_next = args.ws.tiles[it_next.tile];
+          }
           ++issued;
           if (++stage == kStages) {
             stage = 0;
@@ -309,6 +338,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
         }
         if (!ok) break;
+        it = it_next;
+        ti = ti_next;
       }
       if (!ok) atomicOr(&args.ws.flags[0], kErrTimeout);
       // Drain: the pair's MMAs are done reading this CTA's last stages (they commit to
@@ -325,10 +356,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (leader && lane == 0) {
       const uint32_t empty_l = ptx::mapa_shared(ptx::smem_addr(&tail->empty[0]), 0);
       const uint32_t empty_p = ptx::mapa_shared(ptx::smem_addr(&tail->empty[0]), 1);
-      const uint32_t accf_l = ptx::mapa_shared(ptx::smem_addr(&tail->acc_full), 0);
-      const uint32_t accf_p = ptx::mapa_shared(ptx::smem_addr(&tail->acc_full), 1);
+      const uint32_t accf_l = ptx::mapa_shared(ptx::smem_addr(&tail->acc_full[0]), 0);
+      const uint32_t accf_p = ptx::mapa_shared(ptx::smem_addr(&tail->acc_full[0]), 1);
+      // stage 0's operand descriptors; stage s adds s times a stage's bytes / 16
+      const uint64_t da0 = ptx::desc_sw128(ptx::smem_addr(smem + kSmA));
+      const uint64_t db0 = ptx::desc_sw128(ptx::smem_addr(smem + kSmB));
+      const uint64_t dsa0 = ptx::desc_sf(ptx::smem_addr(smem + kSmSfa));
+      const uint64_t dsb0 = ptx::desc_sf(ptx::smem_addr(smem + kSmSfb));
+      const uint32_t sf_t0 = tmem_base + (uint32_t)kSfBase;
       int stage = 0, r = 0;
-      uint32_t phase = 0, rph = 0, acc_phase = 0, sfbuf = 0;
+      uint32_t phase = 0, rph = 0, sfbuf = 0;
+      int items = 0;   // items issued so far: accumulator buffer items % 2
       bool ok = true;
       while (true) {
         if (!ptx::mbar_wait(&tail->ring_full[r], rph, abort_flag, kWaitLimitNs)) {
@@ -346,38 +384,52 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int n = rec.z & 0xFFFF;
         const int nmma = (n + 31) / 32 * 32;
         const int nblk = nmma > kBN ? 2 : 1;
-        if (!ptx::mbar_wait(&tail->acc_empty, acc_phase ^ 1u, abort_flag, kWaitLimitNs)) {
+        const int ab = items & 1;
+        const uint32_t use = (uint32_t)(items >> 1);   // earlier uses of this buffer
+        // the epilogue of this buffer's previous item has read it
+        if (!ptx::mbar_wait(&tail->acc_empty[ab], (use & 1u) ^ 1u, abort_flag, kWaitLimitNs)) {
           ok = false;
           break;
         }
         ptx::tc_fence_after();
+        // This one thread issues every tensor-core instruction of the pair, so its own
+        // work per k-block is kept to the instructions themselves: descriptors advance
+        // with the stage, the two instruction descriptors are set per item, and a
+        // whole k-block's copies and MMAs are unrolled.
+        const uint32_t d_tmem = tmem_base + (uint32_t)(ab * kAccCols);
+        const uint32_t id0 = ptx::idesc_mxf4_m(2 * kBM, nmma, 0);
+        const uint32_t id2 = ptx::idesc_mxf4_m(2 * kBM, nmma, 2);
+        const int whole_kb = P.K / kBK;   // a last k-block of 128 elements follows these
         for (int kb = 0; kb < P.num_kb; ++kb) {
           if (!ptx::mbar_wait(&tail->full[stage], phase, abort_flag, kWaitLimitNs)) {
             ok = false;
             break;
           }
           ptx::tc_fence_after();
-          const int kvalid = min(kBK, P.K - kb * kBK);
-          const int atoms = kvalid / 128;
-          const uint32_t sfa_t = tmem_base + (uint32_t)(kSfBase + sfbuf * kSfCols);
+          const uint32_t sfa_t = sf_t0 + (sfbuf ? (uint32_t)kSfCols : 0u);
           const uint32_t sfb_t = sfa_t + kSfaCols;
-          const uint32_t sa = ptx::smem_addr(smem + kSmSfa + (size_t)stage * kSfaBytes);
-          const uint32_t sb = ptx::smem_addr(smem + kSmSfb + (size_t)stage * kSfbBytes);
-          for (int a = 0; a < atoms; ++a) {
-            ptx::tc_cp_sf_pair(sfa_t + a * 4, ptx::desc_sf(sa + a * kSFAtomBytes));
-            for (int b = 0; b < nblk; ++b)
-              ptx::tc_cp_sf_pair(sfb_t + a * 8 + b * 4,
-                                 ptx::desc_sf(sb + b * kSfaBytes + a * kSFAtomBytes));
+          const uint64_t da = da0 + (uint64_t)(stage * (kATileBytes >> 4));
+          const uint64_t db = db0 + (uint64_t)(stage * (kBSlot >> 4));
+          const uint64_t dsa = dsa0 + (uint64_t)(stage * (kSfaBytes >> 4));
+          const uint64_t dsb = dsb0 + (uint64_t)(stage * (kSfbBytes >> 4));
+          const uint32_t acc0 = kb != 0 ? 1u : 0u;
+          // scale block a of B's 128-row block b: smem dsb + (b * 1024 + a * 512) / 16,
+          // tensor memory sfb_t + 8 a + 4 b; A's atom a: dsa + a * 512 / 16, sfa_t + 4 a
+          ptx::tc_cp_sf_pair(sfa_t, dsa);
+          ptx::tc_cp_sf_pair(sfb_t, dsb);
+          if (nblk == 2) ptx::tc_cp_sf_pair(sfb_t + 4, dsb + 64);
+          if (kb < whole_kb) {
+            ptx::tc_cp_sf_pair(sfa_t + 4, dsa + 32);
+            ptx::tc_cp_sf_pair(sfb_t + 8, dsb + 32);
+            if (nblk == 2) ptx::tc_cp_sf_pair(sfb_t + 12, dsb + 96);
           }
-          const uint32_t a_base = ptx::smem_addr(smem + kSmA + (size_t)stage * kATileBytes);
-          const uint32_t b_base = ptx::smem_addr(smem + kSmB + (size_t)stage * kBTileBytes);
-          const int steps = kvalid / 64;   // K = 64 per MMA
-          for (int s = 0; s < steps; ++s)
-            ptx::tc_mma_mxf4_pair(tmem_base, ptx::desc_sw128(a_base + s * 32),
-                                  ptx::desc_sw128(b_base + s * 32),
-                                  ptx::idesc_mxf4_m(2 * kBM, nmma, (s & 1) * 2),
-                                  sfa_t + (s >> 1) * 4, sfb_t + (s >> 1) * 8,
-                                  (kb | s) != 0 ? 1u : 0u);
+          // K = 64 per MMA (32 bytes of each operand row: +2 in a descriptor)
+          ptx::tc_mma_mxf4_pair(d_tmem, da, db, id0, sfa_t, sfb_t, acc0);
+          ptx::tc_mma_mxf4_pair(d_tmem, da + 2, db + 2, id2, sfa_t, sfb_t, 1u);
+          if (kb < whole_kb) {
+            ptx::tc_mma_mxf4_pair(d_tmem, da + 4, db + 4, id0, sfa_t + 4, sfb_t + 8, 1u);
+            ptx::tc_mma_mxf4_pair(d_tmem, da + 6, db + 6, id2, sfa_t + 4, sfb_t + 8, 1u);
+          }
           ptx::tc_commit_pair(empty_l + (uint32_t)stage * 8u);
           ptx::tc_commit_pair(empty_p + (uint32_t)stage * 8u);
           sfbuf ^= 1u;
@@ -387,9 +439,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
         }
         if (!ok) break;
-        ptx::tc_commit_pair(accf_l);
-        ptx::tc_commit_pair(accf_p);
-        acc_phase ^= 1u;
+        ptx::tc_commit_pair(accf_l + (uint32_t)ab * 8u);
+        ptx::tc_commit_pair(accf_p + (uint32_t)ab * 8u);
+        ++items;
       }
       if (!ok) atomicOr(&args.ws.flags[0], kErrTimeout);
       // Whatever happened, every MMA issued here finishes before the pair's memory goes.
@@ -401,11 +453,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ epilogue
     const int ew = warp - 2;                 // 0..7
     const int q = warp & 3;                  // tensor-memory lane quarter of this warp
-    const int hh = ew >> 2;                  // column half: tile columns [128 hh, 128 hh + 128)
+    const int hh = ew >> 2;                  // chunk parity: chunks hh, hh + 2, ...
     const int ep_tid = threadIdx.x - 64;     // 0..255
-    const uint32_t acc_empty_l = ptx::mapa_shared(ptx::smem_addr(&tail->acc_empty), 0);
-    int r = 0, xb = 0;
-    uint32_t rph = 0, acc_phase = 0;
+    const uint32_t acc_empty_l = ptx::mapa_shared(ptx::smem_addr(&tail->acc_empty[0]), 0);
+    int r = 0, xb = 0, items = 0;
+    uint32_t rph = 0;
     while (true) {
       if (!ptx::mbar_wait(&tail->ring_full[r], rph, abort_flag, kWaitLimitNs)) {
         if (ep_tid == 0) atomicOr(&args.ws.flags[0], kErrTimeout);
@@ -423,41 +475,43 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const int item_phase = item < n0 ? 0 : 1;
       const int row0 = rec.y, n = rec.z & 0xFFFF, mp = rec.z >> 16, item_tile = rec.w;
       const int slab = mp * 2 + (int)rank;   // this CTA's 128-row weight slab of the expert
-      const int cbase = hh * kBN;            // first tile column of this half
-      const int nh = max(0, min(kBN, n - cbase));
-      const int hrow0 = row0 + cbase;        // workspace row of this half's column 0
-      // Down items: the half's row metadata, read while the MMAs run (lane l holds
-      // columns l, l+32, l+64, l+96).
-      int tok_r[kBN / 32];
-      float w_r[kBN / 32];
+      const int ab = items & 1;
+      const uint32_t use = (uint32_t)(items >> 1);
+      ++items;
+      const int nch = (n + kEpiCols - 1) / kEpiCols;
+      // Down items: row metadata of this warp's chunks (ci = hh + 2k covers columns
+      // 32k + 16hh .. +15), read while the MMAs run: lane 16hh + j holds column
+      // 32k + 16hh + j in register k.
+      int tok_r[kMaxChunks / 2];
+      float w_r[kMaxChunks / 2];
 #pragma unroll
-      for (int i = 0; i < kBN / 32; ++i) {
-        tok_r[i] = 0;
-        w_r[i] = 0.f;
-        if (MODE == kModeLayer && item_phase == 1 && lane + 32 * i < nh) {
-          tok_r[i] = args.ws.slot_token[hrow0 + lane + 32 * i];
-          w_r[i] = args.ws.slot_weight[hrow0 + lane + 32 * i];
+      for (int k = 0; k < kMaxChunks / 2; ++k) {
+        const int col = 32 * k + lane;
+        tok_r[k] = 0;
+        w_r[k] = 0.f;
+        if (MODE == kModeLayer && item_phase == 1 && (lane >> 4) == hh && col < n) {
+          tok_r[k] = args.ws.slot_token[row0 + col];
+          w_r[k] = args.ws.slot_weight[row0 + col];
         }
       }
-      if (!ptx::mbar_wait(&tail->acc_full, acc_phase, abort_flag, kWaitLimitNs)) {
+      if (!ptx::mbar_wait(&tail->acc_full[ab], use & 1u, abort_flag, kWaitLimitNs)) {
         if (ep_tid == 0) atomicOr(&args.ws.flags[0], kErrTimeout);
         break;
       }
-      acc_phase ^= 1u;
       ptx::tc_fence_after();
-      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)cbase;
-      const uint32_t tspare = tmem_base + ((uint32_t)(q * 32) << 16) +
-                              (uint32_t)(kSpareBase + hh * kSpareChunks * kEpiCols);
-      auto chunk = [&](const int ci, const float(&v)[kEpiCols]) {
+      const uint32_t taddr =
+          tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(ab * kAccCols);
+      // Chunk ci = hh + 2k of this warp (k: its index among the warp's chunks).
+      auto chunk = [&](const int ci, const int k, const float(&v)[kEpiCols]) {
         const int c0 = ci * kEpiCols;
-        const int ncol = min(kEpiCols, nh - c0);
+        const int ncol = min(kEpiCols, n - c0);
         if (MODE == kModeRaw) {
           const int m = slab * kBM + q * 32 + lane;
           const int col = gate_up_source_row(m, args.I);
 #pragma unroll
           for (int j = 0; j < kEpiCols; ++j) {
             if (j < ncol) {
-              const int a = args.ws.slot_assign[hrow0 + c0 + j];
+              const int a = args.ws.slot_assign[row0 + c0 + j];
               args.gate_up_debug[(size_t)a * 2 * args.I + col] = v[j];
             }
           }
@@ -466,18 +520,41 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           // (slab * 4 + q) * 16 ..+15; lane l and l ^ 8 hold one feature's gate and up.
           // Gate lanes compute column 2p, up lanes column 2p+1: one exchange each.
           const bool up_lane = (lane & 8) != 0;
-          float hv[kEpiCols / 2];
+          float hv[kEpiCols / 2], am[kEpiCols / 2];
 #pragma unroll
           for (int p = 0; p < kEpiCols / 2; ++p) {
             const float x = __shfl_xor_sync(kFull, up_lane ? v[2 * p] : v[2 * p + 1], 8);
             const float h = up_lane ? silu_times(x, v[2 * p + 1]) : silu_times(v[2 * p], x);
             hv[p] = h;
-            float a = fabsf(h);
-            a = fmaxf(a, __shfl_xor_sync(kFull, a, 1));
-            a = fmaxf(a, __shfl_xor_sync(kFull, a, 2));
-            a = fmaxf(a, __shfl_xor_sync(kFull, a, 4));
-            a = fmaxf(a, __shfl_xor_sync(kFull, a, 16));
-            if ((lane & 23) == 0) tail->xchg[hh][xb][q][2 * p + (up_lane ? 1 : 0)] = a;
+            am[p] = fabsf(h);
+          }
+          // Max |h| of each of the lane's 8 columns over the 16 lanes holding that
+          // column (lane bits 0, 1, 2 and 4), as a transposing butterfly: after the
+          // steps over bits 0, 1 and 2 each lane keeps one column, p = 4 b0 + 2 b1 + b2.
+          const bool b0 = (lane & 1) != 0, b1 = (lane & 2) != 0, b2 = (lane & 4) != 0;
+          float a4[4], a2[2];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float send = b0 ? am[i] : am[4 + i];
+            const float keep = b0 ? am[4 + i] : am[i];
+            a4[i] = fmaxf(keep, __shfl_xor_sync(kFull, send, 1));
+          }
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            const float send = b1 ? a4[i] : a4[2 + i];
+            const float keep = b1 ? a4[2 + i] : a4[i];
+            a2[i] = fmaxf(keep, __shfl_xor_sync(kFull, send, 2));
+          }
+          float a1;
+          {
+            const float send = b2 ? a2[0] : a2[1];
+            const float keep = b2 ? a2[1] : a2[0];
+            a1 = fmaxf(keep, __shfl_xor_sync(kFull, send, 4));
+          }
+          a1 = fmaxf(a1, __shfl_xor_sync(kFull, a1, 16));
+          if ((lane & 16) == 0) {
+            const int pm = (b0 ? 4 : 0) + (b1 ? 2 : 0) + (b2 ? 1 : 0);
+            tail->xchg[hh][xb][q][2 * pm + (up_lane ? 1 : 0)] = a1;
           }
           ptx::named_bar_sync(1 + hh, 128);
           const int i_kc4 = args.I / 128;
@@ -512,7 +589,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (lane < 8) {
             const int jc = q * 4 + (lane >> 1);
             if (jc < ncol) {
-              const size_t row = (size_t)hrow0 + c0 + jc;
+              const size_t row = (size_t)row0 + c0 + jc;
               const uint4 cv =
                   *reinterpret_cast<const uint4*>(&tail->hstage[hh][xb][jc][(lane & 1) * 16]);
               *reinterpret_cast<uint4*>(args.ws.hb + row * (size_t)(args.I / 2) +
@@ -521,7 +598,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           } else if (lane < 12) {
             const int jc = q * 4 + (lane - 8);
             if (jc < ncol) {
-              const size_t row = (size_t)hrow0 + c0 + jc;
+              const size_t row = (size_t)row0 + c0 + jc;
               const uint16_t sv = *reinterpret_cast<const uint16_t*>(&tail->sstage[hh][xb][jc][0]);
               *reinterpret_cast<uint16_t*>(args.ws.hsf + sf_atom_offset(row, slab * 2, i_kc4)) = sv;
             }
@@ -530,84 +607,57 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         } else {
           // Down projection: this warp holds output features slab*128 + q*32 + lane of
           // up to 16 token columns; add them, weighted, into the fp32 accumulator.
-          const int my_tok = tok_r[ci >> 1];
-          const float my_w = w_r[ci >> 1];
+          const int my_tok = tok_r[k];
+          const float my_w = w_r[k];
           const size_t feat = (size_t)slab * kBM + q * 32 + lane;
 #pragma unroll
           for (int j = 0; j < kEpiCols; ++j) {
-            const int src = (ci & 1) * kEpiCols + j;
+            const int src = hh * kEpiCols + j;
             const int tok = __shfl_sync(kFull, my_tok, src);
             const float wt = __shfl_sync(kFull, my_w, src);
             if (j < ncol) atomicAdd(args.ws.acc + (size_t)tok * args.H + feat, wt * v[j]);
           }
         }
       };
-      const int nch = (nh + kEpiCols - 1) / kEpiCols;
-      const int ncopy = min(nch, kSpareChunks);
-      // 1. The first chunks of this half into spare tensor memory, two loads in flight.
-#pragma unroll
-      for (int ci = 0; ci < kSpareChunks; ci += 2) {
-        if (ci < ncopy) {
-          uint32_t r0[kEpiCols], r1[kEpiCols];
-          const bool two = ci + 1 < ncopy;
-          ptx::tmem_ld16_issue(taddr + (uint32_t)(ci * kEpiCols), r0);
-          if (two) ptx::tmem_ld16_issue(taddr + (uint32_t)((ci + 1) * kEpiCols), r1);
-          ptx::tmem_wait_ld(r0);
-          if (two) ptx::tmem_wait_ld(r1);
-          ptx::tmem_st16(tspare + (uint32_t)(ci * kEpiCols), r0);
-          if (two) ptx::tmem_st16(tspare + (uint32_t)((ci + 1) * kEpiCols), r1);
-        }
-      }
-      // 2. The last two chunks straight into registers; then the accumulator goes back
-      //    to the MMA issuer (one arrival per warp, on the leader's barrier), so the
-      //    next item's MMAs run during this item's math.
-      constexpr int kLastTwo = kBN / kEpiCols - 2;
-      static_assert(kSpareChunks == kLastTwo, "tensor memory layout");
-      uint32_t rd[2][kEpiCols];
-#pragma unroll
-      for (int d = 0; d < 2; ++d)
-        if (kLastTwo + d < nch)
-          ptx::tmem_ld16_issue(taddr + (uint32_t)((kLastTwo + d) * kEpiCols), rd[d]);
-#pragma unroll
-      for (int d = 0; d < 2; ++d)
-        if (kLastTwo + d < nch) ptx::tmem_wait_ld(rd[d]);
-      ptx::tmem_wait_st();
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive_cluster(acc_empty_l);
-#pragma unroll
-      for (int d = 0; d < 2; ++d) {
-        if (kLastTwo + d < nch) {
-          float v[kEpiCols];
-#pragma unroll
-          for (int j = 0; j < kEpiCols; ++j) v[j] = __uint_as_float(rd[d][j]);
-          chunk(kLastTwo + d, v);
-        }
-      }
-      // 3. The copied chunks; the load of chunk ci+1 runs during the math of ci.
+      // This warp's chunks, each load issued one chunk ahead of its math; once the
+      // last load has landed the buffer goes back to the MMA issuer (one arrival per
+      // warp on the leader's barrier; the next item already runs on the other buffer).
       uint32_t ra[kEpiCols], rb[kEpiCols];
-      if (ncopy > 0) {
-        ptx::tmem_ld16_issue(tspare, ra);
-        ptx::tmem_wait_ld(ra);
-      }
+      if (hh < nch) ptx::tmem_ld16_issue(taddr + (uint32_t)(hh * kEpiCols), ra);
+      bool released = false;
 #pragma unroll
-      for (int ci = 0; ci < kSpareChunks; ++ci) {
-        if (ci >= ncopy) break;
-        uint32_t(&cur)[kEpiCols] = (ci & 1) ? rb : ra;
-        uint32_t(&nxt)[kEpiCols] = (ci & 1) ? ra : rb;
-        const bool more = ci + 1 < ncopy;
-        if (more) ptx::tmem_ld16_issue(tspare + (uint32_t)((ci + 1) * kEpiCols), nxt);
+      for (int k = 0; k < kMaxChunks / 2; ++k) {
+        const int ci = hh + 2 * k;
+        if (ci >= nch) break;
+        uint32_t(&cur)[kEpiCols] = (k & 1) ? rb : ra;
+        uint32_t(&nxt)[kEpiCols] = (k & 1) ? ra : rb;
+        ptx::tmem_wait_ld(cur);
+        if (ci + 2 < nch) {
+          ptx::tmem_ld16_issue(taddr + (uint32_t)((ci + 2) * kEpiCols), nxt);
+        } else {
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive_cluster(acc_empty_l + (uint32_t)ab * 8u);
+          released = true;
+        }
         float v[kEpiCols];
 #pragma unroll
         for (int j = 0; j < kEpiCols; ++j) v[j] = __uint_as_float(cur[j]);
-        chunk(ci, v);
-        if (more) ptx::tmem_wait_ld(nxt);
+        chunk(ci, k, v);
+      }
+      if (!released) {
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive_cluster(acc_empty_l + (uint32_t)ab * 8u);
       }
       if (MODE == kModeLayer && item_phase == 0) {
         // Publish: this CTA's slab of the tile's intermediate rows is written.
-        __threadfence();
+        // The epilogue threads' stores are ordered before the barrier at block scope;
+        // one thread's GPU-scope fence after it then releases them all (fences are
+        // cumulative), instead of every thread waiting out a fence of its own.
         ptx::named_bar_sync(3, 2 * 128);
         if (ep_tid == 0) {
+          __threadfence();
           ptx::fence_proxy_async_global();
           atomicAdd(&args.ws.tile_done[item_tile], 1);
         }
@@ -725,15 +775,18 @@ cudaError_t launch_layer_pair(const LayerLaunch& g, cudaStream_t st) {
   cudaError_t err;
   if ((err = make_map(&maps.w[0], g.w1_codes, kBKBytes, w1_rows, kBKBytes, kBM, true)) ||
       (err = make_map(&maps.w[1], g.w2_codes, kBKBytes, w2_rows, kBKBytes, kBM, true)) ||
-      (err = make_map(&maps.t128[0], g.ws.xb, xrow, (uint64_t)g.R_cap, kBKBytes, kBN, true)) ||
-      (err = make_map(&maps.t128[1], g.ws.hb, hrow, (uint64_t)g.R_cap, kBKBytes, kBN, true)) ||
-      (err = make_map(&maps.t16[0], g.ws.xb, xrow, (uint64_t)g.R_cap, kBKBytes, kBoxRows, true)) ||
-      (err = make_map(&maps.t16[1], g.ws.hb, hrow, (uint64_t)g.R_cap, kBKBytes, kBoxRows, true)) ||
+
       (err = make_sf_map(&maps.wsf[0], g.w1_sf, w1sf)) ||
       (err = make_sf_map(&maps.wsf[1], g.w2_sf, w2sf)) ||
       (err = make_sf_map(&maps.tsf[0], g.ws.xsf, xsf)) ||
       (err = make_sf_map(&maps.tsf[1], g.ws.hsf, hsf)))
     return err;
+  for (int h = 0; h < kHalfSizes; ++h) {
+    const uint32_t rows = (uint32_t)((h + 1) * kBoxRows);
+    if ((err = make_map(&maps.t[0][h], g.ws.xb, xrow, (uint64_t)g.R_cap, kBKBytes, rows, true)) ||
+        (err = make_map(&maps.t[1][h], g.ws.hb, hrow, (uint64_t)g.R_cap, kBKBytes, rows, true)))
+      return err;
+  }
   PairArgs a;
   for (int p = 0; p < 2; ++p) {
     const int rows = p == 0 ? 2 * s.I : s.H;

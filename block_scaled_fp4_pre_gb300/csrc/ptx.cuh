@@ -425,13 +425,14 @@ __device__ __forceinline__ void tc_commit_pair(uint32_t bar_cluster) {
           bar_cluster)
       : "memory");
 }
-// 2-D tiled load into this CTA's shared memory whose completion (bytes) is signalled
-// on an mbarrier of either CTA of the pair (given by its shared::cluster address).
-__device__ __forceinline__ void tma_load_2d_pair(void* smem_dst, const void* tmap, int32_t x,
+// 2-D tiled load into this CTA's shared memory (dst: its shared-window address) whose
+// completion (bytes) is signalled on an mbarrier of either CTA of the pair (given by
+// its shared::cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void* tmap, int32_t x,
                                                  int32_t y, uint32_t bar_cluster, uint64_t policy) {
   asm volatile(
       "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::"
-      "bytes.L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_addr(smem_dst)),
+      "bytes.L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar_cluster), "l"(policy)
       : "memory");
 }

@@ -141,11 +141,13 @@ MXMOE_API moe_status moe_workspace_set_dispatch(void *ws_dev, int32_t mode);
  *                     which pays when experts hold few tokens (decode-sized loads).
  *   MOE_TILES_MEDIUM: up to 64 rows a tile (segments padded to 64), four stages where
  *                     shared memory allows (three for nvf4xnvf4).
- *   MOE_TILES_PAIR:   up to 256 rows a tile (segments padded to 128), each item of the
- *                     layer run by two SMs together (a 2-CTA cluster issuing M=256
- *                     tcgen05 MMAs over both SMs' shared memory: twice the FLOPs per
- *                     staged operand byte).  mxf4xmxf4 with the bucketed dispatch and
- *                     H a multiple of 256 only; otherwise it falls back to wide tiles.
+ *   MOE_TILES_PAIR:   up to 192 rows a tile, each tile starting a 256-row span of the
+ *                     expert's segment (the last one padded to 128 rows), each item of
+ *                     the layer run by two SMs together (a 2-CTA cluster issuing M=256
+ *                     tcgen05 MMAs over both SMs' shared memory: 1.6 times the FLOPs
+ *                     per staged operand byte).  mxf4xmxf4 with the bucketed dispatch
+ *                     and H a multiple of 256 only; otherwise it falls back to wide
+ *                     tiles.
  *   MOE_TILES_AUTO (default after moe_workspace_init): narrow when num_tokens * k <=
  *                     16 * num_experts, medium when <= 64 * num_experts, else wide.
  * The choice is made at each moe_pre_dispatch and holds for the forward that
