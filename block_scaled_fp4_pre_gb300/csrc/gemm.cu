@@ -446,6 +446,12 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
+      // stage 0's operand and scale descriptors; stage s adds s times a stage's bytes / 16
+      const uint64_t da0 = ptx::desc_sw128(ptx::smem_addr(smem + SM::kA));
+      const uint64_t db0 = ptx::desc_sw128(ptx::smem_addr(smem + SM::kB));
+      const uint64_t dsa0 = ptx::desc_sf(ptx::smem_addr(smem + SM::kSFA));
+      const uint64_t dsb0 = ptx::desc_sf(ptx::smem_addr(smem + SM::kSFB));
+      const uint32_t sf_t0 = tmem_base + (uint32_t)kSfTmemBase;
       int stage = 0, r = 0;
       uint32_t phase = 0, rph = 0, acc_phase = 0, sfbuf = 0;
       bool ok = true;
@@ -473,6 +479,16 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
           break;
         }
         ptx::tc_fence_after();
+        // Whole k-blocks take a short path: this one thread issues every
+        // tensor-core instruction of the block, and the dependent latency of its own
+        // work per k-block paces the stream unless that work is little more than the
+        // instructions -- descriptors are stage 0's plus a constant, the two
+        // instruction descriptors are set per item, copies and MMAs unrolled.
+        const uint32_t id0 = ptx::idesc_mxf4(n_mma, 0), id2 = ptx::idesc_mxf4(n_mma, 2);
+        const uint32_t idn = ptx::idesc_nvf4(n_mma);
+        const uint32_t if8[4] = {ptx::idesc_f8f4(n_mma, 0), ptx::idesc_f8f4(n_mma, 1),
+                                 ptx::idesc_f8f4(n_mma, 2), ptx::idesc_f8f4(n_mma, 3)};
+        const int whole_kb = P.K / kKb;
         for (int kb = 0; kb < P.num_kb; ++kb) {
           if (!ptx::mbar_wait(&tail->full[stage], phase, abort_flag, kWaitLimitNs)) {
             ok = false;
@@ -480,6 +496,54 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
           }
           ptx::tc_fence_after();
           if (pulled) ptx::fence_proxy_async_smem();
+          if (kb < whole_kb) {
+            const uint32_t sfa_t = sf_t0 + (sfbuf ? (uint32_t)TM::kSfCols : 0u);
+            const uint32_t sfb_t = sfa_t + TM::kSfCols / 2;
+            const uint64_t dsa = dsa0 + (uint64_t)(stage * (int)(SM::kSF >> 4));
+            const uint64_t dsb = dsb0 + (uint64_t)(stage * (int)(SM::kSF >> 4));
+            const uint64_t da = da0 + (uint64_t)(stage * (kATileBytes >> 4));
+            const uint64_t db = db0 + (uint64_t)(stage * (int)(SM::kBSlot >> 4));
+            const uint32_t acc0 = kb != 0 ? 1u : 0u;
+            // Four MMAs a k-block, each 32 bytes further along every operand row (+2
+            // in a descriptor); scale blocks 512 bytes (+32) apart.
+            if constexpr (NV) {
+              // four 64-element scale blocks, MMA step s takes block s whole
+#pragma unroll
+              for (int a = 0; a < 4; ++a) {
+                ptx::tc_cp_sf(sfa_t + a * 4, dsa + 32 * a);
+                ptx::tc_cp_sf(sfb_t + a * 4, dsb + 32 * a);
+              }
+#pragma unroll
+              for (int s2 = 0; s2 < 4; ++s2)
+                ptx::tc_mma_nvf4(tmem_base, da + 2 * s2, db + 2 * s2, idn, sfa_t + s2 * 4,
+                                 sfb_t + s2 * 4, s2 == 0 ? acc0 : 1u);
+            } else if constexpr (F8) {
+              // one scale block: MMA step s takes scale byte s of each row
+              ptx::tc_cp_sf(sfa_t, dsa);
+              ptx::tc_cp_sf(sfb_t, dsb);
+              ptx::tc_mma_f8f4(tmem_base, da, db, if8[0], sfa_t, sfb_t, acc0);
+              ptx::tc_mma_f8f4(tmem_base, da + 2, db + 2, if8[1], sfa_t, sfb_t, 1u);
+              ptx::tc_mma_f8f4(tmem_base, da + 4, db + 4, if8[2], sfa_t, sfb_t, 1u);
+              ptx::tc_mma_f8f4(tmem_base, da + 6, db + 6, if8[3], sfa_t, sfb_t, 1u);
+            } else {
+              // two 128-element scale blocks, steps 0-1 and 2-3 take byte pairs 0/2
+              ptx::tc_cp_sf(sfa_t, dsa);
+              ptx::tc_cp_sf(sfb_t, dsb);
+              ptx::tc_cp_sf(sfa_t + 4, dsa + 32);
+              ptx::tc_cp_sf(sfb_t + 4, dsb + 32);
+              ptx::tc_mma_mxf4(tmem_base, da, db, id0, sfa_t, sfb_t, acc0);
+              ptx::tc_mma_mxf4(tmem_base, da + 2, db + 2, id2, sfa_t, sfb_t, 1u);
+              ptx::tc_mma_mxf4(tmem_base, da + 4, db + 4, id0, sfa_t + 4, sfb_t + 4, 1u);
+              ptx::tc_mma_mxf4(tmem_base, da + 6, db + 6, id2, sfa_t + 4, sfb_t + 4, 1u);
+            }
+            ptx::tc_commit(&tail->empty[stage]);
+            sfbuf ^= 1u;
+            if (++stage == kSt) {
+              stage = 0;
+              phase ^= 1u;
+            }
+            continue;
+          }
           const int kvalid = min(kKb, P.K - kb * kKb);
           const int atoms = kvalid / kAtomK;
           const uint32_t sfa_t = tmem_base + (uint32_t)(kSfTmemBase + sfbuf * TM::kSfCols);
