@@ -144,15 +144,31 @@ struct Item {
 
 // Item g of the phase-major, expert-major, slab-major, tile-minor order.
 // tile_start[e] is the first tile of expert e (experts without tokens repeat it).
+// grp1 > 0 (wide tiles): the down items run in groups of grp1 output slabs -- all
+// experts' items of slabs [grp1 * j, grp1 * (j + 1)) before the next group, expert-major
+// inside a group -- so that the fp32 accumulator columns a group adds into (tokens x
+// grp1 * 128 floats) stay in L2 while each token's k contributions arrive; a token's
+// adds to one column otherwise come from experts far apart in the order, after the
+// row has left L2.
 __device__ __forceinline__ Item decode_item(int g, int n0, int m0, int m1, int E,
-                                            const int32_t* __restrict__ tile_start) {
+                                            const int32_t* __restrict__ tile_start,
+                                            int num_tiles = 0, int grp1 = 0) {
   Item it;
   int m = m0;
+  int slab0 = 0;   // first slab of the item's group
   it.phase = 0;
   if (g >= n0) {
     g -= n0;
     m = m1;
     it.phase = 1;
+    if (grp1 > 0 && grp1 < m1) {
+      const int ngrp = (m1 + grp1 - 1) / grp1;
+      int j = g / (num_tiles * grp1);
+      if (j > ngrp - 1) j = ngrp - 1;
+      g -= j * num_tiles * grp1;
+      slab0 = j * grp1;
+      m = min(grp1, m1 - slab0);
+    }
   }
   // last expert e with tile_start[e] * m <= g (that expert has tiles)
   int lo = 0, hi = E - 1;
@@ -167,10 +183,19 @@ __device__ __forceinline__ Item decode_item(int g, int n0, int m0, int m1, int E
   it.e = lo;
   it.ntiles = tile_start[lo + 1] - t0;
   const int local = g - t0 * m;
-  it.mt = local / it.ntiles;
+  it.mt = slab0 + local / it.ntiles;
   it.tile = t0 + local % it.ntiles;
   return it;
 }
+
+// Output slabs a group of down items spans (wide tiles): 4 x 128 features, so that at
+// 16384 tokens the accumulator columns in use are 32 MiB.  Under the grouping the
+// intermediate rows of down items are loaded with the normal L2 policy (they are read
+// again only by the next group) and the reductions mark accumulator lines evict-last,
+// so that the group's accumulator columns, not the intermediate rows, stay in L2.
+constexpr int kDownGroup = 4;
+constexpr bool kDownRowsNormal = true;
+constexpr bool kAccKeep = true;
 
 // silu(g) * u with fast exp and divide (a few ulp; well inside the MXFP4 rounding)
 __device__ __forceinline__ float silu_times(float g, float u) {
@@ -263,6 +288,7 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
   // A tile's intermediate rows are complete once every gate/up slab has stored its
   // part (one count per slab, from whichever block computed it).
   const int slabs0 = args.ph[0].m_tiles;
+  constexpr int kGrp1 = (MODE == kModeLayer && TROWS == kBN) ? kDownGroup : 0;
 
   if (warp == 0) {
     // ------------------------------------------------- scheduler + producer
@@ -277,6 +303,8 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
     uint32_t phase = 0, rph = 0;
     int64_t issued = 0;
     bool ok = true;
+    // intermediate rows of down items under the grouped order (see kDownGroup)
+    const uint64_t pol_h = (kGrp1 > 0 && kDownRowsNormal) ? pol_shared : pol_t;
     // Items are claimed one ahead so that the claim and the table reads of the
     // next item overlap the loads of the current one.
     int g = 0;
@@ -285,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
     if (leader) {
       g = atomicAdd(&args.ws.flags[kFlagSched], 1);
       if (g < total) {
-        it = decode_item(g, n0, m0, m1, E, tile_start);
+        it = decode_item(g, n0, m0, m1, E, tile_start, num_tiles, kGrp1);
         ti = args.ws.tiles[it.tile];
       }
     }
@@ -324,6 +352,7 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
       const CUtensorMap* tt = it.phase ? &tmap_h : &tmap_x;
       // a full tile's token rows in one box
       const CUtensorMap* tt_full = it.phase ? &tmap_h_full : &tmap_x_full;
+      const uint64_t pol_tt = it.phase ? pol_h : pol_t;
       // A slab read by one token tile only is not kept; one shared by several
       // tiles of the expert stays for them.
       const uint64_t pol_w = it.ntiles > 1 ? pol_shared : pol_once;
@@ -404,18 +433,18 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
                          bar, pol_w);
           if (!pulled) {
             if (nb * kBBoxRows == SM::kBRows) {
-              ptx::tma_load_2d(b_dst, tt_full, kb * kBKBytes, row0, bar, pol_t);
+              ptx::tma_load_2d(b_dst, tt_full, kb * kBKBytes, row0, bar, pol_tt);
             } else {
               for (int j = 0; j < nb; ++j)
                 ptx::tma_load_2d(b_dst + j * kBBoxRows * kBKBytes, tt, kb * kBKBytes,
-                                 row0 + j * kBBoxRows, bar, pol_t);
+                                 row0 + j * kBBoxRows, bar, pol_tt);
             }
             ptx::bulk_load(smem + SM::kSFB + (size_t)stage * SM::kSF,
                            tsf + (size_t)kb * (kKb / kAtomK) * kSFAtomBytes, atoms * kSFAtomBytes,
-                           bar, pol_t);
+                           bar, pol_tt);
           }
           if (kb == 0 && g_next < total) {
-            it_next = decode_item(g_next, n0, m0, m1, E, tile_start);
+            it_next = decode_item(g_next, n0, m0, m1, E, tile_start, num_tiles, kGrp1);
             ti_next = args.ws.tiles[it_next.tile];
           }
         }
@@ -598,6 +627,7 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int ep_tid = threadIdx.x - 64;
+    const uint64_t pol_acc = ptx::policy_evict_last();
     int r = 0, xb = 0;
     uint32_t rph = 0, acc_phase = 0;
     while (true) {
@@ -795,7 +825,13 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
             const int src = (ci & 1) * kEpiCols + j;
             const int tok = __shfl_sync(kFull, my_tok, src);
             const float wt = __shfl_sync(kFull, my_w, src);
-            if (j < ncol) atomicAdd(args.ws.acc + (size_t)tok * args.H + feat, wt * v[j]);
+            if (j < ncol) {
+              float* dst = args.ws.acc + (size_t)tok * args.H + feat;
+              if constexpr (kGrp1 > 0 && kAccKeep)
+                ptx::red_add_f32(dst, wt * v[j], pol_acc);
+              else
+                atomicAdd(dst, wt * v[j]);
+            }
           }
         }
       };
