@@ -690,49 +690,79 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
           // gate and the up of lane+8, up lanes (8-15, 24-31) column 2p+1 from their up
           // and the gate of lane-8 -- one exchange, and no lane idles.
           const bool up_lane = (lane & 8) != 0;
-          float hv[kEpiCols / 2];
+          float hv[kEpiCols / 2], am[kEpiCols / 2];
 #pragma unroll
           for (int p = 0; p < kEpiCols / 2; ++p) {
             const float x = __shfl_xor_sync(kFull, up_lane ? v[2 * p] : v[2 * p + 1], 8);
             const float h = up_lane ? silu_times(x, v[2 * p + 1]) : silu_times(v[2 * p], x);
             hv[p] = h;
-            // max |h| over the 16 lanes of this column (lanes differing in bits 0-2, 4)
-            float a = fabsf(h);
-            a = fmaxf(a, __shfl_xor_sync(kFull, a, 1));
-            a = fmaxf(a, __shfl_xor_sync(kFull, a, 2));
-            a = fmaxf(a, __shfl_xor_sync(kFull, a, 4));
-            a = fmaxf(a, __shfl_xor_sync(kFull, a, 16));
-            if ((lane & 23) == 0) tail->xchg[xb][q][2 * p + (up_lane ? 1 : 0)] = a;  // lanes 0, 8
+            am[p] = fabsf(h);
+          }
+          // Max |h| of each of the lane's 8 columns over the 16 lanes holding that
+          // column (lane bits 0, 1, 2 and 4), as a transposing butterfly: after the
+          // steps over bits 0, 1 and 2 each lane keeps one column, p = 4 b0 + 2 b1 + b2
+          // (8 shuffles for the 8 columns instead of 32).
+          {
+            const bool b0 = (lane & 1) != 0, b1 = (lane & 2) != 0, b2 = (lane & 4) != 0;
+            float a4[4], a2[2];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const float send = b0 ? am[i] : am[4 + i];
+              const float keep = b0 ? am[4 + i] : am[i];
+              a4[i] = fmaxf(keep, __shfl_xor_sync(kFull, send, 1));
+            }
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+              const float send = b1 ? a4[i] : a4[2 + i];
+              const float keep = b1 ? a4[2 + i] : a4[i];
+              a2[i] = fmaxf(keep, __shfl_xor_sync(kFull, send, 2));
+            }
+            const float send = b2 ? a2[0] : a2[1];
+            const float keep = b2 ? a2[1] : a2[0];
+            float a1 = fmaxf(keep, __shfl_xor_sync(kFull, send, 4));
+            a1 = fmaxf(a1, __shfl_xor_sync(kFull, a1, 16));
+            if ((lane & 16) == 0) {
+              const int pm = (b0 ? 4 : 0) + (b1 ? 2 : 0) + (b2 ? 1 : 0);
+              tail->xchg[xb][q][2 * pm + (up_lane ? 1 : 0)] = a1;
+            }
           }
           ptx::named_bar_sync(1, 128);
           const int i_kc4 = args.I / kAtomK;   // scale blocks of an intermediate row
           const size_t hrow_bytes = F8 ? (size_t)args.I : (size_t)args.I / 2;
-          // All shared-memory reads first, then the arithmetic, then the writes: the
-          // eight columns' work is independent and overlaps instead of forming one
-          // chain through shared memory.
-          float amax[kEpiCols / 2];
-#pragma unroll
-          for (int p = 0; p < kEpiCols / 2; ++p) {
-            const int jc = 2 * p + (up_lane ? 1 : 0);  // this lane's column
-            // 32-feature group = this warp's 16 features + the partner warp's 16
-            // (NVFP4: the 16-feature group is this warp's alone)
-            amax[p] = NV ? tail->xchg[xb][q][jc]
-                         : fmaxf(tail->xchg[xb][q][jc], tail->xchg[xb][q ^ 1][jc]);
+          // The scale of each column is worked out once, by the lane that holds the
+          // column after the butterfly (column 2 pm + up, pm as above), and handed to the
+          // lanes that need it with one shuffle per column: that lane's scale byte goes
+          // to the staging area directly.
+          const int pm = ((lane & 1) << 2) | (lane & 2) | ((lane >> 2) & 1);
+          const int cm = 2 * pm + (up_lane ? 1 : 0);
+          // 32-feature group = this warp's 16 features + the partner warp's 16 (NVFP4:
+          // the 16-feature group is this warp's alone)
+          const float am_m = NV ? tail->xchg[xb][q][cm]
+                                : fmaxf(tail->xchg[xb][q][cm], tail->xchg[xb][q ^ 1][cm]);
+          float mul_m;   // MX: 2^-e; NVFP4: the E4M3 scale's value
+          uint32_t sb_m;
+          if (NV) {
+            sb_m = ptx::nvfp4_scale_byte(am_m);   // E4M3 of amax/6
+            mul_m = ptx::ue4m3_value(sb_m);
+          } else {
+            const int e = F8 ? ptx::mxfp8_exponent(am_m) : ptx::mx_scale_exponent(am_m);
+            sb_m = (uint32_t)(e + 127);
+            mul_m = ptx::pow2_neg(e);
+          }
+          if ((lane & 16) == 0) {
+            if (NV)
+              tail->sstage[xb][cm][q] = (uint8_t)sb_m;
+            else if ((q & 1) == 0)
+              tail->sstage[xb][cm][q >> 1] = (uint8_t)sb_m;
           }
           uint32_t code[kEpiCols / 2];
-          int ex[kEpiCols / 2];
 #pragma unroll
           for (int p = 0; p < kEpiCols / 2; ++p) {
-            float qv;
-            if (NV) {
-              // E4M3 scale of amax/6 (kept as its byte in ex), element h / scale
-              ex[p] = (int)ptx::nvfp4_scale_byte(amax[p]);
-              const float sc = ptx::ue4m3_value((uint32_t)ex[p]);
-              qv = sc > 0.f ? __fdiv_rn(hv[p], sc) : copysignf(0.f, hv[p]);
-            } else {
-              ex[p] = F8 ? ptx::mxfp8_exponent(amax[p]) : ptx::mx_scale_exponent(amax[p]);
-              qv = hv[p] * ptx::pow2_neg(ex[p]);
-            }
+            // column 2p + up is held by the lane with pm == p and the same up bit
+            const int src = ((p >> 2) & 1) | (((p >> 1) & 1) << 1) | ((p & 1) << 2) | (lane & 8);
+            const float m = __shfl_sync(kFull, mul_m, src);
+            const float qv = NV ? (m > 0.f ? __fdiv_rn(hv[p], m) : copysignf(0.f, hv[p]))
+                                : hv[p] * m;
             if (F8) {
               code[p] = ptx::e4m3x2(qv, 0.f) & 0xFFu;
             } else {
@@ -749,8 +779,6 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
             for (int p = 0; p < kEpiCols / 2; ++p) {
               const int jc = 2 * p + (up_lane ? 1 : 0);
               tail->hstage[xb][jc][f] = (uint8_t)code[p];
-              if ((lane & 23) == 0 && (q & 1) == 0)
-                tail->sstage[xb][jc][q >> 1] = (uint8_t)(ex[p] + 127);
             }
           } else if (lane < 16) {
             // lanes 0-7 (column 2p) and 8-15 (column 2p+1) each hold one of the 8
@@ -759,11 +787,6 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
             for (int p = 0; p < kEpiCols / 2; ++p) {
               const int jc = 2 * p + (up_lane ? 1 : 0);
               tail->hstage[xb][jc][q * 8 + (lane & 7)] = (uint8_t)code[p];
-              if (NV) {
-                if ((lane & 7) == 0) tail->sstage[xb][jc][q] = (uint8_t)ex[p];
-              } else if ((lane & 7) == 0 && (q & 1) == 0) {
-                tail->sstage[xb][jc][q >> 1] = (uint8_t)(ex[p] + 127);
-              }
             }
           }
           ptx::named_bar_sync(1, 128);
