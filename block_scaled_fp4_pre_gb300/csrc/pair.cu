@@ -558,19 +558,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           ptx::named_bar_sync(1 + hh, 128);
           const int i_kc4 = args.I / 128;
-          float amax[kEpiCols / 2];
-#pragma unroll
-          for (int p = 0; p < kEpiCols / 2; ++p) {
-            const int jc = 2 * p + (up_lane ? 1 : 0);
-            // 32-feature group: this warp's 16 features and the partner quarter's
-            amax[p] = fmaxf(tail->xchg[hh][xb][q][jc], tail->xchg[hh][xb][q ^ 1][jc]);
-          }
+          // Each column's scale once, by the lane holding the column after the
+          // butterfly (column 2 pm + up), shuffled to the lanes that need it; that
+          // lane stages the scale byte.  32-feature group: this warp's 16 features
+          // and the partner quarter's.
+          const int pm = ((lane & 1) << 2) | (lane & 2) | ((lane >> 2) & 1);
+          const int cm = 2 * pm + (up_lane ? 1 : 0);
+          const float am_m = fmaxf(tail->xchg[hh][xb][q][cm], tail->xchg[hh][xb][q ^ 1][cm]);
+          const int e_m = ptx::mx_scale_exponent(am_m);
+          const float mul_m = ptx::pow2_neg(e_m);
+          if ((lane & 16) == 0 && (q & 1) == 0) tail->sstage[hh][xb][cm][q >> 1] = (uint8_t)(e_m + 127);
           uint32_t code[kEpiCols / 2];
-          int ex[kEpiCols / 2];
 #pragma unroll
           for (int p = 0; p < kEpiCols / 2; ++p) {
-            ex[p] = ptx::mx_scale_exponent(amax[p]);
-            const float qv = hv[p] * ptx::pow2_neg(ex[p]);
+            const int src = ((p >> 2) & 1) | (((p >> 1) & 1) << 1) | ((p & 1) << 2) | (lane & 8);
+            const float qv = hv[p] * __shfl_sync(kFull, mul_m, src);
             const float qodd = __shfl_down_sync(kFull, qv, 16);
             code[p] = ptx::e2m1x2(qv, qodd);
           }
@@ -579,8 +581,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             for (int p = 0; p < kEpiCols / 2; ++p) {
               const int jc = 2 * p + (up_lane ? 1 : 0);
               tail->hstage[hh][xb][jc][q * 8 + (lane & 7)] = (uint8_t)code[p];
-              if ((lane & 7) == 0 && (q & 1) == 0)
-                tail->sstage[hh][xb][jc][q >> 1] = (uint8_t)(ex[p] + 127);
             }
           }
           ptx::named_bar_sync(1 + hh, 128);

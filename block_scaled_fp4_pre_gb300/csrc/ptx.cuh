@@ -465,10 +465,10 @@ __device__ __forceinline__ float pow2_neg(int e) {
   return __uint_as_float((uint32_t)(127 - e) << 23);
 }
 
-// Eight magnitudes (each <= 6) to E2M1 codes packed in 32 bits, element i in
-// bits 4i..4i+3, round to nearest even.  Sign bits are added by the caller.
-__device__ __forceinline__ uint32_t e2m1x8_mag(float m0, float m1, float m2, float m3, float m4,
-                                               float m5, float m6, float m7) {
+// E2M1 codes of eight scaled values (|v| <= 6) with their signs, element i in bits
+// 4i..4i+3 (so element 2j sits in the low nibble of byte j).  The conversion keeps
+// each value's sign, so a negative value that rounds to zero gives code 0x8.
+__device__ __forceinline__ uint32_t e2m1x8(const float (&v)[8]) {
   uint32_t r;
   asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
       "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
@@ -477,17 +477,7 @@ __device__ __forceinline__ uint32_t e2m1x8_mag(float m0, float m1, float m2, flo
       "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
       "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
       : "=r"(r)
-      : "f"(m0), "f"(m1), "f"(m2), "f"(m3), "f"(m4), "f"(m5), "f"(m6), "f"(m7));
-  return r;
-}
-
-// E2M1 codes of eight scaled values (|v| <= 6) with their signs, element i in bits
-// 4i..4i+3 (so element 2j sits in the low nibble of byte j).
-__device__ __forceinline__ uint32_t e2m1x8(const float (&v)[8]) {
-  uint32_t r = e2m1x8_mag(fabsf(v[0]), fabsf(v[1]), fabsf(v[2]), fabsf(v[3]), fabsf(v[4]),
-                          fabsf(v[5]), fabsf(v[6]), fabsf(v[7]));
-#pragma unroll
-  for (int i = 0; i < 8; ++i) r |= (__float_as_uint(v[i]) >> 31) << (4 * i + 3);
+      : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]));
   return r;
 }
 
@@ -498,9 +488,8 @@ __device__ __forceinline__ uint32_t e2m1x2(float a, float b) {
       "cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\t"
       "mov.b16 %0, {t, t};\n\t}"
       : "=h"(r)
-      : "f"(fabsf(b)), "f"(fabsf(a)));
-  return ((uint32_t)r & 0xFFu) | ((__float_as_uint(a) >> 31) << 3) |
-         ((__float_as_uint(b) >> 31) << 7);
+      : "f"(b), "f"(a));
+  return (uint32_t)r & 0xFFu;
 }
 
 // ---- MXFP8 element math ----------------------------------------------------
