@@ -65,6 +65,7 @@ struct TmemMap {
 };
 static_assert(TmemMap<false>::kSpareChunks == 6 && TmemMap<true>::kSpareChunks == 4,
               "tensor memory layout");
+static_assert(kBN / 32 == 4, "row metadata: four registers a lane");
 constexpr int kEpiCols = 16;               // accumulator columns per epilogue load
 constexpr int kRing = 8;                   // work items in flight inside a block
 constexpr unsigned kFull = 0xFFFFFFFFu;
@@ -840,20 +841,30 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
           // Down projection: this warp holds output features mt*128 + q*32 + lane of
           // up to 16 token columns; add them, weighted, into the fp32 accumulator.
           // Column c0+j's row metadata sits in lane (c0+j) % 32, register (c0+j) / 32.
-          const int my_tok = tok_r[ci >> 1];
-          const float my_w = w_r[ci >> 1];
-          const size_t feat = (size_t)mt * kBM + q * 32 + lane;
+          // Every column's token and weight are fetched before the first reduction, so
+          // that the 32 shuffles overlap one another instead of each waiting behind the
+          // reduction before it.
+          // (the chunk index is a loop variable: select, not index, the register)
+          const int hi = ci >> 1;
+          const int my_tok = hi == 0 ? tok_r[0] : hi == 1 ? tok_r[1] : hi == 2 ? tok_r[2] : tok_r[3];
+          const float my_w = hi == 0 ? w_r[0] : hi == 1 ? w_r[1] : hi == 2 ? w_r[2] : w_r[3];
+          int tok_j[kEpiCols];
+          float w_j[kEpiCols];
 #pragma unroll
           for (int j = 0; j < kEpiCols; ++j) {
             const int src = (ci & 1) * kEpiCols + j;
-            const int tok = __shfl_sync(kFull, my_tok, src);
-            const float wt = __shfl_sync(kFull, my_w, src);
+            tok_j[j] = __shfl_sync(kFull, my_tok, src);
+            w_j[j] = __shfl_sync(kFull, my_w, src);
+          }
+          float* const col0 = args.ws.acc + (size_t)mt * kBM + q * 32 + lane;
+#pragma unroll
+          for (int j = 0; j < kEpiCols; ++j) {
             if (j < ncol) {
-              float* dst = args.ws.acc + (size_t)tok * args.H + feat;
+              float* dst = col0 + (size_t)tok_j[j] * args.H;
               if constexpr (kGrp1 > 0 && kAccKeep)
-                ptx::red_add_f32(dst, wt * v[j], pol_acc);
+                ptx::red_add_f32(dst, w_j[j] * v[j], pol_acc);
               else
-                atomicAdd(dst, wt * v[j]);
+                atomicAdd(dst, w_j[j] * v[j]);
             }
           }
         }
@@ -922,24 +933,33 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
         }
       }
       ptx::tmem_wait_st();
-      // 3. The copied chunks; the load of chunk ci+1 runs during the math of ci.
+      // 3. The copied chunks; the load of chunk ci+1 runs during the math of ci.  A
+      //    rolled loop over pairs of chunks: every unrolled copy of the chunk math
+      //    costs instruction-cache room that the epilogue warps then wait on.
       uint32_t ra[kEpiCols], rb[kEpiCols];
       if (ncopy > 0) {
         ptx::tmem_ld16_issue(tspare, ra);
         ptx::tmem_wait_ld(ra);
       }
+#pragma unroll 1
+      for (int ci = 0; ci < ncopy; ci += 2) {
+        const bool m1 = ci + 1 < ncopy, m2 = ci + 2 < ncopy;
+        if (m1) ptx::tmem_ld16_issue(tspare + (uint32_t)((ci + 1) * kEpiCols), rb);
+        {
+          float v[kEpiCols];
 #pragma unroll
-      for (int ci = 0; ci < kSpareChunks; ++ci) {
-        if (ci >= ncopy) break;
-        uint32_t(&cur)[kEpiCols] = (ci & 1) ? rb : ra;
-        uint32_t(&nxt)[kEpiCols] = (ci & 1) ? ra : rb;
-        const bool more = ci + 1 < ncopy;
-        if (more) ptx::tmem_ld16_issue(tspare + (uint32_t)((ci + 1) * kEpiCols), nxt);
-        float v[kEpiCols];
+          for (int j = 0; j < kEpiCols; ++j) v[j] = __uint_as_float(ra[j]);
+          chunk(ci, v);
+        }
+        if (m1) ptx::tmem_wait_ld(rb);
+        if (m2) ptx::tmem_ld16_issue(tspare + (uint32_t)((ci + 2) * kEpiCols), ra);
+        if (m1) {
+          float v[kEpiCols];
 #pragma unroll
-        for (int j = 0; j < kEpiCols; ++j) v[j] = __uint_as_float(cur[j]);
-        chunk(ci, v);
-        if (more) ptx::tmem_wait_ld(nxt);
+          for (int j = 0; j < kEpiCols; ++j) v[j] = __uint_as_float(rb[j]);
+          chunk(ci + 1, v);
+        }
+        if (m2) ptx::tmem_wait_ld(ra);
       }
       if (MODE == kModeLayer && item_phase == 0) {
         // Publish: this item's intermediate rows (and scales) are written.

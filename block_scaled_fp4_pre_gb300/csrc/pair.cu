@@ -607,16 +607,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         } else {
           // Down projection: this warp holds output features slab*128 + q*32 + lane of
           // up to 16 token columns; add them, weighted, into the fp32 accumulator.
+          // Every column's token and weight first, so the shuffles overlap.
           const int my_tok = tok_r[k];
           const float my_w = w_r[k];
-          const size_t feat = (size_t)slab * kBM + q * 32 + lane;
+          int tok_j[kEpiCols];
+          float w_j[kEpiCols];
 #pragma unroll
           for (int j = 0; j < kEpiCols; ++j) {
             const int src = hh * kEpiCols + j;
-            const int tok = __shfl_sync(kFull, my_tok, src);
-            const float wt = __shfl_sync(kFull, my_w, src);
-            if (j < ncol) atomicAdd(args.ws.acc + (size_t)tok * args.H + feat, wt * v[j]);
+            tok_j[j] = __shfl_sync(kFull, my_tok, src);
+            w_j[j] = __shfl_sync(kFull, my_w, src);
           }
+          float* const col0 = args.ws.acc + (size_t)slab * kBM + q * 32 + lane;
+#pragma unroll
+          for (int j = 0; j < kEpiCols; ++j)
+            if (j < ncol) atomicAdd(col0 + (size_t)tok_j[j] * args.H, w_j[j] * v[j]);
         }
       };
       // This warp's chunks, each load issued one chunk ahead of its math; once the
