@@ -124,3 +124,39 @@ def test_w4a8_full_size_sampled_tokens(dsv4_w4a8, name):
     every token row bit-exact; on sampled tokens, intermediate flips within 0.1% (one
     step each) and outputs within the oracle's bar."""
     full_size_check(dsv4_w4a8, synth.WORKLOADS[name], "w4a8", n_sample=8, seed=23)
+
+
+@pytest.mark.parametrize("name", ["ragged", "oddslab"])
+def test_w4a8_tile_widths_agree(name):
+    """E4M3 tokens on 32- and 64-row tiles stage two 128-element k-blocks at a time;
+    128-row tiles one.  Shapes with an odd number of k-blocks (K = 384: the last stage
+    holds one) must give the same gate/up accumulators and intermediate codes on every
+    tile width (the tile width changes which token rows share an MMA, not any element's
+    K reduction), and outputs equal up to the order of the combine's fp32 additions."""
+    layer, W = _layer(name)
+    w = layer.w
+    x = synth.hidden_bf16(w)
+    ids, tw = synth.routing(w)
+    ref = oracle.moe_w4a8(x, ids, tw, *W)
+    seen = {}
+    try:
+        for tiles in (mx.MOE_TILES_NARROW, mx.MOE_TILES_MEDIUM, mx.MOE_TILES_WIDE):
+            mx.moe_workspace_set_tiles(layer.ws, tiles)
+            mx.moe_pre_dispatch(layer.dims, to_dev(x), to_dev(ids), to_dev(tw), w.T, layer.ws)
+            gu = torch.full((w.T * w.k, 2 * w.I), float("nan"), dtype=torch.float32,
+                            device=device())
+            mx.moe_debug_gate_up(layer.dims, layer.prepared, layer.ws, gu, w.T)
+            mx.moe_check(layer.ws)
+            out = layer.run(x, ids, tw)
+            inter = mx.moe_read_intermediate(layer.dims, layer.ws, w.T)
+            seen[tiles] = (gu.cpu().numpy(), inter["h_codes"], inter["h_scales"], out)
+            assert normwise_rel_err(oracle.bf16_bits_to_f64(out), ref["out_f64"]) <= 2e-3
+    finally:
+        mx.moe_workspace_set_tiles(layer.ws, mx.MOE_TILES_AUTO)
+    g0, c0, s0, o0 = seen[mx.MOE_TILES_WIDE]
+    assert np.all(np.isfinite(g0))
+    for tiles in (mx.MOE_TILES_NARROW, mx.MOE_TILES_MEDIUM):
+        g, c, sc, o = seen[tiles]
+        assert np.array_equal(g, g0), tiles
+        assert np.array_equal(c, c0) and np.array_equal(sc, s0), tiles
+        assert normwise_rel_err(oracle.bf16_bits_to_f64(o), oracle.bf16_bits_to_f64(o0)) <= 1e-3
