@@ -70,7 +70,7 @@ def parse_args():
     p.add_argument("--dispatch", choices=["bucketed", "pull"], default="bucketed",
                    help="token rows copied per expert by pre_dispatch, or gathered by the layer")
     p.add_argument("--tiles", choices=["auto", "wide", "medium", "narrow", "pair"], default="auto",
-                   help="token tiles: 128 rows (wide), 64 (medium), 32 (narrow), 256 on SM pairs "
+                   help="token tiles: 128 rows (wide), 64 (medium), 32 (narrow), 192 on SM pairs "
                         "(pair) or the layer's choice")
     p.add_argument("--mma", choices=["mxf4xmxf4", "fp8xfp4", "nvf4xnvf4"], default="mxf4xmxf4",
                    help="formats: MXFP4 (W4A4, the headline), MXFP8 activations (W4A8) or NVFP4")
@@ -196,6 +196,23 @@ OTHER_WORKLOADS = ("decode_T64", "prefill_T4096", "prefill_T16384_zipf")
 # FP8 : bf16 (4.5 : 2.25) for the fp8xfp4 MMAs (kind::mxf8f6f4 runs at the FP8 rate).
 FP4_PER_BF16 = 6.0
 FP8_PER_BF16 = 2.0
+
+
+# The pages' own layer times for the benchmark's workload (the DeepSeek-V4-Flash layer at
+# ntok=512, one rank in isolation; "[deepseek-v4] Bump sgl-deep-gemm for packed FP4xFP4
+# mega-MoE (W4A4)", Appendix B), measured on B200: context for the ratio, not a target.
+PAGES_US_T512 = {"mxf4xmxf4": 537.6, "fp8xfp4": 753.2}
+
+
+def pages_ratio(args, w, world: int, value: float):
+    """value / the pages' tokens/s for the same workload and mma type on one GPU, and
+    what the ratio is against; (None, None) where the pages give no figure."""
+    us = PAGES_US_T512.get(args.mma)
+    if us is None or w.name != "layer_T512" or world != 1 or args.tokens or args.experts:
+        return None, None
+    ref = w.T / (us * 1e-6)
+    return value / ref, (f"the pages' {us} us per layer ({ref:.0f} tokens/s) for this layer at "
+                         "ntok=512, one rank, measured on B200 (another GPU: context)")
 
 
 def fp4_peak_from_bf16(peaks: dict) -> float:
@@ -700,11 +717,13 @@ def run_ours(args):
 
     if rank != 0:
         return
+    vs, vs_basis = pages_ratio(args, w, world, value)
     line = {
         "metric": metric(args),
         "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "us_per_layer": ms * 1e3,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": vs,
+        "vs_baseline_basis": vs_basis,
         "dtype": ("mxfp4 weights (e2m1 x ue8m0) x mxfp8 activations (e4m3 x ue8m0), fp32 accumulate"
                   if w4a8(args) else
                   "nvfp4 (e2m1 x ue4m3 per 16), fp32 accumulate" if nvf4(args) else
