@@ -19,6 +19,12 @@
 // staged byte, with no multicast.  Two 192-column accumulators fit one SM's tensor
 // memory with the scale registers, so an item's MMAs never wait for the previous
 // item's epilogue to read its accumulator.
+// Measured on GB300 it is slower than the single-block kernel (T=16384: 2.25 against
+// 1.64 ms): the staged bytes turned out not to bind, the MMA issuer does.  One thread
+// issues every tensor-core instruction of a pair -- a k-block's copies, MMAs and
+// commits plus the stage round trip, ~900 cycles whatever the MMA's N -- for two SMs,
+// where the single-block kernel has two issuers on every SM.  So the layer uses this
+// kernel only when asked (MOE_TILES_PAIR).
 //
 // Items are (token tile <= 192 rows, pair of 128-row weight slabs), first every
 // gate/up item, then every down item, each phase expert by expert, slab pair by slab

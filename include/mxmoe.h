@@ -147,7 +147,8 @@ MXMOE_API moe_status moe_workspace_set_dispatch(void *ws_dev, int32_t mode);
  *                     tcgen05 MMAs over both SMs' shared memory: 1.6 times the FLOPs
  *                     per staged operand byte).  mxf4xmxf4 with the bucketed dispatch
  *                     and H a multiple of 256 only; otherwise it falls back to wide
- *                     tiles.
+ *                     tiles.  Slower than wide tiles on GB300 (one MMA-issuing thread
+ *                     per two SMs), so MOE_TILES_AUTO never picks it.
  *   MOE_TILES_AUTO (default after moe_workspace_init): narrow when num_tokens * k <=
  *                     16 * num_experts, medium when <= 64 * num_experts, else wide.
  * The choice is made at each moe_pre_dispatch and holds for the forward that
